@@ -1,0 +1,29 @@
+"""CPU oracle for one bit-grouped-expert MoE layer (test infrastructure only).
+
+This package is the plain, slow, fp64 statement of what the layer computes. It
+exists to check the CUDA library and to serve as the timed CPU baseline; only
+the tests, the smoke check and the benchmark's CPU-baseline leg may import it.
+The product path never calls it and shares no code with it.
+
+Sources (three web pages on Perplexity's Lily engine for Qwen3.6-35B-A3B):
+  [dothoosh]  "Perplexity Lily: 1.35x faster decode for Qwen3.6 on Apple
+              silicon", dothoosh.com
+  [aikraft]   "Perplexity open-sources Lily, a Rust/Metal inference engine for
+              Qwen3.6", aikraft.ru
+  [droneth]   Lily inference engine article, droneth.or.th
+
+Every function in `moe.py` names the section it follows. Where the pages are
+silent (affine formula, nibble order, softmax/top-k order, shared-expert gate,
+activation), the reading taken is stated in that function's docstring.
+"""
+from .moe import (  # noqa: F401
+    bf16_bits_to_f64,
+    dequant,
+    router_logits,
+    select_top_k,
+    route,
+    routing_tables,
+    swiglu_expert,
+    moe_forward,
+    topk_gap,
+)

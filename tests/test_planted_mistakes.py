@@ -1,0 +1,135 @@
+"""Plants plausible mistakes in the CPU oracle (on the CPU, by swapping one of
+its functions for a mutated copy) and checks that at least one pin fails for
+each: the pins are sensitive to dropped terms, wrong signs, wrong indices and
+transposed operands, not only to crashes."""
+import numpy as np
+import pytest
+
+import oracle.moe as M
+from tests.oracle_pins import PINS
+
+_dequant = M.dequant
+_route = M.route
+_routing = M.routing_tables
+_swiglu = M.swiglu_expert
+_select = M.select_top_k
+_logits = M.router_logits
+
+
+def nibble_order_reversed(codes, scales, biases, group=64):
+    c = np.asarray(codes).view(np.uint32)
+    N, KW = c.shape
+    sh = 4 * (7 - np.arange(8, dtype=np.uint32))
+    q = ((c[:, :, None] >> sh[None, None, :]) & np.uint32(15)).reshape(N, KW * 8).astype(np.float64)
+    s = np.repeat(M.bf16_bits_to_f64(scales), group, axis=1)
+    b = np.repeat(M.bf16_bits_to_f64(biases), group, axis=1)
+    return s * q + b
+
+
+def bias_subtracted(codes, scales, biases, group=64):
+    W0 = _dequant(codes, scales, np.zeros_like(np.asarray(biases)), group)
+    return W0 - np.repeat(M.bf16_bits_to_f64(biases), group, axis=1)
+
+
+def signed_codes(codes, scales, biases, group=64):
+    W = _dequant(codes, scales, biases, group)
+    q = (W - np.repeat(M.bf16_bits_to_f64(biases), group, axis=1))
+    s = np.repeat(M.bf16_bits_to_f64(scales), group, axis=1)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        qq = np.where(s != 0, np.rint(q / np.where(s != 0, s, 1)), 0)
+    qq = np.where(qq >= 8, qq - 16, qq)
+    return s * qq + np.repeat(M.bf16_bits_to_f64(biases), group, axis=1)
+
+
+def scale_per_group_of_32(codes, scales, biases, group=64):
+    return _dequant(codes, np.repeat(scales, 2, axis=1)[:, : np.asarray(scales).shape[1]], biases, group)
+
+
+def ties_to_higher_index(logits, top_k):
+    l32 = np.asarray(logits).astype(np.float32)
+    E = l32.shape[1]
+    order = np.argsort(-l32[:, ::-1], axis=1, kind="stable")
+    return (E - 1 - order[:, :top_k]).astype(np.int32)
+
+
+def logits_transposed_bias(x, wr, bias=None):
+    l = _logits(x, wr, None)
+    if bias is not None:
+        l = l - np.asarray(bias, dtype=np.float64)[None, :]
+    return l
+
+
+def no_renormalisation(x, wr, bias, wsg, top_k):
+    ids, w, g, l = _route(x, wr, bias, wsg, top_k)
+    p = np.exp(l - l.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    return ids, np.take_along_axis(p, ids.astype(np.int64), axis=1), g, l
+
+
+def gate_is_one_minus_sigmoid(x, wr, bias, wsg, top_k):
+    ids, w, g, l = _route(x, wr, bias, wsg, top_k)
+    return ids, w, (None if g is None else 1.0 - g), l
+
+
+def scatter_reversed_within_expert(ids, E, block_m, shared=True):
+    tab = _routing(ids, E, block_m, shared)
+    off, srt = tab["offsets"], tab["sorted"].copy()
+    for e in range(E):
+        srt[off[e]:off[e + 1]] = srt[off[e]:off[e + 1]][::-1]
+    inv = np.zeros_like(srt)
+    inv[srt] = np.arange(srt.size, dtype=srt.dtype)
+    return dict(tab, sorted=srt, inv=inv)
+
+
+def tiles_off_by_one(ids, E, block_m, shared=True):
+    tab = _routing(ids, E, block_m, shared)
+    return dict(tab, tile_rows=np.minimum(tab["tile_rows"] + 1, block_m + 1))
+
+
+def offsets_inclusive(ids, E, block_m, shared=True):
+    tab = _routing(ids, E, block_m, shared)
+    off = tab["offsets"].copy()
+    off[:-1] = off[1:]
+    return dict(tab, offsets=off)
+
+
+def gate_up_swapped(xrows, w_gu, w_dn):
+    I = w_gu.shape[0] // 2
+    return _swiglu(xrows, np.concatenate([w_gu[I:], w_gu[:I]]), w_dn)
+
+
+def relu_instead_of_silu(xrows, w_gu, w_dn):
+    I = w_gu.shape[0] // 2
+    gu = xrows @ w_gu.T
+    return (np.maximum(gu[:, :I], 0) * gu[:, I:]) @ w_dn.T
+
+
+def down_transposed(xrows, w_gu, w_dn):
+    I = w_gu.shape[0] // 2
+    gu = xrows @ w_gu.T
+    h = gu[:, :I] / (1 + np.exp(-gu[:, :I])) * gu[:, I:]
+    H = w_dn.shape[0]
+    return h @ (w_dn if H == I else w_dn.reshape(I, H))
+
+
+MUTANTS = [
+    ("dequant", nibble_order_reversed), ("dequant", bias_subtracted), ("dequant", signed_codes),
+    ("dequant", scale_per_group_of_32), ("select_top_k", ties_to_higher_index),
+    ("router_logits", logits_transposed_bias), ("route", no_renormalisation),
+    ("route", gate_is_one_minus_sigmoid), ("routing_tables", scatter_reversed_within_expert),
+    ("routing_tables", tiles_off_by_one), ("routing_tables", offsets_inclusive),
+    ("swiglu_expert", gate_up_swapped), ("swiglu_expert", relu_instead_of_silu),
+    ("swiglu_expert", down_transposed),
+]
+
+
+@pytest.mark.parametrize("name,mutant", MUTANTS, ids=[m.__name__ for _, m in MUTANTS])
+def test_planted_mistake_is_caught(monkeypatch, name, mutant):
+    monkeypatch.setattr(M, name, mutant)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake {mutant.__name__}"
