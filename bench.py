@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 MoE layer (one JSON line on stdout).
+
+Default workload: decode, T = 1 token through 40 MoE layers with distinct
+weights (H = 2048, I = 512, E = 256 top-8 + shared, 4-bit group-64 weights,
+18.2 GB of weights, far larger than L2), one step = one pass over the 40
+layers; the metric is microseconds per layer. --workload picks another
+shape (prefill-zipf-512, prefill-4096, long-skew-16384, decode-t4, tiny).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (tests' fp64 reference) on the host
+cores, on a bounded sample of the same workload. Under torchrun (N > 1)
+every rank runs an independent replica (the layer has no exchange step) and
+rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+BYTES_PER_WEIGHT = 0.5 + 4.0 / 64.0  # 4-bit code + bf16 scale + bf16 bias per 64
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][2]) if rows[0][2].replace(".", "").isdigit() else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- workload --
+
+class Workload:
+    """Device-resident inputs of one workload and the per-step launch list."""
+
+    def __init__(self, m, spec, device, block_m, rank=0):
+        self.m, self.spec, self.dev = m, spec, device
+        self.layers = spec.layers
+        self.T = spec.chunk if spec.chunk else spec.T
+        self.calls = (spec.T // spec.chunk) if spec.chunk else 1
+        self.shape = m.make_shape(self.T, spec.H, spec.I, spec.E, spec.top_k, spec.shared, block_m)
+        self.L = [synth.layer(spec, li, device) for li in range(self.layers)]
+        self.experts = []
+        for L in self.L:
+            routed = ((L.gu[0], L.gu[1], L.gu[2]), (L.dn[0], L.dn[1], L.dn[2]))
+            shared = None if L.sgu is None else ((L.sgu[0], L.sgu[1], L.sgu[2]), (L.sdn[0], L.sdn[1], L.sdn[2]))
+            self.experts.append((routed, shared))
+        # token rows (replica r of a multi-rank job takes its own rows)
+        self.x = synth.activations(spec, device=device, start=rank * spec.T).view(self.calls, self.T, spec.H)
+        self.ws = m.alloc_workspace(self.shape, device)
+        self.y = torch.empty(self.layers, self.calls, self.T, spec.H, dtype=torch.float32, device=device)
+        self.route = [m.alloc_route_out(self.shape, device) for _ in range(self.layers)]
+
+    def launches_per_step(self):
+        return 5 * self.layers * self.calls
+
+    def call(self, li, c, events=None):
+        L = self.L[li]
+        routed, shared = self.experts[li]
+        if events is None:
+            self.m.forward(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg, self.y[li, c], self.ws,
+                           route_out=self.route[li])
+        else:
+            self.m.forward_timed(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg, self.y[li, c], self.ws,
+                                 events, route_out=self.route[li])
+
+    def step(self):
+        for c in range(self.calls):
+            for li in range(self.layers):
+                self.call(li, c)
+
+    # -- algorithmic work (counted from the routing of the last call) --
+    def work(self):
+        s = self.spec
+        H, I, E = s.H, s.I, s.E
+        wbytes_expert = 3 * H * I * BYTES_PER_WEIGHT
+        router_bytes = (E + (1 if s.shared else 0)) * H * 2
+        tot_bytes = gu_bytes = 0.0
+        distinct = []
+        for li in range(self.layers):
+            counts = self.route[li]["counts"].cpu()
+            d = int((counts[:E] > 0).sum())
+            distinct.append(d)
+            n_exp = d + (1 if s.shared else 0)
+            per_call = n_exp * wbytes_expert + router_bytes + self.T * H * 2 + self.T * H * 4
+            tot_bytes += per_call * self.calls
+            gu_bytes += n_exp * (2 * I * H * BYTES_PER_WEIGHT) * self.calls
+        flops_tok = 2 * H * E + s.top_k * 6 * H * I + (6 * H * I if s.shared else 0) + (2 * H if s.shared else 0)
+        return dict(bytes_per_step=tot_bytes, gate_up_bytes_per_step=gu_bytes,
+                    flops_per_step=flops_tok * self.T * self.calls * self.layers,
+                    distinct_experts_mean=sum(distinct) / len(distinct))
+
+
+def time_region(fn, steps, stream):
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def stage_times(W, steps, stream):
+    """Per-kernel averages (ms) from events recorded between the kernels of
+    every call, on the launching stream."""
+    sums = [0.0] * 5
+    n = 0
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(W.layers * W.calls)]
+    for e6 in ev:           # torch creates the CUDA event at its first record
+        for e in e6:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        k = 0
+        for c in range(W.calls):
+            for li in range(W.layers):
+                W.call(li, c, events=[e.cuda_event for e in ev[k]])
+                k += 1
+        torch.cuda.synchronize()
+        for e6 in ev:
+            for i in range(5):
+                sums[i] += e6[i].elapsed_time(e6[i + 1])
+            n += 1
+    return [s_ / n for s_ in sums]
+
+
+def run_ours(args, spec, rank, world, local_rank):
+    import bit_grouped_expert_moe_gb300 as m
+    from bit_grouped_expert_moe_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    block_m = args.block_m or (16 if spec.T <= 64 else 64 if spec.T <= 1024 else 128)
+    W = Workload(m, spec, dev, block_m, rank)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        W.step()
+    torch.cuda.synchronize()
+    for li in range(W.layers):
+        assert m.status_read(W.route[li]["status"]) == 0
+    work = W.work()
+
+    barrier(world)
+    with ClockSampler(local_rank) as clk:
+        ms = time_region(W.step, args.steps, stream)
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    clocks = clk.summary()
+
+    # per-kernel breakdown (events between the kernels of every call)
+    prof_steps = max(1, min(args.steps, 20))
+    st = stage_times(W, prof_steps, stream)
+    names = ["router", "routing", "expert_gate_up", "expert_down", "combine"]
+    per_call_ms = dict(zip(names, st))
+
+    # end to end through the same C ABI with host buffers: copy x in from
+    # pinned memory, run, read every layer's y back
+    x_host = W.x.cpu().pin_memory()
+    y_host = torch.empty(W.y.shape, dtype=W.y.dtype).pin_memory()
+
+    def e2e_step():
+        W.x.copy_(x_host, non_blocking=True)
+        W.step()
+        y_host.copy_(W.y, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    e2e_ms = max_over_ranks(time_region(e2e_step, max(1, args.steps // 2), stream), world, dev) / max(1, args.steps // 2)
+
+    pk, pk_src = peaks()
+    layers_calls = W.layers * W.calls
+    tokens_step = spec.T * W.layers
+    if spec.T <= 4:
+        unit = "us/layer"
+        value = ms_step * 1000.0 / W.layers
+        e2e_value = e2e_ms * 1000.0 / W.layers
+        higher = False
+    else:
+        unit = "tokens/s"
+        value = world * tokens_step / (ms_step / 1000.0)
+        e2e_value = world * tokens_step / (e2e_ms / 1000.0)
+        higher = True
+    gu_ms = per_call_ms["expert_gate_up"]
+    gu_bytes_launch = work["gate_up_bytes_per_step"] / layers_calls
+    achieved = gu_bytes_launch / (gu_ms / 1000.0) / 1e9
+    peak = pk["hbm_gbs"]
+    roofline = {"kernel": "expert_gate_up", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": pk_src, "algorithmic_bytes_per_launch": int(gu_bytes_launch)}
+    layer_bytes = work["bytes_per_step"] / layers_calls
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": higher, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": spec.name, "T": spec.T, "H": spec.H, "I": spec.I, "E": spec.E, "top_k": spec.top_k,
+                   "shared_expert": spec.shared, "layers": W.layers, "tokens_per_call": W.T, "block_m": block_m,
+                   "router_bias": spec.bias, "seed": spec.seed,
+                   "l2": f"inputs larger than L2: {W.layers} layers x {layer_bytes / 1e6:.0f} MB touched per step"
+                   if W.layers > 1 else "weights 455.8 MB per layer, larger than the 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": roofline,
+        "layer": {"us_per_layer": round(ms_step * 1000.0 / layers_calls, 3),
+                  "algorithmic_bytes_per_layer": int(layer_bytes),
+                  "hbm_frac_per_layer": round(layer_bytes / (ms_step / 1000.0 / layers_calls) / 1e9 / peak, 4),
+                  "distinct_experts_mean": work["distinct_experts_mean"],
+                  "tflops": round(work["flops_per_step"] / (ms_step / 1000.0) / 1e12, 3)},
+        "kernels_us_per_call": {k: round(v * 1000.0, 3) for k, v in per_call_ms.items()},
+        "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": x_host.numel() * 2,
+                "d2h_bytes_per_step": y_host.numel() * 4},
+        "gpu_launches": W.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out
+
+
+# ----------------------------------------------------------- CPU oracle --
+
+def _oracle_layer_sample(spec, layer_idx, tokens):
+    """One oracle call of the workload on `tokens` of a layer; weights are
+    regenerated on the CPU (not timed) and the oracle's own work (routing,
+    dequantisation of every used expert, the products) is timed."""
+    import numpy as np
+    import oracle
+    from tests._util import bits16, expert_fn_lazy
+    x = synth.activations(spec, T=max(tokens) + 1)
+    wr, wsg = synth.router_weights(spec, layer_idx)
+    b = synth.router_bias(spec)
+    xb = bits16(x)
+    wrb = bits16(wr)
+    wsgb = None if wsg is None else bits16(wsg)
+    bias = None if b is None else b.numpy()
+    # regenerate the experts these tokens use before the clock starts
+    ids, *_ = oracle.route(xb[tokens], wrb, bias, wsgb, spec.top_k)
+    fn = expert_fn_lazy(spec, layer_idx)
+    cache = {e: fn(int(e)) for e in list(np.unique(ids)) + ([spec.E] if spec.shared else [])}
+    t0 = time.perf_counter()
+    oracle.moe_forward(xb, wrb, bias, wsgb, spec.top_k, lambda e: cache[e], tokens=np.asarray(tokens))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(spec, seconds):
+    """The oracle, as it stands, timed on this host's cores on a bounded
+    sample of the workload, in the workload's unit."""
+    import numpy as np
+    spent, calls, toks = 0.0, 0, 0
+    if spec.T <= 4:
+        li = 0
+        while spent < seconds and li < spec.layers:
+            spent += _oracle_layer_sample(spec, li, list(range(spec.T)))
+            calls += 1
+            li += 1
+        value, unit = spent / calls * 1e6, "us/layer"
+        sample = f"{calls} of the {spec.layers} layers at T={spec.T}"
+    else:
+        n = min(spec.chunk or spec.T, 256)
+        rng = np.random.default_rng(1)
+        while spent < seconds and calls < 8:
+            tokens = sorted(rng.choice(spec.chunk or spec.T, n, replace=False).tolist())
+            spent += _oracle_layer_sample(spec, 0, tokens)
+            calls += 1
+            toks += n
+        value, unit = toks / spent, "tokens/s"
+        sample = f"{calls} calls of {n} sampled tokens of layer 0"
+    return {"value": round(value, 3), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": sample + " (numpy fp64; BLAS multithreaded, dequantisation single-threaded)",
+            "seconds": round(spent, 2)}
+
+
+def run_reference(args, spec, rank, world):
+    """The reference arm: the CPU oracle on the host cores (rank 0 only)."""
+    if rank != 0:
+        return None
+    budget = 150.0
+    times = []
+    t_start = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        if time.perf_counter() - t_start > budget and len(times) >= 1:
+            break
+        if spec.T <= 4:
+            dt = _oracle_layer_sample(spec, i % spec.layers, list(range(spec.T)))
+        else:
+            import numpy as np
+            rng = np.random.default_rng(i)
+            n = min(spec.chunk or spec.T, 64)
+            dt = _oracle_layer_sample(spec, 0, sorted(rng.choice(spec.chunk or spec.T, n, replace=False).tolist()))
+        if i >= args.warmup:
+            times.append(dt)
+    if not times:
+        times.append(dt)
+    mean = sum(times) / len(times)
+    if spec.T <= 4:
+        value, unit, higher = mean * 1e6, "us/layer", False
+        sample = f"one layer at T={spec.T} per step"
+    else:
+        n = min(spec.chunk or spec.T, 64)
+        value, unit, higher = n / mean, "tokens/s", True
+        sample = f"{n} sampled tokens of layer 0 per step"
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world,
+           "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(mean * 1000, 3), "higher_is_better": higher, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": spec.name, "T": spec.T, "H": spec.H, "I": spec.I, "E": spec.E,
+                      "top_k": spec.top_k, "layers": spec.layers},
+           "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
+                            "sample": sample + f"; capped at {budget:.0f} s of oracle work"},
+           "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode-t1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    spec = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        out = run_reference(args, spec, rank, world)
+    else:
+        out = run_ours(args, spec, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

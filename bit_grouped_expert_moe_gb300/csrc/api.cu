@@ -1,0 +1,330 @@
+// C ABI of the MoE layer: argument checks, workspace layout and the launch
+// sequence router -> routing -> expert gate/up -> expert down -> combine, all
+// enqueued on the caller's stream with no host synchronisation.
+#include <cstdio>
+#include <cstring>
+
+#include "kernels.h"
+
+namespace bgmoe {
+namespace {
+
+constexpr long long kDefaultTimeoutNs = 1000000000ll;  // 1 s per device-side wait
+constexpr int kMaxRouteBlocks = 128;
+constexpr int kMinTokensPerRouteBlock = 16;
+constexpr int kMaxTokens = 1 << 18;
+
+thread_local char g_detail[256] = "";
+
+moe_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+moe_status check_shape(const moe_shape* s) {
+  if (!s) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->H <= 0 || s->I <= 0 || s->E <= 0 || s->top_k <= 0 || s->I_shared < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (s->T > kMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->group_size != kGroup) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->H % 64 || s->H < 64 || s->H > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->I % 64 || s->I < 64 || s->I > 4096) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->I_shared != 0 && s->I_shared != s->I) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->top_k > kMaxTopK || s->top_k > s->E || s->E > kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (s->block_m != 16 && s->block_m != 32 && s->block_m != 64 && s->block_m != 128)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+Geometry geometry(const moe_shape& s) {
+  Geometry g{};
+  g.T = s.T;
+  g.H = s.H;
+  g.I = s.I;
+  g.E = s.E;
+  g.K = s.top_k;
+  g.BM = s.block_m;
+  g.shared = s.I_shared > 0 ? 1 : 0;
+  g.A = s.T * s.top_k;
+  g.rows = g.A + (g.shared ? s.T : 0);
+  const int ce = (g.A + g.BM - 1) / g.BM;
+  g.max_tiles = ce + (g.A < g.E ? g.A : g.E) + (g.shared ? (g.T + g.BM - 1) / g.BM : 0);
+  int P = (g.T + kMinTokensPerRouteBlock - 1) / kMinTokensPerRouteBlock;
+  if (P > kMaxRouteBlocks) P = kMaxRouteBlocks;
+  if (P < 1) P = 1;
+  g.route_blocks = P;
+  g.tokens_per_block = (g.T + P - 1) / P;
+  return g;
+}
+
+// Workspace regions, each 256-byte aligned, in this order.
+struct Workspace {
+  int32_t* status;
+  float* logits;              // [T][E+1]
+  unsigned long long* state;  // [P][E]
+  int32_t* ids;               // routing tables kept here when the caller passes none
+  float* weights;
+  float* gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted;
+  int32_t* inv;
+  int32_t* tile_expert;
+  int32_t* tile_row0;
+  int32_t* tile_rows;
+  int32_t* num_tiles;
+  uint16_t* x16;              // [T][H] fp16 activations for the tensor-core path
+  __half* h;                  // [rows][I]
+  __half* o;                  // [rows][H]
+  size_t bytes;
+};
+
+Workspace carve(const Geometry& g, void* base) {
+  Workspace w{};
+  size_t off = 0;
+  char* b = static_cast<char*>(base);
+  auto take = [&](size_t n) -> void* {
+    void* p = b ? b + off : nullptr;
+    off += (n + 255) & ~size_t(255);
+    return p;
+  };
+  w.status = static_cast<int32_t*>(take(sizeof(int32_t)));
+  w.logits = static_cast<float*>(take(sizeof(float) * (size_t)g.T * (g.E + 1)));
+  w.state = static_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)g.route_blocks * g.E));
+  w.ids = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.A));
+  w.weights = static_cast<float*>(take(sizeof(float) * (size_t)g.A));
+  w.gate = static_cast<float*>(take(sizeof(float) * (size_t)g.T));
+  w.counts = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(g.E + 1)));
+  w.offsets = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)(g.E + 2)));
+  w.sorted = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.A));
+  w.inv = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.A));
+  w.tile_expert = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
+  w.tile_row0 = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
+  w.tile_rows = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
+  w.num_tiles = static_cast<int32_t*>(take(sizeof(int32_t)));
+  w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)g.T * g.H));
+  w.h = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.I));
+  w.o = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.H));
+  w.bytes = off;
+  return w;
+}
+
+bool route_out_ok(const moe_route_out* o, bool shared) {
+  return o && o->ids && o->weights && o->counts && o->offsets && o->sorted && o->inv && o->tile_expert &&
+         o->tile_row0 && o->tile_rows && o->num_tiles && o->status && (!shared || o->gate);
+}
+
+moe_route_out ws_route_out(const Workspace& w) {
+  moe_route_out r{};
+  r.ids = w.ids;
+  r.weights = w.weights;
+  r.gate = w.gate;
+  r.counts = w.counts;
+  r.offsets = w.offsets;
+  r.sorted = w.sorted;
+  r.inv = w.inv;
+  r.tile_expert = w.tile_expert;
+  r.tile_row0 = w.tile_row0;
+  r.tile_rows = w.tile_rows;
+  r.num_tiles = w.num_tiles;
+  r.status = w.status;
+  return r;
+}
+
+moe_status enqueue_routing_only(const Geometry& g, const float* router_bias, const moe_route_out& r,
+                                const Workspace& w, int stalled_block, long long timeout_ns, cudaStream_t stream) {
+  RouteArgs a{};
+  a.logits = w.logits;
+  a.bias = router_bias;
+  a.T = g.T;
+  a.E = g.E;
+  a.K = g.K;
+  a.BM = g.BM;
+  a.shared = g.shared;
+  a.P = g.route_blocks;
+  a.tpb = g.tokens_per_block;
+  a.ids = r.ids;
+  a.weights = r.weights;
+  a.gate = r.gate;
+  a.counts = r.counts;
+  a.offsets = r.offsets;
+  a.sorted = r.sorted;
+  a.inv = r.inv;
+  a.tile_expert = r.tile_expert;
+  a.tile_row0 = r.tile_row0;
+  a.tile_rows = r.tile_rows;
+  a.num_tiles = r.num_tiles;
+  a.status = r.status;
+  a.state = w.state;
+  a.stalled_block = stalled_block;
+  a.timeout_ns = timeout_ns;
+  cudaError_t e = launch_route(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
+  return MOE_OK;
+}
+
+moe_status enqueue_route(const Geometry& g, const void* x, const void* w_router, const float* router_bias,
+                         const void* w_shared_gate, const moe_route_out& r, const Workspace& w,
+                         int stalled_block, long long timeout_ns, cudaStream_t stream) {
+  cudaError_t e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
+                                       g.route_blocks * g.E, r.status, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
+  return enqueue_routing_only(g, router_bias, r, w, stalled_block, timeout_ns, stream);
+}
+
+moe_status route_common(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,
+                        const void* w_shared_gate, const moe_route_out* out, void* workspace, size_t ws_bytes,
+                        int stalled_block, long long timeout_ns, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const Geometry g = geometry(*shape);
+  if (!route_out_ok(out, g.shared)) return MOE_ERR_INVALID_ARG;
+  if (g.T == 0) return MOE_OK;
+  if (!x || !w_router || (g.shared && !w_shared_gate) || !workspace) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOE_ERR_INVALID_ARG;
+  const Workspace w = carve(g, workspace);
+  if (ws_bytes < w.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return enqueue_route(g, x, w_router, router_bias, w_shared_gate, *out, w, stalled_block, timeout_ns,
+                       static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace bgmoe
+
+using namespace bgmoe;
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+moe_status moe_workspace_bytes(const moe_shape* shape, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  *bytes = carve(geometry(*shape), nullptr).bytes;
+  return MOE_OK;
+}
+
+moe_status moe_max_tiles(const moe_shape* shape, int32_t* max_tiles) {
+  if (!max_tiles) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  *max_tiles = geometry(*shape).max_tiles;
+  return MOE_OK;
+}
+
+moe_status moe_route_blocks(const moe_shape* shape, int32_t* blocks) {
+  if (!blocks) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  *blocks = geometry(*shape).route_blocks;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,
+                     const void* w_shared_gate, const moe_route_out* out, void* workspace, size_t ws_bytes,
+                     void* stream) {
+  return route_common(shape, x, w_router, router_bias, w_shared_gate, out, workspace, ws_bytes, -1,
+                      kDefaultTimeoutNs, stream);
+}
+
+moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const void* w_router,
+                                const float* router_bias, const void* w_shared_gate, const moe_route_out* out,
+                                void* workspace, size_t ws_bytes, int32_t stalled_block, int64_t timeout_ns,
+                                void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const Geometry g = geometry(*shape);
+  if (stalled_block < 0 || stalled_block >= g.route_blocks || timeout_ns <= 0 || timeout_ns > kDefaultTimeoutNs)
+    return MOE_ERR_INVALID_ARG;
+  return route_common(shape, x, w_router, router_bias, w_shared_gate, out, workspace, ws_bytes, stalled_block,
+                      timeout_ns, stream);
+}
+
+moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* w_router,
+                             const float* router_bias, const moe_experts* experts, const moe_experts* shared,
+                             const void* w_shared_gate, float* y, const moe_route_out* route_out, void* workspace,
+                             size_t ws_bytes, void* const* events, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const Geometry g = geometry(*shape);
+  if (route_out && !route_out_ok(route_out, g.shared)) return MOE_ERR_INVALID_ARG;
+  if (g.T == 0) return MOE_OK;
+  if (!x || !w_router || !y || !experts || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!experts->gate_up.codes || !experts->gate_up.scales || !experts->gate_up.biases || !experts->down.codes ||
+      !experts->down.scales || !experts->down.biases)
+    return MOE_ERR_INVALID_ARG;
+  if (g.shared && (!shared || !w_shared_gate || !shared->gate_up.codes || !shared->gate_up.scales ||
+                   !shared->gate_up.biases || !shared->down.codes || !shared->down.scales || !shared->down.biases))
+    return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MOE_ERR_INVALID_ARG;
+  const Workspace w = carve(g, workspace);
+  if (ws_bytes < w.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const moe_route_out r = route_out ? *route_out : ws_route_out(w);
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  cudaError_t e = mark(0);
+  if (e != cudaSuccess) return cuda_fail(e, "event record");
+
+  // Router logits, then the routing pipeline (two launches).
+  e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
+                           g.route_blocks * g.E, r.status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
+  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
+  st = enqueue_routing_only(g, router_bias, r, w, -1, kDefaultTimeoutNs, s);
+  if (st != MOE_OK) return st;
+  if ((e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
+
+  TileArgs t{r.tile_expert, r.tile_row0, r.tile_rows, r.num_tiles, r.sorted, r.status};
+  ExpertArgs gu{experts->gate_up.codes, experts->gate_up.scales, experts->gate_up.biases,
+                g.shared ? shared->gate_up.codes : nullptr, g.shared ? shared->gate_up.scales : nullptr,
+                g.shared ? shared->gate_up.biases : nullptr};
+  ExpertArgs dn{experts->down.codes, experts->down.scales, experts->down.biases,
+                g.shared ? shared->down.codes : nullptr, g.shared ? shared->down.scales : nullptr,
+                g.shared ? shared->down.biases : nullptr};
+  e = launch_gemv_gate_up(g, static_cast<const uint16_t*>(x), gu, t, w.h, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
+  if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
+  e = launch_gemv_down(g, w.h, dn, t, w.o, s);
+  if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
+  if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event record");
+  e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if ((e = mark(5)) != cudaSuccess) return cuda_fail(e, "event record");
+  return MOE_OK;
+}
+
+moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,
+                       const moe_experts* experts, const moe_experts* shared, const void* w_shared_gate, float* y,
+                       const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* stream) {
+  return moe_forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out,
+                           workspace, ws_bytes, nullptr, stream);
+}
+
+moe_status moe_status_read(const int32_t* device_status, void* stream, int32_t* host_status) {
+  if (!device_status || !host_status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host_status, device_status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "status copy");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "status sync");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Host-side launchers of the layer's kernels (one per .cu file).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace bgmoe {
+
+struct RouteArgs {
+  const float* logits;  // [T][E+1], column E = shared gate logit
+  const float* bias;    // [E] or null
+  int T, E, K, BM, shared, P, tpb;
+  int32_t* ids;
+  float* weights;
+  float* gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted;
+  int32_t* inv;
+  int32_t* tile_expert;
+  int32_t* tile_row0;
+  int32_t* tile_rows;
+  int32_t* num_tiles;
+  int32_t* status;
+  unsigned long long* state;  // [P][E] look-back words, zeroed by the router kernel
+  int stalled_block;          // test hook: this block never publishes (-1: none)
+  long long timeout_ns;       // limit of every device-side wait
+};
+
+struct ExpertArgs {
+  const uint32_t* codes;   // routed experts
+  const uint16_t* scales;
+  const uint16_t* biases;
+  const uint32_t* s_codes; // shared expert (or null)
+  const uint16_t* s_scales;
+  const uint16_t* s_biases;
+};
+
+struct TileArgs {
+  const int32_t* tile_expert;
+  const int32_t* tile_row0;
+  const int32_t* tile_rows;
+  const int32_t* num_tiles;
+  const int32_t* sorted;
+  const int32_t* status;
+};
+
+cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* wr, const void* wsg,
+                                 float* logits, unsigned long long* state, int n_state,
+                                 int32_t* status, cudaStream_t stream);
+
+size_t route_smem_bytes(const Geometry& g);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
+
+cudaError_t launch_gemv_gate_up(const Geometry& g, const uint16_t* x, const ExpertArgs& w,
+                                const TileArgs& t, __half* h, cudaStream_t stream);
+cudaError_t launch_gemv_down(const Geometry& g, const __half* h, const ExpertArgs& w,
+                             const TileArgs& t, __half* o, cudaStream_t stream);
+
+cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,
+                           const float* gate, const int32_t* status, float* y, cudaStream_t stream);
+
+}  // namespace bgmoe

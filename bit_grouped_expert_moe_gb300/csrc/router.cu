@@ -1,0 +1,109 @@
+// Router scores: l[t, e] = x[t, :] . W_r[e, :] for the E routed experts and,
+// in column E, the shared-expert gate logit x[t, :] . w_sg.
+// [dothoosh.com "Perplexity Lily: 1.35x faster decode for Qwen3.6 on Apple
+// silicon", "Model specification": the router scores 256 experts per token.]
+//
+// One warp owns one weight row (expert e, or the gate row); a block covers
+// kRouterTokens tokens whose bf16 rows sit in shared memory, so each 16-byte
+// weight load feeds 8 x kRouterTokens FMAs. The block also clears the routing
+// kernel's look-back words and the call's status word (the routing kernel runs
+// after this one on the same stream).
+#include "common.cuh"
+
+namespace bgmoe {
+
+constexpr int kRouterWarps = 8;
+constexpr int kRouterTokens = 8;
+
+__global__ void __launch_bounds__(kRouterWarps * 32)
+router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
+                     const uint16_t* __restrict__ wsg, float* __restrict__ logits, int T, int H,
+                     int E, int ld, unsigned long long* __restrict__ state, int n_state,
+                     int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) uint16_t xs[];  // [kRouterTokens][H]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.y * kRouterTokens;
+  const int nt = min(kRouterTokens, T - t0);
+
+  // Clear the look-back words and the status word for this call.
+  {
+    const int nblocks = gridDim.x * gridDim.y;
+    const int b = blockIdx.y * gridDim.x + blockIdx.x;
+    for (int i = b * blockDim.x + threadIdx.x; i < n_state; i += nblocks * blockDim.x) state[i] = 0ull;
+    if (b == 0 && threadIdx.x == 0) *status = 0;
+  }
+
+  // Stage the block's token rows (16-byte copies; H is a multiple of 64).
+  const int vec_per_row = H / 8;
+  for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
+    const int j = i / vec_per_row, v = i - j * vec_per_row;
+    reinterpret_cast<uint4*>(xs)[j * vec_per_row + v] =
+        reinterpret_cast<const uint4*>(x + (size_t)(t0 + j) * H)[v];
+  }
+  __syncthreads();
+
+  const int e = blockIdx.x * kRouterWarps + warp;
+  const bool has_gate = wsg != nullptr;
+  if (e > E || (e == E && !has_gate)) return;
+  const uint16_t* row = (e < E) ? wr + (size_t)e * H : wsg;
+
+  float acc[kRouterTokens];
+#pragma unroll
+  for (int j = 0; j < kRouterTokens; ++j) acc[j] = 0.f;
+
+  for (int v = lane; v < vec_per_row; v += 32) {
+    const uint4 w4 = ldg_nc_v4(row + (size_t)v * 8);
+    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
+    float wf[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      wf[2 * m] = bf16_bits_to_f32(wv[m] & 0xFFFFu);
+      wf[2 * m + 1] = bf16_bits_to_f32(wv[m] >> 16);
+    }
+#pragma unroll
+    for (int j = 0; j < kRouterTokens; ++j) {
+      if (j < nt) {
+        const uint4 x4 = reinterpret_cast<const uint4*>(xs)[j * vec_per_row + v];
+        const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
+        float a = acc[j];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          a = fmaf(wf[2 * m], bf16_bits_to_f32(xv[m] & 0xFFFFu), a);
+          a = fmaf(wf[2 * m + 1], bf16_bits_to_f32(xv[m] >> 16), a);
+        }
+        acc[j] = a;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRouterTokens; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+  }
+  if (lane < nt) {
+    float mine = acc[0];
+#pragma unroll
+    for (int j = 1; j < kRouterTokens; ++j)
+      if (lane == j) mine = acc[j];
+    logits[(size_t)(t0 + lane) * ld + e] = mine;
+  }
+}
+
+cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* wr, const void* wsg,
+                                 float* logits, unsigned long long* state, int n_state,
+                                 int32_t* status, cudaStream_t stream) {
+  const int rows = g.E + (wsg ? 1 : 0);
+  dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (g.T + kRouterTokens - 1) / kRouterTokens);
+  const size_t smem = (size_t)kRouterTokens * g.H * sizeof(uint16_t);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  router_logits_kernel<<<grid, kRouterWarps * 32, smem, stream>>>(
+      static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wr), static_cast<const uint16_t*>(wsg),
+      logits, g.T, g.H, g.E, g.E + 1, state, n_state, status);
+  return cudaGetLastError();
+}
+
+}  // namespace bgmoe

@@ -1,0 +1,215 @@
+/*
+ * bit_grouped_expert_moe_gb300 — C ABI of one Mixture-of-Experts layer with
+ * 4-bit group-64 affine expert weights, for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (Qwen3.6-35B-A3B shape, as described on the pages about
+ * Perplexity's Lily engine):
+ *   1. router:  l[t,e] = x[t,:] . W_r[e,:] (+ b[e]); the top_k experts by l
+ *               (ties: lower index first); weights w[t,k] = softmax over the
+ *               selected logits (= softmax over all E renormalised over the
+ *               top_k); shared gate g[t] = sigmoid(x[t,:] . w_sg).
+ *               [dothoosh.com "Perplexity Lily: 1.35x faster decode for
+ *               Qwen3.6 on Apple silicon", section "Model specification":
+ *               the router scores 256 experts and picks 8, plus one shared
+ *               expert that processes every token.]
+ *   2. routing: histogram, prefix scan, scatter and block map, all on the GPU
+ *               with no host synchronisation. [same page, "Prefill
+ *               optimisations", GPU-resident routing item.]
+ *   3. experts: SwiGLU experts h = silu(x W_gate^T) * (x W_up^T),
+ *               o = h W_down^T, whose weights are 4-bit codes with one bf16
+ *               scale and one bf16 bias per 64 weights, dequantised inside the
+ *               grouped GEMM with FP32 accumulation. [same page, "Prefill
+ *               optimisations", fused-dequantisation item.]
+ *   4. combine: y[t] = sum_k w[t,k] o[t,k] + g[t] o_shared[t].
+ *
+ * Data formats (shared by every entry point):
+ *   bf16 values are passed as their 16-bit patterns (uint16_t / void*).
+ *   A packed matrix W[N][K] (output-major, K contiguous) is
+ *     codes  uint32_t [N][K/8]   code k in bits 4*(k%8)..+3 of word k/8;
+ *     scales uint16_t [N][K/64]  bf16 scale of weights k = 64g .. 64g+63;
+ *     biases uint16_t [N][K/64]  bf16 bias of the same group;
+ *   and W[n][k] = scale[n][k/64] * code(n,k) + bias[n][k/64], code in 0..15.
+ *   Expert e's matrices start at e * (matrix size) in each array.
+ *
+ * Ownership and synchronisation: every pointer is a DEVICE pointer owned by
+ * the caller (except shape/struct pointers, which are host pointers read
+ * during the call). The library allocates no memory, keeps no state between
+ * calls and never synchronises the host, except moe_status_read. All work is
+ * enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream);
+ * buffers must stay valid until the stream passes the call.
+ *
+ * Errors: argument, shape and workspace errors, and launch errors, are
+ * returned synchronously. A device-side failure (a bounded wait that expired)
+ * is written to the int32 status word of the call (route_out->status, or the
+ * workspace's own status word for moe_forward without route_out) and the
+ * kernels after it do no work; read it with moe_status_read.
+ *
+ * Numerics: logits, softmax, gate and y are fp32. Routed and shared expert
+ * intermediates h and o are stored as fp16 (|value| < 65504 is required);
+ * the tensor-core path feeds the MMA fp16 operands (dequantised weights and
+ * x converted from bf16, which is exact for |x| >= 2^-14) with fp32
+ * accumulation. Results are bit-identical from run to run (no float atomics).
+ */
+#ifndef BGMOE_MOE_H
+#define BGMOE_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, negative size, ... */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* shape outside the supported set below */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_bytes() */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5       /* a bounded device-side wait expired */
+} moe_status;
+
+/* Shape of one call. Supported: T >= 0; H and I multiples of 64 with
+ * 64 <= H <= 8192 and 64 <= I <= 4096; I_shared == I (one shared expert of
+ * the same shape) or 0 (none); 1 <= top_k <= 8; top_k <= E <= 256;
+ * group_size == 64; block_m in {16, 32, 64, 128}. */
+typedef struct moe_shape {
+  int32_t T;          /* tokens in this call */
+  int32_t H;          /* hidden size */
+  int32_t I;          /* routed expert intermediate size */
+  int32_t I_shared;   /* shared expert intermediate size (I or 0) */
+  int32_t E;          /* routed experts */
+  int32_t top_k;      /* experts per token */
+  int32_t group_size; /* weights per scale/bias pair (64) */
+  int32_t block_m;    /* rows per block-map tile */
+} moe_shape;
+
+/* One packed 4-bit matrix stack (device pointers; layout in the file header). */
+typedef struct moe_qmat {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* biases;
+} moe_qmat;
+
+/* The expert weights of a layer: gate_up is [n][2I][H] (gate rows 0..I-1,
+ * up rows I..2I-1), down is [n][H][I]; n = E for the routed experts, 1 for
+ * the shared expert. */
+typedef struct moe_experts {
+  moe_qmat gate_up;
+  moe_qmat down;
+} moe_experts;
+
+/* Routing outputs (device pointers, caller-owned; A = T * top_k):
+ *   ids        int32 [T][top_k]  chosen experts, best first
+ *   weights    fp32  [T][top_k]  renormalised softmax weights
+ *   gate       fp32  [T]         shared-expert gate (may be NULL if I_shared == 0)
+ *   counts     int32 [E+1]       assignments per expert; counts[E] = T if a
+ *                                shared expert exists, else 0
+ *   offsets    int32 [E+2]       exclusive prefix sum of counts
+ *   sorted     int32 [A]         assignment a = t*top_k + k at each position;
+ *                                positions of one expert follow increasing a
+ *   inv        int32 [A]         position of each assignment
+ *   tile_expert, tile_row0, tile_rows  int32 [moe_max_tiles()]  block map:
+ *                                for e = 0..E in order, ceil(counts[e]/block_m)
+ *                                tiles of <= block_m consecutive positions;
+ *                                rows A + t belong to the shared expert (token t)
+ *   num_tiles  int32 [1]         number of valid block-map entries
+ *   status     int32 [1]         MOE_OK, or MOE_ERR_DEVICE_TIMEOUT
+ * [dothoosh.com "Perplexity Lily...", "Prefill optimisations": routing
+ * histogram, prefix scan, scatter and block map kept on the GPU.] */
+typedef struct moe_route_out {
+  int32_t* ids;
+  float* weights;
+  float* gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted;
+  int32_t* inv;
+  int32_t* tile_expert;
+  int32_t* tile_row0;
+  int32_t* tile_rows;
+  int32_t* num_tiles;
+  int32_t* status;
+} moe_route_out;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION). */
+int32_t moe_abi_version(void);
+
+/* Text of a status code (static storage; never NULL). */
+const char* moe_status_string(moe_status s);
+
+/* Detail of the last MOE_ERR_CUDA returned on the calling thread (the CUDA
+ * call and its error string); "" if none. Thread-local storage. */
+const char* moe_last_error_detail(void);
+
+/* Workspace bytes moe_route / moe_forward need for `shape` (a pure function
+ * of the shape; no CUDA call). Errors: INVALID_ARG, UNSUPPORTED_SHAPE. */
+moe_status moe_workspace_bytes(const moe_shape* shape, size_t* bytes);
+
+/* Upper bound on the block-map length for `shape`:
+ * ceil(A/block_m) + min(E, A) + ceil(T/block_m) (the last term only with a
+ * shared expert). The tile_* arrays must hold this many entries. */
+moe_status moe_max_tiles(const moe_shape* shape, int32_t* max_tiles);
+
+/* Steps 1-2: router, top-k, weights, gate and the routing tables.
+ *   x              bf16 [T][H]
+ *   w_router       bf16 [E][H]
+ *   router_bias    fp32 [E] or NULL (added to the logits before selection)
+ *   w_shared_gate  bf16 [H]; required iff I_shared > 0
+ *   out            every field required, except gate when I_shared == 0
+ *   workspace      device buffer of >= moe_workspace_bytes() bytes, 256-byte
+ *                  aligned; its contents need no initialisation */
+moe_status moe_route(const moe_shape* shape, const void* x, const void* w_router,
+                     const float* router_bias, const void* w_shared_gate,
+                     const moe_route_out* out, void* workspace, size_t ws_bytes,
+                     void* stream);
+
+/* Steps 1-4: the whole layer, y fp32 [T][H].
+ *   experts        routed experts (n = E)
+ *   shared         the shared expert (n = 1); required iff I_shared > 0
+ *   route_out      NULL, or routing outputs to keep (as moe_route)
+ * Other arguments as moe_route. T == 0 is a no-op. */
+moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_router,
+                       const float* router_bias, const moe_experts* experts,
+                       const moe_experts* shared, const void* w_shared_gate,
+                       float* y, const moe_route_out* route_out,
+                       void* workspace, size_t ws_bytes, void* stream);
+
+/* moe_forward that also records caller-owned CUDA events (cudaEvent_t,
+ * created by the caller) on `stream` around its kernels: events[0] before
+ * the router kernel, [1] after it, [2] after the routing kernel, [3] after
+ * the expert gate/up kernel, [4] after the expert down kernel, [5] after the
+ * combine kernel. events == NULL behaves exactly as moe_forward. For
+ * measuring per-kernel time on the launching stream. */
+moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* w_router,
+                             const float* router_bias, const moe_experts* experts,
+                             const moe_experts* shared, const void* w_shared_gate,
+                             float* y, const moe_route_out* route_out,
+                             void* workspace, size_t ws_bytes, void* const* events,
+                             void* stream);
+
+/* Reads a device status word written by a previous call: synchronises
+ * `stream`, copies the word to *host_status. */
+moe_status moe_status_read(const int32_t* device_status, void* stream, int32_t* host_status);
+
+/* Test hook: moe_route with routing block `stalled_block` never publishing
+ * its histogram, so that the blocks after it wait out `timeout_ns` and the
+ * call ends with MOE_ERR_DEVICE_TIMEOUT in out->status (no hang, no trap).
+ * Requires T * top_k large enough for more than one routing block
+ * (moe_route_blocks() > stalled_block). */
+moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const void* w_router,
+                                const float* router_bias, const void* w_shared_gate,
+                                const moe_route_out* out, void* workspace, size_t ws_bytes,
+                                int32_t stalled_block, int64_t timeout_ns, void* stream);
+
+/* Number of thread blocks the routing kernel uses for `shape` on the current
+ * device (the co-resident grid of the single-launch routing pipeline). */
+moe_status moe_route_blocks(const moe_shape* shape, int32_t* blocks);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BGMOE_MOE_H */

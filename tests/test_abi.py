@@ -1,0 +1,110 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/moe.h declares, and rejects bad arguments on the host before any
+CUDA work (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(moelib):
+    syms = declared_symbols()
+    assert len(syms) >= 10
+    L = moelib.lib()
+    for s in syms:
+        assert hasattr(L, s), s
+
+
+def test_abi_version_and_strings(moelib):
+    L = moelib.lib()
+    assert L.moe_abi_version() == 1
+    for s in range(6):
+        assert moelib.status_string(s)
+    assert moelib.status_string(99) == "unknown status"
+
+
+def test_workspace_bytes_grows_with_tokens(moelib):
+    sizes = [moelib.workspace_bytes(moelib.make_shape(T, 2048, 512)) for T in (1, 4, 512, 4096)]
+    assert all(b > a for a, b in zip(sizes, sizes[1:]))
+    assert sizes[-1] % 256 == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=100), 2), (dict(I=96), 2), (dict(top_k=9), 2), (dict(E=300), 2), (dict(block_m=48), 2),
+    (dict(group_size=32), 2), (dict(T=-1), 1), (dict(E=4, top_k=8), 2)])
+def test_shape_rejected(moelib, kw, code):
+    args = dict(T=4, H=512, I=128, E=256, top_k=8, shared=True, block_m=16, group_size=64)
+    args.update(kw)
+    sh = moelib.make_shape(**args)
+    n = ctypes.c_size_t()
+    assert moelib.lib().moe_workspace_bytes(ctypes.byref(sh), ctypes.byref(n)) == code
+
+
+def test_max_tiles_formula(moelib):
+    for T, bm in [(1, 16), (64, 16), (4096, 128), (37, 32)]:
+        sh = moelib.make_shape(T, 512, 128, block_m=bm)
+        A = T * 8
+        want = -(-A // bm) + min(256, A) + -(-T // bm)
+        assert moelib.max_tiles(sh) == want
+
+
+def _fake_route_out(moelib, shared=True):
+    vals = [0x10000 * (i + 1) for i in range(len(moelib.ROUTE_FIELDS))]
+    r = moelib.RouteOutC(*vals)
+    if not shared:
+        r.gate = None
+    return r
+
+
+def test_host_side_errors_before_any_cuda_call(moelib):
+    """Null pointers, short or misaligned workspaces and T == 0 are settled on
+    the host; the fake device addresses below are never dereferenced."""
+    L = moelib.lib()
+    sh = moelib.make_shape(64, 512, 128)
+    need = moelib.workspace_bytes(sh)
+    r = _fake_route_out(moelib)
+    x, w, g, ws = 0x100000, 0x200000, 0x300000, 0x400000
+    assert L.moe_route(ctypes.byref(sh), x, w, None, g, ctypes.byref(r), ws, need - 1, None) == 3
+    assert L.moe_route(ctypes.byref(sh), None, w, None, g, ctypes.byref(r), ws, need, None) == 1
+    assert L.moe_route(ctypes.byref(sh), x, w, None, None, ctypes.byref(r), ws, need, None) == 1
+    assert L.moe_route(ctypes.byref(sh), x, w, None, g, ctypes.byref(r), ws + 16, need, None) == 1
+    r2 = _fake_route_out(moelib)
+    r2.sorted = None
+    assert L.moe_route(ctypes.byref(sh), x, w, None, g, ctypes.byref(r2), ws, need, None) == 1
+    sh0 = moelib.make_shape(0, 512, 128)
+    assert L.moe_route(ctypes.byref(sh0), x, w, None, g, ctypes.byref(r), ws, 0, None) == 0
+    ex = moelib.ExpertsC(moelib.QMat(1 << 20, 2 << 20, 3 << 20), moelib.QMat(4 << 20, 5 << 20, 6 << 20))
+    assert L.moe_forward(ctypes.byref(sh), x, w, None, ctypes.byref(ex), None, g, 0x500000, None, ws, need,
+                         None) == 1  # shared expert missing
+    assert L.moe_forward(ctypes.byref(sh), x, w, None, ctypes.byref(ex), ctypes.byref(ex), g, 0x500000, None, ws,
+                         need - 256, None) == 3
+    assert L.moe_forward(ctypes.byref(sh0), x, w, None, ctypes.byref(ex), ctypes.byref(ex), g, 0x500000, None, ws,
+                         0, None) == 0
+    shn = moelib.make_shape(64, 512, 128, shared=False)
+    rn = _fake_route_out(moelib, shared=False)
+    assert L.moe_route(ctypes.byref(shn), x, w, None, None, ctypes.byref(rn), ws,
+                       moelib.workspace_bytes(shn) - 1, None) == 3
+
+
+def test_stall_hook_argument_checks(moelib):
+    L = moelib.lib()
+    sh = moelib.make_shape(64, 512, 128)
+    r = _fake_route_out(moelib)
+    nb = moelib.route_blocks(sh)
+    assert nb == 4
+    for blk, to in [(-1, 10**6), (nb, 10**6), (0, 0), (0, 10**10)]:
+        assert L.moe_test_route_stall(ctypes.byref(sh), 0x100000, 0x200000, None, 0x300000, ctypes.byref(r),
+                                      0x400000, 1 << 30, blk, to, None) == 1

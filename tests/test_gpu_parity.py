@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA library through its C ABI against the CPU oracle on
+the same seeded inputs, for every workload shape and the edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import parity
+from tests._util import bits16, bf16_from_f64, read_golden
+from tests.oracle_pins import check_routing_invariants
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_and_check(moelib, dev, spec, block_m=16, tokens=None, layer_idx=0):
+    L = parity.device_layer(spec, layer_idx, dev)
+    x = synth.activations(spec, device=dev)
+    y, ro = parity.gpu_forward(moelib, spec, L, x, block_m)
+    y_ref, ids_ref, w_ref, g_ref, logits = parity.oracle_forward(spec, L, x, tokens=tokens)
+    sel = np.arange(spec.T) if tokens is None else np.asarray(tokens)
+    K = spec.top_k
+    ids_gpu = ro["ids"][: spec.T * K].reshape(spec.T, K)
+    excl = parity.check_ids(ids_gpu[sel], ids_ref, logits, K)
+    ok = ~excl
+    assert np.allclose(ro["weights"][: spec.T * K].reshape(spec.T, K)[sel][ok], w_ref[ok], rtol=2e-6, atol=1e-7)
+    if spec.shared:
+        assert np.allclose(ro["gate"][: spec.T][sel], g_ref, rtol=2e-6, atol=1e-7)
+    parity.check_tables(ro, ids_gpu, spec, spec.T, block_m)
+    return parity.check_y(y[sel], y_ref, excl)
+
+
+def test_generator_is_device_independent(cuda_dev):
+    spec = synth.WORKLOADS["prefill-4096"]
+    xg = synth.activations(spec, T=64, device=cuda_dev).cpu()
+    xc = synth.activations(spec, T=64)
+    assert torch.equal(xg.view(torch.int16), xc.view(torch.int16))
+    gg, dg = synth.expert_weights(spec, [3, 256], 0, cuda_dev)
+    gc, dc = synth.expert_weights(spec, [3, 256], 0, "cpu")
+    for a, b in zip(gg + dg, gc + dc):
+        assert torch.equal(a.cpu().view(torch.int16) if a.dtype == torch.bfloat16 else a.cpu(),
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+def test_tiny_layer(moelib, cuda_dev):
+    rel, mx = _run_and_check(moelib, cuda_dev, synth.WORKLOADS["tiny"])
+    assert rel < 1e-3
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64, 128])
+def test_tiny_block_sizes(moelib, cuda_dev, block_m):
+    _run_and_check(moelib, cuda_dev, synth.WORKLOADS["tiny"], block_m=block_m)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 17, 37, 100])
+def test_ragged_token_counts(moelib, cuda_dev, T):
+    spec = synth.LayerSpec("ragged", T=T, H=512, I=128, seed=20260011)
+    _run_and_check(moelib, cuda_dev, spec)
+
+
+@pytest.mark.parametrize("E,K,shared,H,I", [(64, 8, True, 256, 128), (16, 2, False, 128, 64),
+                                             (8, 1, True, 64, 64), (256, 8, False, 512, 192),
+                                             (32, 4, True, 384, 320)])
+def test_other_shapes(moelib, cuda_dev, E, K, shared, H, I):
+    spec = synth.LayerSpec("shape", T=45, H=H, I=I, E=E, top_k=K, shared=shared, seed=20260012)
+    _run_and_check(moelib, cuda_dev, spec, block_m=32)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_decode_full_size(moelib, cuda_dev, T):
+    spec = synth.WORKLOADS[f"decode-t{T}"]
+    _run_and_check(moelib, cuda_dev, spec)
+    _run_and_check(moelib, cuda_dev, spec, layer_idx=39)
+
+
+def test_prefill_zipf_512(moelib, cuda_dev):
+    spec = synth.WORKLOADS["prefill-zipf-512"]
+    _run_and_check(moelib, cuda_dev, spec, block_m=64)
+
+
+def test_prefill_4096(moelib, cuda_dev):
+    spec = synth.WORKLOADS["prefill-4096"]
+    _run_and_check(moelib, cuda_dev, spec, block_m=128)
+
+
+def test_long_skew_chunks(moelib, cuda_dev):
+    """16384 tokens in 2048-token calls reusing one workspace; every chunk is
+    checked on a token sample, the first one in full."""
+    spec = synth.WORKLOADS["long-skew-16384"]
+    L = parity.device_layer(spec, 0, cuda_dev)
+    C = spec.chunk
+    chunk_spec = synth.LayerSpec(spec.name, T=C, H=spec.H, I=spec.I, bias=spec.bias, hot_logit=spec.hot_logit,
+                                 seed=spec.seed)
+    shape = moelib.make_shape(C, spec.H, spec.I, block_m=128)
+    ws = moelib.alloc_workspace(shape, cuda_dev)
+    ro = moelib.alloc_route_out(shape, cuda_dev)
+    routed, shared = parity.experts_arg(L)
+    rng = np.random.default_rng(5)
+    hot_share = []
+    for c in range(spec.T // C):
+        x = synth.activations(spec, T=C, device=cuda_dev, start=c * C)
+        y = torch.empty(C, spec.H, dtype=torch.float32, device=cuda_dev)
+        moelib.forward(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro)
+        torch.cuda.synchronize()
+        assert moelib.status_read(ro["status"]) == 0
+        tokens = None if c == 0 else np.sort(rng.choice(C, 96, replace=False))
+        y_ref, ids_ref, w_ref, g_ref, logits = parity.oracle_forward(chunk_spec, L, x, tokens=tokens)
+        sel = np.arange(C) if tokens is None else tokens
+        ids_gpu = ro["ids"].cpu().numpy()[: C * 8].reshape(C, 8)
+        excl = parity.check_ids(ids_gpu[sel], ids_ref, logits, 8)
+        parity.check_y(y.cpu().numpy()[sel], y_ref, excl)
+        counts = ro["counts"].cpu().numpy()
+        b = L.bias.cpu().numpy()
+        hot_share.append(counts[:256][b > 0].sum() / (C * 8))
+        assert counts[:256][b < -1].sum() == 0
+    assert 0.17 < np.mean(hot_share) < 0.23
+
+
+def test_topk_ties_through_gpu(moelib, cuda_dev):
+    """The hand-ranked tie cases of tests/golden/topk_ties.txt through
+    moe_route (lowest index first among equal logits)."""
+    for (k,), logits, want in read_golden("topk_ties.txt"):
+        E = len(logits)
+        H = 64
+        x = np.zeros((1, H))
+        x[0, 0] = 1.0
+        wr = np.zeros((E, H))
+        wr[:, 0] = [float(v) for v in logits]
+        xt = torch.from_numpy(bf16_from_f64(x).view(np.int16)).view(torch.bfloat16).to(cuda_dev)
+        wt = torch.from_numpy(bf16_from_f64(wr).view(np.int16)).view(torch.bfloat16).to(cuda_dev)
+        shape = moelib.make_shape(1, H, 64, E=E, top_k=int(k), shared=False)
+        out = moelib.alloc_route_out(shape, cuda_dev)
+        ws = moelib.alloc_workspace(shape, cuda_dev)
+        moelib.route(shape, xt, wt, None, None, out, ws)
+        torch.cuda.synchronize()
+        assert out["ids"][: int(k)].tolist() == [int(v) for v in want]
+
+
+@pytest.mark.parametrize("T,bm", [(64, 16), (1000, 32), (4096, 128), (2048, 16)])
+def test_routing_tables_invariants_and_bitexact(moelib, cuda_dev, T, bm):
+    spec = synth.LayerSpec("route", T=T, H=256, I=64, seed=20260013)
+    wr, wsg = synth.router_weights(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    shape = moelib.make_shape(T, spec.H, spec.I, block_m=bm)
+    out = moelib.alloc_route_out(shape, cuda_dev)
+    ws = moelib.alloc_workspace(shape, cuda_dev)
+    moelib.route(shape, x, wr, None, wsg, out, ws)
+    torch.cuda.synchronize()
+    ro = {k: v.cpu().numpy() for k, v in out.items()}
+    assert ro["status"][0] == 0
+    ids = ro["ids"][: T * 8].reshape(T, 8)
+    tab = parity.check_tables(ro, ids, spec, T, bm)
+    check_routing_invariants(ids, 256, bm, tab)
+    ids_ref, w_ref, g_ref, logits = oracle.route(bits16(x), bits16(wr), None, bits16(wsg), 8)
+    parity.check_ids(ids, ids_ref, logits, 8)
+
+
+def test_deterministic(moelib, cuda_dev):
+    spec = synth.WORKLOADS["prefill-zipf-512"]
+    L = parity.device_layer(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    y1, r1 = parity.gpu_forward(moelib, spec, L, x, 64)
+    y2, r2 = parity.gpu_forward(moelib, spec, L, x, 64)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    for k in r1:
+        assert np.array_equal(r1[k], r2[k]), k
+
+
+def test_zero_tokens_is_noop(moelib, cuda_dev):
+    spec = synth.LayerSpec("z", T=0, H=512, I=128)
+    shape = moelib.make_shape(0, 512, 128)
+    L = synth.layer(synth.LayerSpec("z", T=1, H=512, I=128, E=8), 0, cuda_dev)
+    y = torch.full((1, 512), 7.0, device=cuda_dev)
+    routed, shared = parity.experts_arg(L)
+    ws = torch.empty(256, dtype=torch.uint8, device=cuda_dev)
+    x = torch.zeros(1, 512, dtype=torch.bfloat16, device=cuda_dev)
+    moelib.forward(shape, x, L.wr, None, routed, shared, L.wsg, y, ws)
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+def test_device_timeout_is_reported_not_hung(moelib, cuda_dev):
+    """A routing block that never publishes its histogram makes the others
+    wait out a short limit and report MOE_ERR_DEVICE_TIMEOUT; the context stays
+    usable and the next normal call succeeds."""
+    spec = synth.LayerSpec("stall", T=64, H=256, I=64, seed=20260014)
+    wr, wsg = synth.router_weights(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    shape = moelib.make_shape(64, spec.H, spec.I)
+    assert moelib.route_blocks(shape) >= 2
+    out = moelib.alloc_route_out(shape, cuda_dev)
+    ws = moelib.alloc_workspace(shape, cuda_dev)
+    moelib.test_route_stall(shape, x, wr, None, wsg, out, ws, stalled_block=0, timeout_ns=20_000_000)
+    assert moelib.status_read(out["status"]) == moelib.MOE_ERR_DEVICE_TIMEOUT
+    moelib.route(shape, x, wr, None, wsg, out, ws)
+    assert moelib.status_read(out["status"]) == 0
+    ids = out["ids"].cpu().numpy()[: 64 * 8].reshape(64, 8)
+    ids_ref, *_ , logits = oracle.route(bits16(x), bits16(wr), None, bits16(wsg), 8)
+    parity.check_ids(ids, ids_ref, logits, 8)
