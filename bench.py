@@ -156,7 +156,7 @@ class Workload:
                            route_out=self.route[li])
         else:
             self.m.forward_timed(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg, self.y[li, c], self.ws,
-                                 events, route_out=self.route[li])
+                                 events=events, route_out=self.route[li])
 
     def step(self):
         for c in range(self.calls):

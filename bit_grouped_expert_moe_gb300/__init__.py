@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libbgmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE = 0, 1, 2
 MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = 3, 4, 5
+PATH_AUTO, PATH_GEMV, PATH_TENSOR_CORE = 0, 1, 2
 
 P = ctypes.c_void_p
 
@@ -73,7 +74,7 @@ def lib() -> ctypes.CDLL:
         L.moe_forward.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                   ctypes.POINTER(RouteOutC), P, sz, P]
         L.moe_forward_timed.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
-                                        ctypes.POINTER(RouteOutC), P, sz, ctypes.POINTER(P), P]
+                                        ctypes.POINTER(RouteOutC), P, sz, ctypes.POINTER(P), i32, P]
         L.moe_status_read.argtypes = [P, P, ctypes.POINTER(i32)]
         L.moe_test_route_stall.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P, sz, i32, ctypes.c_int64, P]
         for f in ("moe_workspace_bytes", "moe_max_tiles", "moe_route_blocks", "moe_route", "moe_forward",
@@ -176,19 +177,20 @@ def forward(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, 
                              workspace.numel() * workspace.element_size(), _stream(stream)), "moe_forward")
 
 
-def forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, workspace, events,
-                  route_out=None, stream=None):
-    """forward() that records six caller-created CUDA events (raw cudaEvent_t
-    handles, e.g. torch.cuda.Event(enable_timing=True).cuda_event) around its
-    kernels."""
+def forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, workspace, events=None,
+                  route_out=None, path=PATH_AUTO, stream=None):
+    """forward() with a chosen expert path (PATH_AUTO, PATH_GEMV,
+    PATH_TENSOR_CORE) that records six caller-created CUDA events (raw
+    cudaEvent_t handles, e.g. torch.cuda.Event(enable_timing=True).cuda_event
+    after one record()) around its kernels when `events` is given."""
     ec = _experts_c(experts)
     sc = _experts_c(shared)
     r = _route_c(route_out) if route_out is not None else None
-    ev = (P * 6)(*events)
+    ev = (P * 6)(*events) if events is not None else None
     _check(lib().moe_forward_timed(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(router_bias), ctypes.byref(ec),
                                    ctypes.byref(sc) if sc is not None else None, _ptr(w_shared_gate), _ptr(y),
                                    ctypes.byref(r) if r is not None else None, _ptr(workspace),
-                                   workspace.numel() * workspace.element_size(), ev, _stream(stream)),
+                                   workspace.numel() * workspace.element_size(), ev, int(path), _stream(stream)),
            "moe_forward_timed")
 
 

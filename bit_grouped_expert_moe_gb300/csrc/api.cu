@@ -13,6 +13,7 @@ constexpr long long kDefaultTimeoutNs = 1000000000ll;  // 1 s per device-side wa
 constexpr int kMaxRouteBlocks = 128;
 constexpr int kMinTokensPerRouteBlock = 16;
 constexpr int kMaxTokens = 1 << 18;
+constexpr int kTensorCoreMinTokens = 64;
 
 thread_local char g_detail[256] = "";
 
@@ -167,7 +168,7 @@ moe_status enqueue_route(const Geometry& g, const void* x, const void* w_router,
                          const void* w_shared_gate, const moe_route_out& r, const Workspace& w,
                          int stalled_block, long long timeout_ns, cudaStream_t stream) {
   cudaError_t e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
-                                       g.route_blocks * g.E, r.status, stream);
+                                       g.route_blocks * g.E, r.status, nullptr, stream);
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   return enqueue_routing_only(g, router_bias, r, w, stalled_block, timeout_ns, stream);
 }
@@ -258,8 +259,9 @@ moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const voi
 moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* w_router,
                              const float* router_bias, const moe_experts* experts, const moe_experts* shared,
                              const void* w_shared_gate, float* y, const moe_route_out* route_out, void* workspace,
-                             size_t ws_bytes, void* const* events, void* stream) {
+                             size_t ws_bytes, void* const* events, int32_t expert_path, void* stream) {
   moe_status st = check_shape(shape);
+  if (expert_path < MOE_PATH_AUTO || expert_path > MOE_PATH_TENSOR_CORE) return MOE_ERR_INVALID_ARG;
   if (st != MOE_OK) return st;
   const Geometry g = geometry(*shape);
   if (route_out && !route_out_ok(route_out, g.shared)) return MOE_ERR_INVALID_ARG;
@@ -282,9 +284,15 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
 
+  // Expert path: tensor cores once the tile rows are many enough to feed
+  // them, the bandwidth-bound GEMV for decode-sized calls.
+  const bool tc_ok = tc_path_supported(g);
+  if (expert_path == MOE_PATH_TENSOR_CORE && !tc_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const bool tc = expert_path == MOE_PATH_TENSOR_CORE || (expert_path == MOE_PATH_AUTO && g.T >= kTensorCoreMinTokens && tc_ok);
+
   // Router logits, then the routing pipeline (two launches).
   e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
-                           g.route_blocks * g.E, r.status, s);
+                           g.route_blocks * g.E, r.status, tc ? w.x16 : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   st = enqueue_routing_only(g, router_bias, r, w, -1, kDefaultTimeoutNs, s);
@@ -298,10 +306,11 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
   ExpertArgs dn{experts->down.codes, experts->down.scales, experts->down.biases,
                 g.shared ? shared->down.codes : nullptr, g.shared ? shared->down.scales : nullptr,
                 g.shared ? shared->down.biases : nullptr};
-  e = launch_gemv_gate_up(g, static_cast<const uint16_t*>(x), gu, t, w.h, s);
+  e = tc ? launch_gate_up_tc(g, w.x16, gu, t, w.h, r.status, kDefaultTimeoutNs, s)
+         : launch_gemv_gate_up(g, static_cast<const uint16_t*>(x), gu, t, w.h, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = launch_gemv_down(g, w.h, dn, t, w.o, s);
+  e = tc ? launch_down_tc(g, w.h, dn, t, w.o, r.status, kDefaultTimeoutNs, s) : launch_gemv_down(g, w.h, dn, t, w.o, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
   if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event record");
   e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, s);
@@ -314,7 +323,7 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_rout
                        const moe_experts* experts, const moe_experts* shared, const void* w_shared_gate, float* y,
                        const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* stream) {
   return moe_forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out,
-                           workspace, ws_bytes, nullptr, stream);
+                           workspace, ws_bytes, nullptr, MOE_PATH_AUTO, stream);
 }
 
 moe_status moe_status_read(const int32_t* device_status, void* stream, int32_t* host_status) {

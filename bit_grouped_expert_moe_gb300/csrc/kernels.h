@@ -49,7 +49,7 @@ struct TileArgs {
 
 cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* wr, const void* wsg,
                                  float* logits, unsigned long long* state, int n_state,
-                                 int32_t* status, cudaStream_t stream);
+                                 int32_t* status, uint16_t* x16, cudaStream_t stream);
 
 size_t route_smem_bytes(const Geometry& g);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
@@ -58,6 +58,13 @@ cudaError_t launch_gemv_gate_up(const Geometry& g, const uint16_t* x, const Expe
                                 const TileArgs& t, __half* h, cudaStream_t stream);
 cudaError_t launch_gemv_down(const Geometry& g, const __half* h, const ExpertArgs& w,
                              const TileArgs& t, __half* o, cudaStream_t stream);
+
+// Tensor-core grouped GEMMs (gemm_tc.cu).
+bool tc_path_supported(const Geometry& g);
+cudaError_t launch_gate_up_tc(const Geometry& g, const uint16_t* x16, const ExpertArgs& w, const TileArgs& t,
+                              __half* h, int32_t* status, long long timeout_ns, cudaStream_t stream);
+cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs& w, const TileArgs& t, __half* o,
+                           int32_t* status, long long timeout_ns, cudaStream_t stream);
 
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,
                            const float* gate, const int32_t* status, float* y, cudaStream_t stream);

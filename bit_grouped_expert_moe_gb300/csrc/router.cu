@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
                      const uint16_t* __restrict__ wsg, float* __restrict__ logits, int T, int H,
                      int E, int ld, unsigned long long* __restrict__ state, int n_state,
-                     int32_t* __restrict__ status) {
+                     int32_t* __restrict__ status, uint16_t* __restrict__ x16) {
   extern __shared__ __align__(16) uint16_t xs[];  // [kRouterTokens][H]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.y * kRouterTokens;
@@ -41,6 +41,18 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
         reinterpret_cast<const uint4*>(x + (size_t)(t0 + j) * H)[v];
   }
   __syncthreads();
+
+  // The tensor-core expert path reads x as fp16 (exact for bf16 values of
+  // magnitude >= 2^-14), K-permuted within groups of 8 as 0,4,1,5,2,6,3,7 to
+  // match the order in which the 4-bit codes unpack.
+  if (x16 != nullptr && blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < nt * H; i += blockDim.x) {
+      const int j = i / H, k = i - j * H;
+      const int r = k & 7;
+      const int pk = (k & ~7) | (r < 4 ? 2 * r : 2 * (r - 4) + 1);
+      x16[(size_t)(t0 + j) * H + pk] = __half_as_ushort(__float2half_rn(bf16_bits_to_f32(xs[j * H + k])));
+    }
+  }
 
   const int e = blockIdx.x * kRouterWarps + warp;
   const bool has_gate = wsg != nullptr;
@@ -91,7 +103,7 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
 
 cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* wr, const void* wsg,
                                  float* logits, unsigned long long* state, int n_state,
-                                 int32_t* status, cudaStream_t stream) {
+                                 int32_t* status, uint16_t* x16, cudaStream_t stream) {
   const int rows = g.E + (wsg ? 1 : 0);
   dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (g.T + kRouterTokens - 1) / kRouterTokens);
   const size_t smem = (size_t)kRouterTokens * g.H * sizeof(uint16_t);
@@ -102,7 +114,7 @@ cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* w
   }
   router_logits_kernel<<<grid, kRouterWarps * 32, smem, stream>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wr), static_cast<const uint16_t*>(wsg),
-      logits, g.T, g.H, g.E, g.E + 1, state, n_state, status);
+      logits, g.T, g.H, g.E, g.E + 1, state, n_state, status, x16);
   return cudaGetLastError();
 }
 

@@ -177,18 +177,27 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_rout
                        float* y, const moe_route_out* route_out,
                        void* workspace, size_t ws_bytes, void* stream);
 
-/* moe_forward that also records caller-owned CUDA events (cudaEvent_t,
- * created by the caller) on `stream` around its kernels: events[0] before
- * the router kernel, [1] after it, [2] after the routing kernel, [3] after
- * the expert gate/up kernel, [4] after the expert down kernel, [5] after the
- * combine kernel. events == NULL behaves exactly as moe_forward. For
- * measuring per-kernel time on the launching stream. */
+/* Expert-GEMM implementations selectable through moe_forward_timed. */
+typedef enum moe_expert_path {
+  MOE_PATH_AUTO = 0,        /* tensor cores for T >= 64 when the shape allows, else GEMV */
+  MOE_PATH_GEMV = 1,        /* bandwidth-bound grouped GEMV (CUDA cores), any shape */
+  MOE_PATH_TENSOR_CORE = 2  /* tcgen05 grouped GEMM; needs H % 512 == 0, I % 128 == 0 and
+                               (I/64) * block_m * 128 <= 131072 (else UNSUPPORTED_SHAPE) */
+} moe_expert_path;
+
+/* moe_forward with a chosen expert path that also records caller-owned CUDA
+ * events (cudaEvent_t created by the caller; events may be NULL) on `stream`
+ * around its kernels: events[0] before the router kernel, [1] after it, [2]
+ * after the routing kernel, [3] after the expert gate/up kernel, [4] after
+ * the expert down kernel, [5] after the combine kernel. With events == NULL
+ * and MOE_PATH_AUTO it is exactly moe_forward. For per-kernel timing on the
+ * launching stream and for comparing the two expert paths. */
 moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* w_router,
                              const float* router_bias, const moe_experts* experts,
                              const moe_experts* shared, const void* w_shared_gate,
                              float* y, const moe_route_out* route_out,
                              void* workspace, size_t ws_bytes, void* const* events,
-                             void* stream);
+                             int32_t expert_path, void* stream);
 
 /* Reads a device status word written by a previous call: synchronises
  * `stream`, copies the word to *host_status. */

@@ -50,8 +50,9 @@ def experts_arg(L):
     return routed, shared
 
 
-def gpu_forward(m, spec, L, x, block_m=16, keep_route=True):
-    """One moe_forward call through the C ABI. Returns (y fp32 [T,H] on CPU,
+def gpu_forward(m, spec, L, x, block_m=16, keep_route=True, path=None):
+    """One moe_forward call through the C ABI (moe_forward_timed with the
+    given expert path when `path` is set). Returns (y fp32 [T,H] on CPU,
     routing outputs as CPU numpy arrays or None)."""
     T = x.shape[0]
     shape = m.make_shape(T, spec.H, spec.I, spec.E, spec.top_k, spec.shared, block_m)
@@ -60,7 +61,10 @@ def gpu_forward(m, spec, L, x, block_m=16, keep_route=True):
     y = torch.empty(T, spec.H, dtype=torch.float32, device=dev)
     ro = m.alloc_route_out(shape, dev) if keep_route else None
     routed, shared = experts_arg(L)
-    m.forward(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro)
+    if path is None:
+        m.forward(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro)
+    else:
+        m.forward_timed(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro, path=path)
     torch.cuda.synchronize()
     if ro is not None:
         assert m.status_read(ro["status"]) == 0

@@ -13,10 +13,10 @@ from tests.oracle_pins import check_routing_invariants
 pytestmark = pytest.mark.gpu
 
 
-def _run_and_check(moelib, dev, spec, block_m=16, tokens=None, layer_idx=0):
+def _run_and_check(moelib, dev, spec, block_m=16, tokens=None, layer_idx=0, path=None):
     L = parity.device_layer(spec, layer_idx, dev)
     x = synth.activations(spec, device=dev)
-    y, ro = parity.gpu_forward(moelib, spec, L, x, block_m)
+    y, ro = parity.gpu_forward(moelib, spec, L, x, block_m, path=path)
     y_ref, ids_ref, w_ref, g_ref, logits = parity.oracle_forward(spec, L, x, tokens=tokens)
     sel = np.arange(spec.T) if tokens is None else np.asarray(tokens)
     K = spec.top_k
@@ -114,6 +114,38 @@ def test_long_skew_chunks(moelib, cuda_dev):
         hot_share.append(counts[:256][b > 0].sum() / (C * 8))
         assert counts[:256][b < -1].sum() == 0
     assert 0.17 < np.mean(hot_share) < 0.23
+
+
+@pytest.mark.parametrize("block_m", [16, 32, 64, 128])
+def test_tensor_core_tiny(moelib, cuda_dev, block_m):
+    _run_and_check(moelib, cuda_dev, synth.WORKLOADS["tiny"], block_m=block_m, path=moelib.PATH_TENSOR_CORE)
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 17, 37, 100, 300])
+def test_tensor_core_ragged(moelib, cuda_dev, T):
+    spec = synth.LayerSpec("ragged", T=T, H=512, I=128, seed=20260015)
+    _run_and_check(moelib, cuda_dev, spec, block_m=32, path=moelib.PATH_TENSOR_CORE)
+
+
+@pytest.mark.parametrize("E,K,shared,H,I,bm", [(64, 8, True, 1024, 256, 64), (16, 2, False, 512, 128, 16),
+                                                (32, 4, True, 1536, 384, 32), (256, 8, True, 2048, 512, 128)])
+def test_tensor_core_shapes(moelib, cuda_dev, E, K, shared, H, I, bm):
+    spec = synth.LayerSpec("tc-shape", T=200, H=H, I=I, E=E, top_k=K, shared=shared, seed=20260016)
+    _run_and_check(moelib, cuda_dev, spec, block_m=bm, path=moelib.PATH_TENSOR_CORE)
+
+
+def test_gemv_path_prefill_shape(moelib, cuda_dev):
+    spec = synth.LayerSpec("gemv-prefill", T=256, H=2048, I=512, bias="zipf", seed=20260017)
+    _run_and_check(moelib, cuda_dev, spec, block_m=64, path=moelib.PATH_GEMV)
+
+
+def test_tensor_core_unsupported_shape_is_refused(moelib, cuda_dev):
+    spec = synth.LayerSpec("no-tc", T=64, H=320, I=128, E=16, seed=20260018)
+    L = parity.device_layer(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    with pytest.raises(moelib.MoeError) as ei:
+        parity.gpu_forward(moelib, spec, L, x, 16, path=moelib.PATH_TENSOR_CORE)
+    assert ei.value.status == moelib.MOE_ERR_UNSUPPORTED_SHAPE
 
 
 def test_topk_ties_through_gpu(moelib, cuda_dev):
