@@ -196,22 +196,42 @@ def time_region(fn, steps, stream):
     return start.elapsed_time(end)
 
 
-def stage_times(W, steps, stream):
+def capture(fn):
+    """One CUDA graph of everything fn() enqueues (the library's launches are
+    captured from the current stream)."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm the launch path (attribute setup) outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def stage_times(W, steps):
     """Per-kernel averages (ms) from events recorded between the kernels of
-    every call, on the launching stream."""
-    sums = [0.0] * 5
-    n = 0
+    every call (event nodes inside a graph of one step)."""
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(W.layers * W.calls)]
     for e6 in ev:           # torch creates the CUDA event at its first record
         for e in e6:
-            e.record(stream)
+            e.record()
     torch.cuda.synchronize()
-    for _ in range(steps):
+
+    def timed_step():
         k = 0
         for c in range(W.calls):
             for li in range(W.layers):
                 W.call(li, c, events=[e.cuda_event for e in ev[k]])
                 k += 1
+    g = capture(timed_step)
+    sums = [0.0] * 5
+    n = 0
+    for _ in range(steps):
+        g.replay()
         torch.cuda.synchronize()
         for e6 in ev:
             for i in range(5):
@@ -232,8 +252,9 @@ def run_ours(args, spec, rank, world, local_rank):
     block_m = args.block_m or (16 if spec.T <= 64 else 64 if spec.T <= 1024 else 128)
     W = Workload(m, spec, dev, block_m, rank)
     stream = torch.cuda.current_stream()
+    graph = capture(W.step)
     for _ in range(args.warmup):
-        W.step()
+        graph.replay()
     torch.cuda.synchronize()
     for li in range(W.layers):
         assert m.status_read(W.route[li]["status"]) == 0
@@ -241,14 +262,14 @@ def run_ours(args, spec, rank, world, local_rank):
 
     barrier(world)
     with ClockSampler(local_rank) as clk:
-        ms = time_region(W.step, args.steps, stream)
+        ms = time_region(graph.replay, args.steps, stream)
     ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
     clocks = clk.summary()
 
     # per-kernel breakdown (events between the kernels of every call)
     prof_steps = max(1, min(args.steps, 20))
-    st = stage_times(W, prof_steps, stream)
+    st = stage_times(W, prof_steps)
     names = ["router", "routing", "expert_gate_up", "expert_down", "combine"]
     per_call_ms = dict(zip(names, st))
 
@@ -261,9 +282,11 @@ def run_ours(args, spec, rank, world, local_rank):
         W.x.copy_(x_host, non_blocking=True)
         W.step()
         y_host.copy_(W.y, non_blocking=True)
+    g_e2e = capture(e2e_step)
     for _ in range(2):
-        e2e_step()
-    e2e_ms = max_over_ranks(time_region(e2e_step, max(1, args.steps // 2), stream), world, dev) / max(1, args.steps // 2)
+        g_e2e.replay()
+    n_e2e = max(1, args.steps // 2)
+    e2e_ms = max_over_ranks(time_region(g_e2e.replay, n_e2e, stream), world, dev) / n_e2e
 
     pk, pk_src = peaks()
     layers_calls = W.layers * W.calls
@@ -306,6 +329,7 @@ def run_ours(args, spec, rank, world, local_rank):
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": x_host.numel() * 2,
                 "d2h_bytes_per_step": y_host.numel() * 4},
         "gpu_launches": W.launches_per_step() * args.steps,
+        "launch": "one CUDA graph per step",
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -132,6 +132,16 @@ moe_route_out ws_route_out(const Workspace& w) {
   return r;
 }
 
+// Router scores: tensor cores for calls with many tokens, the CUDA-core GEMV
+// (one warp per expert row) for decode-sized calls.
+cudaError_t launch_router(const Geometry& g, const void* x, const void* w_router, const void* wsg,
+                          const Workspace& w, int32_t* status, uint16_t* x16, cudaStream_t stream) {
+  if (g.T >= kTensorCoreMinTokens && router_tc_supported(g))
+    return launch_router_tc(g, x, w_router, wsg, w.logits, w.state, g.route_blocks * g.E, status, x16,
+                            kDefaultTimeoutNs, stream);
+  return launch_router_logits(g, x, w_router, wsg, w.logits, w.state, g.route_blocks * g.E, status, x16, stream);
+}
+
 moe_status enqueue_routing_only(const Geometry& g, const float* router_bias, const moe_route_out& r,
                                 const Workspace& w, int stalled_block, long long timeout_ns, cudaStream_t stream) {
   RouteArgs a{};
@@ -167,8 +177,7 @@ moe_status enqueue_routing_only(const Geometry& g, const float* router_bias, con
 moe_status enqueue_route(const Geometry& g, const void* x, const void* w_router, const float* router_bias,
                          const void* w_shared_gate, const moe_route_out& r, const Workspace& w,
                          int stalled_block, long long timeout_ns, cudaStream_t stream) {
-  cudaError_t e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
-                                       g.route_blocks * g.E, r.status, nullptr, stream);
+  cudaError_t e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, nullptr, stream);
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   return enqueue_routing_only(g, router_bias, r, w, stalled_block, timeout_ns, stream);
 }
@@ -291,8 +300,7 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
   const bool tc = expert_path == MOE_PATH_TENSOR_CORE || (expert_path == MOE_PATH_AUTO && g.T >= kTensorCoreMinTokens && tc_ok);
 
   // Router logits, then the routing pipeline (two launches).
-  e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
-                           g.route_blocks * g.E, r.status, tc ? w.x16 : nullptr, s);
+  e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, tc ? w.x16 : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   st = enqueue_routing_only(g, router_bias, r, w, -1, kDefaultTimeoutNs, s);

@@ -65,6 +65,17 @@ __device__ __forceinline__ bool device_failed(const int32_t* status) {
   return *reinterpret_cast<const volatile int32_t*>(status) != 0;
 }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` the first time a
+// launch needs it (the value is cached, so launches inside a CUDA-graph
+// capture make no attribute call once a first, uncaptured call has run).
+template <typename Kernel>
+inline cudaError_t ensure_smem(Kernel k, size_t bytes, int* configured) {
+  if (bytes <= 48 * 1024 || (int)bytes <= *configured) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) *configured = (int)bytes;
+  return e;
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"

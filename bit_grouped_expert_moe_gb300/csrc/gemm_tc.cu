@@ -529,7 +529,8 @@ cudaError_t launch_gate_up_tc(const Geometry& g, const uint16_t* x16, const Expe
   GateUpTcParams p{g.H, g.I, g.E, g.K, g.A, x16, w.scales, w.biases, w.s_scales, w.s_biases, t, h, status,
                    timeout_ns};
   const size_t smem = gate_up_smem();
-  e = cudaFuncSetAttribute(gate_up_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int configured = 0;
+  e = ensure_smem(gate_up_tc_kernel, smem, &configured);
   if (e != cudaSuccess) return e;
   dim3 grid(g.max_tiles, g.I / 128);
   gate_up_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tm, tms, p);
@@ -557,7 +558,8 @@ cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs&
   while (mbc > 1 && mb_total % mbc) --mbc;
   DownTcParams p{g.H, g.I, g.E, g.BM, mbc, w.scales, w.biases, w.s_scales, w.s_biases, t, o, status, timeout_ns};
   const size_t smem = down_smem(g.I, g.BM);
-  e = cudaFuncSetAttribute(down_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int configured = 0;
+  e = ensure_smem(down_tc_kernel, smem, &configured);
   if (e != cudaSuccess) return e;
   dim3 grid(g.max_tiles, mb_total / mbc);
   down_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tm, tms, tmh, p);

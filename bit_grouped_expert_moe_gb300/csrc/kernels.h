@@ -51,6 +51,12 @@ cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* w
                                  float* logits, unsigned long long* state, int n_state,
                                  int32_t* status, uint16_t* x16, cudaStream_t stream);
 
+// Router on the tensor cores (router_tc.cu), for calls with many tokens.
+bool router_tc_supported(const Geometry& g);
+cudaError_t launch_router_tc(const Geometry& g, const void* x, const void* wr, const void* wsg, float* logits,
+                             unsigned long long* state, int n_state, int32_t* status, uint16_t* x16,
+                             long long timeout_ns, cudaStream_t stream);
+
 size_t route_smem_bytes(const Geometry& g);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream);
 

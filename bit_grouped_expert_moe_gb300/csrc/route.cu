@@ -292,10 +292,9 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
   g.K = a.K;
   g.E = a.E;
   const size_t smem = route_smem_bytes(g);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  static int configured = 0;
+  cudaError_t err = ensure_smem(route_kernel, smem, &configured);
+  if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.P);
   cfg.blockDim = dim3(kRouteThreads);

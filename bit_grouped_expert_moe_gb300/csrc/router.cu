@@ -107,11 +107,9 @@ cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* w
   const int rows = g.E + (wsg ? 1 : 0);
   dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (g.T + kRouterTokens - 1) / kRouterTokens);
   const size_t smem = (size_t)kRouterTokens * g.H * sizeof(uint16_t);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(router_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  static int configured = 0;
+  cudaError_t e = ensure_smem(router_logits_kernel, smem, &configured);
+  if (e != cudaSuccess) return e;
   router_logits_kernel<<<grid, kRouterWarps * 32, smem, stream>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wr), static_cast<const uint16_t*>(wsg),
       logits, g.T, g.H, g.E, g.E + 1, state, n_state, status, x16);
