@@ -442,6 +442,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode-t1", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
@@ -449,6 +450,9 @@ def main(argv=None):
         args.warmup = 3
     rank, world, local_rank = dist_env()
     spec = synth.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        spec = dataclasses.replace(spec, layers=args.layers)
     if args.impl == "reference":
         out = run_reference(args, spec, rank, world)
     else:
