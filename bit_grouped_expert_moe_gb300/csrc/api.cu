@@ -287,8 +287,15 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
   if (ws_bytes < w.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const moe_route_out r = route_out ? *route_out : ws_route_out(w);
+  // Inside a stream capture a plain event record only orders streams; the
+  // external flag makes it a timed event node of the graph.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (events && cudaStreamIsCapturing(s, &cap) != cudaSuccess) return cuda_fail(cudaGetLastError(), "capture query");
   auto mark = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+    if (!events) return cudaSuccess;
+    cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+    return cap == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                                : cudaEventRecord(ev, s);
   };
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
