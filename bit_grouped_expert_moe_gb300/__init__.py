@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
                                   ctypes.POINTER(RouteOutC), P, sz, P]
         L.moe_forward_timed.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                         ctypes.POINTER(RouteOutC), P, sz, ctypes.POINTER(P), i32, P]
+        L.moe_route_noalloc.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P]
+        L.moe_route_noalloc.restype = i32
         L.moe_status_read.argtypes = [P, P, ctypes.POINTER(i32)]
         L.moe_test_route_stall.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P, sz, i32, ctypes.c_int64, P]
         for f in ("moe_workspace_bytes", "moe_max_tiles", "moe_route_blocks", "moe_route", "moe_forward",
@@ -164,6 +166,14 @@ def route(shape, x, w_router, router_bias, w_shared_gate, out: dict, workspace, 
     _check(lib().moe_route(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(router_bias), _ptr(w_shared_gate),
                            ctypes.byref(r), _ptr(workspace), workspace.numel() * workspace.element_size(),
                            _stream(stream)), "moe_route")
+
+
+def route_noalloc(shape, x, w_router, router_bias, w_shared_gate, out: dict, stream=None):
+    """moe_route without a workspace (the library's own static device
+    scratch; see include/moe.h for the size limit and the sharing rules)."""
+    r = _route_c(out)
+    _check(lib().moe_route_noalloc(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(router_bias),
+                                   _ptr(w_shared_gate), ctypes.byref(r), _stream(stream)), "moe_route_noalloc")
 
 
 def forward(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, workspace, route_out=None,

@@ -3,6 +3,7 @@
 // enqueued on the caller's stream with no host synchronisation.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "kernels.h"
 
@@ -352,3 +353,76 @@ moe_status moe_status_read(const int32_t* device_status, void* stream, int32_t* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Routing for callers that cannot allocate device memory.
+//
+// moe_route needs a workspace from its caller. Some callers have none to give
+// at the point where they route: code running inside a host callback or a
+// real-time loop that must not enter the CUDA allocator (cudaMalloc can
+// synchronise the device and take unbounded time), plugins that are handed
+// only the buffers of their inputs and outputs, and embedders whose device
+// memory is owned and budgeted by a host framework. moe_route_noalloc keeps
+// its scratch (router logits and the routing kernel's look-back words) in
+// the file-scope device array below, which every GPU that loads this library
+// holds until the process exits. The router kernel clears the look-back
+// words at the start of every call; the logits are overwritten.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[1u << 20];
+
+namespace bgmoe {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = sizeof(g_noalloc_scratch);
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side name of a __device__ array is not its address).
+cudaError_t noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace bgmoe
+
+extern "C" moe_status moe_route_noalloc(const moe_shape* shape, const void* x, const void* w_router,
+                                        const float* router_bias, const void* w_shared_gate,
+                                        const moe_route_out* out, void* stream) {
+  moe_status st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  const Geometry g = geometry(*shape);
+  if (!route_out_ok(out, g.shared)) return MOE_ERR_INVALID_ARG;
+  if (g.T == 0) return MOE_OK;
+  if (!x || !w_router || (g.shared && !w_shared_gate)) return MOE_ERR_INVALID_ARG;
+  const size_t logits_bytes = align256(sizeof(float) * (size_t)g.T * (g.E + 1));
+  const size_t need = logits_bytes + align256(sizeof(unsigned long long) * (size_t)g.route_blocks * g.E);
+  if (need > kNoAllocScratchBytes) {
+    snprintf(g_detail, sizeof(g_detail),
+             "moe_route_noalloc: this shape needs %zu bytes of scratch, the static buffer holds %zu", need,
+             kNoAllocScratchBytes);
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
+  void* base = nullptr;
+  cudaError_t e = noalloc_scratch(&base);
+  if (e != cudaSuccess) return cuda_fail(e, "moe_route_noalloc scratch address");
+  Workspace w{};
+  w.logits = static_cast<float*>(base);
+  w.state = reinterpret_cast<unsigned long long*>(static_cast<char*>(base) + logits_bytes);
+  return enqueue_route(g, x, w_router, router_bias, w_shared_gate, *out, w, -1, kDefaultTimeoutNs,
+                       static_cast<cudaStream_t>(stream));
+}

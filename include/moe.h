@@ -199,6 +199,28 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
                              void* workspace, size_t ws_bytes, void* const* events,
                              int32_t expert_path, void* stream);
 
+/* moe_route without a workspace, for callers that cannot allocate device
+ * memory where they route (a host callback or real-time loop that must not
+ * enter the CUDA allocator, a plugin given only its input and output buffers,
+ * an embedder whose device memory is budgeted by a host framework). The
+ * pages have no counterpart: this is a deployment convenience, not a step
+ * of the layer. Same arguments and outputs as moe_route, minus the workspace.
+ *   Scratch: a 1 MiB file-scope device array that every GPU loading this
+ *   library holds until the process exits. A shape whose router logits
+ *   (T * (E+1) * 4 bytes) plus look-back words no longer fit is refused with
+ *   MOE_ERR_UNSUPPORTED_SHAPE (moe_last_error_detail gives both sizes); at
+ *   E = 256 that is about 900 tokens per call.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call on a device shares the one array and leaves its contents
+ *   behind; each call clears what must start at zero. Calls that overlap on
+ *   the GPU (two streams, or two host threads) race on the array: serialise
+ *   them. The library allocates nothing on this path. */
+moe_status moe_route_noalloc(const moe_shape* shape, const void* x, const void* w_router,
+                             const float* router_bias, const void* w_shared_gate,
+                             const moe_route_out* out, void* stream);
+
 /* Reads a device status word written by a previous call: synchronises
  * `stream`, copies the word to *host_status. */
 moe_status moe_status_read(const int32_t* device_status, void* stream, int32_t* host_status);
