@@ -145,8 +145,11 @@ class Workload:
         self.y = torch.empty(self.layers, self.calls, self.T, spec.H, dtype=torch.float32, device=device)
         self.route = [m.alloc_route_out(self.shape, device) for _ in range(self.layers)]
 
+    def fused(self):
+        return self.T <= 4  # the library runs decode-sized calls as router + fused decode kernel
+
     def launches_per_step(self):
-        return 5 * self.layers * self.calls
+        return (2 if self.fused() else 5) * self.layers * self.calls
 
     def call(self, li, c, events=None):
         L = self.L[li]
@@ -169,7 +172,7 @@ class Workload:
         H, I, E = s.H, s.I, s.E
         wbytes_expert = 3 * H * I * BYTES_PER_WEIGHT
         router_bytes = (E + (1 if s.shared else 0)) * H * 2
-        tot_bytes = gu_bytes = 0.0
+        tot_bytes = gu_bytes = fused_bytes = 0.0
         distinct = []
         for li in range(self.layers):
             counts = self.route[li]["counts"].cpu()
@@ -179,8 +182,9 @@ class Workload:
             per_call = n_exp * wbytes_expert + router_bytes + self.T * H * 2 + self.T * H * 4
             tot_bytes += per_call * self.calls
             gu_bytes += n_exp * (2 * I * H * BYTES_PER_WEIGHT) * self.calls
+            fused_bytes += (n_exp * wbytes_expert + self.T * H * 6 + self.T * (E + 1) * 4) * self.calls
         flops_tok = 2 * H * E + s.top_k * 6 * H * I + (6 * H * I if s.shared else 0) + (2 * H if s.shared else 0)
-        return dict(bytes_per_step=tot_bytes, gate_up_bytes_per_step=gu_bytes,
+        return dict(bytes_per_step=tot_bytes, gate_up_bytes_per_step=gu_bytes, fused_bytes_per_step=fused_bytes,
                     flops_per_step=flops_tok * self.T * self.calls * self.layers,
                     distinct_experts_mean=sum(distinct) / len(distinct))
 
@@ -301,11 +305,18 @@ def run_ours(args, spec, rank, world, local_rank):
         value = world * tokens_step / (ms_step / 1000.0)
         e2e_value = world * tokens_step / (e2e_ms / 1000.0)
         higher = True
-    gu_ms = per_call_ms["expert_gate_up"]
-    gu_bytes_launch = work["gate_up_bytes_per_step"] / layers_calls
+    if W.fused():
+        # events[2..3] bracket the fused decode kernel (top-k, tables, gate/up, down, combine)
+        names = ["router", "routing", "fused_decode_layer", "-", "-"]
+        per_call_ms = {k: v for k, v in zip(names, st) if k != "-"}
+        dom, dom_bytes = "fused_decode_layer", work["fused_bytes_per_step"] / layers_calls
+    else:
+        dom, dom_bytes = "expert_gate_up", work["gate_up_bytes_per_step"] / layers_calls
+    gu_ms = per_call_ms[dom]
+    gu_bytes_launch = dom_bytes
     achieved = gu_bytes_launch / (gu_ms / 1000.0) / 1e9
     peak = pk["hbm_gbs"]
-    roofline = {"kernel": "expert_gate_up", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                 "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": pk_src, "algorithmic_bytes_per_launch": int(gu_bytes_launch)}
     layer_bytes = work["bytes_per_step"] / layers_calls

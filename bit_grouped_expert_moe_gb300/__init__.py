@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libbgmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE = 0, 1, 2
 MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = 3, 4, 5
-PATH_AUTO, PATH_GEMV, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_TENSOR_CORE, PATH_FUSED_DECODE = 0, 1, 2, 3
 
 P = ctypes.c_void_p
 

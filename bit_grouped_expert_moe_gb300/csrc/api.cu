@@ -76,6 +76,8 @@ struct Workspace {
   int32_t* tile_rows;
   int32_t* num_tiles;
   uint16_t* x16;              // [T][H] fp16 activations for the tensor-core path
+  float* h32;                 // [rows][I] fp32 h of the fused decode path (T <= 4 only)
+  unsigned int* bar;          // grid-barrier counter of the fused decode kernel
   __half* h;                  // [rows][I]
   __half* o;                  // [rows][H]
   size_t bytes;
@@ -105,6 +107,8 @@ Workspace carve(const Geometry& g, void* base) {
   w.tile_rows = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
   w.num_tiles = static_cast<int32_t*>(take(sizeof(int32_t)));
   w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)g.T * g.H));
+  w.h32 = static_cast<float*>(take(g.T <= kDecodeMaxTokens ? sizeof(float) * (size_t)g.rows * g.I : 0));
+  w.bar = static_cast<unsigned int*>(take(sizeof(unsigned int)));
   w.h = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.I));
   w.o = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.H));
   w.bytes = off;
@@ -271,7 +275,7 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
                              const void* w_shared_gate, float* y, const moe_route_out* route_out, void* workspace,
                              size_t ws_bytes, void* const* events, int32_t expert_path, void* stream) {
   moe_status st = check_shape(shape);
-  if (expert_path < MOE_PATH_AUTO || expert_path > MOE_PATH_TENSOR_CORE) return MOE_ERR_INVALID_ARG;
+  if (expert_path < MOE_PATH_AUTO || expert_path > MOE_PATH_FUSED_DECODE) return MOE_ERR_INVALID_ARG;
   if (st != MOE_OK) return st;
   const Geometry g = geometry(*shape);
   if (route_out && !route_out_ok(route_out, g.shared)) return MOE_ERR_INVALID_ARG;
@@ -301,11 +305,59 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
   cudaError_t e = mark(0);
   if (e != cudaSuccess) return cuda_fail(e, "event record");
 
-  // Expert path: tensor cores once the tile rows are many enough to feed
-  // them, the bandwidth-bound GEMV for decode-sized calls.
+  // Expert path: the fused decode kernel for decode-sized calls, tensor
+  // cores once the tile rows are many enough to feed them, else the GEMV.
+  const bool dec_ok = decode_supported(g);
+  if (expert_path == MOE_PATH_FUSED_DECODE && !dec_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const bool fused = expert_path == MOE_PATH_FUSED_DECODE || (expert_path == MOE_PATH_AUTO && dec_ok);
   const bool tc_ok = tc_path_supported(g);
   if (expert_path == MOE_PATH_TENSOR_CORE && !tc_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
-  const bool tc = expert_path == MOE_PATH_TENSOR_CORE || (expert_path == MOE_PATH_AUTO && g.T >= kTensorCoreMinTokens && tc_ok);
+  const bool tc = expert_path == MOE_PATH_TENSOR_CORE ||
+                  (expert_path == MOE_PATH_AUTO && !fused && g.T >= kTensorCoreMinTokens && tc_ok);
+
+  if (fused) {
+    e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
+                             g.route_blocks * g.E, r.status, nullptr, s, w.bar);
+    if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
+    if ((e = mark(1)) != cudaSuccess || (e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
+    DecodeArgs d{};
+    d.T = g.T;
+    d.H = g.H;
+    d.I = g.I;
+    d.E = g.E;
+    d.K = g.K;
+    d.shared = g.shared;
+    d.x = static_cast<const uint16_t*>(x);
+    d.logits = w.logits;
+    d.bias = router_bias;
+    d.gu = ExpertArgs{experts->gate_up.codes, experts->gate_up.scales, experts->gate_up.biases,
+                      g.shared ? shared->gate_up.codes : nullptr, g.shared ? shared->gate_up.scales : nullptr,
+                      g.shared ? shared->gate_up.biases : nullptr};
+    d.dn = ExpertArgs{experts->down.codes, experts->down.scales, experts->down.biases,
+                      g.shared ? shared->down.codes : nullptr, g.shared ? shared->down.scales : nullptr,
+                      g.shared ? shared->down.biases : nullptr};
+    d.ids = r.ids;
+    d.weights = r.weights;
+    d.gate = r.gate;
+    d.counts = r.counts;
+    d.offsets = r.offsets;
+    d.sorted = r.sorted;
+    d.inv = r.inv;
+    d.tile_expert = r.tile_expert;
+    d.tile_row0 = r.tile_row0;
+    d.tile_rows = r.tile_rows;
+    d.num_tiles = r.num_tiles;
+    d.status = r.status;
+    d.h = w.h32;
+    d.y = y;
+    d.bar = w.bar;
+    d.timeout_ns = kDefaultTimeoutNs;
+    e = launch_decode(d, g, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode launch");
+    for (int i = 3; i < 6; ++i)
+      if ((e = mark(i)) != cudaSuccess) return cuda_fail(e, "event record");
+    return MOE_OK;
+  }
 
   // Router logits, then the routing pipeline (two launches).
   e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, tc ? w.x16 : nullptr, s);

@@ -8,6 +8,8 @@
 
 namespace bgmoe {
 
+constexpr int kDecodeMaxTokens = 4;  // tokens per call handled by the fused decode kernel
+
 struct RouteArgs {
   const float* logits;  // [T][E+1], column E = shared gate logit
   const float* bias;    // [E] or null
@@ -49,7 +51,8 @@ struct TileArgs {
 
 cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* wr, const void* wsg,
                                  float* logits, unsigned long long* state, int n_state,
-                                 int32_t* status, uint16_t* x16, cudaStream_t stream);
+                                 int32_t* status, uint16_t* x16, cudaStream_t stream,
+                                 unsigned int* bar = nullptr);
 
 // Router on the tensor cores (router_tc.cu), for calls with many tokens.
 bool router_tc_supported(const Geometry& g);
@@ -71,6 +74,34 @@ cudaError_t launch_gate_up_tc(const Geometry& g, const uint16_t* x16, const Expe
                               __half* h, int32_t* status, long long timeout_ns, cudaStream_t stream);
 cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs& w, const TileArgs& t, __half* o,
                            int32_t* status, long long timeout_ns, cudaStream_t stream);
+
+// Fused decode layer (decode.cu): top-k, tables, gate/up, down and combine
+// after the router kernel, for T <= kDecodeMaxTokens.
+struct DecodeArgs {
+  int T, H, I, E, K, shared;
+  const uint16_t* x;     // bf16 [T][H]
+  const float* logits;   // [T][E+1] written by the router kernel
+  const float* bias;     // [E] or null
+  ExpertArgs gu, dn;
+  int32_t* ids;
+  float* weights;
+  float* gate;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted;
+  int32_t* inv;
+  int32_t* tile_expert;
+  int32_t* tile_row0;
+  int32_t* tile_rows;
+  int32_t* num_tiles;
+  int32_t* status;
+  float* h;              // fp32 [A+T][I]
+  float* y;              // fp32 [T][H]
+  unsigned int* bar;     // grid-barrier counter, cleared by the router kernel
+  long long timeout_ns;
+};
+bool decode_supported(const Geometry& g);
+cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);
 
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,
                            const float* gate, const int32_t* status, float* y, cudaStream_t stream);

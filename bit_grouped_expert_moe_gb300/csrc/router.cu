@@ -19,18 +19,28 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wr,
                      const uint16_t* __restrict__ wsg, float* __restrict__ logits, int T, int H,
                      int E, int ld, unsigned long long* __restrict__ state, int n_state,
-                     int32_t* __restrict__ status, uint16_t* __restrict__ x16) {
+                     int32_t* __restrict__ status, uint16_t* __restrict__ x16,
+                     unsigned int* __restrict__ bar) {
   extern __shared__ __align__(16) uint16_t xs[];  // [kRouterTokens][H]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.y * kRouterTokens;
   const int nt = min(kRouterTokens, T - t0);
 
-  // Clear the look-back words and the status word for this call.
+  // Let a kernel launched after this one with programmatic dependent launch
+  // start its weight prefetch now; it waits for this grid before reading
+  // anything this kernel writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  // Clear the look-back words, the status word and the decode kernel's
+  // grid-barrier counter for this call.
   {
     const int nblocks = gridDim.x * gridDim.y;
     const int b = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = b * blockDim.x + threadIdx.x; i < n_state; i += nblocks * blockDim.x) state[i] = 0ull;
-    if (b == 0 && threadIdx.x == 0) *status = 0;
+    if (b == 0 && threadIdx.x == 0) {
+      *status = 0;
+      if (bar != nullptr) *bar = 0u;
+    }
   }
 
   // Stage the block's token rows (16-byte copies; H is a multiple of 64).
@@ -103,7 +113,7 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
 
 cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* wr, const void* wsg,
                                  float* logits, unsigned long long* state, int n_state,
-                                 int32_t* status, uint16_t* x16, cudaStream_t stream) {
+                                 int32_t* status, uint16_t* x16, cudaStream_t stream, unsigned int* bar) {
   const int rows = g.E + (wsg ? 1 : 0);
   dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (g.T + kRouterTokens - 1) / kRouterTokens);
   const size_t smem = (size_t)kRouterTokens * g.H * sizeof(uint16_t);
@@ -112,7 +122,7 @@ cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* w
   if (e != cudaSuccess) return e;
   router_logits_kernel<<<grid, kRouterWarps * 32, smem, stream>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wr), static_cast<const uint16_t*>(wsg),
-      logits, g.T, g.H, g.E, g.E + 1, state, n_state, status, x16);
+      logits, g.T, g.H, g.E, g.E + 1, state, n_state, status, x16, bar);
   return cudaGetLastError();
 }
 

@@ -179,10 +179,14 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_rout
 
 /* Expert-GEMM implementations selectable through moe_forward_timed. */
 typedef enum moe_expert_path {
-  MOE_PATH_AUTO = 0,        /* tensor cores for T >= 64 when the shape allows, else GEMV */
+  MOE_PATH_AUTO = 0,        /* fused decode for T <= 4, tensor cores for T >= 64 when the
+                               shape allows, else GEMV */
   MOE_PATH_GEMV = 1,        /* bandwidth-bound grouped GEMV (CUDA cores), any shape */
-  MOE_PATH_TENSOR_CORE = 2  /* tcgen05 grouped GEMM; needs H % 512 == 0, I % 128 == 0 and
+  MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 512 == 0, I % 128 == 0 and
                                (I/64) * block_m * 128 <= 131072 (else UNSUPPORTED_SHAPE) */
+  MOE_PATH_FUSED_DECODE = 3 /* router kernel + one fused kernel for top-k, tables, expert
+                               GEMVs and combine; T <= 4 (else UNSUPPORTED_SHAPE). Its
+                               events[2] == events[1] and events[4..5] == events[3] */
 } moe_expert_path;
 
 /* moe_forward with a chosen expert path that also records caller-owned CUDA

@@ -151,6 +151,34 @@ def test_tensor_core_unsupported_shape_is_refused(moelib, cuda_dev):
     assert ei.value.status == moelib.MOE_ERR_UNSUPPORTED_SHAPE
 
 
+@pytest.mark.parametrize("T,E,K,shared,H,I", [(1, 256, 8, True, 2048, 512), (4, 256, 8, True, 2048, 512),
+                                               (3, 64, 8, True, 256, 128), (2, 16, 2, False, 128, 64),
+                                               (4, 8, 1, True, 512, 192), (1, 32, 4, False, 1024, 320)])
+def test_fused_decode(moelib, cuda_dev, T, E, K, shared, H, I):
+    spec = synth.LayerSpec("fused", T=T, H=H, I=I, E=E, top_k=K, shared=shared, seed=20260019)
+    _run_and_check(moelib, cuda_dev, spec, path=moelib.PATH_FUSED_DECODE)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_gemv_path_decode(moelib, cuda_dev, T):
+    _run_and_check(moelib, cuda_dev, synth.WORKLOADS[f"decode-t{T}"], path=moelib.PATH_GEMV)
+
+
+def test_fused_decode_deterministic_and_refuses_prefill(moelib, cuda_dev):
+    spec = synth.WORKLOADS["decode-t4"]
+    L = parity.device_layer(spec, 3, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    y1, r1 = parity.gpu_forward(moelib, spec, L, x, 16, path=moelib.PATH_FUSED_DECODE)
+    y2, r2 = parity.gpu_forward(moelib, spec, L, x, 16, path=moelib.PATH_FUSED_DECODE)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+    big = synth.LayerSpec("big", T=8, H=512, I=128, seed=20260020)
+    Lb = parity.device_layer(big, 0, cuda_dev)
+    with pytest.raises(moelib.MoeError) as ei:
+        parity.gpu_forward(moelib, big, Lb, synth.activations(big, device=cuda_dev), 16,
+                           path=moelib.PATH_FUSED_DECODE)
+    assert ei.value.status == moelib.MOE_ERR_UNSUPPORTED_SHAPE
+
+
 def test_topk_ties_through_gpu(moelib, cuda_dev):
     """The hand-ranked tie cases of tests/golden/topk_ties.txt through
     moe_route (lowest index first among equal logits)."""
