@@ -112,9 +112,30 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 
   // ---- phase 1a: stage x (fp32, padded chunks) and select the top-k
   float* xs = dsm;  // [T][H/32][kDecPad]
-  for (int i = tid; i < T * H; i += kDecThreads) {
-    const int t = i / H, k = i - t * H;
-    xs[(t * nvec + (k >> 5)) * kDecPad + (k & 31)] = bf16_bits_to_f32(a.x[(size_t)t * H + k]);
+  {
+    const int xvec = T * H / 8;  // 16-byte chunks of x; all loads of a batch before any store
+    for (int i0 = tid; i0 < xvec; i0 += 2 * kDecThreads) {
+      uint4 v[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u * kDecThreads;
+        if (i < xvec) v[u] = ldg_nc_v4(a.x + (size_t)i * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = i0 + u * kDecThreads;
+        if (i < xvec) {
+          const int t = (i * 8) / H, k = i * 8 - t * H;
+          float* d = xs + (t * nvec + (k >> 5)) * kDecPad + (k & 31);
+          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          *reinterpret_cast<float4*>(d) = make_float4(bf16_bits_to_f32(w[0] & 0xFFFFu), bf16_bits_to_f32(w[0] >> 16),
+                                                      bf16_bits_to_f32(w[1] & 0xFFFFu), bf16_bits_to_f32(w[1] >> 16));
+          *reinterpret_cast<float4*>(d + 4) = make_float4(bf16_bits_to_f32(w[2] & 0xFFFFu),
+                                                          bf16_bits_to_f32(w[2] >> 16),
+                                                          bf16_bits_to_f32(w[3] & 0xFFFFu), bf16_bits_to_f32(w[3] >> 16));
+        }
+      }
+    }
   }
   if (tid == 0) S.failed = 0;
   if (warp < T) {
@@ -270,74 +291,86 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     }
   }
 
-  // ---- phase 1c: gate/up units (slot, h column n), shared slot first
+  // ---- phase 1c: gate/up units (slot, h column n), shared slot first. A warp
+  // takes two units at a time and issues both units' loads before any math.
   const int units = nslots * I;
-  for (int u = gw; u < units; u += nw) {
-    const int s = u / I, n = u - s * I;
-    const int e = S.slot_e[s];
-    const bool sh = e == E;
-    const uint32_t* codes = sh ? a.gu.s_codes : a.gu.codes + (size_t)e * 2 * I * (H / 8);
-    const uint16_t* sc = sh ? a.gu.s_scales : a.gu.scales + (size_t)e * 2 * I * gpr;
-    const uint16_t* bi = sh ? a.gu.s_biases : a.gu.biases + (size_t)e * 2 * I * gpr;
-    uint4 cg[kDecMaxIt], cu[kDecMaxIt];
-    float sg[kDecMaxIt], bg[kDecMaxIt], su[kDecMaxIt], bu[kDecMaxIt];
-    const bool reuse = pre && u == gw;  // the shared unit loaded in phase 0
+  for (int u0 = gw; u0 < units; u0 += 2 * nw) {
+    uint4 cg[2][kDecMaxIt], cu[2][kDecMaxIt];
+    float sg[2][kDecMaxIt], bg[2][kDecMaxIt], su[2][kDecMaxIt], bu[2][kDecMaxIt];
 #pragma unroll
-    for (int it = 0; it < kDecMaxIt; ++it) {
-      const int v = lane + 32 * it;
-      if (v < nvec) {
-        if (reuse) {
-          cg[it] = pc_g[it];
-          cu[it] = pc_u[it];
-          sg[it] = ps_g[it];
-          bg[it] = pb_g[it];
-          su[it] = ps_u[it];
-          bu[it] = pb_u[it];
-        } else {
-          cg[it] = ldg_nc_v4(codes + (size_t)n * (H / 8) + 4 * v);
-          cu[it] = ldg_nc_v4(codes + (size_t)(I + n) * (H / 8) + 4 * v);
-          sg[it] = bf16_bits_to_f32(__ldg(sc + (size_t)n * gpr + v / 2));
-          bg[it] = bf16_bits_to_f32(__ldg(bi + (size_t)n * gpr + v / 2));
-          su[it] = bf16_bits_to_f32(__ldg(sc + (size_t)(I + n) * gpr + v / 2));
-          bu[it] = bf16_bits_to_f32(__ldg(bi + (size_t)(I + n) * gpr + v / 2));
-        }
-      }
-    }
-    const int nr = S.slot_n[s];
-    float ag[kDecodeMaxTokens], au[kDecodeMaxTokens];
+    for (int b = 0; b < 2; ++b) {
+      const int u = u0 + b * nw;
+      if (u >= units) break;
+      const int s = u / I, n = u - s * I;
+      const int e = S.slot_e[s];
+      const bool sh = e == E;
+      const uint32_t* codes = sh ? a.gu.s_codes : a.gu.codes + (size_t)e * 2 * I * (H / 8);
+      const uint16_t* sc = sh ? a.gu.s_scales : a.gu.scales + (size_t)e * 2 * I * gpr;
+      const uint16_t* bi = sh ? a.gu.s_biases : a.gu.biases + (size_t)e * 2 * I * gpr;
+      const bool reuse = pre && u == gw;  // the shared unit loaded in phase 0
 #pragma unroll
-    for (int j = 0; j < kDecodeMaxTokens; ++j) ag[j] = au[j] = 0.f;
-#pragma unroll
-    for (int it = 0; it < kDecMaxIt; ++it) {
-      const int v = lane + 32 * it;
-      if (v < nvec) {
-#pragma unroll
-        for (int j = 0; j < kDecodeMaxTokens; ++j) {
-          if (j < nr) {
-            const float* xr = xs + (S.slot_tok[s][j] * nvec + v) * kDecPad;
-            ag[j] = dot32_f(cg[it], sg[it], bg[it], xr, ag[j]);
-            au[j] = dot32_f(cu[it], su[it], bu[it], xr, au[j]);
+      for (int it = 0; it < kDecMaxIt; ++it) {
+        const int v = lane + 32 * it;
+        if (v < nvec) {
+          if (reuse) {
+            cg[b][it] = pc_g[it];
+            cu[b][it] = pc_u[it];
+            sg[b][it] = ps_g[it];
+            bg[b][it] = pb_g[it];
+            su[b][it] = ps_u[it];
+            bu[b][it] = pb_u[it];
+          } else {
+            cg[b][it] = ldg_nc_v4(codes + (size_t)n * (H / 8) + 4 * v);
+            cu[b][it] = ldg_nc_v4(codes + (size_t)(I + n) * (H / 8) + 4 * v);
+            sg[b][it] = bf16_bits_to_f32(__ldg(sc + (size_t)n * gpr + v / 2));
+            bg[b][it] = bf16_bits_to_f32(__ldg(bi + (size_t)n * gpr + v / 2));
+            su[b][it] = bf16_bits_to_f32(__ldg(sc + (size_t)(I + n) * gpr + v / 2));
+            bu[b][it] = bf16_bits_to_f32(__ldg(bi + (size_t)(I + n) * gpr + v / 2));
           }
         }
       }
     }
 #pragma unroll
-    for (int j = 0; j < kDecodeMaxTokens; ++j) {
+    for (int b = 0; b < 2; ++b) {
+      const int u = u0 + b * nw;
+      if (u >= units) break;
+      const int s = u / I, n = u - s * I;
+      const int nr = S.slot_n[s];
+      float ag[kDecodeMaxTokens], au[kDecodeMaxTokens];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        ag[j] += __shfl_xor_sync(0xffffffffu, ag[j], o);
-        au[j] += __shfl_xor_sync(0xffffffffu, au[j], o);
-      }
-    }
-    if (lane < nr) {
-      float gv = ag[0], uv = au[0];
+      for (int j = 0; j < kDecodeMaxTokens; ++j) ag[j] = au[j] = 0.f;
 #pragma unroll
-      for (int j = 1; j < kDecodeMaxTokens; ++j)
-        if (lane == j) {
-          gv = ag[j];
-          uv = au[j];
+      for (int it = 0; it < kDecMaxIt; ++it) {
+        const int v = lane + 32 * it;
+        if (v < nvec) {
+#pragma unroll
+          for (int j = 0; j < kDecodeMaxTokens; ++j) {
+            if (j < nr) {
+              const float* xr = xs + (S.slot_tok[s][j] * nvec + v) * kDecPad;
+              ag[j] = dot32_f(cg[b][it], sg[b][it], bg[b][it], xr, ag[j]);
+              au[j] = dot32_f(cu[b][it], su[b][it], bu[b][it], xr, au[j]);
+            }
+          }
         }
-      a.h[(size_t)S.slot_row[s][lane] * I + n] = silu_f32(gv) * uv;
+      }
+#pragma unroll
+      for (int j = 0; j < kDecodeMaxTokens; ++j) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          ag[j] += __shfl_xor_sync(0xffffffffu, ag[j], o);
+          au[j] += __shfl_xor_sync(0xffffffffu, au[j], o);
+        }
+      }
+      if (lane < nr) {
+        float gv = ag[0], uv = au[0];
+#pragma unroll
+        for (int j = 1; j < kDecodeMaxTokens; ++j)
+          if (lane == j) {
+            gv = ag[j];
+            uv = au[j];
+          }
+        a.h[(size_t)S.slot_row[s][lane] * I + n] = silu_f32(gv) * uv;
+      }
     }
   }
 
@@ -365,9 +398,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const int ivec = I / 32, igpr = I / kGroup;
   float* hs = dsm;                                  // [R][I/32][kDecPad] (x is no longer needed)
   float* res = dsm + (size_t)R * ivec * kDecPad;    // [R][rows_per_blk]
-  for (int i = tid; i < R * I; i += kDecThreads) {
-    const int r = i / I, k = i - r * I;
-    hs[(r * ivec + (k >> 5)) * kDecPad + (k & 31)] = __ldcg(a.h + (size_t)r * I + k);
+  {
+    const int hv = R * I / 4;  // float4 chunks of h; a batch of loads before any store
+    for (int i0 = tid; i0 < hv; i0 += 4 * kDecThreads) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kDecThreads;
+        if (i < hv) v[u] = __ldcg(reinterpret_cast<const float4*>(a.h) + i);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kDecThreads;
+        if (i < hv) {
+          const int r = (i * 4) / I, k = i * 4 - r * I;
+          *reinterpret_cast<float4*>(hs + (r * ivec + (k >> 5)) * kDecPad + (k & 31)) = v[u];
+        }
+      }
+    }
   }
   __syncthreads();
   int L = 1;  // lanes per W_down row: largest power of two <= min(32, I/32)
@@ -376,36 +424,72 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const int its = (ivec + L - 1) / L;
   const int mrows = m1 - m0;
   const int dunits = nslots * mrows;
-  for (int ub = warp * per_warp; ub < dunits; ub += kDecWarps * per_warp) {
-    const int u = ub + rw;
-    const bool live = u < dunits;
-    const int s = live ? u / mrows : 0, ml = live ? u - s * mrows : 0;
-    const int m = m0 + ml;
-    const int e = S.slot_e[s];
-    const bool sh = e == E;
-    const uint32_t* codes = sh ? a.dn.s_codes : a.dn.codes + (size_t)e * H * (I / 8);
-    const uint16_t* sc = sh ? a.dn.s_scales : a.dn.scales + (size_t)e * H * igpr;
-    const uint16_t* bi = sh ? a.dn.s_biases : a.dn.biases + (size_t)e * H * igpr;
-    const int nr = live ? S.slot_n[s] : 0;
-    float acc[kDecodeMaxTokens];
+  constexpr int kSlots = 4;                  // (pass, load) entries issued together
+  const int passes_per_batch = its >= kSlots ? 1 : kSlots / its;
+  const int pass_stride = kDecWarps * per_warp;
+  for (int ub0 = warp * per_warp; ub0 < dunits; ub0 += passes_per_batch * pass_stride) {
+    uint4 c[kSlots];
+    float sv[kSlots], bv[kSlots];
 #pragma unroll
-    for (int j = 0; j < kDecodeMaxTokens; ++j) acc[j] = 0.f;
-    for (int it = 0; it < its; ++it) {
+    for (int q = 0; q < kSlots; ++q) {
+      const int pss = q / (its < kSlots ? its : kSlots), it = q - pss * (its < kSlots ? its : kSlots);
+      const int u = ub0 + pss * pass_stride + rw;
       const int v = sub + L * it;
-      if (live && v < ivec) {
-        const uint4 c = *reinterpret_cast<const uint4*>(codes + (size_t)m * (I / 8) + 4 * v);
-        const float sv = bf16_bits_to_f32(sc[(size_t)m * igpr + v / 2]);
-        const float bv = bf16_bits_to_f32(bi[(size_t)m * igpr + v / 2]);
-#pragma unroll
-        for (int j = 0; j < kDecodeMaxTokens; ++j)
-          if (j < nr) acc[j] = dot32_f(c, sv, bv, hs + (S.slot_row[s][j] * ivec + v) * kDecPad, acc[j]);
+      if (pss < passes_per_batch && it < its && u < dunits && v < ivec) {
+        const int s = u / mrows, m = m0 + (u - s * mrows);
+        const int e = S.slot_e[s];
+        const bool sh = e == E;
+        const uint32_t* codes = sh ? a.dn.s_codes : a.dn.codes + (size_t)e * H * (I / 8);
+        const uint16_t* sc = sh ? a.dn.s_scales : a.dn.scales + (size_t)e * H * igpr;
+        const uint16_t* bi = sh ? a.dn.s_biases : a.dn.biases + (size_t)e * H * igpr;
+        c[q] = *reinterpret_cast<const uint4*>(codes + (size_t)m * (I / 8) + 4 * v);
+        sv[q] = bf16_bits_to_f32(sc[(size_t)m * igpr + v / 2]);
+        bv[q] = bf16_bits_to_f32(bi[(size_t)m * igpr + v / 2]);
       }
     }
+    for (int pss = 0; pss < passes_per_batch; ++pss) {
+      const int u = ub0 + pss * pass_stride + rw;
+      const bool live = u < dunits;
+      const int s = live ? u / mrows : 0, ml = live ? u - s * mrows : 0;
+      const int nr = live ? S.slot_n[s] : 0;
+      float acc[kDecodeMaxTokens];
 #pragma unroll
-    for (int j = 0; j < kDecodeMaxTokens; ++j)
-      for (int off = L >> 1; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
-    if (live && sub == 0)
-      for (int j = 0; j < nr; ++j) res[S.slot_row[s][j] * rows_per_blk + ml] = acc[j];
+      for (int j = 0; j < kDecodeMaxTokens; ++j) acc[j] = 0.f;
+#pragma unroll
+      for (int q = 0; q < kSlots; ++q) {
+        const int ip = its < kSlots ? its : kSlots;
+        const int qp = q / ip, it = q - qp * ip;
+        const int v = sub + L * it;
+        if (qp == pss && it < its && live && v < ivec) {
+#pragma unroll
+          for (int j = 0; j < kDecodeMaxTokens; ++j)
+            if (j < nr) acc[j] = dot32_f(c[q], sv[q], bv[q], hs + (S.slot_row[s][j] * ivec + v) * kDecPad, acc[j]);
+        }
+      }
+      // more 16-byte loads than one batch holds (I > 2048): finish the row directly
+      for (int it = kSlots; it < its; ++it) {
+        const int v = sub + L * it;
+        if (live && v < ivec) {
+          const int e = S.slot_e[s];
+          const bool sh = e == E;
+          const int m = m0 + ml;
+          const uint32_t* codes = sh ? a.dn.s_codes : a.dn.codes + (size_t)e * H * (I / 8);
+          const uint16_t* sc = sh ? a.dn.s_scales : a.dn.scales + (size_t)e * H * igpr;
+          const uint16_t* bi = sh ? a.dn.s_biases : a.dn.biases + (size_t)e * H * igpr;
+          const uint4 cc = *reinterpret_cast<const uint4*>(codes + (size_t)m * (I / 8) + 4 * v);
+          const float s1 = bf16_bits_to_f32(sc[(size_t)m * igpr + v / 2]);
+          const float b1 = bf16_bits_to_f32(bi[(size_t)m * igpr + v / 2]);
+#pragma unroll
+          for (int j = 0; j < kDecodeMaxTokens; ++j)
+            if (j < nr) acc[j] = dot32_f(cc, s1, b1, hs + (S.slot_row[s][j] * ivec + v) * kDecPad, acc[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kDecodeMaxTokens; ++j)
+        for (int off = L >> 1; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
+      if (live && sub == 0)
+        for (int j = 0; j < nr; ++j) res[S.slot_row[s][j] * rows_per_blk + ml] = acc[j];
+    }
   }
   __syncthreads();
   for (int i = tid; i < T * mrows; i += kDecThreads) {

@@ -73,27 +73,40 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
 #pragma unroll
   for (int j = 0; j < kRouterTokens; ++j) acc[j] = 0.f;
 
-  for (int v = lane; v < vec_per_row; v += 32) {
-    const uint4 w4 = ldg_nc_v4(row + (size_t)v * 8);
-    const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-    float wf[8];
+  // All of this warp's weight loads of a batch are issued before any use, so
+  // the row costs one memory round trip (8 x 16 B per lane covers H = 2048).
+  constexpr int kBatch = 8;
+  for (int v0 = lane; v0 < vec_per_row; v0 += 32 * kBatch) {
+    uint4 w4[kBatch];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      wf[2 * m] = bf16_bits_to_f32(wv[m] & 0xFFFFu);
-      wf[2 * m + 1] = bf16_bits_to_f32(wv[m] >> 16);
+    for (int u = 0; u < kBatch; ++u) {
+      const int v = v0 + 32 * u;
+      if (v < vec_per_row) w4[u] = ldg_nc_v4(row + (size_t)v * 8);
     }
 #pragma unroll
-    for (int j = 0; j < kRouterTokens; ++j) {
-      if (j < nt) {
-        const uint4 x4 = reinterpret_cast<const uint4*>(xs)[j * vec_per_row + v];
-        const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
-        float a = acc[j];
+    for (int u = 0; u < kBatch; ++u) {
+      const int v = v0 + 32 * u;
+      if (v >= vec_per_row) break;
+      const uint32_t wv[4] = {w4[u].x, w4[u].y, w4[u].z, w4[u].w};
+      float wf[8];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          a = fmaf(wf[2 * m], bf16_bits_to_f32(xv[m] & 0xFFFFu), a);
-          a = fmaf(wf[2 * m + 1], bf16_bits_to_f32(xv[m] >> 16), a);
+      for (int m = 0; m < 4; ++m) {
+        wf[2 * m] = bf16_bits_to_f32(wv[m] & 0xFFFFu);
+        wf[2 * m + 1] = bf16_bits_to_f32(wv[m] >> 16);
+      }
+#pragma unroll
+      for (int j = 0; j < kRouterTokens; ++j) {
+        if (j < nt) {
+          const uint4 x4 = reinterpret_cast<const uint4*>(xs)[j * vec_per_row + v];
+          const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
+          float a = acc[j];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            a = fmaf(wf[2 * m], bf16_bits_to_f32(xv[m] & 0xFFFFu), a);
+            a = fmaf(wf[2 * m + 1], bf16_bits_to_f32(xv[m] >> 16), a);
+          }
+          acc[j] = a;
         }
-        acc[j] = a;
       }
     }
   }

@@ -182,8 +182,8 @@ typedef enum moe_expert_path {
   MOE_PATH_AUTO = 0,        /* fused decode for T <= 4, tensor cores for T >= 64 when the
                                shape allows, else GEMV */
   MOE_PATH_GEMV = 1,        /* bandwidth-bound grouped GEMV (CUDA cores), any shape */
-  MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 512 == 0, I % 128 == 0 and
-                               (I/64) * block_m * 128 <= 131072 (else UNSUPPORTED_SHAPE) */
+  MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 256 == 0 and I % 128 == 0
+                               (else UNSUPPORTED_SHAPE) */
   MOE_PATH_FUSED_DECODE = 3 /* router kernel + one fused kernel for top-k, tables, expert
                                GEMVs and combine; T <= 4 (else UNSUPPORTED_SHAPE). Its
                                events[2] == events[1] and events[4..5] == events[3] */
