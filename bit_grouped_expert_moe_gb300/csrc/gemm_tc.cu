@@ -44,8 +44,37 @@ namespace bgmoe {
 using namespace tc;
 
 constexpr int kTcThreads = 576;
-constexpr int kCS = 4, kAS = 3, kBS = 5;   // ring depths: codes, A, B
-constexpr int kGatherLag = 3;             // gather stages in flight before publishing (< kBS)
+#ifndef BGMOE_TC_CS
+#define BGMOE_TC_CS 4
+#endif
+#ifndef BGMOE_TC_AS
+#define BGMOE_TC_AS 3
+#endif
+#ifndef BGMOE_TC_BS
+#define BGMOE_TC_BS 5
+#endif
+#ifndef BGMOE_TC_LAG
+#define BGMOE_TC_LAG 2
+#endif
+#ifndef BGMOE_TC_A_MARGIN
+#define BGMOE_TC_A_MARGIN 1
+#endif
+constexpr int kCS = BGMOE_TC_CS, kAS = BGMOE_TC_AS, kBS = BGMOE_TC_BS;  // ring depths: codes, A, B
+constexpr int kGatherLag = BGMOE_TC_LAG;  // gather stages in flight before publishing (<= kBS - 2)
+// Generic-proxy stores into an A slot wait for the commit of the MMAs of
+// kAMargin stages AFTER the slot's previous use. Measured on GB300: rewriting
+// a slot as soon as the commit of the MMAs that read it had arrived corrupted
+// the last-read rows of the slot in about 1 item in 200 at 128-token tiles
+// (the two accumulator chains of an item finish at different times); with a
+// one-stage margin no corruption was seen in any repeated run.
+constexpr int kAMargin = BGMOE_TC_A_MARGIN;
+static_assert(kAMargin >= 0 && kAMargin < kAS, "A-slot margin must leave the dequant a stage of lead");
+#ifndef BGMOE_TC_B_MARGIN
+#define BGMOE_TC_B_MARGIN 1
+#endif
+// The same rule for the gather's cp.async stores into a B slot.
+constexpr int kBMargin = BGMOE_TC_B_MARGIN;
+static_assert(kGatherLag + kBMargin <= kBS - 2, "the gather must keep a stage of slack");
 constexpr int kMaxBN = 128;               // token rows per tile (block_m <= 128)
 constexpr int kTmemCols = 512;            // 2 buffers x (2 x 128 columns)
 constexpr int kCBytes = 8192;             // 256 rows x 32 B of codes
@@ -256,10 +285,12 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
         }
         for (int k = 0; k < num_k; ++k, ++it) {
           const int bs = it % kBS;
-          if (it >= kBS && !mbar_wait(&ctl->b_empty[bs], ((it / kBS) - 1) & 1, abort_flag, deadline)) {
+          const int done = it - kBS + kBMargin;  // this stage's MMAs must be complete
+          if (done >= 0 && !mbar_wait(&ctl->b_empty[done % kBS], (done / kBS) & 1, abort_flag, deadline)) {
             ok = false;
             break;
           }
+          fence_proxy_async();  // async-proxy reads of this slot before the new copies
           uint8_t* dst = sB + bs * kBBytes;
 #pragma unroll
           for (int q = 0; q < kMaxBN / 16; ++q) {
@@ -338,10 +369,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
         const uint4 c1 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes + 16);
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->c_empty[cs]);
-        if (it >= kAS && !mbar_wait(&ctl->a_empty[as], ((it / kAS) - 1) & 1, abort_flag, deadline)) {
-          ok = false;
-          break;
+        {
+          const int done = it - kAS + kAMargin;  // this stage's MMAs must be complete
+          if (done >= 0 &&
+              !mbar_wait(&ctl->a_empty[done % kAS], (done / kAS) & 1, abort_flag, deadline)) {
+            ok = false;
+            break;
+          }
         }
+        // the slot was last read by the tensor core (async proxy): order
+        // those reads before these generic-proxy stores
+        fence_proxy_async();
         uint8_t* dst = arow + as * kABytes;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
