@@ -76,7 +76,6 @@ struct Workspace {
   int32_t* tile_rows;
   int32_t* num_tiles;
   uint16_t* x16;              // [T][H] fp16 activations for the tensor-core path
-  float* h32;                 // [rows][I] fp32 h of the fused decode path (T <= 4 only)
   unsigned int* bar;          // grid-barrier counter of the fused decode kernel
   __half* h;                  // [rows][I]
   __half* o;                  // [rows][H]
@@ -107,7 +106,6 @@ Workspace carve(const Geometry& g, void* base) {
   w.tile_rows = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
   w.num_tiles = static_cast<int32_t*>(take(sizeof(int32_t)));
   w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)g.T * g.H));
-  w.h32 = static_cast<float*>(take(g.T <= kDecodeMaxTokens ? sizeof(float) * (size_t)g.rows * g.I : 0));
   w.bar = static_cast<unsigned int*>(take(sizeof(unsigned int)));
   w.h = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.I));
   w.o = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.H));
@@ -307,7 +305,12 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
 
   // Expert path: the fused decode kernel for decode-sized calls, tensor
   // cores once the tile rows are many enough to feed them, else the GEMV.
-  const bool dec_ok = decode_supported(g);
+  // The fused decode kernel copies weight tiles with bulk async copies, which
+  // need 16-byte aligned sources.
+  auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  auto mat16 = [&](const moe_qmat& q) { return a16(q.codes) && a16(q.scales) && a16(q.biases); };
+  const bool dec_ok = decode_supported(g) && mat16(experts->gate_up) && mat16(experts->down) &&
+                      (!g.shared || (mat16(shared->gate_up) && mat16(shared->down)));
   if (expert_path == MOE_PATH_FUSED_DECODE && !dec_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   const bool fused = expert_path == MOE_PATH_FUSED_DECODE || (expert_path == MOE_PATH_AUTO && dec_ok);
   const bool tc_ok = tc_path_supported(g);
@@ -348,7 +351,7 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
     d.tile_rows = r.tile_rows;
     d.num_tiles = r.num_tiles;
     d.status = r.status;
-    d.h = w.h32;
+    d.h = w.h;
     d.y = y;
     d.bar = w.bar;
     d.timeout_ns = kDefaultTimeoutNs;

@@ -67,10 +67,12 @@ __device__ __forceinline__ bool device_failed(const int32_t* status) {
 
 // Raises a kernel's dynamic shared-memory limit to `bytes` the first time a
 // launch needs it (the value is cached, so launches inside a CUDA-graph
-// capture make no attribute call once a first, uncaptured call has run).
+// capture make no attribute call once a first, uncaptured call has run). The
+// default limit is 48 KB minus the kernel's static shared memory, so even a
+// small request is raised once.
 template <typename Kernel>
 inline cudaError_t ensure_smem(Kernel k, size_t bytes, int* configured) {
-  if (bytes <= 48 * 1024 || (int)bytes <= *configured) return cudaSuccess;
+  if (bytes == 0 || (int)bytes <= *configured) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess) *configured = (int)bytes;
   return e;

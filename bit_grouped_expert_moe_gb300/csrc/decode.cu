@@ -7,42 +7,75 @@
 // Apple silicon", "Decode optimisations", kernel fusion: chains of kernels
 // fused so intermediates stay on chip.]
 //
-// One block per SM, every block resident. Phases:
-//   0  before the router finishes (programmatic dependent launch): warps
-//      that will compute a column of the shared expert issue its weight loads
-//      (the shared expert does not depend on routing);
-//   1  every block selects the top-k experts of the T tokens itself (T * 257
-//      logits); block 0 also writes the routing tables. Each block prefetches
-//      into L2 the down-projection rows it will need in phase 3, then warps
-//      compute gate/up units (one expert, one h column: two weight rows) for
-//      the shared expert and every distinct routed expert: h fp32 [A+T][I];
-//   2  one grid barrier (counter cleared by the router kernel, bounded wait);
-//   3  each block owns a slice of output columns m: for every expert in use
-//      it dots W_down[m] with that expert's h rows, then forms
-//      y[t][m] = sum_k w[t,k] o[t,k][m] + g[t] o_shared[t][m] in that fixed
-//      order, so o never leaves the SM.
+// Weights stream through a ring of shared-memory stages filled by bulk async
+// copies (cp.async.bulk, completion counted on an mbarrier), so a block keeps
+// up to `stages` tiles in flight whatever the compute between them does. One
+// ring item is either
+//   a gate/up unit: expert slot s, h columns n0..n0+7 -> gate rows n0..n0+7
+//     and up rows I+n0..I+n0+7 with their scales and biases (9H bytes), or
+//   a down item: rows m0..m0+15 of W_down for up to `per_item` slots.
+// The products run on mma.sync.m16n8k16 (fp16 operands, fp32 accumulation):
+// 16 weight rows x 8 token columns per instruction. In a gate/up unit the 16
+// MMA rows are the 8 gate rows then the 8 up rows, so the lane that holds
+// gate(n, j) also holds up(n, j). Each lane dequantises whole code words into
+// A fragments; one word unpacks as the pairs (k0,k4), (k1,k5), (k2,k6),
+// (k3,k7), so the activations are kept in that K order inside every group of
+// 8 (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte shared-memory load.
+//
+// One block per SM, every block resident: 16 consumer warps and one producer
+// warp whose lane 0 issues the copies (kept out of the consumer warps: a lane
+// issuing while its warp-mates wait on an mbarrier is held up by them).
+// Phases:
+//   0  before the router finishes (programmatic dependent launch): x is
+//      staged as fp16 and a block whose first unit belongs to the shared
+//      expert (which every token uses) starts its copy;
+//   1  every block selects the top-k experts of the T tokens itself and
+//      derives the expert slots; from here the producer fills the ring as
+//      the consumers release stages (one "empty" mbarrier per stage);
+//   2  gate/up units: the 16 warps split K, the partial sums of unit i are
+//      added in a fixed order by warp i % 16 while the others go on, and
+//      h = w * silu(gate) * up (the token's routing weight, or the shared
+//      gate, folded in) goes to global memory as fp16;
+//   3  one grid barrier (counter cleared by the router kernel, bounded wait);
+//   4  block b owns output rows 16b..16b+15: with the weights folded into h,
+//      y[t][m] = sum over slots of W_down[m] . h_slot,t, so every warp keeps one
+//      accumulator over its (slot, K block) tasks and the 16 accumulators are
+//      added in a fixed order at the end. The last block writes the routing
+//      tables.
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace bgmoe {
 
-constexpr int kDecThreads = 512;
-constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kDecWarps = 16;                        // consumer warps
+constexpr int kDecConsumers = kDecWarps * 32;
+constexpr int kDecThreads = kDecConsumers + 32;      // + the producer warp
 constexpr int kDecMaxA = kDecodeMaxTokens * kMaxTopK;
 constexpr int kDecMaxSlots = kDecMaxA + 1;
-constexpr int kDecPad = 36;                 // floats per staged 32-value chunk
 
 struct DecodeSmall {
   int ids[kDecMaxA];
   float w[kDecMaxA];
   float g[kDecodeMaxTokens];
-  int pos[kDecMaxA];                        // expert-sorted position of assignment a
-  int first[kDecMaxA];
-  int slot_e[kDecMaxSlots];                 // expert of each slot (slot 0 = shared when present)
-  int slot_n[kDecMaxSlots];                 // rows of the slot
+  int pos[kDecMaxA];                             // expert-sorted position of assignment a
+  int slot_e[kDecMaxSlots];                      // expert of each slot (slot 0 = shared when present)
+  int slot_n[kDecMaxSlots];                      // rows (tokens) of the slot
   int slot_row[kDecMaxSlots][kDecodeMaxTokens];
   int slot_tok[kDecMaxSlots][kDecodeMaxTokens];
+  float slot_w[kDecMaxSlots][kDecodeMaxTokens];  // routing weight (shared slot: gate) of each slot row
+  int tok_row[kDecMaxSlots][kDecodeMaxTokens];   // h row of (slot, token), -1 if the token skips it
+  const uint8_t* slot_src[kDecMaxSlots][6];     // gate/up codes, scales, biases; down codes, scales, biases
+  float zero_row[kMaxExperts + 1];               // warm-up input of the top-k
+  int warm_ids[kMaxTopK];
+  float warm_w[kMaxTopK];
+  float warm_g[kDecodeMaxTokens];
   int nslots;
-  int failed;
+  int status_in;
+  int failed;    // consumer abort flag (a stage or grid-barrier wait ran out)
+  int pfail;     // producer abort flag (kept apart: consumers branch on `failed` only)
+  uint64_t full[kDecodeMaxStages];               // stage filled (bulk-copy bytes landed)
+  uint64_t empty[kDecodeMaxStages];              // stage released by all consumer warps
+  float part[2][kDecWarps][4][32];               // per-warp MMA partials: [item parity][warp][reg][lane]
 };
 
 __device__ __forceinline__ float dec_key_to_float(uint32_t k) {
@@ -52,207 +85,425 @@ __device__ __forceinline__ float dec_key_to_float(uint32_t k) {
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-// 32 weights of one 16-byte code chunk against a staged fp32 activation chunk
-__device__ __forceinline__ float dot32_f(const uint4 c, float s, float b, const float* xr, float acc) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float4 x0 = *reinterpret_cast<const float4*>(xr + 8 * m);
-    const float4 x1 = *reinterpret_cast<const float4*>(xr + 8 * m + 4);
-    const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc = fmaf(fmaf(s, (float)((w[m] >> (4 * q)) & 15u), b), xv[q], acc);
-  }
-  return acc;
+// Bulk async copy global -> this CTA's shared memory, completion counted in
+// bytes on `bar` (both addresses and the size multiples of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   tc::smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
+               : "memory");
 }
 
-template <int kDecMaxIt>  // 16-byte loads per lane per gate/up row: ceil(H / 1024)
+// d += A * B with A 16x16 (row), B 16x8 (col), fp16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ __half2 bf16_h2(uint16_t bits16) {
+  const __half h = __float2half_rn(bf16_bits_to_f32(bits16));
+  return __halves2half2(h, h);
+}
+
+// The 32 K of one lane's 16-byte code chunk for its two rows (fragment rows g
+// and g+8) against the matching B fragments xb[w] (permuted activations,
+// 8 K per 16-byte word): 8 MMAs. With g = lane / 4 and c = lane % 4, MMA k
+// slots 2c, 2c+1, 2c+8, 2c+9 of word w hold K offsets 8w + {0,4}, {1,5} (first
+// MMA) and 8w + {2,6}, {3,7} (second), on A and B alike.
+__device__ __forceinline__ void mma_chunk(float (&d)[4], const uint4& r0, const uint4& r1, __half2 s0, __half2 b0,
+                                          __half2 s1, __half2 b1, const uint4 (&xb)[4]) {
+  const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint32_t p0[4], p1[4];
+    tc::dequant8_f16(w0[w], s0, b0, p0);
+    tc::dequant8_f16(w1[w], s1, b1, p1);
+    mma_16816(d, p0[0], p1[0], p0[1], p1[1], xb[w].x, xb[w].y);
+    mma_16816(d, p0[2], p1[2], p0[3], p1[3], xb[w].z, xb[w].w);
+  }
+}
+
+__device__ __forceinline__ void load_b(uint4 (&xb)[4], const __half* row, bool live) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w)
+    xb[w] = live ? *reinterpret_cast<const uint4*>(row + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Top-k of one token by one warp: ids (best first), renormalised softmax
+// weights and the shared-expert gate. Keys are fp32 order keys (0 marks an
+// empty or taken entry; a finite logit never maps to 0). Each lane keeps the
+// best of its own 8 entries; a round takes the warp maximum and, among lanes
+// holding it, the lowest expert index, so equal logits go to the lower index.
+// Not inlined: the kernel runs it once on a dummy row first (see phase 0).
+__device__ __noinline__ void select_experts(const float* lrow, const float* bias, int E, int K, int shared, int lane,
+                                            int* ids_out, float* w_out, float* g_out) {
+  const float gate_logit = shared ? lrow[E] : 0.f;
+  uint32_t key[kMaxExperts / 32];
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) {
+    const int e = lane + 32 * j;
+    key[j] = e < E ? float_order_key(lrow[e] + (bias ? bias[e] : 0.f)) : 0u;
+  }
+  uint32_t lb = 0u;
+  int lbj = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j)
+    if (key[j] > lb) {
+      lb = key[j];
+      lbj = j;
+    }
+  uint32_t my_key = 0u, top_key = 0u;
+  int my_e = 0;
+  for (int k = 0; k < K; ++k) {
+    const uint32_t M = __reduce_max_sync(0xffffffffu, lb);
+    const uint32_t ew = __reduce_min_sync(0xffffffffu, lb == M ? (uint32_t)(lane + 32 * lbj) : 0xFFFFFFFFu);
+    if (k == 0) top_key = M;
+    if (lane == k) {
+      my_key = M;
+      my_e = (int)ew;
+    }
+    if (lane == (int)(ew & 31u)) {
+      const int jr = (int)(ew >> 5);
+      lb = 0u;
+      lbj = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j) {
+        if (j == jr) key[j] = 0u;
+        if (key[j] > lb) {
+          lb = key[j];
+          lbj = j;
+        }
+      }
+    }
+  }
+  // weights: exp(v_k - v_0) / sum over the selected (lanes k < K in parallel)
+  const float z = lane < K ? expf(dec_key_to_float(my_key) - dec_key_to_float(top_key)) : 0.f;
+  float sum = z;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane < K) {
+    ids_out[lane] = my_e;
+    w_out[lane] = z / sum;
+  }
+  if (lane == 0) *g_out = shared ? 1.f / (1.f + expf(-gate_logit)) : 0.f;
+}
+
+// Named barrier of the 16 consumer warps (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDecConsumers) : "memory");
+}
+
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(16) float dsm[];
+  extern __shared__ __align__(128) uint8_t dsm_raw[];
   __shared__ DecodeSmall S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool producer = warp == kDecWarps;
+  const int g8 = lane >> 2, c4 = lane & 3;  // fragment coordinates
   const int T = a.T, H = a.H, I = a.I, E = a.E, K = a.K;
   const int A = T * K;
-  const int G = gridDim.x;
-  const int gw = blockIdx.x * kDecWarps + warp, nw = G * kDecWarps;
-  const int nvec = H / 32, gpr = H / kGroup;
-  const int shared_units = a.shared ? I : 0;
+  const int G = gridDim.x, b = blockIdx.x;
+  const int gpr = H / kGroup, igpr = I / kGroup;
+  const int NST = a.stages;
+  const int cpb = I / 8;             // gate/up units per slot
+  const int mblocks = H / 16;        // blocks with output rows
+  const int m0 = b * 16;
+  const int kbs = I / 128, nkb = H / 128;
+  const int per_item = a.per_item;   // down slots per ring item
+  const size_t stage_bytes = (size_t)a.stage_bytes;
+  __half* xs = reinterpret_cast<__half*>(dsm_raw);  // phases 0-2: x16 [T][H]; phase 4: h [R][I]
+  uint8_t* ring = dsm_raw + a.ring_offset;
+  const uint64_t deadline0 = global_timer_ns() + (uint64_t)a.timeout_ns;
 
-  // ---- phase 0: the shared expert's weight rows of this warp's first unit
-  uint4 pc_g[kDecMaxIt], pc_u[kDecMaxIt];
-  float ps_g[kDecMaxIt], pb_g[kDecMaxIt], ps_u[kDecMaxIt], pb_u[kDecMaxIt];
-  const bool pre = gw < shared_units;
-  if (pre) {
-    const int n = gw;
-#pragma unroll
-    for (int it = 0; it < kDecMaxIt; ++it) {
-      const int v = lane + 32 * it;
-      if (v < nvec) {
-        pc_g[it] = ldg_nc_v4(a.gu.s_codes + (size_t)n * (H / 8) + 4 * v);
-        pc_u[it] = ldg_nc_v4(a.gu.s_codes + (size_t)(I + n) * (H / 8) + 4 * v);
-        ps_g[it] = bf16_bits_to_f32(__ldg(a.gu.s_scales + (size_t)n * gpr + v / 2));
-        pb_g[it] = bf16_bits_to_f32(__ldg(a.gu.s_biases + (size_t)n * gpr + v / 2));
-        ps_u[it] = bf16_bits_to_f32(__ldg(a.gu.s_scales + (size_t)(I + n) * gpr + v / 2));
-        pb_u[it] = bf16_bits_to_f32(__ldg(a.gu.s_biases + (size_t)(I + n) * gpr + v / 2));
+  // ---- ring producer (the producer warp): item i -> stage i % NST. Lane 0
+  // posts the expected bytes, then each copy of the item is issued by its own
+  // lane, so the warp spends one instruction stream on all of them.
+  int n2 = 0;  // gate/up units of this block (known after routing); down items follow them
+  const uint32_t gcb = 8u * (H / 2), gsb = 8u * gpr * 2;        // gate/up unit: 8 code rows / scale rows
+  const uint32_t dcb = 16u * (I / 2), dsb = 16u * igpr * 2;     // down item: 16 code rows / scale rows per slot
+  auto issue = [&](int i, int nslots) {  // called by all 32 lanes of the producer warp
+    const int st = i % NST;
+    uint8_t* dst = ring + (size_t)st * stage_bytes;
+    uint64_t* bar = &S.full[st];
+    if (nslots < 0 || i < n2) {  // gate/up unit (nslots < 0: the shared unit issued before routing)
+      const int u = b + i * G;
+      const int s = u / cpb, n0 = (u - s * cpb) * 8;
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar, 2 * gcb + 4 * gsb);
+      __syncwarp();
+      if (lane < 6) {
+        const int kind = lane >> 1, up = lane & 1;  // codes / scales / biases, gate / up
+        const uint8_t* base;
+        if (nslots < 0)
+          base = kind == 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_codes)
+                           : reinterpret_cast<const uint8_t*>(kind == 1 ? a.gu.s_scales : a.gu.s_biases);
+        else
+          base = S.slot_src[s][kind];
+        const size_t row = (size_t)(up ? I + n0 : n0);
+        const uint32_t bytes = kind == 0 ? gcb : gsb;
+        const size_t row_bytes = kind == 0 ? (size_t)(H / 2) : (size_t)gpr * 2;
+        const uint32_t off = kind == 0 ? up * gcb : 2 * gcb + (2 * (kind - 1) + up) * gsb;
+        bulk_g2s(dst + off, base + row * row_bytes, bytes, bar);
+      }
+    } else {  // down item: rows m0..m0+15 of slots p0..p0+np-1
+      const int p0 = (i - n2) * per_item;
+      const int np = min(per_item, nslots - p0);
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)np * (dcb + 2 * dsb));
+      __syncwarp();
+      for (int c = lane; c < 3 * np; c += 32) {
+        const int p = c / 3, kind = c - 3 * p;
+        const uint8_t* base = S.slot_src[p0 + p][3 + kind];
+        const size_t row_bytes = kind == 0 ? (size_t)(I / 2) : (size_t)igpr * 2;
+        const uint32_t off = (uint32_t)p * (dcb + 2 * dsb) + (kind == 0 ? 0u : dcb + (kind - 1) * dsb);
+        bulk_g2s(dst + off, base + (size_t)m0 * row_bytes, kind == 0 ? dcb : dsb, bar);
       }
     }
-  }
-  grid_dep_wait();  // the router kernel (logits, cleared barrier) is complete
-  if (device_failed(a.status)) return;
+  };
+  int issued = 0;  // items issued so far (producer warp)
+  // Waits (bounded) until the last copy of every stage has landed, so the
+  // block never exits with copies into its shared memory in flight.
+  auto drain = [&]() {
+    for (int i = issued > NST ? issued - NST : 0; i < issued; ++i) {
+      const uint64_t dl = global_timer_ns() + (uint64_t)a.timeout_ns;
+      while (!tc::mbar_try_wait(&S.full[i % NST], (uint32_t)((i / NST) & 1)))
+        if (global_timer_ns() > dl) break;
+    }
+  };
 
-  // ---- phase 1a: stage x (fp32, padded chunks) and select the top-k
-  float* xs = dsm;  // [T][H/32][kDecPad]
-  {
-    const int xvec = T * H / 8;  // 16-byte chunks of x; all loads of a batch before any store
-    for (int i0 = tid; i0 < xvec; i0 += 2 * kDecThreads) {
-      uint4 v[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u * kDecThreads;
-        if (i < xvec) v[u] = ldg_nc_v4(a.x + (size_t)i * 8);
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int i = i0 + u * kDecThreads;
-        if (i < xvec) {
-          const int t = (i * 8) / H, k = i * 8 - t * H;
-          float* d = xs + (t * nvec + (k >> 5)) * kDecPad + (k & 31);
-          const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-          *reinterpret_cast<float4*>(d) = make_float4(bf16_bits_to_f32(w[0] & 0xFFFFu), bf16_bits_to_f32(w[0] >> 16),
-                                                      bf16_bits_to_f32(w[1] & 0xFFFFu), bf16_bits_to_f32(w[1] >> 16));
-          *reinterpret_cast<float4*>(d + 4) = make_float4(bf16_bits_to_f32(w[2] & 0xFFFFu),
-                                                          bf16_bits_to_f32(w[2] >> 16),
-                                                          bf16_bits_to_f32(w[3] & 0xFFFFu), bf16_bits_to_f32(w[3] >> 16));
-        }
-      }
-    }
-  }
-  if (tid == 0) S.failed = 0;
-  if (warp < T) {
-    const int t = warp;
-    const float* lrow = a.logits + (size_t)t * (E + 1);
-    unsigned long long key[kMaxExperts / 32];
-#pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = 0ull;
-      if (e < E) {
-        const float v = lrow[e] + (a.bias ? a.bias[e] : 0.f);
-        key[j] = ((unsigned long long)float_order_key(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-      }
-    }
-    float sel_v[kMaxTopK];
-#pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-      if (k < K) {
-        unsigned long long best = key[0];
-#pragma unroll
-        for (int j = 1; j < kMaxExperts / 32; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-          best = other > best ? other : best;
-        }
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)best);
-        sel_v[k] = dec_key_to_float((uint32_t)(best >> 32));
-        if (lane == 0) S.ids[t * K + k] = e;
-#pragma unroll
-        for (int j = 0; j < kMaxExperts / 32; ++j)
-          if (lane == (e & 31) && j == (e >> 5)) key[j] = 0ull;
-      }
-    }
+  // ---- phase 0: barriers, x as fp16 in the permuted K order, the shared unit
+  if (producer) {
     if (lane == 0) {
-      float z[kMaxTopK], sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < kMaxTopK; ++k)
-        if (k < K) {
-          z[k] = expf(sel_v[k] - sel_v[0]);
-          sum += z[k];
-        }
-#pragma unroll
-      for (int k = 0; k < kMaxTopK; ++k)
-        if (k < K) S.w[t * K + k] = z[k] / sum;
-      S.g[t] = a.shared ? 1.f / (1.f + expf(-lrow[E])) : 0.f;
+      for (int st = 0; st < NST; ++st) {
+        tc::mbar_init(&S.full[st], 1);
+        tc::mbar_init(&S.empty[st], kDecWarps);
+      }
+      tc::fence_barrier_init();
+      S.failed = 0;
+      S.pfail = 0;
+    }
+    __syncwarp();
+    if (a.shared && b < cpb) {  // this block's first unit belongs to the shared expert
+      issue(0, -1);
+      issued = 1;
     }
   }
-  __syncthreads();
+  for (int i = tid; i < kDecMaxSlots * kDecodeMaxTokens; i += kDecThreads) (&S.tok_row[0][0])[i] = -1;
+  for (int i = tid; i < T * H / 8; i += kDecThreads) {
+    const uint4 v = ldg_nc_v4(a.x + (size_t)i * 8);
+    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      f[2 * q] = bf16_bits_to_f32(wv[q] & 0xFFFFu);
+      f[2 * q + 1] = bf16_bits_to_f32(wv[q] >> 16);
+    }
+    const __half2 p0 = __floats2half2_rn(f[0], f[4]), p1 = __floats2half2_rn(f[1], f[5]);
+    const __half2 p2 = __floats2half2_rn(f[2], f[6]), p3 = __floats2half2_rn(f[3], f[7]);
+    uint4 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&p0);
+    o.y = *reinterpret_cast<const uint32_t*>(&p1);
+    o.z = *reinterpret_cast<const uint32_t*>(&p2);
+    o.w = *reinterpret_cast<const uint32_t*>(&p3);
+    reinterpret_cast<uint4*>(xs)[i] = o;
+  }
 
-  // ---- phase 1b: expert-sorted positions and the slots (distinct experts)
-  if (tid < A) {
-    const int e = S.ids[tid];
-    int fst = 1;
-    for (int b = 0; b < tid; ++b) fst &= (S.ids[b] != e);
-    S.first[tid] = fst;
+  // Run the top-k once on a row of zeros while the router is still working:
+  // it is straight-line code met once per launch, and this brings it into
+  // the instruction cache before the real call.
+  if (warp < T) {
+    for (int i = lane; i <= E; i += 32) S.zero_row[i] = 0.f;
+    __syncwarp();
+    select_experts(S.zero_row, nullptr, E, K, a.shared, lane, S.warm_ids, S.warm_w, S.warm_g + warp);
   }
+
+  grid_dep_wait();  // the router kernel (logits, cleared barrier, status) is complete
+  if (tid == 0) S.status_in = *reinterpret_cast<const volatile int32_t*>(a.status);
+
+  // ---- phase 1a: top-k, renormalised weights, shared gate (warp per token)
+  if (warp < T) select_experts(a.logits + (size_t)warp * (E + 1), a.bias, E, K, a.shared, lane, S.ids + warp * K,
+                               S.w + warp * K, S.g + warp);
   __syncthreads();
-  if (tid < A) {
-    const int e = S.ids[tid];
-    int lt = 0, before = 0, dlt = 0;
-    for (int b = 0; b < A; ++b) {
-      const int eb = S.ids[b];
-      lt += eb < e;
-      before += (b < tid) & (eb == e);
-      dlt += (eb < e) & S.first[b];
+  if (S.status_in != 0) {  // an earlier kernel of this call failed
+    if (producer && lane == 0) drain();
+    return;
+  }
+
+  // ---- phase 1b: expert-sorted positions and slots (one lane per assignment)
+  if (warp == 0) {
+    const bool live = lane < A;
+    const int e = live ? S.ids[lane] : kMaxExperts + 1;
+    const unsigned same = __match_any_sync(0xffffffffu, e) & __ballot_sync(0xffffffffu, live);
+    const int before = __popc(same & lanemask_lt());  // earlier assignments of the same expert
+    const bool first = live && before == 0;
+    int lt = 0, dlt = 0;  // assignments / distinct experts with a lower index
+    for (int q = 0; q < A; ++q) {
+      const int vq = __shfl_sync(0xffffffffu, 2 * e + (first ? 1 : 0), q);
+      const int lower = (vq >> 1) < e;
+      lt += lower;
+      dlt += lower & vq;
     }
-    S.pos[tid] = lt + before;
-    const int slot = dlt + (a.shared ? 1 : 0);
-    S.slot_row[slot][before] = lt + before;
-    S.slot_tok[slot][before] = tid / K;
-    if (S.first[tid]) S.slot_e[slot] = e;
-    if (S.first[tid]) {
-      int n = 0;
-      for (int b = 0; b < A; ++b) n += S.ids[b] == e;
-      S.slot_n[slot] = n;
+    const int sh = a.shared ? 1 : 0;
+    if (live) {
+      const int slot = dlt + sh, tok = lane / K;
+      S.pos[lane] = lt + before;
+      S.slot_row[slot][before] = lt + before;
+      S.slot_tok[slot][before] = tok;
+      S.slot_w[slot][before] = S.w[lane];
+      S.tok_row[slot][tok] = lt + before;
+      if (first) {
+        S.slot_e[slot] = e;
+        S.slot_n[slot] = __popc(same);
+      }
+    }
+    const int d = __popc(__ballot_sync(0xffffffffu, first));
+    if (lane == 0) {
+      S.nslots = d + sh;
+      if (sh) {
+        S.slot_e[0] = E;
+        S.slot_n[0] = T;
+      }
+    }
+    if (sh && lane < T) {
+      S.slot_row[0][lane] = A + lane;
+      S.slot_tok[0][lane] = lane;
+      S.slot_w[0][lane] = S.g[lane];
+      S.tok_row[0][lane] = A + lane;
+    }
+    __syncwarp();
+    // weight addresses of every slot, for the producer
+    const int ns = d + sh;
+    for (int q = lane; q < ns; q += 32) {
+      const int ex = S.slot_e[q];
+      const bool shq = ex == E;
+      S.slot_src[q][0] = reinterpret_cast<const uint8_t*>(shq ? a.gu.s_codes : a.gu.codes + (size_t)ex * 2 * I * (H / 8));
+      S.slot_src[q][1] = reinterpret_cast<const uint8_t*>(shq ? a.gu.s_scales : a.gu.scales + (size_t)ex * 2 * I * gpr);
+      S.slot_src[q][2] = reinterpret_cast<const uint8_t*>(shq ? a.gu.s_biases : a.gu.biases + (size_t)ex * 2 * I * gpr);
+      S.slot_src[q][3] = reinterpret_cast<const uint8_t*>(shq ? a.dn.s_codes : a.dn.codes + (size_t)ex * H * (I / 8));
+      S.slot_src[q][4] = reinterpret_cast<const uint8_t*>(shq ? a.dn.s_scales : a.dn.scales + (size_t)ex * H * igpr);
+      S.slot_src[q][5] = reinterpret_cast<const uint8_t*>(shq ? a.dn.s_biases : a.dn.biases + (size_t)ex * H * igpr);
     }
   }
-  if (tid == 0) {
-    int d = 0;
-    for (int b = 0; b < A; ++b) d += S.first[b];
-    S.nslots = d + (a.shared ? 1 : 0);
-    if (a.shared) {
-      S.slot_e[0] = E;
-      S.slot_n[0] = T;
-      for (int t = 0; t < T; ++t) {
-        S.slot_row[0][t] = A + t;
-        S.slot_tok[0][t] = t;
+  __syncthreads();  // the last block-wide barrier: from here on the producer runs on its own
+  const int nslots = S.nslots;
+  const int units = nslots * cpb;
+  n2 = units > b ? (units - b + G - 1) / G : 0;
+  const int n4 = b < mblocks ? (nslots + per_item - 1) / per_item : 0;
+  const int items = n2 + n4;
+
+  if (producer) {
+    for (int i = issued; i < items; ++i) {
+      // stage i % NST is free once every consumer warp released item i - NST
+      if (i >= NST && !tc::mbar_wait(&S.empty[i % NST], (uint32_t)((i / NST - 1) & 1), &S.pfail, deadline0))
+        break;
+      issue(i, nslots);
+      issued = i + 1;
+    }
+    if (lane == 0) drain();
+    return;
+  }
+
+  // ---- phase 2: gate/up units (consumer warps)
+  const int R = A + (a.shared ? T : 0);
+  for (int i = 0; i < n2; ++i) {
+    // On a timeout every consumer still runs every iteration (skipping the
+    // math), so all of them pass the same named barriers.
+    const int st = i % NST;
+    const uint8_t* sp = ring + (size_t)st * stage_bytes;
+    const bool ok = tc::mbar_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0);
+    const int u = b + i * G;
+    const int s = u / cpb, n0 = (u - s * cpb) * 8;
+    const int nr = S.slot_n[s];
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if (ok) {
+      const bool col_live = g8 < nr;
+      const __half* xrow = xs + (size_t)(col_live ? S.slot_tok[s][g8] : 0) * H;
+      const uint32_t cb = gcb, sb = gsb;
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sp + 2 * cb);  // gate sc, up sc, gate bi, up bi
+      for (int kb = warp; kb < nkb; kb += kDecWarps) {
+        const int koff = kb * 64 + 16 * c4;  // byte offset of this lane's 32 K inside a code row
+        const int gi = g8 * gpr + 2 * kb + (c4 >> 1);
+        const uint4 cg = *reinterpret_cast<const uint4*>(sp + g8 * (H / 2) + koff);
+        const uint4 cu = *reinterpret_cast<const uint4*>(sp + cb + g8 * (H / 2) + koff);
+        const __half2 sg = bf16_h2(s16[gi]), su = bf16_h2(s16[sb / 2 + gi]);
+        const __half2 bg = bf16_h2(s16[sb + gi]), bu = bf16_h2(s16[3 * sb / 2 + gi]);
+        uint4 xb[4];
+        load_b(xb, xrow + kb * 128 + 32 * c4, col_live);
+        mma_chunk(d, cg, cu, sg, bg, su, bu, xb);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&S.empty[st]);  // this warp is done with the stage
+#pragma unroll
+    for (int r = 0; r < 4; ++r) S.part[i & 1][warp][r][lane] = d[r];
+    consumer_sync();
+    if (ok && warp == i % kDecWarps) {
+      // d0, d1: gate(n0+g, slot rows 2c, 2c+1); d2, d3: up of the same
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w = 0; w < kDecWarps; ++w)  // fixed order: the same bits on every run
+#pragma unroll
+        for (int r = 0; r < 4; ++r) v[r] += S.part[i & 1][w][r][lane];
+      const int pn = tc::perm8_pos(n0 + g8);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = 2 * c4 + q;
+        if (j < nr)
+          a.h[(size_t)S.slot_row[s][j] * I + pn] = __float2half_rn(silu_f32(v[q]) * v[2 + q] * S.slot_w[s][j]);
       }
     }
   }
-  __syncthreads();
-  const int nslots = S.nslots;
 
-  // block 0 publishes the routing outputs (same definitions as moe_route)
-  if (blockIdx.x == 0) {
-    for (int i = tid; i < A; i += kDecThreads) {
+  // ---- phase 3: grid barrier (every block resident; bounded wait)
+  consumer_sync();
+  if (tid == 0) {
+    if (!S.failed) {
+      __threadfence();
+      atomicAdd(a.bar, 1u);
+      while (ld_acquire_u32(a.bar) < (unsigned)G) {
+        if (global_timer_ns() > deadline0) {
+          S.failed = 1;
+          break;
+        }
+        __nanosleep(32);
+      }
+      __threadfence();
+    }
+    if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+  }
+  consumer_sync();
+  if (S.failed) return;  // the producer drains the copies in flight
+
+  // The routing outputs (same definitions as moe_route), written by the last
+  // block: it has no output rows when H / 16 < gridDim.x, so this costs the
+  // layer nothing.
+  if (b == G - 1) {
+    for (int i = tid; i < A; i += kDecConsumers) {
       a.ids[i] = S.ids[i];
       a.weights[i] = S.w[i];
       a.sorted[S.pos[i]] = i;
       a.inv[i] = S.pos[i];
     }
     if (a.shared)
-      for (int t = tid; t < T; t += kDecThreads) a.gate[t] = S.g[t];
-    for (int e = tid; e <= E + 1; e += kDecThreads) {
+      for (int t = tid; t < T; t += kDecConsumers) a.gate[t] = S.g[t];
+    for (int e = tid; e <= E + 1; e += kDecConsumers) {
       int lt = 0, eq = 0;
-      for (int b = 0; b < A; ++b) {
-        lt += S.ids[b] < e;
-        eq += S.ids[b] == e;
+      for (int q = 0; q < A; ++q) {
+        lt += S.ids[q] < e;
+        eq += S.ids[q] == e;
       }
       if (e <= E) a.counts[e] = e < E ? eq : (a.shared ? T : 0);
       a.offsets[e] = e <= E ? lt : A + (a.shared ? T : 0);
     }
     // one tile per expert in use (counts <= T <= 4 < block_m), then the shared tile
     const int d = nslots - (a.shared ? 1 : 0);
-    for (int s = tid; s < d; s += kDecThreads) {
+    for (int s = tid; s < d; s += kDecConsumers) {
       const int slot = s + (a.shared ? 1 : 0);
       a.tile_expert[s] = S.slot_e[slot];
       a.tile_row0[s] = S.slot_row[slot][0];
@@ -267,245 +518,54 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       *a.num_tiles = nslots;
     }
   }
+  if (n4 == 0) return;
 
-  // prefetch into L2 the down rows this block reads in phase 3
-  const int rows_per_blk = (H + G - 1) / G;
-  const int m0 = blockIdx.x * rows_per_blk, m1 = min(H, m0 + rows_per_blk);
-  {
-    const int mrows = max(0, m1 - m0);
-    const int row_bytes = I / 2;
-    const int lines_per_row = (row_bytes + 127) / 128;
-    const int total = nslots * mrows * lines_per_row;
-    for (int i = tid; i < total; i += kDecThreads) {
-      const int s = i / (mrows * lines_per_row), r = i - s * mrows * lines_per_row;
-      const int m = m0 + r / lines_per_row, l = r % lines_per_row;
-      const int e = S.slot_e[s];
-      const uint32_t* codes = e == E ? a.dn.s_codes : a.dn.codes + (size_t)e * H * (I / 8);
-      prefetch_l2(codes + (size_t)m * (I / 8) + l * 32);
-      if (l == 0) {
-        const uint16_t* sc = e == E ? a.dn.s_scales : a.dn.scales + (size_t)e * H * (I / kGroup);
-        const uint16_t* bi = e == E ? a.dn.s_biases : a.dn.biases + (size_t)e * H * (I / kGroup);
-        prefetch_l2(sc + (size_t)m * (I / kGroup));
-        prefetch_l2(bi + (size_t)m * (I / kGroup));
+  // ---- phase 4: W_down rows m0..m0+15 of every slot against the weighted h
+  __half* hs = xs;  // [R][I] (x is no longer needed)
+  for (int i = tid; i < R * I / 8; i += kDecConsumers)
+    reinterpret_cast<uint4*>(hs)[i] = __ldcg(reinterpret_cast<const uint4*>(a.h) + i);
+  consumer_sync();
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows g, g+8 x tokens 2c, 2c+1 over this warp's tasks
+  for (int i = n2; i < items; ++i) {
+    const int st = i % NST;
+    const uint8_t* sp = ring + (size_t)st * stage_bytes;
+    if (tc::mbar_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0)) {
+      const int p0 = (i - n2) * per_item;
+      const int np = min(per_item, nslots - p0);
+      for (int task = warp; task < np * kbs; task += kDecWarps) {
+        const int p = task / kbs, kb = task - p * kbs;
+        const int s = p0 + p;
+        const uint8_t* dp = sp + (size_t)p * (dcb + 2 * dsb);
+        const int koff = kb * 64 + 16 * c4;
+        const int gi = g8 * igpr + 2 * kb + (c4 >> 1), gi8 = gi + 8 * igpr;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(dp + g8 * (I / 2) + koff);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(dp + (g8 + 8) * (I / 2) + koff);
+        const uint16_t* s16 = reinterpret_cast<const uint16_t*>(dp + dcb);  // scales, then biases
+        const __half2 s0 = bf16_h2(s16[gi]), s1 = bf16_h2(s16[gi8]);
+        const __half2 b0 = bf16_h2(s16[dsb / 2 + gi]), b1 = bf16_h2(s16[dsb / 2 + gi8]);
+        const int row = g8 < T ? S.tok_row[s][g8] : -1;  // B column = token
+        uint4 xb[4];
+        load_b(xb, hs + (size_t)(row < 0 ? 0 : row) * I + kb * 128 + 32 * c4, row >= 0);
+        mma_chunk(acc, c0, c1, s0, b0, s1, b1, xb);
       }
     }
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&S.empty[st]);
   }
-
-  // ---- phase 1c: gate/up units (slot, h column n), shared slot first. A warp
-  // takes two units at a time and issues both units' loads before any math.
-  const int units = nslots * I;
-  for (int u0 = gw; u0 < units; u0 += 2 * nw) {
-    uint4 cg[2][kDecMaxIt], cu[2][kDecMaxIt];
-    float sg[2][kDecMaxIt], bg[2][kDecMaxIt], su[2][kDecMaxIt], bu[2][kDecMaxIt];
 #pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int u = u0 + b * nw;
-      if (u >= units) break;
-      const int s = u / I, n = u - s * I;
-      const int e = S.slot_e[s];
-      const bool sh = e == E;
-      const uint32_t* codes = sh ? a.gu.s_codes : a.gu.codes + (size_t)e * 2 * I * (H / 8);
-      const uint16_t* sc = sh ? a.gu.s_scales : a.gu.scales + (size_t)e * 2 * I * gpr;
-      const uint16_t* bi = sh ? a.gu.s_biases : a.gu.biases + (size_t)e * 2 * I * gpr;
-      const bool reuse = pre && u == gw;  // the shared unit loaded in phase 0
-#pragma unroll
-      for (int it = 0; it < kDecMaxIt; ++it) {
-        const int v = lane + 32 * it;
-        if (v < nvec) {
-          if (reuse) {
-            cg[b][it] = pc_g[it];
-            cu[b][it] = pc_u[it];
-            sg[b][it] = ps_g[it];
-            bg[b][it] = pb_g[it];
-            su[b][it] = ps_u[it];
-            bu[b][it] = pb_u[it];
-          } else {
-            cg[b][it] = ldg_nc_v4(codes + (size_t)n * (H / 8) + 4 * v);
-            cu[b][it] = ldg_nc_v4(codes + (size_t)(I + n) * (H / 8) + 4 * v);
-            sg[b][it] = bf16_bits_to_f32(__ldg(sc + (size_t)n * gpr + v / 2));
-            bg[b][it] = bf16_bits_to_f32(__ldg(bi + (size_t)n * gpr + v / 2));
-            su[b][it] = bf16_bits_to_f32(__ldg(sc + (size_t)(I + n) * gpr + v / 2));
-            bu[b][it] = bf16_bits_to_f32(__ldg(bi + (size_t)(I + n) * gpr + v / 2));
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const int u = u0 + b * nw;
-      if (u >= units) break;
-      const int s = u / I, n = u - s * I;
-      const int nr = S.slot_n[s];
-      float ag[kDecodeMaxTokens], au[kDecodeMaxTokens];
-#pragma unroll
-      for (int j = 0; j < kDecodeMaxTokens; ++j) ag[j] = au[j] = 0.f;
-#pragma unroll
-      for (int it = 0; it < kDecMaxIt; ++it) {
-        const int v = lane + 32 * it;
-        if (v < nvec) {
-#pragma unroll
-          for (int j = 0; j < kDecodeMaxTokens; ++j) {
-            if (j < nr) {
-              const float* xr = xs + (S.slot_tok[s][j] * nvec + v) * kDecPad;
-              ag[j] = dot32_f(cg[b][it], sg[b][it], bg[b][it], xr, ag[j]);
-              au[j] = dot32_f(cu[b][it], su[b][it], bu[b][it], xr, au[j]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kDecodeMaxTokens; ++j) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          ag[j] += __shfl_xor_sync(0xffffffffu, ag[j], o);
-          au[j] += __shfl_xor_sync(0xffffffffu, au[j], o);
-        }
-      }
-      if (lane < nr) {
-        float gv = ag[0], uv = au[0];
-#pragma unroll
-        for (int j = 1; j < kDecodeMaxTokens; ++j)
-          if (lane == j) {
-            gv = ag[j];
-            uv = au[j];
-          }
-        a.h[(size_t)S.slot_row[s][lane] * I + n] = silu_f32(gv) * uv;
-      }
-    }
+  for (int r = 0; r < 4; ++r) S.part[0][warp][r][lane] = acc[r];
+  consumer_sync();
+  if (S.failed) {
+    if (tid == 0) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+    return;
   }
-
-  // ---- phase 2: grid barrier (every block resident; bounded wait)
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    atomicAdd(a.bar, 1u);
-    const uint64_t deadline = global_timer_ns() + (uint64_t)a.timeout_ns;
-    while (ld_acquire_u32(a.bar) < (unsigned)G) {
-      if (global_timer_ns() > deadline) {
-        S.failed = 1;
-        atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
-        break;
-      }
-      __nanosleep(32);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  if (S.failed || m0 >= H) return;
-
-  // ---- phase 3: down projection of this block's output columns + combine
-  const int R = A + (a.shared ? T : 0);
-  const int ivec = I / 32, igpr = I / kGroup;
-  float* hs = dsm;                                  // [R][I/32][kDecPad] (x is no longer needed)
-  float* res = dsm + (size_t)R * ivec * kDecPad;    // [R][rows_per_blk]
-  {
-    const int hv = R * I / 4;  // float4 chunks of h; a batch of loads before any store
-    for (int i0 = tid; i0 < hv; i0 += 4 * kDecThreads) {
-      float4 v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kDecThreads;
-        if (i < hv) v[u] = __ldcg(reinterpret_cast<const float4*>(a.h) + i);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kDecThreads;
-        if (i < hv) {
-          const int r = (i * 4) / I, k = i * 4 - r * I;
-          *reinterpret_cast<float4*>(hs + (r * ivec + (k >> 5)) * kDecPad + (k & 31)) = v[u];
-        }
-      }
-    }
-  }
-  __syncthreads();
-  int L = 1;  // lanes per W_down row: largest power of two <= min(32, I/32)
-  while (L * 2 <= ivec && L * 2 <= 32) L *= 2;
-  const int per_warp = 32 / L, sub = lane % L, rw = lane / L;
-  const int its = (ivec + L - 1) / L;
-  const int mrows = m1 - m0;
-  const int dunits = nslots * mrows;
-  constexpr int kSlots = 4;                  // (pass, load) entries issued together
-  const int passes_per_batch = its >= kSlots ? 1 : kSlots / its;
-  const int pass_stride = kDecWarps * per_warp;
-  for (int ub0 = warp * per_warp; ub0 < dunits; ub0 += passes_per_batch * pass_stride) {
-    uint4 c[kSlots];
-    float sv[kSlots], bv[kSlots];
-#pragma unroll
-    for (int q = 0; q < kSlots; ++q) {
-      const int pss = q / (its < kSlots ? its : kSlots), it = q - pss * (its < kSlots ? its : kSlots);
-      const int u = ub0 + pss * pass_stride + rw;
-      const int v = sub + L * it;
-      if (pss < passes_per_batch && it < its && u < dunits && v < ivec) {
-        const int s = u / mrows, m = m0 + (u - s * mrows);
-        const int e = S.slot_e[s];
-        const bool sh = e == E;
-        const uint32_t* codes = sh ? a.dn.s_codes : a.dn.codes + (size_t)e * H * (I / 8);
-        const uint16_t* sc = sh ? a.dn.s_scales : a.dn.scales + (size_t)e * H * igpr;
-        const uint16_t* bi = sh ? a.dn.s_biases : a.dn.biases + (size_t)e * H * igpr;
-        c[q] = *reinterpret_cast<const uint4*>(codes + (size_t)m * (I / 8) + 4 * v);
-        sv[q] = bf16_bits_to_f32(sc[(size_t)m * igpr + v / 2]);
-        bv[q] = bf16_bits_to_f32(bi[(size_t)m * igpr + v / 2]);
-      }
-    }
-    for (int pss = 0; pss < passes_per_batch; ++pss) {
-      const int u = ub0 + pss * pass_stride + rw;
-      const bool live = u < dunits;
-      const int s = live ? u / mrows : 0, ml = live ? u - s * mrows : 0;
-      const int nr = live ? S.slot_n[s] : 0;
-      float acc[kDecodeMaxTokens];
-#pragma unroll
-      for (int j = 0; j < kDecodeMaxTokens; ++j) acc[j] = 0.f;
-#pragma unroll
-      for (int q = 0; q < kSlots; ++q) {
-        const int ip = its < kSlots ? its : kSlots;
-        const int qp = q / ip, it = q - qp * ip;
-        const int v = sub + L * it;
-        if (qp == pss && it < its && live && v < ivec) {
-#pragma unroll
-          for (int j = 0; j < kDecodeMaxTokens; ++j)
-            if (j < nr) acc[j] = dot32_f(c[q], sv[q], bv[q], hs + (S.slot_row[s][j] * ivec + v) * kDecPad, acc[j]);
-        }
-      }
-      // more 16-byte loads than one batch holds (I > 2048): finish the row directly
-      for (int it = kSlots; it < its; ++it) {
-        const int v = sub + L * it;
-        if (live && v < ivec) {
-          const int e = S.slot_e[s];
-          const bool sh = e == E;
-          const int m = m0 + ml;
-          const uint32_t* codes = sh ? a.dn.s_codes : a.dn.codes + (size_t)e * H * (I / 8);
-          const uint16_t* sc = sh ? a.dn.s_scales : a.dn.scales + (size_t)e * H * igpr;
-          const uint16_t* bi = sh ? a.dn.s_biases : a.dn.biases + (size_t)e * H * igpr;
-          const uint4 cc = *reinterpret_cast<const uint4*>(codes + (size_t)m * (I / 8) + 4 * v);
-          const float s1 = bf16_bits_to_f32(sc[(size_t)m * igpr + v / 2]);
-          const float b1 = bf16_bits_to_f32(bi[(size_t)m * igpr + v / 2]);
-#pragma unroll
-          for (int j = 0; j < kDecodeMaxTokens; ++j)
-            if (j < nr) acc[j] = dot32_f(cc, s1, b1, hs + (S.slot_row[s][j] * ivec + v) * kDecPad, acc[j]);
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kDecodeMaxTokens; ++j)
-        for (int off = L >> 1; off > 0; off >>= 1) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], off);
-      if (live && sub == 0)
-        for (int j = 0; j < nr; ++j) res[S.slot_row[s][j] * rows_per_blk + ml] = acc[j];
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < T * mrows; i += kDecThreads) {
-    const int t = i / mrows, ml = i - t * mrows;
+  for (int i = tid; i < T * 16; i += kDecConsumers) {
+    const int t = i >> 4, row = i & 15;
+    const int ln = (row & 7) * 4 + (t >> 1), r = (t & 1) + ((row >> 3) << 1);
     float v = 0.f;
-    for (int k = 0; k < K; ++k) v = fmaf(S.w[t * K + k], res[S.pos[t * K + k] * rows_per_blk + ml], v);
-    if (a.shared) v = fmaf(S.g[t], res[(A + t) * rows_per_blk + ml], v);
-    a.y[(size_t)t * H + m0 + ml] = v;
+    for (int w = 0; w < kDecWarps; ++w) v += S.part[0][w][r][ln];  // fixed order
+    a.y[(size_t)t * H + m0 + row] = v;
   }
-}
-
-size_t decode_smem_bytes(const Geometry& g, int rows_per_blk) {
-  const int R = g.A + (g.shared ? g.T : 0);
-  const size_t xs = (size_t)g.T * (g.H / 32) * kDecPad * sizeof(float);
-  const size_t hs = (size_t)R * (g.I / 32) * kDecPad * sizeof(float) + (size_t)R * rows_per_blk * sizeof(float);
-  return xs > hs ? xs : hs;
 }
 
 namespace {
@@ -517,47 +577,70 @@ int sm_count(int dev) {
   return sms[dev];
 }
 
-template <int kIt>
-cudaError_t launch_decode_it(const DecodeArgs& args, int grid, size_t smem, cudaStream_t stream) {
+constexpr size_t kDecDynamicLimit = 200 * 1024;
+
+// Dynamic shared memory: x16 [T][H] (phases 0-2) / h [R][I] (phase 4), then
+// the ring. A stage holds one gate/up unit (9H bytes: 16 code rows of H/2,
+// 16 scale rows and 16 bias rows of H/32) or W_down rows of `per_item` slots
+// (9I bytes each).
+struct DecodeLayout {
+  size_t ring_offset, stage_bytes, total;
+  int stages, per_item;
+};
+
+DecodeLayout decode_layout(const Geometry& g) {
+  DecodeLayout L{};
+  const int R = g.A + (g.shared ? g.T : 0);
+  const size_t xs = (size_t)g.T * g.H * 2, hs = (size_t)R * g.I * 2;
+  L.ring_offset = ((xs > hs ? xs : hs) + 127) & ~size_t(127);
+  const int big = g.H > g.I ? g.H : g.I;
+  L.stage_bytes = 9 * (size_t)big;
+  L.per_item = big / g.I;
+  const size_t room = kDecDynamicLimit > L.ring_offset ? kDecDynamicLimit - L.ring_offset : 0;
+  const size_t fit = room / L.stage_bytes;
+  L.stages = (int)(fit < (size_t)kDecodeMaxStages ? fit : kDecodeMaxStages);
+  L.total = L.ring_offset + (size_t)L.stages * L.stage_bytes;
+  return L;
+}
+}  // namespace
+
+// One block per SM, all resident (the grid barrier needs that); 16 output
+// rows per block; K in whole 128-wide blocks on both projections; at least
+// two ring stages.
+bool decode_supported(const Geometry& g) {
+  int dev = 0;
+  if (g.T < 1 || g.T > kDecodeMaxTokens || g.H % 128 || g.I % 128 || cudaGetDevice(&dev) != cudaSuccess)
+    return false;
+  const int sms = sm_count(dev);
+  return sms > 0 && g.H / 16 <= sms && decode_layout(g).stages >= 2;
+}
+
+cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count(dev);
+  if (grid <= 0) return cudaErrorInvalidDevice;
+  const DecodeLayout L = decode_layout(g);
+  DecodeArgs args = args_in;
+  args.stages = L.stages;
+  args.per_item = L.per_item;
+  args.stage_bytes = (long long)L.stage_bytes;
+  args.ring_offset = (long long)L.ring_offset;
   static int configured = 0;
-  cudaError_t e = ensure_smem(decode_layer_kernel<kIt>, smem, &configured);
+  e = ensure_smem(decode_layer_kernel, L.total, &configured);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = L.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<kIt>, args);
-}
-}  // namespace
-
-// One block per SM (all resident: the grid barrier needs that).
-bool decode_supported(const Geometry& g) {
-  int dev = 0;
-  if (g.T < 1 || g.T > kDecodeMaxTokens || g.H > 8192 || cudaGetDevice(&dev) != cudaSuccess) return false;
-  const int sms = sm_count(dev);
-  if (sms <= 0) return false;
-  const int rows_per_blk = (g.H + sms - 1) / sms;
-  return decode_smem_bytes(g, rows_per_blk) <= 200 * 1024;
-}
-
-cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const int grid = sm_count(dev);
-  if (grid <= 0) return cudaErrorInvalidDevice;
-  const size_t smem = decode_smem_bytes(g, (g.H + grid - 1) / grid);
-  const int its = (g.H / 32 + 31) / 32;
-  if (its <= 1) return launch_decode_it<1>(args, grid, smem, stream);
-  if (its <= 2) return launch_decode_it<2>(args, grid, smem, stream);
-  if (its <= 4) return launch_decode_it<4>(args, grid, smem, stream);
-  return launch_decode_it<8>(args, grid, smem, stream);
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel, args);
 }
 
 }  // namespace bgmoe

@@ -9,6 +9,7 @@
 namespace bgmoe {
 
 constexpr int kDecodeMaxTokens = 4;  // tokens per call handled by the fused decode kernel
+constexpr int kDecodeMaxStages = 8;  // shared-memory ring depth of the fused decode kernel
 
 struct RouteArgs {
   const float* logits;  // [T][E+1], column E = shared gate logit
@@ -95,10 +96,13 @@ struct DecodeArgs {
   int32_t* tile_rows;
   int32_t* num_tiles;
   int32_t* status;
-  float* h;              // fp32 [A+T][I]
+  __half* h;             // fp16 [A+T][I], K order permuted within groups of 8
   float* y;              // fp32 [T][H]
   unsigned int* bar;     // grid-barrier counter, cleared by the router kernel
   long long timeout_ns;
+  // ring geometry, filled in by launch_decode
+  int stages, per_item;
+  long long stage_bytes, ring_offset;
 };
 bool decode_supported(const Geometry& g);
 cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);

@@ -43,8 +43,27 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
     }
   }
 
-  // Stage the block's token rows (16-byte copies; H is a multiple of 64).
   const int vec_per_row = H / 8;
+  const int e = blockIdx.x * kRouterWarps + warp;
+  const bool has_gate = wsg != nullptr;
+  const bool has_row = e < E || (e == E && has_gate);
+  const uint16_t* row = (e < E) ? wr + (size_t)e * H : wsg;
+
+  // The first batch of this warp's weight loads goes out before x is staged
+  // (the two do not depend on each other); every batch is issued before any
+  // use, so a row of H <= 2048 costs one memory round trip.
+  constexpr int kBatch = 8;
+  uint4 w4[kBatch];
+  auto load_batch = [&](int v0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int v = v0 + 32 * u;
+      if (has_row && v < vec_per_row) w4[u] = ldg_nc_v4(row + (size_t)v * 8);
+    }
+  };
+  load_batch(lane);
+
+  // Stage the block's token rows (16-byte copies; H is a multiple of 64).
   for (int i = threadIdx.x; i < nt * vec_per_row; i += blockDim.x) {
     const int j = i / vec_per_row, v = i - j * vec_per_row;
     reinterpret_cast<uint4*>(xs)[j * vec_per_row + v] =
@@ -63,26 +82,14 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
       x16[(size_t)(t0 + j) * H + pk] = __half_as_ushort(__float2half_rn(bf16_bits_to_f32(xs[j * H + k])));
     }
   }
-
-  const int e = blockIdx.x * kRouterWarps + warp;
-  const bool has_gate = wsg != nullptr;
-  if (e > E || (e == E && !has_gate)) return;
-  const uint16_t* row = (e < E) ? wr + (size_t)e * H : wsg;
+  if (!has_row) return;
 
   float acc[kRouterTokens];
 #pragma unroll
   for (int j = 0; j < kRouterTokens; ++j) acc[j] = 0.f;
 
-  // All of this warp's weight loads of a batch are issued before any use, so
-  // the row costs one memory round trip (8 x 16 B per lane covers H = 2048).
-  constexpr int kBatch = 8;
   for (int v0 = lane; v0 < vec_per_row; v0 += 32 * kBatch) {
-    uint4 w4[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int v = v0 + 32 * u;
-      if (v < vec_per_row) w4[u] = ldg_nc_v4(row + (size_t)v * 8);
-    }
+    if (v0 != lane) load_batch(v0);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int v = v0 + 32 * u;

@@ -179,13 +179,15 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_rout
 
 /* Expert-GEMM implementations selectable through moe_forward_timed. */
 typedef enum moe_expert_path {
-  MOE_PATH_AUTO = 0,        /* fused decode for T <= 4, tensor cores for T >= 64 when the
-                               shape allows, else GEMV */
+  MOE_PATH_AUTO = 0,        /* fused decode for T <= 4 when its conditions hold, tensor
+                               cores for T >= 64 when the shape allows, else GEMV */
   MOE_PATH_GEMV = 1,        /* bandwidth-bound grouped GEMV (CUDA cores), any shape */
   MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 256 == 0 and I % 128 == 0
                                (else UNSUPPORTED_SHAPE) */
   MOE_PATH_FUSED_DECODE = 3 /* router kernel + one fused kernel for top-k, tables, expert
-                               GEMVs and combine; T <= 4 (else UNSUPPORTED_SHAPE). Its
+                               GEMVs and combine; needs T <= 4, H % 128 == 0,
+                               I % 128 == 0, H / 16 <= the SM count and 16-byte aligned
+                               codes, scales and biases (else UNSUPPORTED_SHAPE). Its
                                events[2] == events[1] and events[4..5] == events[3] */
 } moe_expert_path;
 

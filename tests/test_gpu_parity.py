@@ -152,11 +152,26 @@ def test_tensor_core_unsupported_shape_is_refused(moelib, cuda_dev):
 
 
 @pytest.mark.parametrize("T,E,K,shared,H,I", [(1, 256, 8, True, 2048, 512), (4, 256, 8, True, 2048, 512),
-                                               (3, 64, 8, True, 256, 128), (2, 16, 2, False, 128, 64),
-                                               (4, 8, 1, True, 512, 192), (1, 32, 4, False, 1024, 320)])
+                                               (3, 64, 8, True, 256, 128), (2, 16, 2, False, 128, 128),
+                                               (4, 8, 1, True, 512, 256), (1, 32, 4, False, 1024, 384),
+                                               (4, 4, 4, True, 2048, 128), (2, 256, 8, True, 1536, 640)])
 def test_fused_decode(moelib, cuda_dev, T, E, K, shared, H, I):
     spec = synth.LayerSpec("fused", T=T, H=H, I=I, E=E, top_k=K, shared=shared, seed=20260019)
     _run_and_check(moelib, cuda_dev, spec, path=moelib.PATH_FUSED_DECODE)
+
+
+@pytest.mark.parametrize("H,I", [(128, 64), (320, 128), (4096, 512)])
+def test_fused_decode_shape_limits(moelib, cuda_dev, H, I):
+    """K of both projections must come in whole 128-wide blocks and the
+    output rows 16 per SM: other decode shapes are refused on the fused path
+    and served by the GEMV path under the automatic choice."""
+    spec = synth.LayerSpec("fused-limits", T=2, H=H, I=I, E=16, top_k=2, seed=20260021)
+    L = parity.device_layer(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    with pytest.raises(moelib.MoeError) as ei:
+        parity.gpu_forward(moelib, spec, L, x, 16, path=moelib.PATH_FUSED_DECODE)
+    assert ei.value.status == moelib.MOE_ERR_UNSUPPORTED_SHAPE
+    _run_and_check(moelib, cuda_dev, spec, path=moelib.PATH_AUTO)
 
 
 @pytest.mark.parametrize("T", [1, 4])
