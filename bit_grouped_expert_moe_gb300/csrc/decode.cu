@@ -11,13 +11,14 @@
 // copies (cp.async.bulk, completion counted on an mbarrier), so a block keeps
 // up to `stages` tiles in flight whatever the compute between them does. One
 // ring item is either
-//   a gate/up unit: expert slot s, h columns n0..n0+7 -> gate rows n0..n0+7
-//     and up rows I+n0..I+n0+7 with their scales and biases (9H bytes), or
+//   a gate/up item: expert slot s, h columns n0..n0+15 -> gate rows
+//     n0..n0+15 and up rows I+n0..I+n0+15 with their scales and biases
+//     (18H bytes; two MMA units of 8 columns), or
 //   a down item: rows m0..m0+15 of W_down for up to `per_item` slots.
 // The products run on mma.sync.m16n8k16 (fp16 operands, fp32 accumulation):
 // 16 weight rows x 8 token columns per instruction. In a gate/up unit the 16
-// MMA rows are the 8 gate rows then the 8 up rows, so the lane that holds
-// gate(n, j) also holds up(n, j). Each lane dequantises whole code words into
+// MMA rows are 8 gate rows then the matching 8 up rows, so the lane that
+// holds gate(n, j) also holds up(n, j). Each lane dequantises whole code words into
 // A fragments; one word unpacks as the pairs (k0,k4), (k1,k5), (k2,k6),
 // (k3,k7), so the activations are kept in that K order inside every group of
 // 8 (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte shared-memory load.
@@ -75,7 +76,7 @@ struct DecodeSmall {
   int pfail;     // producer abort flag (kept apart: consumers branch on `failed` only)
   uint64_t full[kDecodeMaxStages];               // stage filled (bulk-copy bytes landed)
   uint64_t empty[kDecodeMaxStages];              // stage released by all consumer warps
-  float part[2][kDecWarps][4][32];               // per-warp MMA partials: [item parity][warp][reg][lane]
+  float part[2][2][kDecWarps][4][32];            // per-warp MMA partials: [item parity][sub-unit][warp][reg][lane]
 };
 
 __device__ __forceinline__ float dec_key_to_float(uint32_t k) {
@@ -98,6 +99,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                    tc::smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
                : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
 
 // d += A * B with A 16x16 (row), B 16x8 (col), fp16 in, fp32 accumulate.
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const int G = gridDim.x, b = blockIdx.x;
   const int gpr = H / kGroup, igpr = I / kGroup;
   const int NST = a.stages;
-  const int cpb = I / 8;             // gate/up units per slot
+  const int cpb = I / 16;            // gate/up items per slot (16 h columns each)
   const int mblocks = H / 16;        // blocks with output rows
   const int m0 = b * 16;
   const int kbs = I / 128, nkb = H / 128;
@@ -224,47 +231,52 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   uint8_t* ring = dsm_raw + a.ring_offset;
   const uint64_t deadline0 = global_timer_ns() + (uint64_t)a.timeout_ns;
 
-  // ---- ring producer (the producer warp): item i -> stage i % NST. Lane 0
-  // posts the expected bytes, then each copy of the item is issued by its own
-  // lane, so the warp spends one instruction stream on all of them.
-  int n2 = 0;  // gate/up units of this block (known after routing); down items follow them
-  const uint32_t gcb = 8u * (H / 2), gsb = 8u * gpr * 2;        // gate/up unit: 8 code rows / scale rows
-  const uint32_t dcb = 16u * (I / 2), dsb = 16u * igpr * 2;     // down item: 16 code rows / scale rows per slot
+  // ---- ring producer (the producer warp): item i -> stage i % NST. The
+  // big contiguous parts (code rows) are single bulk copies posted by lane 0
+  // (each copy costs the copy engine a fixed slot, so there are few of
+  // them); the small scale and bias rows are 16-byte cp.async copies spread
+  // over the 32 lanes, each lane then arriving on the stage's mbarrier once
+  // its copies have landed (cp.async.mbarrier.arrive.noinc).
+  int n2 = 0;  // gate/up items of this block (known after routing); down items follow them
+  const uint32_t gcb = 16u * (H / 2), gsb = 16u * gpr * 2;     // gate/up item: 16 code rows / scale rows
+  const uint32_t dcb = 16u * (I / 2), dsb = 16u * igpr * 2;    // down item, per slot: 16 code rows / scale rows
   auto issue = [&](int i, int nslots) {  // called by all 32 lanes of the producer warp
     const int st = i % NST;
     uint8_t* dst = ring + (size_t)st * stage_bytes;
     uint64_t* bar = &S.full[st];
-    if (nslots < 0 || i < n2) {  // gate/up unit (nslots < 0: the shared unit issued before routing)
+    if (nslots < 0 || i < n2) {  // gate/up item (nslots < 0: the shared item issued before routing)
       const int u = b + i * G;
-      const int s = u / cpb, n0 = (u - s * cpb) * 8;
-      if (lane == 0) tc::mbar_arrive_expect_tx(bar, 2 * gcb + 4 * gsb);
-      __syncwarp();
-      if (lane < 6) {
-        const int kind = lane >> 1, up = lane & 1;  // codes / scales / biases, gate / up
-        const uint8_t* base;
-        if (nslots < 0)
-          base = kind == 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_codes)
-                           : reinterpret_cast<const uint8_t*>(kind == 1 ? a.gu.s_scales : a.gu.s_biases);
-        else
-          base = S.slot_src[s][kind];
-        const size_t row = (size_t)(up ? I + n0 : n0);
-        const uint32_t bytes = kind == 0 ? gcb : gsb;
-        const size_t row_bytes = kind == 0 ? (size_t)(H / 2) : (size_t)gpr * 2;
-        const uint32_t off = kind == 0 ? up * gcb : 2 * gcb + (2 * (kind - 1) + up) * gsb;
-        bulk_g2s(dst + off, base + row * row_bytes, bytes, bar);
+      const int s = u / cpb, n0 = (u - s * cpb) * 16;
+      const uint8_t* cb = nslots < 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_codes) : S.slot_src[s][0];
+      const uint8_t* sc = nslots < 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_scales) : S.slot_src[s][1];
+      const uint8_t* bi = nslots < 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_biases) : S.slot_src[s][2];
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(bar, 2 * gcb);
+        bulk_g2s(dst, cb + (size_t)n0 * (H / 2), gcb, bar);
+        bulk_g2s(dst + gcb, cb + (size_t)(I + n0) * (H / 2), gcb, bar);
       }
+      // gate scales, up scales, gate biases, up biases: 4 runs of gsb bytes
+      for (uint32_t o = 16u * lane; o < 4 * gsb; o += 16u * 32) {
+        const uint32_t run = o / gsb, r = o - run * gsb;
+        const size_t row0 = (run & 1) ? (size_t)(I + n0) : (size_t)n0;
+        tc::cp_async_16(dst + 2 * gcb + o, (run < 2 ? sc : bi) + row0 * gpr * 2 + r, 16);
+      }
+      cp_async_arrive_noinc(bar);
     } else {  // down item: rows m0..m0+15 of slots p0..p0+np-1
       const int p0 = (i - n2) * per_item;
       const int np = min(per_item, nslots - p0);
-      if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)np * (dcb + 2 * dsb));
+      const uint32_t per = dcb + 2 * dsb;
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)np * dcb);
       __syncwarp();
-      for (int c = lane; c < 3 * np; c += 32) {
-        const int p = c / 3, kind = c - 3 * p;
-        const uint8_t* base = S.slot_src[p0 + p][3 + kind];
-        const size_t row_bytes = kind == 0 ? (size_t)(I / 2) : (size_t)igpr * 2;
-        const uint32_t off = (uint32_t)p * (dcb + 2 * dsb) + (kind == 0 ? 0u : dcb + (kind - 1) * dsb);
-        bulk_g2s(dst + off, base + (size_t)m0 * row_bytes, kind == 0 ? dcb : dsb, bar);
+      if (lane < np) bulk_g2s(dst + (size_t)lane * per, S.slot_src[p0 + lane][3] + (size_t)m0 * (I / 2), dcb, bar);
+      // per slot: scales then biases, dsb bytes each
+      for (uint32_t o = 16u * lane; o < (uint32_t)np * 2 * dsb; o += 16u * 32) {
+        const uint32_t q = o / dsb, r = o - q * dsb;  // q = 2 * slot + (0 scales, 1 biases)
+        const int p = (int)(q >> 1);
+        tc::cp_async_16(dst + (size_t)p * per + dcb + (q & 1) * dsb + r,
+                        S.slot_src[p0 + p][4 + (q & 1)] + (size_t)m0 * igpr * 2 + r, 16);
       }
+      cp_async_arrive_noinc(bar);
     }
   };
   int issued = 0;  // items issued so far (producer warp)
@@ -282,7 +294,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   if (producer) {
     if (lane == 0) {
       for (int st = 0; st < NST; ++st) {
-        tc::mbar_init(&S.full[st], 1);
+        tc::mbar_init(&S.full[st], 1 + 32);  // lane 0's expect_tx + one cp.async arrival per lane
         tc::mbar_init(&S.empty[st], kDecWarps);
       }
       tc::fence_barrier_init();
@@ -410,7 +422,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     return;
   }
 
-  // ---- phase 2: gate/up units (consumer warps)
+  // ---- phase 2: gate/up items (consumer warps). An item is two 8-column
+  // units: unit q takes gate rows 8q..8q+7 and up rows 8q..8q+7 of the stage
+  // as its 16 MMA rows.
   const int R = A + (a.shared ? T : 0);
   for (int i = 0; i < n2; ++i) {
     // On a timeout every consumer still runs every iteration (skipping the
@@ -419,45 +433,53 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     const uint8_t* sp = ring + (size_t)st * stage_bytes;
     const bool ok = tc::mbar_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0);
     const int u = b + i * G;
-    const int s = u / cpb, n0 = (u - s * cpb) * 8;
+    const int s = u / cpb, n0 = (u - s * cpb) * 16;
     const int nr = S.slot_n[s];
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     if (ok) {
       const bool col_live = g8 < nr;
       const __half* xrow = xs + (size_t)(col_live ? S.slot_tok[s][g8] : 0) * H;
-      const uint32_t cb = gcb, sb = gsb;
-      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sp + 2 * cb);  // gate sc, up sc, gate bi, up bi
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sp + 2 * gcb);  // gate sc, up sc, gate bi, up bi
+      const int q16 = gsb / 2;  // uint16 entries per run
       for (int kb = warp; kb < nkb; kb += kDecWarps) {
         const int koff = kb * 64 + 16 * c4;  // byte offset of this lane's 32 K inside a code row
-        const int gi = g8 * gpr + 2 * kb + (c4 >> 1);
-        const uint4 cg = *reinterpret_cast<const uint4*>(sp + g8 * (H / 2) + koff);
-        const uint4 cu = *reinterpret_cast<const uint4*>(sp + cb + g8 * (H / 2) + koff);
-        const __half2 sg = bf16_h2(s16[gi]), su = bf16_h2(s16[sb / 2 + gi]);
-        const __half2 bg = bf16_h2(s16[sb + gi]), bu = bf16_h2(s16[3 * sb / 2 + gi]);
+        const int gi = g8 * gpr + 2 * kb + (c4 >> 1), gi8 = gi + 8 * gpr;
         uint4 xb[4];
         load_b(xb, xrow + kb * 128 + 32 * c4, col_live);
-        mma_chunk(d, cg, cu, sg, bg, su, bu, xb);
+        const uint4 cg0 = *reinterpret_cast<const uint4*>(sp + g8 * (H / 2) + koff);
+        const uint4 cu0 = *reinterpret_cast<const uint4*>(sp + gcb + g8 * (H / 2) + koff);
+        const uint4 cg1 = *reinterpret_cast<const uint4*>(sp + (g8 + 8) * (H / 2) + koff);
+        const uint4 cu1 = *reinterpret_cast<const uint4*>(sp + gcb + (g8 + 8) * (H / 2) + koff);
+        mma_chunk(d0, cg0, cu0, bf16_h2(s16[gi]), bf16_h2(s16[2 * q16 + gi]), bf16_h2(s16[q16 + gi]),
+                  bf16_h2(s16[3 * q16 + gi]), xb);
+        mma_chunk(d1, cg1, cu1, bf16_h2(s16[gi8]), bf16_h2(s16[2 * q16 + gi8]), bf16_h2(s16[q16 + gi8]),
+                  bf16_h2(s16[3 * q16 + gi8]), xb);
       }
     }
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(&S.empty[st]);  // this warp is done with the stage
 #pragma unroll
-    for (int r = 0; r < 4; ++r) S.part[i & 1][warp][r][lane] = d[r];
-    consumer_sync();
-    if (ok && warp == i % kDecWarps) {
-      // d0, d1: gate(n0+g, slot rows 2c, 2c+1); d2, d3: up of the same
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int w = 0; w < kDecWarps; ++w)  // fixed order: the same bits on every run
-#pragma unroll
-        for (int r = 0; r < 4; ++r) v[r] += S.part[i & 1][w][r][lane];
-      const int pn = tc::perm8_pos(n0 + g8);
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int j = 2 * c4 + q;
-        if (j < nr)
-          a.h[(size_t)S.slot_row[s][j] * I + pn] = __float2half_rn(silu_f32(v[q]) * v[2 + q] * S.slot_w[s][j]);
-      }
+    for (int r = 0; r < 4; ++r) {
+      S.part[i & 1][0][warp][r][lane] = d0[r];
+      S.part[i & 1][1][warp][r][lane] = d1[r];
     }
+    consumer_sync();
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (ok && warp == (2 * i + q) % kDecWarps) {
+        // d0, d1: gate(n0+8q+g, slot rows 2c, 2c+1); d2, d3: up of the same
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < kDecWarps; ++w)  // fixed order: the same bits on every run
+#pragma unroll
+          for (int r = 0; r < 4; ++r) v[r] += S.part[i & 1][q][w][r][lane];
+        const int pn = tc::perm8_pos(n0 + 8 * q + g8);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const int j = 2 * c4 + jj;
+          if (j < nr)
+            a.h[(size_t)S.slot_row[s][j] * I + pn] = __float2half_rn(silu_f32(v[jj]) * v[2 + jj] * S.slot_w[s][j]);
+        }
+      }
   }
 
   // ---- phase 3: grid barrier (every block resident; bounded wait)
@@ -553,7 +575,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     if (lane == 0) tc::mbar_arrive(&S.empty[st]);
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r) S.part[0][warp][r][lane] = acc[r];
+  for (int r = 0; r < 4; ++r) S.part[0][0][warp][r][lane] = acc[r];
   consumer_sync();
   if (S.failed) {
     if (tid == 0) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
@@ -563,7 +585,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     const int t = i >> 4, row = i & 15;
     const int ln = (row & 7) * 4 + (t >> 1), r = (t & 1) + ((row >> 3) << 1);
     float v = 0.f;
-    for (int w = 0; w < kDecWarps; ++w) v += S.part[0][w][r][ln];  // fixed order
+    for (int w = 0; w < kDecWarps; ++w) v += S.part[0][0][w][r][ln];  // fixed order
     a.y[(size_t)t * H + m0 + row] = v;
   }
 }
@@ -577,11 +599,11 @@ int sm_count(int dev) {
   return sms[dev];
 }
 
-constexpr size_t kDecDynamicLimit = 200 * 1024;
+constexpr size_t kDecDynamicLimit = 186 * 1024;  // 227 KB per block minus the static part (about 38 KB)
 
 // Dynamic shared memory: x16 [T][H] (phases 0-2) / h [R][I] (phase 4), then
-// the ring. A stage holds one gate/up unit (9H bytes: 16 code rows of H/2,
-// 16 scale rows and 16 bias rows of H/32) or W_down rows of `per_item` slots
+// the ring. A stage holds one gate/up item (18H bytes: 32 code rows of H/2,
+// 32 scale rows and 32 bias rows of H/32) or W_down rows of `per_item` slots
 // (9I bytes each).
 struct DecodeLayout {
   size_t ring_offset, stage_bytes, total;
@@ -594,8 +616,8 @@ DecodeLayout decode_layout(const Geometry& g) {
   const size_t xs = (size_t)g.T * g.H * 2, hs = (size_t)R * g.I * 2;
   L.ring_offset = ((xs > hs ? xs : hs) + 127) & ~size_t(127);
   const int big = g.H > g.I ? g.H : g.I;
-  L.stage_bytes = 9 * (size_t)big;
-  L.per_item = big / g.I;
+  L.stage_bytes = 18 * (size_t)big;
+  L.per_item = 2 * big / g.I;
   const size_t room = kDecDynamicLimit > L.ring_offset ? kDecDynamicLimit - L.ring_offset : 0;
   const size_t fit = room / L.stage_bytes;
   L.stages = (int)(fit < (size_t)kDecodeMaxStages ? fit : kDecodeMaxStages);
