@@ -106,7 +106,7 @@ Workspace carve(const Geometry& g, void* base) {
   w.tile_rows = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
   w.num_tiles = static_cast<int32_t*>(take(sizeof(int32_t)));
   w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)g.T * g.H));
-  w.bar = static_cast<unsigned int*>(take(sizeof(unsigned int)));
+  w.bar = static_cast<unsigned int*>(take(2 * sizeof(unsigned int)));
   w.h = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.I));
   w.o = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.H));
   w.bytes = off;
@@ -319,11 +319,12 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
                   (expert_path == MOE_PATH_AUTO && !fused && g.T >= kTensorCoreMinTokens && tc_ok);
 
   if (fused) {
-    e = launch_router_logits(g, x, w_router, g.shared ? w_shared_gate : nullptr, w.logits, w.state,
-                             g.route_blocks * g.E, r.status, nullptr, s, w.bar);
-    if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
+    // The fused kernel computes the router logits itself; events[1] and [2]
+    // fall right after events[0].
     if ((e = mark(1)) != cudaSuccess || (e = mark(2)) != cudaSuccess) return cuda_fail(e, "event record");
     DecodeArgs d{};
+    d.wr = static_cast<const uint16_t*>(w_router);
+    d.wsg = g.shared ? static_cast<const uint16_t*>(w_shared_gate) : nullptr;
     d.T = g.T;
     d.H = g.H;
     d.I = g.I;

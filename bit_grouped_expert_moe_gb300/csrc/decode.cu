@@ -24,25 +24,34 @@
 // 8 (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte shared-memory load.
 //
 // One block per SM, every block resident: 16 consumer warps and one producer
-// warp whose lane 0 issues the copies (kept out of the consumer warps: a lane
-// issuing while its warp-mates wait on an mbarrier is held up by them).
-// Phases:
-//   0  before the router finishes (programmatic dependent launch): x is
-//      staged as fp16 and a block whose first unit belongs to the shared
-//      expert (which every token uses) starts its copy;
-//   1  every block selects the top-k experts of the T tokens itself and
-//      derives the expert slots; from here the producer fills the ring as
-//      the consumers release stages (one "empty" mbarrier per stage);
-//   2  gate/up units: the 16 warps split K, the partial sums of unit i are
-//      added in a fixed order by warp i % 16 while the others go on, and
-//      h = w * silu(gate) * up (the token's routing weight, or the shared
+// warp whose lane 0 issues the bulk copies (kept out of the consumer warps: a
+// lane issuing while its warp-mates wait on an mbarrier is held up by them).
+// A one-block prelude kernel clears the two grid-barrier counters and the
+// status word; this kernel starts at once (programmatic dependent launch) and
+// waits for the prelude only before its first barrier arrival. Phases:
+//   0  x is staged (fp16 in the permuted K order for the experts, bf16 for
+//      the router) and a block whose first item belongs to the shared expert
+//      (which every token uses) starts its copies;
+//   R  router logits: block b, warp w computes rows b + G*w, G*16 apart, and
+//      writes l[t][r] to global memory; grid barrier A;
+//   1  every block selects the top-k experts of the T tokens itself (reading
+//      the logits through L2) and derives the expert slots; from here the
+//      producer fills the ring as the consumers release stages (one "empty"
+//      mbarrier per stage);
+//   2  gate/up items: the 16 warps split K, the partial sums of each 8-column
+//      unit are added in a fixed order by one warp while the others go on,
+//      and h = w * silu(gate) * up (the token's routing weight, or the shared
 //      gate, folded in) goes to global memory as fp16;
-//   3  one grid barrier (counter cleared by the router kernel, bounded wait);
+//   3  grid barrier B;
 //   4  block b owns output rows 16b..16b+15: with the weights folded into h,
 //      y[t][m] = sum over slots of W_down[m] . h_slot,t, so every warp keeps one
 //      accumulator over its (slot, K block) tasks and the 16 accumulators are
 //      added in a fixed order at the end. The last block writes the routing
 //      tables.
+// Reading, right after a programmatic-dependent-launch wait, values another
+// kernel wrote just before it finished proved slow (about 2.8 us for the
+// logits row on GB300, against 1.5 us for a DRAM miss of unrelated data),
+// which is why the router runs inside this kernel.
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
@@ -66,12 +75,7 @@ struct DecodeSmall {
   float slot_w[kDecMaxSlots][kDecodeMaxTokens];  // routing weight (shared slot: gate) of each slot row
   int tok_row[kDecMaxSlots][kDecodeMaxTokens];   // h row of (slot, token), -1 if the token skips it
   const uint8_t* slot_src[kDecMaxSlots][6];     // gate/up codes, scales, biases; down codes, scales, biases
-  float zero_row[kMaxExperts + 1];               // warm-up input of the top-k
-  int warm_ids[kMaxTopK];
-  float warm_w[kMaxTopK];
-  float warm_g[kDecodeMaxTokens];
   int nslots;
-  int status_in;
   int failed;    // consumer abort flag (a stage or grid-barrier wait ran out)
   int pfail;     // producer abort flag (kept apart: consumers branch on `failed` only)
   uint64_t full[kDecodeMaxStages];               // stage filled (bulk-copy bytes landed)
@@ -99,6 +103,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                    tc::smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
                : "memory");
+}
+
+// Arrival on a grid barrier: release orders the block's earlier writes (made
+// visible to this thread by the preceding block barrier) before the add.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // One arrival on `bar` once every cp.async this thread issued so far has
@@ -147,20 +157,24 @@ __device__ __forceinline__ void load_b(uint4 (&xb)[4], const __half* row, bool l
 }
 
 // Top-k of one token by one warp: ids (best first), renormalised softmax
-// weights and the shared-expert gate. Keys are fp32 order keys (0 marks an
+// weights and the shared-expert gate. The logits come from other blocks of
+// the same kernel (read through L2). Keys are fp32 order keys (0 marks an
 // empty or taken entry; a finite logit never maps to 0). Each lane keeps the
 // best of its own 8 entries; a round takes the warp maximum and, among lanes
 // holding it, the lowest expert index, so equal logits go to the lower index.
-// Not inlined: the kernel runs it once on a dummy row first (see phase 0).
-__device__ __noinline__ void select_experts(const float* lrow, const float* bias, int E, int K, int shared, int lane,
+__device__ __forceinline__ void select_experts(const float* lrow, const float* bias, int E, int K, int shared, int lane,
                                             int* ids_out, float* w_out, float* g_out) {
-  const float gate_logit = shared ? lrow[E] : 0.f;
+  // All loads first (clamped indices, no branches between them), so the row
+  // costs one round trip instead of one per load.
+  float lv[kMaxExperts / 32], bv[kMaxExperts / 32];
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) lv[j] = __ldcg(lrow + min(lane + 32 * j, E - 1));
+  const float gate_logit = __ldcg(lrow + (shared ? E : 0));
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) bv[j] = bias ? __ldg(bias + min(lane + 32 * j, E - 1)) : 0.f;
   uint32_t key[kMaxExperts / 32];
 #pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) {
-    const int e = lane + 32 * j;
-    key[j] = e < E ? float_order_key(lrow[e] + (bias ? bias[e] : 0.f)) : 0u;
-  }
+  for (int j = 0; j < kMaxExperts / 32; ++j) key[j] = lane + 32 * j < E ? float_order_key(lv[j] + bv[j]) : 0u;
   uint32_t lb = 0u;
   int lbj = 0;
 #pragma unroll
@@ -202,7 +216,7 @@ __device__ __noinline__ void select_experts(const float* lrow, const float* bias
     ids_out[lane] = my_e;
     w_out[lane] = z / sum;
   }
-  if (lane == 0) *g_out = shared ? 1.f / (1.f + expf(-gate_logit)) : 0.f;
+  if (lane == 0) *g_out = shared ? 1.f / (1.f + expf(-gate_logit)) : 0.f;  // (gate_logit unused otherwise)
 }
 
 // Named barrier of the 16 consumer warps (the producer warp never joins it).
@@ -228,6 +242,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const int per_item = a.per_item;   // down slots per ring item
   const size_t stage_bytes = (size_t)a.stage_bytes;
   __half* xs = reinterpret_cast<__half*>(dsm_raw);  // phases 0-2: x16 [T][H]; phase 4: h [R][I]
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(xs + (size_t)T * H);  // phases 0-R: x bf16 [T][H]
   uint8_t* ring = dsm_raw + a.ring_offset;
   const uint64_t deadline0 = global_timer_ns() + (uint64_t)a.timeout_ns;
 
@@ -325,25 +340,75 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     o.z = *reinterpret_cast<const uint32_t*>(&p2);
     o.w = *reinterpret_cast<const uint32_t*>(&p3);
     reinterpret_cast<uint4*>(xs)[i] = o;
+    reinterpret_cast<uint4*>(xraw)[i] = v;  // bf16 as given, for the router
+  }
+  __syncthreads();
+
+  // ---- phase R: router logits l[t][r] = x[t] . W_r[r] (r = E: the shared
+  // expert's gate row), fp32, rows r = b + G * warp
+  {
+    const int rows = E + (a.shared ? 1 : 0);
+    const int vec = H / 8;  // 16-byte chunks of a row
+    for (int r = b + G * warp; warp < kDecWarps && r < rows; r += G * kDecWarps) {
+      const uint16_t* wrow = r < E ? a.wr + (size_t)r * H : a.wsg;
+      float acc[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+      for (int v0 = lane; v0 < vec; v0 += 32 * 8) {
+        uint4 w4[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)  // every load of the batch before any use
+          if (v0 + 32 * q < vec) w4[q] = ldg_nc_v4(wrow + (size_t)(v0 + 32 * q) * 8);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int v = v0 + 32 * q;
+          if (v < vec) {
+            const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
+#pragma unroll
+            for (int t = 0; t < kDecodeMaxTokens; ++t)
+              if (t < T) {
+                const uint4 x4 = *reinterpret_cast<const uint4*>(xraw + (size_t)t * H + (size_t)v * 8);
+                const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
+                float sacc = acc[t];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                  sacc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), bf16_bits_to_f32(xv[m] & 0xFFFFu), sacc);
+                  sacc = fmaf(bf16_bits_to_f32(ww[m] >> 16), bf16_bits_to_f32(xv[m] >> 16), sacc);
+                }
+                acc[t] = sacc;
+              }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxTokens; ++t) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+        if (lane == 0 && t < T) a.logits[(size_t)t * (E + 1) + r] = acc[t];
+      }
+    }
   }
 
-  // Run the top-k once on a row of zeros while the router is still working:
-  // it is straight-line code met once per launch, and this brings it into
-  // the instruction cache before the real call.
-  if (warp < T) {
-    for (int i = lane; i <= E; i += 32) S.zero_row[i] = 0.f;
-    __syncwarp();
-    select_experts(S.zero_row, nullptr, E, K, a.shared, lane, S.warm_ids, S.warm_w, S.warm_g + warp);
+  // ---- grid barrier A: every logit written (the prelude kernel cleared the
+  // counters before this grid's wait below returns)
+  grid_dep_wait();
+  __syncthreads();
+  if (tid == 0) {
+    red_release_add(a.bar, 1u);
+    while (ld_acquire_u32(a.bar) < (unsigned)G) {
+      if (global_timer_ns() > deadline0) {
+        S.failed = 1;
+        atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      __nanosleep(20);
+    }
   }
-
-  grid_dep_wait();  // the router kernel (logits, cleared barrier, status) is complete
-  if (tid == 0) S.status_in = *reinterpret_cast<const volatile int32_t*>(a.status);
+  __syncthreads();
 
   // ---- phase 1a: top-k, renormalised weights, shared gate (warp per token)
   if (warp < T) select_experts(a.logits + (size_t)warp * (E + 1), a.bias, E, K, a.shared, lane, S.ids + warp * K,
                                S.w + warp * K, S.g + warp);
   __syncthreads();
-  if (S.status_in != 0) {  // an earlier kernel of this call failed
+  if (S.failed) {  // grid barrier A ran out
     if (producer && lane == 0) drain();
     return;
   }
@@ -486,16 +551,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   consumer_sync();
   if (tid == 0) {
     if (!S.failed) {
-      __threadfence();
-      atomicAdd(a.bar, 1u);
-      while (ld_acquire_u32(a.bar) < (unsigned)G) {
+      red_release_add(a.bar + 1, 1u);
+      while (ld_acquire_u32(a.bar + 1) < (unsigned)G) {
         if (global_timer_ns() > deadline0) {
           S.failed = 1;
           break;
         }
-        __nanosleep(32);
+        __nanosleep(20);
       }
-      __threadfence();
     }
     if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
   }
@@ -601,7 +664,8 @@ int sm_count(int dev) {
 
 constexpr size_t kDecDynamicLimit = 186 * 1024;  // 227 KB per block minus the static part (about 38 KB)
 
-// Dynamic shared memory: x16 [T][H] (phases 0-2) / h [R][I] (phase 4), then
+// Dynamic shared memory: x16 [T][H] and x bf16 [T][H] (phases 0-2) / h [R][I]
+// (phase 4), then
 // the ring. A stage holds one gate/up item (18H bytes: 32 code rows of H/2,
 // 32 scale rows and 32 bias rows of H/32) or W_down rows of `per_item` slots
 // (9I bytes each).
@@ -613,7 +677,7 @@ struct DecodeLayout {
 DecodeLayout decode_layout(const Geometry& g) {
   DecodeLayout L{};
   const int R = g.A + (g.shared ? g.T : 0);
-  const size_t xs = (size_t)g.T * g.H * 2, hs = (size_t)R * g.I * 2;
+  const size_t xs = 2 * (size_t)g.T * g.H * 2, hs = (size_t)R * g.I * 2;  // x16 + x bf16, or h
   L.ring_offset = ((xs > hs ? xs : hs) + 127) & ~size_t(127);
   const int big = g.H > g.I ? g.H : g.I;
   L.stage_bytes = 18 * (size_t)big;
@@ -637,7 +701,22 @@ bool decode_supported(const Geometry& g) {
   return sms > 0 && g.H / 16 <= sms && decode_layout(g).stages >= 2;
 }
 
+// Clears the decode kernel's two grid-barrier counters and the call's status
+// word, and lets the decode kernel start at once (it waits for this grid only
+// before its first barrier arrival).
+__global__ void decode_prelude_kernel(unsigned int* bar, int32_t* status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    bar[0] = 0u;
+    bar[1] = 0u;
+    *status = 0;
+  }
+}
+
 cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStream_t stream) {
+  decode_prelude_kernel<<<1, 32, 0, stream>>>(args_in.bar, args_in.status);
+  cudaError_t pe = cudaGetLastError();
+  if (pe != cudaSuccess) return pe;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

@@ -81,7 +81,9 @@ cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs&
 struct DecodeArgs {
   int T, H, I, E, K, shared;
   const uint16_t* x;     // bf16 [T][H]
-  const float* logits;   // [T][E+1] written by the router kernel
+  const uint16_t* wr;    // bf16 [E][H] router weights
+  const uint16_t* wsg;   // bf16 [H] shared-expert gate row, or null
+  float* logits;         // [T][E+1] written and read by the decode kernel
   const float* bias;     // [E] or null
   ExpertArgs gu, dn;
   int32_t* ids;
@@ -98,13 +100,15 @@ struct DecodeArgs {
   int32_t* status;
   __half* h;             // fp16 [A+T][I], K order permuted within groups of 8
   float* y;              // fp32 [T][H]
-  unsigned int* bar;     // grid-barrier counter, cleared by the router kernel
+  unsigned int* bar;     // two grid-barrier counters, cleared by launch_decode's prelude kernel
   long long timeout_ns;
   // ring geometry, filled in by launch_decode
   int stages, per_item;
   long long stage_bytes, ring_offset;
 };
 bool decode_supported(const Geometry& g);
+// Launches the prelude (clears the grid-barrier counters and the status
+// word) and then the decode kernel with programmatic dependent launch.
 cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);
 
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,

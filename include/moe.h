@@ -184,11 +184,12 @@ typedef enum moe_expert_path {
   MOE_PATH_GEMV = 1,        /* bandwidth-bound grouped GEMV (CUDA cores), any shape */
   MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 256 == 0 and I % 128 == 0
                                (else UNSUPPORTED_SHAPE) */
-  MOE_PATH_FUSED_DECODE = 3 /* router kernel + one fused kernel for top-k, tables, expert
-                               GEMVs and combine; needs T <= 4, H % 128 == 0,
-                               I % 128 == 0, H / 16 <= the SM count and 16-byte aligned
-                               codes, scales and biases (else UNSUPPORTED_SHAPE). Its
-                               events[2] == events[1] and events[4..5] == events[3] */
+  MOE_PATH_FUSED_DECODE = 3 /* a one-block prelude and one fused kernel for the router,
+                               top-k, tables, expert products and combine; needs T <= 4,
+                               H % 128 == 0, I % 128 == 0, H / 16 <= the SM count and
+                               16-byte aligned codes, scales and biases (else
+                               UNSUPPORTED_SHAPE). Its events[1] and events[2] follow
+                               events[0] at once and events[4..5] == events[3] */
 } moe_expert_path;
 
 /* moe_forward with a chosen expert path that also records caller-owned CUDA
