@@ -105,16 +105,28 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 
+// Waits for the mbarrier phase with the given parity, sleeping between polls
+// (up to 256 ns) so that waiting warps leave the issue slots to the warps
+// doing work. Returns false once *abort is set or the deadline passes (then
+// it sets *abort).
+__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t deadline) {
+  unsigned ns = 32;
+  while (!tc::mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (global_timer_ns() > deadline) {
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(ns);
+    ns = ns < 256 ? 2 * ns : 256;
+  }
+  return true;
+}
+
 // Arrival on a grid barrier: release orders the block's earlier writes (made
 // visible to this thread by the preceding block barrier) before the add.
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// One arrival on `bar` once every cp.async this thread issued so far has
-// landed (the barrier's expected count includes it).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
 }
 
 // d += A * B with A 16x16 (row), B 16x8 (col), fp16 in, fp32 accumulate.
@@ -246,12 +258,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   uint8_t* ring = dsm_raw + a.ring_offset;
   const uint64_t deadline0 = global_timer_ns() + (uint64_t)a.timeout_ns;
 
-  // ---- ring producer (the producer warp): item i -> stage i % NST. The
-  // big contiguous parts (code rows) are single bulk copies posted by lane 0
-  // (each copy costs the copy engine a fixed slot, so there are few of
-  // them); the small scale and bias rows are 16-byte cp.async copies spread
-  // over the 32 lanes, each lane then arriving on the stage's mbarrier once
-  // its copies have landed (cp.async.mbarrier.arrive.noinc).
+  // ---- ring producer (the producer warp): item i -> stage i % NST. Every
+  // part of an item is one bulk copy, each posted by its own lane in a single
+  // instruction; the producer shares its scheduler with busy consumer warps,
+  // so it keeps its own instruction count per item small.
   int n2 = 0;  // gate/up items of this block (known after routing); down items follow them
   const uint32_t gcb = 16u * (H / 2), gsb = 16u * gpr * 2;     // gate/up item: 16 code rows / scale rows
   const uint32_t dcb = 16u * (I / 2), dsb = 16u * igpr * 2;    // down item, per slot: 16 code rows / scale rows
@@ -262,36 +272,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     if (nslots < 0 || i < n2) {  // gate/up item (nslots < 0: the shared item issued before routing)
       const int u = b + i * G;
       const int s = u / cpb, n0 = (u - s * cpb) * 16;
-      const uint8_t* cb = nslots < 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_codes) : S.slot_src[s][0];
-      const uint8_t* sc = nslots < 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_scales) : S.slot_src[s][1];
-      const uint8_t* bi = nslots < 0 ? reinterpret_cast<const uint8_t*>(a.gu.s_biases) : S.slot_src[s][2];
-      if (lane == 0) {
-        tc::mbar_arrive_expect_tx(bar, 2 * gcb);
-        bulk_g2s(dst, cb + (size_t)n0 * (H / 2), gcb, bar);
-        bulk_g2s(dst + gcb, cb + (size_t)(I + n0) * (H / 2), gcb, bar);
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar, 2 * gcb + 4 * gsb);
+      __syncwarp();
+      if (lane < 6) {
+        // lane: 0 gate codes, 1 up codes, 2 gate scales, 3 up scales, 4 gate biases, 5 up biases
+        const int kind = lane >> 1, up = lane & 1;
+        const uint8_t* base = nslots >= 0 ? S.slot_src[s][kind]
+                              : reinterpret_cast<const uint8_t*>(kind == 0 ? (const void*)a.gu.s_codes
+                                                                 : kind == 1 ? (const void*)a.gu.s_scales
+                                                                             : (const void*)a.gu.s_biases);
+        const size_t row = up ? (size_t)(I + n0) : (size_t)n0;
+        const uint32_t rb = kind == 0 ? (uint32_t)(H / 2) : (uint32_t)gpr * 2;
+        const uint32_t off = kind == 0 ? up * gcb : 2 * gcb + (uint32_t)(lane - 2) * gsb;
+        bulk_g2s(dst + off, base + row * rb, kind == 0 ? gcb : gsb, bar);
       }
-      // gate scales, up scales, gate biases, up biases: 4 runs of gsb bytes
-      for (uint32_t o = 16u * lane; o < 4 * gsb; o += 16u * 32) {
-        const uint32_t run = o / gsb, r = o - run * gsb;
-        const size_t row0 = (run & 1) ? (size_t)(I + n0) : (size_t)n0;
-        tc::cp_async_16(dst + 2 * gcb + o, (run < 2 ? sc : bi) + row0 * gpr * 2 + r, 16);
-      }
-      cp_async_arrive_noinc(bar);
     } else {  // down item: rows m0..m0+15 of slots p0..p0+np-1
       const int p0 = (i - n2) * per_item;
       const int np = min(per_item, nslots - p0);
-      const uint32_t per = dcb + 2 * dsb;
-      if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)np * dcb);
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)np * (dcb + 2 * dsb));
       __syncwarp();
-      if (lane < np) bulk_g2s(dst + (size_t)lane * per, S.slot_src[p0 + lane][3] + (size_t)m0 * (I / 2), dcb, bar);
-      // per slot: scales then biases, dsb bytes each
-      for (uint32_t o = 16u * lane; o < (uint32_t)np * 2 * dsb; o += 16u * 32) {
-        const uint32_t q = o / dsb, r = o - q * dsb;  // q = 2 * slot + (0 scales, 1 biases)
-        const int p = (int)(q >> 1);
-        tc::cp_async_16(dst + (size_t)p * per + dcb + (q & 1) * dsb + r,
-                        S.slot_src[p0 + p][4 + (q & 1)] + (size_t)m0 * igpr * 2 + r, 16);
+      for (int c = lane; c < 3 * np; c += 32) {  // lane: slot c / 3, part c % 3 (codes, scales, biases)
+        const int p = c / 3, kind = c - 3 * p;
+        const uint32_t rb = kind == 0 ? (uint32_t)(I / 2) : (uint32_t)igpr * 2;
+        const uint32_t off = (uint32_t)p * (dcb + 2 * dsb) + (kind == 0 ? 0u : dcb + (uint32_t)(kind - 1) * dsb);
+        bulk_g2s(dst + off, S.slot_src[p0 + p][3 + kind] + (size_t)m0 * rb, kind == 0 ? dcb : dsb, bar);
       }
-      cp_async_arrive_noinc(bar);
     }
   };
   int issued = 0;  // items issued so far (producer warp)
@@ -309,7 +314,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   if (producer) {
     if (lane == 0) {
       for (int st = 0; st < NST; ++st) {
-        tc::mbar_init(&S.full[st], 1 + 32);  // lane 0's expect_tx + one cp.async arrival per lane
+        tc::mbar_init(&S.full[st], 1);
         tc::mbar_init(&S.empty[st], kDecWarps);
       }
       tc::fence_barrier_init();
@@ -323,6 +328,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     }
   }
   for (int i = tid; i < kDecMaxSlots * kDecodeMaxTokens; i += kDecThreads) (&S.tok_row[0][0])[i] = -1;
+  // The router warps' first weight loads go out before x is staged (they do
+  // not depend on it).
+  const int rrows = E + (a.shared ? 1 : 0), rvec = H / 8;
+  const int r0 = b + G * warp;
+  const bool router_warp = warp < kDecWarps && r0 < rrows;
+  uint4 w4[8];
+  if (router_warp) {
+    const uint16_t* wrow = r0 < E ? a.wr + (size_t)r0 * H : a.wsg;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (lane + 32 * q < rvec) w4[q] = ldg_nc_v4(wrow + (size_t)(lane + 32 * q) * 8);
+  }
   for (int i = tid; i < T * H / 8; i += kDecThreads) {
     const uint4 v = ldg_nc_v4(a.x + (size_t)i * 8);
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -345,45 +362,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   __syncthreads();
 
   // ---- phase R: router logits l[t][r] = x[t] . W_r[r] (r = E: the shared
-  // expert's gate row), fp32, rows r = b + G * warp
-  {
-    const int rows = E + (a.shared ? 1 : 0);
-    const int vec = H / 8;  // 16-byte chunks of a row
-    for (int r = b + G * warp; warp < kDecWarps && r < rows; r += G * kDecWarps) {
-      const uint16_t* wrow = r < E ? a.wr + (size_t)r * H : a.wsg;
-      float acc[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-      for (int v0 = lane; v0 < vec; v0 += 32 * 8) {
-        uint4 w4[8];
+  // expert's gate row), fp32, rows r = b + G * warp (+ G * 16 ...)
+  for (int r = r0; router_warp && r < rrows; r += G * kDecWarps) {
+    const uint16_t* wrow = r < E ? a.wr + (size_t)r * H : a.wsg;
+    float acc[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+    for (int v0 = lane; v0 < rvec; v0 += 32 * 8) {
+      if (r != r0 || v0 != lane) {  // the first batch was loaded before the x staging
 #pragma unroll
         for (int q = 0; q < 8; ++q)  // every load of the batch before any use
-          if (v0 + 32 * q < vec) w4[q] = ldg_nc_v4(wrow + (size_t)(v0 + 32 * q) * 8);
+          if (v0 + 32 * q < rvec) w4[q] = ldg_nc_v4(wrow + (size_t)(v0 + 32 * q) * 8);
+      }
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int v = v0 + 32 * q;
-          if (v < vec) {
-            const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
+      for (int q = 0; q < 8; ++q) {
+        const int v = v0 + 32 * q;
+        if (v < rvec) {
+          const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
 #pragma unroll
-            for (int t = 0; t < kDecodeMaxTokens; ++t)
-              if (t < T) {
-                const uint4 x4 = *reinterpret_cast<const uint4*>(xraw + (size_t)t * H + (size_t)v * 8);
-                const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
-                float sacc = acc[t];
+          for (int t = 0; t < kDecodeMaxTokens; ++t)
+            if (t < T) {
+              const uint4 x4 = *reinterpret_cast<const uint4*>(xraw + (size_t)t * H + (size_t)v * 8);
+              const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
+              float sacc = acc[t];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                  sacc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), bf16_bits_to_f32(xv[m] & 0xFFFFu), sacc);
-                  sacc = fmaf(bf16_bits_to_f32(ww[m] >> 16), bf16_bits_to_f32(xv[m] >> 16), sacc);
-                }
-                acc[t] = sacc;
+              for (int m = 0; m < 4; ++m) {
+                sacc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), bf16_bits_to_f32(xv[m] & 0xFFFFu), sacc);
+                sacc = fmaf(bf16_bits_to_f32(ww[m] >> 16), bf16_bits_to_f32(xv[m] >> 16), sacc);
               }
-          }
+              acc[t] = sacc;
+            }
         }
       }
+    }
 #pragma unroll
-      for (int t = 0; t < kDecodeMaxTokens; ++t) {
+    for (int t = 0; t < kDecodeMaxTokens; ++t) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-        if (lane == 0 && t < T) a.logits[(size_t)t * (E + 1) + r] = acc[t];
-      }
+      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
+      if (lane == 0 && t < T) a.logits[(size_t)t * (E + 1) + r] = acc[t];
     }
   }
 
@@ -478,7 +492,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   if (producer) {
     for (int i = issued; i < items; ++i) {
       // stage i % NST is free once every consumer warp released item i - NST
-      if (i >= NST && !tc::mbar_wait(&S.empty[i % NST], (uint32_t)((i / NST - 1) & 1), &S.pfail, deadline0))
+      if (i >= NST && !ring_wait(&S.empty[i % NST], (uint32_t)((i / NST - 1) & 1), &S.pfail, deadline0))
         break;
       issue(i, nslots);
       issued = i + 1;
@@ -496,7 +510,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     // math), so all of them pass the same named barriers.
     const int st = i % NST;
     const uint8_t* sp = ring + (size_t)st * stage_bytes;
-    const bool ok = tc::mbar_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0);
+    const bool ok = ring_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0);
     const int u = b + i * G;
     const int s = u / cpb, n0 = (u - s * cpb) * 16;
     const int nr = S.slot_n[s];
@@ -614,7 +628,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   for (int i = n2; i < items; ++i) {
     const int st = i % NST;
     const uint8_t* sp = ring + (size_t)st * stage_bytes;
-    if (tc::mbar_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0)) {
+    if (ring_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0)) {
       const int p0 = (i - n2) * per_item;
       const int np = min(per_item, nslots - p0);
       for (int task = warp; task < np * kbs; task += kDecWarps) {
