@@ -43,8 +43,12 @@ METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM 
 CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_expert_moe_gb300", "csrc")
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
-        bytes=16004096, profile="profiles/decode_layer_kernel_decode-t1.md",
-        sources={"decode.cu": "1be64f3aae21e25e034544dbfe246f3f82cc6d6d733c13bc34b4d746127e5031",
+        bytes=17065472, profile="profiles/decode_layer_kernel_decode-t1.md",
+        sources={"decode.cu": "c1e75c302302b2849d815d308de10cd6e9580cab8b012ad127f25870e678b8eb",
+                 "tc_ptx.cuh": "6c9ad49fafff54e9934cda2050748b22b772c935d212e758ccabc4462eac373c"}),
+    ("fused_decode_layer", "decode-t4"): dict(
+        bytes=56006144 + 541952, profile="profiles/decode_layer_kernel_decode-t4.md",
+        sources={"decode.cu": "c1e75c302302b2849d815d308de10cd6e9580cab8b012ad127f25870e678b8eb",
                  "tc_ptx.cuh": "6c9ad49fafff54e9934cda2050748b22b772c935d212e758ccabc4462eac373c"}),
     ("expert_gate_up", "prefill-4096"): dict(
         bytes=402761216 + 27343872, profile="profiles/expert_tc_kernel_prefill-4096.md",
@@ -211,7 +215,8 @@ class Workload:
             tot_bytes += per_call * self.calls
             gu_bytes += n_exp * (2 * I * H * BYTES_PER_WEIGHT) * self.calls
             gu_flops += (s.top_k + (1 if s.shared else 0)) * self.T * 2 * (2 * I) * H * self.calls
-            fused_bytes += (n_exp * wbytes_expert + self.T * H * 6 + self.T * (E + 1) * 4) * self.calls
+            # the fused kernel also reads the router weights (it computes the logits itself)
+            fused_bytes += (n_exp * wbytes_expert + router_bytes + self.T * H * 6 + self.T * (E + 1) * 8) * self.calls
         flops_tok = 2 * H * E + s.top_k * 6 * H * I + (6 * H * I if s.shared else 0) + (2 * H if s.shared else 0)
         return dict(bytes_per_step=tot_bytes, gate_up_bytes_per_step=gu_bytes, fused_bytes_per_step=fused_bytes,
                     gate_up_flops_per_step=gu_flops,
