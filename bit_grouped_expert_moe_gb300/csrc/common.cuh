@@ -36,6 +36,73 @@ __device__ __forceinline__ uint32_t float_order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inverse of float_order_key for the keys it produces from finite values.
+__device__ __forceinline__ float order_key_to_float(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Top-k of one token by one warp over lrow[0..E) (+ bias), with ties to the
+// lower expert index, and the renormalised softmax weight of each pick:
+// lane k < K returns pick k in *e_out and its weight in *w_out; every lane
+// returns sigmoid(lrow[E]) in *gate_out when `shared`.
+// Every logit load is issued before any is used (one L2 round trip); keys
+// are fp32 order keys (0 marks an empty or taken entry: a finite logit never
+// maps to 0). Each lane keeps the best of its own entries; a round takes the
+// warp maximum and, among the lanes holding it, the lowest expert index.
+__device__ __forceinline__ void warp_topk(const float* lrow, const float* bias, int E, int K, bool shared, int lane,
+                                          int* e_out, float* w_out, float* gate_out) {
+  float lv[kMaxExperts / 32], bv[kMaxExperts / 32];
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) lv[j] = __ldcg(lrow + min(lane + 32 * j, E - 1));
+  const float gate_logit = __ldcg(lrow + (shared ? E : 0));
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) bv[j] = bias ? __ldg(bias + min(lane + 32 * j, E - 1)) : 0.f;
+  uint32_t key[kMaxExperts / 32];
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) key[j] = lane + 32 * j < E ? float_order_key(lv[j] + bv[j]) : 0u;
+  uint32_t lb = 0u;
+  int lbj = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j)
+    if (key[j] > lb) {
+      lb = key[j];
+      lbj = j;
+    }
+  uint32_t my_key = 0u, top_key = 0u;
+  int my_e = 0;
+  for (int k = 0; k < K; ++k) {
+    const uint32_t M = __reduce_max_sync(0xffffffffu, lb);
+    const uint32_t ew = __reduce_min_sync(0xffffffffu, lb == M ? (uint32_t)(lane + 32 * lbj) : 0xFFFFFFFFu);
+    if (k == 0) top_key = M;
+    if (lane == k) {
+      my_key = M;
+      my_e = (int)ew;
+    }
+    if (lane == (int)(ew & 31u)) {
+      const int jr = (int)(ew >> 5);
+      lb = 0u;
+      lbj = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxExperts / 32; ++j) {
+        if (j == jr) key[j] = 0u;
+        if (key[j] > lb) {
+          lb = key[j];
+          lbj = j;
+        }
+      }
+    }
+  }
+  // weights: exp(v_k - v_0) / sum over the selected (lanes k < K in parallel)
+  const float z = lane < K ? expf(order_key_to_float(my_key) - order_key_to_float(top_key)) : 0.f;
+  float sum = z;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  *e_out = my_e;
+  *w_out = z / sum;
+  *gate_out = shared ? 1.f / (1.f + expf(-gate_logit)) : 0.f;
+}
+
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");

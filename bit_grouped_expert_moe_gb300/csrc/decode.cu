@@ -83,10 +83,6 @@ struct DecodeSmall {
   float part[2][2][kDecWarps][4][32];            // per-warp MMA partials: [item parity][sub-unit][warp][reg][lane]
 };
 
-__device__ __forceinline__ float dec_key_to_float(uint32_t k) {
-  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-  return __uint_as_float(u);
-}
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -168,68 +164,6 @@ __device__ __forceinline__ void load_b(uint4 (&xb)[4], const __half* row, bool l
     xb[w] = live ? *reinterpret_cast<const uint4*>(row + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// Top-k of one token by one warp: ids (best first), renormalised softmax
-// weights and the shared-expert gate. The logits come from other blocks of
-// the same kernel (read through L2). Keys are fp32 order keys (0 marks an
-// empty or taken entry; a finite logit never maps to 0). Each lane keeps the
-// best of its own 8 entries; a round takes the warp maximum and, among lanes
-// holding it, the lowest expert index, so equal logits go to the lower index.
-__device__ __forceinline__ void select_experts(const float* lrow, const float* bias, int E, int K, int shared, int lane,
-                                            int* ids_out, float* w_out, float* g_out) {
-  // All loads first (clamped indices, no branches between them), so the row
-  // costs one round trip instead of one per load.
-  float lv[kMaxExperts / 32], bv[kMaxExperts / 32];
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) lv[j] = __ldcg(lrow + min(lane + 32 * j, E - 1));
-  const float gate_logit = __ldcg(lrow + (shared ? E : 0));
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) bv[j] = bias ? __ldg(bias + min(lane + 32 * j, E - 1)) : 0.f;
-  uint32_t key[kMaxExperts / 32];
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) key[j] = lane + 32 * j < E ? float_order_key(lv[j] + bv[j]) : 0u;
-  uint32_t lb = 0u;
-  int lbj = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j)
-    if (key[j] > lb) {
-      lb = key[j];
-      lbj = j;
-    }
-  uint32_t my_key = 0u, top_key = 0u;
-  int my_e = 0;
-  for (int k = 0; k < K; ++k) {
-    const uint32_t M = __reduce_max_sync(0xffffffffu, lb);
-    const uint32_t ew = __reduce_min_sync(0xffffffffu, lb == M ? (uint32_t)(lane + 32 * lbj) : 0xFFFFFFFFu);
-    if (k == 0) top_key = M;
-    if (lane == k) {
-      my_key = M;
-      my_e = (int)ew;
-    }
-    if (lane == (int)(ew & 31u)) {
-      const int jr = (int)(ew >> 5);
-      lb = 0u;
-      lbj = 0;
-#pragma unroll
-      for (int j = 0; j < kMaxExperts / 32; ++j) {
-        if (j == jr) key[j] = 0u;
-        if (key[j] > lb) {
-          lb = key[j];
-          lbj = j;
-        }
-      }
-    }
-  }
-  // weights: exp(v_k - v_0) / sum over the selected (lanes k < K in parallel)
-  const float z = lane < K ? expf(dec_key_to_float(my_key) - dec_key_to_float(top_key)) : 0.f;
-  float sum = z;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  if (lane < K) {
-    ids_out[lane] = my_e;
-    w_out[lane] = z / sum;
-  }
-  if (lane == 0) *g_out = shared ? 1.f / (1.f + expf(-gate_logit)) : 0.f;  // (gate_logit unused otherwise)
-}
 
 // Named barrier of the 16 consumer warps (the producer warp never joins it).
 __device__ __forceinline__ void consumer_sync() {
@@ -419,8 +353,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   __syncthreads();
 
   // ---- phase 1a: top-k, renormalised weights, shared gate (warp per token)
-  if (warp < T) select_experts(a.logits + (size_t)warp * (E + 1), a.bias, E, K, a.shared, lane, S.ids + warp * K,
-                               S.w + warp * K, S.g + warp);
+  if (warp < T) {
+    int e;
+    float w, g;
+    warp_topk(a.logits + (size_t)warp * (E + 1), a.bias, E, K, a.shared, lane, &e, &w, &g);
+    if (lane < K) {
+      S.ids[warp * K + lane] = e;
+      S.w[warp * K + lane] = w;
+    }
+    if (lane == 0) S.g[warp] = g;
+  }
   __syncthreads();
   if (S.failed) {  // grid barrier A ran out
     if (producer && lane == 0) drain();

@@ -56,11 +56,6 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return before + incl - v;
 }
 
-__device__ __forceinline__ float key_to_float(uint32_t k) {
-  const uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-  return __uint_as_float(u);
-}
-
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   extern __shared__ __align__(16) int smem[];
   const int E = a.E, K = a.K;
@@ -83,56 +78,15 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   // ---- top-k, renormalised softmax weights and shared gate (warp per token)
   for (int tl = warp; tl < nt; tl += kRouteWarps) {
     const int t = t0 + tl;
-    const float* lrow = a.logits + (size_t)t * (E + 1);
-    unsigned long long key[kMaxExperts / 32];
-#pragma unroll
-    for (int j = 0; j < kMaxExperts / 32; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = 0ull;
-      if (e < E) {
-        const float v = lrow[e] + (a.bias ? a.bias[e] : 0.f);
-        key[j] = ((unsigned long long)float_order_key(v) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-      }
+    int e;
+    float w, g;
+    warp_topk(a.logits + (size_t)t * (E + 1), a.bias, E, K, a.shared != 0, lane, &e, &w, &g);
+    if (lane < K) {
+      a.ids[(size_t)t * K + lane] = e;
+      a.weights[(size_t)t * K + lane] = w;
+      ids_s[tl * K + lane] = e;
     }
-    float sel_v[kMaxTopK];
-    int sel_e[kMaxTopK];
-#pragma unroll
-    for (int k = 0; k < kMaxTopK; ++k) {
-      if (k < K) {
-        unsigned long long best = key[0];
-#pragma unroll
-        for (int j = 1; j < kMaxExperts / 32; ++j) best = key[j] > best ? key[j] : best;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-          best = other > best ? other : best;
-        }
-        const int e = (int)(0xFFFFFFFFu - (uint32_t)best);
-        sel_e[k] = e;
-        sel_v[k] = key_to_float((uint32_t)(best >> 32));
-#pragma unroll
-        for (int j = 0; j < kMaxExperts / 32; ++j)
-          if (lane == (e & 31) && j == (e >> 5)) key[j] = 0ull;
-      }
-    }
-    if (lane == 0) {
-      float z[kMaxTopK];
-      float sum = 0.f;
-#pragma unroll
-      for (int k = 0; k < kMaxTopK; ++k)
-        if (k < K) {
-          z[k] = expf(sel_v[k] - sel_v[0]);
-          sum += z[k];
-        }
-#pragma unroll
-      for (int k = 0; k < kMaxTopK; ++k)
-        if (k < K) {
-          a.ids[(size_t)t * K + k] = sel_e[k];
-          a.weights[(size_t)t * K + k] = z[k] / sum;
-          ids_s[tl * K + k] = sel_e[k];
-        }
-      if (a.shared) a.gate[t] = 1.f / (1.f + expf(-lrow[E]));
-    }
+    if (lane == 0 && a.shared) a.gate[t] = g;
   }
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) hist[i] = 0;
   __syncthreads();
