@@ -21,6 +21,8 @@ namespace bgmoe {
 using namespace tc;
 
 constexpr int kRtThreads = 256;
+constexpr int kRtWarps = kRtThreads / 32;
+constexpr int kMaxH = 2048;                 // largest H this kernel serves (larger: the CUDA-core router)
 constexpr int kRtStages = 4;
 constexpr int kRtTok = 64;                  // tokens per block (MMA N)
 constexpr int kRtA = 128 * 128;             // 128 experts x 64 k bf16
@@ -125,19 +127,33 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
       }
       mma_commit(&ctl->acc_full);
     }
-  } else if (warp < 4) {
-    // shared-gate logit and fp16 copy of x for this block's tokens
+  }
+  if (warp >= 2) {
+    // Shared-gate logit and fp16 copy of x for this block's tokens, on warps
+    // 2-7 (the epilogue warps have nothing to do until the accumulator is
+    // ready): w_sg stays in registers, and all of a token's x loads go out
+    // before any is used.
     if (eb == 0 && (p.wsg != nullptr || p.x16 != nullptr)) {
       const int per_lane = p.H / 256;  // 16-byte chunks per lane (H % 512 == 0 on this path)
-      for (int tl = warp - 2; tl < kRtTok; tl += 2) {
+      constexpr int kMaxPer = kMaxH / 256;
+      uint4 wv[kMaxPer];
+#pragma unroll
+      for (int i = 0; i < kMaxPer; ++i)
+        if (i < per_lane && p.wsg != nullptr) wv[i] = ldg_nc_v4(p.wsg + (lane + 32 * i) * 8);
+      for (int tl = warp - 2; tl < kRtTok; tl += kRtWarps - 2) {
         const int t = t0 + tl;
         if (t >= p.T) break;
         const uint16_t* xr = p.x + (size_t)t * p.H;
+        uint4 xv[kMaxPer];
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i)
+          if (i < per_lane) xv[i] = ldg_nc_v4(xr + (lane + 32 * i) * 8);
         float acc = 0.f;
-        for (int i = 0; i < per_lane; ++i) {
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i) {
+          if (i >= per_lane) break;
           const int k0 = (lane + 32 * i) * 8;
-          const uint4 xv = ldg_nc_v4(xr + k0);
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          const uint32_t xw[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
           float xf[8];
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
@@ -145,8 +161,7 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             xf[2 * m + 1] = bf16_bits_to_f32(xw[m] >> 16);
           }
           if (p.wsg != nullptr) {
-            const uint4 wv = ldg_nc_v4(p.wsg + k0);
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+            const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               acc = fmaf(xf[2 * m], bf16_bits_to_f32(ww[m] & 0xFFFFu), acc);
@@ -172,7 +187,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
         }
       }
     }
-  } else {
+  }
+  if (warp >= 4) {
     // epilogue: lane = expert, column = token
     const int q = warp & 3;
     if (mbar_wait(&ctl->acc_full, 0, abort_flag, deadline)) {
@@ -230,7 +246,7 @@ cudaError_t bf16_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
 }
 }  // namespace
 
-bool router_tc_supported(const Geometry& g) { return g.H % 512 == 0 && rt_encode_fn() != nullptr; }
+bool router_tc_supported(const Geometry& g) { return g.H % 512 == 0 && g.H <= kMaxH && rt_encode_fn() != nullptr; }
 
 cudaError_t launch_router_tc(const Geometry& g, const void* x, const void* wr, const void* wsg, float* logits,
                              unsigned long long* state, int n_state, int32_t* status, uint16_t* x16,
