@@ -231,6 +231,9 @@ WORKLOADS = {
     "decode-t4": LayerSpec("decode-t4", T=4, H=2048, I=512, seed=20260002, layers=40),
     "prefill-zipf-512": LayerSpec("prefill-zipf-512", T=512, H=2048, I=512, bias="zipf", seed=20260003),
     "prefill-4096": LayerSpec("prefill-4096", T=4096, H=2048, I=512, seed=20260004),
+    # 2048 tokens, unbiased router: the prompt length of the tile-height
+    # ablation (rows per expert tile, 16 -> 32 and beyond)
+    "prefill-2048": LayerSpec("prefill-2048", T=2048, H=2048, I=512, seed=20260006),
     "long-skew-16384": LayerSpec("long-skew-16384", T=16384, H=2048, I=512, bias="hot",
                                  hot_logit=1.65, seed=20260005, chunk=2048),
 }
