@@ -43,17 +43,20 @@ METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM 
 CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_expert_moe_gb300", "csrc")
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
-        bytes=17065472, profile="profiles/decode_layer_kernel_decode-t1.md",
-        sources={"decode.cu": "c1e75c302302b2849d815d308de10cd6e9580cab8b012ad127f25870e678b8eb",
-                 "tc_ptx.cuh": "6c9ad49fafff54e9934cda2050748b22b772c935d212e758ccabc4462eac373c"}),
+        bytes=17067264, profile="profiles/decode_layer_kernel_decode-t1.md",
+        sources={"decode.cu": "ef11f3fd1f7d2ca367faf5d274b014e6f0ad280922bf404b246f58caae7e0660",
+                 "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
+                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("fused_decode_layer", "decode-t4"): dict(
-        bytes=56006144 + 541952, profile="profiles/decode_layer_kernel_decode-t4.md",
-        sources={"decode.cu": "c1e75c302302b2849d815d308de10cd6e9580cab8b012ad127f25870e678b8eb",
-                 "tc_ptx.cuh": "6c9ad49fafff54e9934cda2050748b22b772c935d212e758ccabc4462eac373c"}),
+        bytes=56008448 + 532480, profile="profiles/decode_layer_kernel_decode-t4.md",
+        sources={"decode.cu": "ef11f3fd1f7d2ca367faf5d274b014e6f0ad280922bf404b246f58caae7e0660",
+                 "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
+                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=402761216 + 27343872, profile="profiles/expert_tc_kernel_prefill-4096.md",
+        bytes=401553920 + 27580928, profile="profiles/expert_tc_kernel_prefill-4096.md",
         sources={"gemm_tc.cu": "db9eb0bbb9984e0d1b5324361e7cbfdc3b905c71650b57e854168a9a67dca674",
-                 "tc_ptx.cuh": "6c9ad49fafff54e9934cda2050748b22b772c935d212e758ccabc4462eac373c"}),
+                 "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
+                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
 
 
