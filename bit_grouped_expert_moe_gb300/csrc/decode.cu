@@ -27,11 +27,14 @@
 // warp whose lane 0 issues the bulk copies (kept out of the consumer warps: a
 // lane issuing while its warp-mates wait on an mbarrier is held up by them).
 // A one-block prelude kernel clears the two grid-barrier counters and the
-// status word; this kernel starts at once (programmatic dependent launch) and
-// waits for the prelude only before its first barrier arrival. Phases:
-//   0  x is staged (fp16 in the permuted K order for the experts, bf16 for
-//      the router) and a block whose first item belongs to the shared expert
-//      (which every token uses) starts its copies;
+// status word. Both kernels use programmatic dependent launch: the prelude
+// starts while the previous layer's kernel finishes (after that kernel's
+// barrier B) and waits for it before clearing; this kernel starts at once,
+// loads weights, and waits for the prelude before it reads x. Phases:
+//   0  the router's first weight loads and, in a block whose first item
+//      belongs to the shared expert (which every token uses), that item's
+//      copies go out; after the wait x is staged (fp16 in the permuted K
+//      order for the experts, bf16 for the router);
 //   R  router logits: block b, warp w computes rows b + G*w, G*16 apart, and
 //      writes l[t][r] to global memory; grid barrier A;
 //   1  every block selects the top-k experts of the T tokens itself (reading
@@ -274,6 +277,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     for (int q = 0; q < 8; ++q)
       if (lane + 32 * q < rvec) w4[q] = ldg_nc_v4(wrow + (size_t)(lane + 32 * q) * 8);
   }
+  // Everything above reads only weights. x (and this call's workspace) may be
+  // the previous kernel's output: wait for the prelude, which itself waits
+  // for the previous layer's kernels to finish.
+  grid_dep_wait();
   for (int i = tid; i < T * H / 8; i += kDecThreads) {
     const uint4 v = ldg_nc_v4(a.x + (size_t)i * 8);
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
@@ -336,8 +343,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   }
 
   // ---- grid barrier A: every logit written (the prelude kernel cleared the
-  // counters before this grid's wait below returns)
-  grid_dep_wait();
+  // counters before this grid's wait returned)
   __syncthreads();
   if (tid == 0) {
     red_release_add(a.bar, 1u);
@@ -519,6 +525,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
   }
   consumer_sync();
+  // The next call's prelude may now be scheduled; it waits for this grid to
+  // finish before it clears the counters.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (S.failed) return;  // the producer drains the copies in flight
 
   // The routing outputs (same definitions as moe_route), written by the last
@@ -658,10 +667,14 @@ bool decode_supported(const Geometry& g) {
 }
 
 // Clears the decode kernel's two grid-barrier counters and the call's status
-// word, and lets the decode kernel start at once (it waits for this grid only
-// before its first barrier arrival).
+// word. Launched with programmatic dependent launch, it starts while the
+// previous kernel on the stream (often the previous layer's decode kernel) is
+// finishing, lets the decode kernel start at once, and waits for the previous
+// kernel to complete before it touches the counters; the decode kernel waits
+// for this grid before it reads x or the counters.
 __global__ void decode_prelude_kernel(unsigned int* bar, int32_t* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     bar[0] = 0u;
     bar[1] = 0u;
@@ -670,9 +683,19 @@ __global__ void decode_prelude_kernel(unsigned int* bar, int32_t* status) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStream_t stream) {
-  decode_prelude_kernel<<<1, 32, 0, stream>>>(args_in.bar, args_in.status);
-  cudaError_t pe = cudaGetLastError();
-  if (pe != cudaSuccess) return pe;
+  {
+    cudaLaunchConfig_t pc{};
+    pc.gridDim = dim3(1);
+    pc.blockDim = dim3(32);
+    pc.stream = stream;
+    cudaLaunchAttribute pa[1];
+    pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pa[0].val.programmaticStreamSerializationAllowed = 1;
+    pc.attrs = pa;
+    pc.numAttrs = 1;
+    const cudaError_t pe = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.bar, args_in.status);
+    if (pe != cudaSuccess) return pe;
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
