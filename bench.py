@@ -54,7 +54,7 @@ PROFILED_TRAFFIC = {
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
         bytes=401553920 + 27580928, profile="profiles/expert_tc_kernel_prefill-4096.md",
-        sources={"gemm_tc.cu": "db9eb0bbb9984e0d1b5324361e7cbfdc3b905c71650b57e854168a9a67dca674",
+        sources={"gemm_tc.cu": "c9eebdfedfe44e74156d7963bce257c0937de3bb3b0356e1b36ed5449f7fee74",
                  "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
