@@ -79,9 +79,11 @@ def lib() -> ctypes.CDLL:
         L.moe_route_noalloc.restype = i32
         L.moe_status_read.argtypes = [P, P, ctypes.POINTER(i32)]
         L.moe_test_route_stall.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P, sz, i32, ctypes.c_int64, P]
+        L.moe_test_decode_stall.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
+                                            ctypes.POINTER(RouteOutC), P, sz, i32, ctypes.c_int64, P]
         for f in ("moe_workspace_bytes", "moe_max_tiles", "moe_route_blocks", "moe_route", "moe_forward",
                   "moe_forward_timed",
-                  "moe_status_read", "moe_test_route_stall"):
+                  "moe_status_read", "moe_test_route_stall", "moe_test_decode_stall"):
             getattr(L, f).restype = i32
         _lib = L
     return _lib
@@ -202,6 +204,20 @@ def forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gat
                                    ctypes.byref(r) if r is not None else None, _ptr(workspace),
                                    workspace.numel() * workspace.element_size(), ev, int(path), _stream(stream)),
            "moe_forward_timed")
+
+
+def test_decode_stall(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, workspace, route_out: dict,
+                      stalled_block: int, timeout_ns: int, stream=None):
+    """moe_test_decode_stall: the fused decode path with one block that never
+    arrives at the kernel's second grid barrier and a short device timeout."""
+    ec = _experts_c(experts)
+    sc = _experts_c(shared)
+    r = _route_c(route_out)
+    _check(lib().moe_test_decode_stall(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(router_bias),
+                                       ctypes.byref(ec), ctypes.byref(sc) if sc is not None else None,
+                                       _ptr(w_shared_gate), _ptr(y), ctypes.byref(r), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), stalled_block, timeout_ns,
+                                       _stream(stream)), "moe_test_decode_stall")
 
 
 def status_read(status: torch.Tensor, stream=None) -> int:

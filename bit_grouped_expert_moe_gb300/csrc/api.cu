@@ -268,10 +268,14 @@ moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const voi
                       timeout_ns, stream);
 }
 
-moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* w_router,
-                             const float* router_bias, const moe_experts* experts, const moe_experts* shared,
-                             const void* w_shared_gate, float* y, const moe_route_out* route_out, void* workspace,
-                             size_t ws_bytes, void* const* events, int32_t expert_path, void* stream) {
+namespace {
+// moe_forward_timed, plus the test-only fused-decode stall: with
+// stall_block >= 0 that block of the fused decode kernel never arrives at its
+// second grid barrier and every wait of the call gives up after timeout_ns.
+moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,
+                        const moe_experts* experts, const moe_experts* shared, const void* w_shared_gate, float* y,
+                        const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* const* events,
+                        int32_t expert_path, void* stream, int32_t stall_block, int64_t timeout_ns) {
   moe_status st = check_shape(shape);
   if (expert_path < MOE_PATH_AUTO || expert_path > MOE_PATH_FUSED_DECODE) return MOE_ERR_INVALID_ARG;
   if (st != MOE_OK) return st;
@@ -355,7 +359,8 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
     d.h = w.h;
     d.y = y;
     d.bar = w.bar;
-    d.timeout_ns = kDefaultTimeoutNs;
+    d.timeout_ns = timeout_ns;
+    d.stall_block = stall_block;
     e = launch_decode(d, g, s);
     if (e != cudaSuccess) return cuda_fail(e, "fused decode launch");
     for (int i = 3; i < 6; ++i)
@@ -389,6 +394,26 @@ moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* 
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if ((e = mark(5)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;
+}
+
+}  // namespace
+
+moe_status moe_forward_timed(const moe_shape* shape, const void* x, const void* w_router,
+                             const float* router_bias, const moe_experts* experts, const moe_experts* shared,
+                             const void* w_shared_gate, float* y, const moe_route_out* route_out, void* workspace,
+                             size_t ws_bytes, void* const* events, int32_t expert_path, void* stream) {
+  return forward_impl(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out, workspace,
+                      ws_bytes, events, expert_path, stream, -1, kDefaultTimeoutNs);
+}
+
+moe_status moe_test_decode_stall(const moe_shape* shape, const void* x, const void* w_router,
+                                 const float* router_bias, const moe_experts* experts, const moe_experts* shared,
+                                 const void* w_shared_gate, float* y, const moe_route_out* route_out,
+                                 void* workspace, size_t ws_bytes, int32_t stalled_block, int64_t timeout_ns,
+                                 void* stream) {
+  if (stalled_block < 0 || timeout_ns <= 0 || timeout_ns > kDefaultTimeoutNs) return MOE_ERR_INVALID_ARG;
+  return forward_impl(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out, workspace,
+                      ws_bytes, nullptr, MOE_PATH_FUSED_DECODE, stream, stalled_block, timeout_ns);
 }
 
 moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,

@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   consumer_sync();
   if (tid == 0) {
     if (!S.failed) {
-      red_release_add(a.bar + 1, 1u);
+      if (b != a.stall_block) red_release_add(a.bar + 1, 1u);
       while (ld_acquire_u32(a.bar + 1) < (unsigned)G) {
         if (global_timer_ns() > deadline0) {
           S.failed = 1;

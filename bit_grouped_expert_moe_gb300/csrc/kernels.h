@@ -102,6 +102,7 @@ struct DecodeArgs {
   float* y;              // fp32 [T][H]
   unsigned int* bar;     // two grid-barrier counters, cleared by launch_decode's prelude kernel
   long long timeout_ns;
+  int stall_block;       // test only: this block never arrives at grid barrier B (-1: none)
   // ring geometry, filled in by launch_decode
   int stages, per_item;
   long long stage_bytes, ring_offset;

@@ -242,6 +242,21 @@ moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const voi
                                 const moe_route_out* out, void* workspace, size_t ws_bytes,
                                 int32_t stalled_block, int64_t timeout_ns, void* stream);
 
+/* Test hook for the fused decode kernel's failure path: moe_forward_timed
+ * with MOE_PATH_FUSED_DECODE, except that block `stalled_block` of the
+ * decode kernel never arrives at its second grid barrier and every device
+ * wait gives up after `timeout_ns` (0 < timeout_ns <= 1 s). The call's status
+ * word then reads MOE_ERR_DEVICE_TIMEOUT, every block has returned (having
+ * let its own copies land) and the context stays usable. Same arguments as
+ * moe_forward; UNSUPPORTED_SHAPE where the fused path is refused;
+ * INVALID_ARG for a negative block or a timeout out of range (a block index
+ * past the grid stalls nothing). */
+moe_status moe_test_decode_stall(const moe_shape* shape, const void* x, const void* w_router,
+                                 const float* router_bias, const moe_experts* experts, const moe_experts* shared,
+                                 const void* w_shared_gate, float* y, const moe_route_out* route_out,
+                                 void* workspace, size_t ws_bytes, int32_t stalled_block, int64_t timeout_ns,
+                                 void* stream);
+
 /* Number of thread blocks the routing kernel uses for `shape` on the current
  * device (the co-resident grid of the single-launch routing pipeline). */
 moe_status moe_route_blocks(const moe_shape* shape, int32_t* blocks);

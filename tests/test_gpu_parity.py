@@ -275,3 +275,29 @@ def test_device_timeout_is_reported_not_hung(moelib, cuda_dev):
     ids = out["ids"].cpu().numpy()[: 64 * 8].reshape(64, 8)
     ids_ref, *_ , logits = oracle.route(bits16(x), bits16(wr), None, bits16(wsg), 8)
     parity.check_ids(ids, ids_ref, logits, 8)
+
+
+def test_fused_decode_timeout_is_reported_not_hung(moelib, cuda_dev):
+    """One block of the fused decode kernel never arrives at its second grid
+    barrier: every block gives up after a 20 ms limit, lets its own copies
+    land and returns, the call reports MOE_ERR_DEVICE_TIMEOUT, and the next
+    normal call on the same context and workspace is correct."""
+    spec = synth.WORKLOADS["decode-t1"]
+    L = parity.device_layer(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    shape = moelib.make_shape(spec.T, spec.H, spec.I, spec.E, spec.top_k, spec.shared, 16)
+    routed, shared = parity.experts_arg(L)
+    ws = moelib.alloc_workspace(shape, cuda_dev)
+    y = torch.empty(spec.T, spec.H, dtype=torch.float32, device=cuda_dev)
+    ro = moelib.alloc_route_out(shape, cuda_dev)
+    moelib.test_decode_stall(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, ro, stalled_block=3,
+                             timeout_ns=20_000_000)
+    torch.cuda.synchronize()
+    assert moelib.status_read(ro["status"]) == moelib.MOE_ERR_DEVICE_TIMEOUT
+    moelib.forward_timed(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro,
+                         path=moelib.PATH_FUSED_DECODE)
+    torch.cuda.synchronize()
+    assert moelib.status_read(ro["status"]) == 0
+    y_ref, ids_ref, w_ref, g_ref, logits = parity.oracle_forward(spec, L, x)
+    excl = parity.check_ids(ro["ids"][: spec.top_k].cpu().numpy().reshape(1, -1), ids_ref, logits, spec.top_k)
+    parity.check_y(y.cpu().numpy(), y_ref, excl)
