@@ -309,15 +309,17 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
 
   // Expert path: the fused decode kernel for decode-sized calls, tensor
   // cores once the tile rows are many enough to feed them, else the GEMV.
-  // The fused decode kernel copies weight tiles with bulk async copies, which
-  // need 16-byte aligned sources.
+  // The fused decode kernel copies weight tiles with bulk async copies and
+  // the tensor-core kernels read codes, scales and biases 16 bytes at a
+  // time: both need 16-byte aligned weight arrays.
   auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   auto mat16 = [&](const moe_qmat& q) { return a16(q.codes) && a16(q.scales) && a16(q.biases); };
-  const bool dec_ok = decode_supported(g) && mat16(experts->gate_up) && mat16(experts->down) &&
-                      (!g.shared || (mat16(shared->gate_up) && mat16(shared->down)));
+  const bool aligned = mat16(experts->gate_up) && mat16(experts->down) &&
+                       (!g.shared || (mat16(shared->gate_up) && mat16(shared->down)));
+  const bool dec_ok = decode_supported(g) && aligned;
   if (expert_path == MOE_PATH_FUSED_DECODE && !dec_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   const bool fused = expert_path == MOE_PATH_FUSED_DECODE || (expert_path == MOE_PATH_AUTO && dec_ok);
-  const bool tc_ok = tc_path_supported(g);
+  const bool tc_ok = tc_path_supported(g) && aligned;
   if (expert_path == MOE_PATH_TENSOR_CORE && !tc_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   const bool tc = expert_path == MOE_PATH_TENSOR_CORE ||
                   (expert_path == MOE_PATH_AUTO && !fused && g.T >= kTensorCoreMinTokens && tc_ok);

@@ -23,7 +23,9 @@
 // Persistent blocks (one per SM) walk the items with a stride of the grid;
 // every ring runs on across item boundaries and the TMEM accumulator is
 // double buffered, so one item's epilogue overlaps the next item's MMAs.
-// Rings: codes (TMA) 4 deep, dequantised A 3 deep, B 5 deep.
+// Rings: codes (TMA) 4 deep, dequantised A 3 deep, B 5 deep; the MMAs of
+// each stage are committed once, to a ring of 8 stage-done barriers that
+// every producer of a slot waits on.
 // Warp roles (576 threads):
 //   warp 0      TMA producer: code tiles (and h boxes for the down GEMM)
 //   warp 1      TMEM allocation and the single MMA-issuing thread
@@ -81,6 +83,13 @@ static_assert(kAS - kAMargin <= 2, "the dequant may wait for the MMAs at most tw
 // The same rule for the gather's cp.async stores into a B slot.
 constexpr int kBMargin = BGMOE_TC_B_MARGIN;
 static_assert(kGatherLag + kBMargin <= kBS - 2, "the gather must keep a stage of slack");
+// One commit per stage: the MMAs of stage s arrive on stage_done[s % kDone],
+// which the dequantisation, the gather and the down kernel's B copies all
+// wait on. A waiter checks every stage in order, so it has seen the phase
+// kDone stages back before it tests a parity, and no waiter falls kDone
+// stages behind the MMAs (they need its output first).
+constexpr int kDone = 8;
+static_assert(kDone >= kAS && kDone >= kBS, "stage_done ring shorter than a data ring");
 constexpr int kMaxBN = 128;               // token rows per tile (block_m <= 128)
 constexpr int kTmemCols = 512;            // 2 buffers x (2 x 128 columns)
 constexpr int kCBytes = 8192;             // 256 rows x 32 B of codes
@@ -90,8 +99,9 @@ constexpr int kSmemData = kCS * kCBytes + kAS * kABytes + kBS * kBBytes;
 
 struct TcCtl {
   uint64_t c_full[kCS], c_empty[kCS];
-  uint64_t a_full[kAS], a_empty[kAS];
-  uint64_t b_full[kBS], b_empty[kBS];
+  uint64_t a_full[kAS];
+  uint64_t b_full[kBS];
+  uint64_t stage_done[kDone];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t mma_done;
   uint32_t tmem;
@@ -159,14 +169,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       mbar_init(&ctl->c_full[s], 1);
       mbar_init(&ctl->c_empty[s], 8);
     }
-    for (int s = 0; s < kAS; ++s) {
-      mbar_init(&ctl->a_full[s], 8);
-      mbar_init(&ctl->a_empty[s], 1);
-    }
-    for (int s = 0; s < kBS; ++s) {
-      mbar_init(&ctl->b_full[s], kGateUp ? 4 : 1);
-      mbar_init(&ctl->b_empty[s], 1);
-    }
+    for (int s = 0; s < kAS; ++s) mbar_init(&ctl->a_full[s], 8);
+    for (int s = 0; s < kBS; ++s) mbar_init(&ctl->b_full[s], kGateUp ? 4 : 1);
+    for (int s = 0; s < kDone; ++s) mbar_init(&ctl->stage_done[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->acc_full[b], 1);
       mbar_init(&ctl->acc_empty[b], 4);
@@ -218,8 +223,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           tma_load_2d(sC + cs * kCBytes + 4096, map, k * 8, r_hi, &ctl->c_full[cs]);
           issued_c = it + 1;
           if (!kGateUp) {
-            const int bs = it % kBS;
-            if (it >= kBS && !mbar_wait(&ctl->b_empty[bs], ((it / kBS) - 1) & 1, abort_flag, deadline)) {
+            const int bs = it % kBS, j = it - kBS;  // the MMAs of stage j last read this slot
+            if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) {
               ok = false;
               break;
             }
@@ -258,15 +263,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + as * kABytes), a1 = a0 + 16384, b = smem_u32(sB + bs * kBBytes);
+          // descriptor start addresses count 16-byte units: 16 fp16 along K
+          // is +2, the second 128-row half of the A stage (+16384 B) is +1024
+          const uint64_t da = sw128_desc(smem_u32(sA + as * kABytes));
+          const uint64_t db = sw128_desc(smem_u32(sB + bs * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc = (k | kk) != 0;
-            mma_f16(d0, sw128_desc(a0 + kk * 32), sw128_desc(b + kk * 32), idesc, acc);
-            mma_f16(d1, sw128_desc(a1 + kk * 32), sw128_desc(b + kk * 32), idesc, acc);
+            mma_f16(d0, da + 2 * kk, db + 2 * kk, idesc, acc);
+            mma_f16(d1, da + 1024 + 2 * kk, db + 2 * kk, idesc, acc);
           }
-          mma_commit(&ctl->a_empty[as]);
-          mma_commit(&ctl->b_empty[bs]);
+          mma_commit(&ctl->stage_done[it % kDone]);
         }
         if (ok) mma_commit(&ctl->acc_full[buf]);
       }
@@ -291,8 +298,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
         }
         for (int k = 0; k < num_k; ++k, ++it) {
           const int bs = it % kBS;
-          const int done = it - kBS + kBMargin;  // this stage's MMAs must be complete
-          if (done >= 0 && !mbar_wait(&ctl->b_empty[done % kBS], (done / kBS) & 1, abort_flag, deadline)) {
+          const int j = it - kBS + kBMargin;  // the MMAs of stage j must be complete
+          if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) {
             ok = false;
             break;
           }
@@ -326,8 +333,19 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     const int gpr = kdim / 64;        // groups (scale, bias) per weight row
     uint8_t* arow = sA + (r >> 7) * 16384 + (r & 127) * 128;
     const uint8_t* crow = sC + (r >> 7) * 4096 + (r & 127) * 32;
+    // This block runs `total` stages; the codes of stage it + 1 are read
+    // while the stores of stage it drain, and one lane then releases both
+    // the A slot of stage it and the code slot of stage it + 1.
+    const int total = ((items - 1 - (int)blockIdx.x) / G + 1) * num_k;
+    uint4 c0, c1;
+    bool ok = mbar_wait(&ctl->c_full[0], 0, abort_flag, deadline);
+    if (ok) {
+      c0 = *reinterpret_cast<const uint4*>(crow);
+      c1 = *reinterpret_cast<const uint4*>(crow + 16);
+    }
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(&ctl->c_empty[0]);
     int it = 0;
-    bool ok = true;
     for (int w = blockIdx.x; ok && w < items; w += G) {
       const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
       const int e = p.t.tile_expert[tile];
@@ -337,51 +355,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       else wrow = (size_t)sub * 256 + r + (sh ? 0 : (size_t)e * H);
       const uint16_t* srow = (sh ? p.s_scales : p.scales) + wrow * gpr;
       const uint16_t* brow = (sh ? p.s_biases : p.biases) + wrow * gpr;
-      // scales/biases: 8 groups per 16-byte load, the next 8 prefetched one
-      // chunk ahead (rows of a multiple of 8 groups); else one load per stage
-      const bool chunked = (gpr & 7) == 0;
-      uint4 sc = make_uint4(0, 0, 0, 0), bi = sc, sc_n = sc, bi_n = sc;
-      if (chunked) {
-        sc = ldg_nc_v4(srow);
-        bi = ldg_nc_v4(brow);
-        if (gpr > 8) {
-          sc_n = ldg_nc_v4(srow + 8);
-          bi_n = ldg_nc_v4(brow + 8);
-        }
-      }
-      for (int k = 0; k < num_k; ++k, ++it) {
-        __half2 s2, b2;
-        if (chunked) {
-          if ((k & 7) == 0 && k > 0) {
-            sc = sc_n;
-            bi = bi_n;
-            if (k + 8 < gpr) {
-              sc_n = ldg_nc_v4(srow + k + 8);
-              bi_n = ldg_nc_v4(brow + k + 8);
-            }
-          }
-          s2 = bf16_to_h2(bf16_of(sc, k & 7));
-          b2 = bf16_to_h2(bf16_of(bi, k & 7));
-        } else {
-          s2 = bf16_to_h2(__ldg(srow + k));
-          b2 = bf16_to_h2(__ldg(brow + k));
-        }
-        const int cs = it % kCS, as = it % kAS;
-        if (!mbar_wait(&ctl->c_full[cs], (it / kCS) & 1, abort_flag, deadline)) {
-          ok = false;
-          break;
-        }
-        const uint4 c0 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes + 16);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->c_empty[cs]);
+      // One stage: wait until the MMAs that last read this A slot are done,
+      // write the slot, read the next stage's codes while the stores drain,
+      // then one lane releases the slot and the code slot.
+      auto stage = [&](__half2 s2, __half2 b2) -> bool {
+        const int as = it % kAS;
         {
-          const int done = it - kAS + kAMargin;  // this stage's MMAs must be complete
-          if (done >= 0 &&
-              !mbar_wait(&ctl->a_empty[done % kAS], (done / kAS) & 1, abort_flag, deadline)) {
-            ok = false;
-            break;
-          }
+          const int j = it - kAS + kAMargin;  // the MMAs of stage j must be complete
+          if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) return false;
         }
         // the slot was last read by the tensor core (async proxy): order
         // those reads before these generic-proxy stores
@@ -393,9 +374,54 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           dequant8_f16(q < 4 ? u4_get(c0, q) : u4_get(c1, q - 4), s2, b2, o);
           *reinterpret_cast<uint4*>(dst + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
         }
+        const bool more = it + 1 < total;
+        const int cs = (it + 1) % kCS;
+        bool good = true;
+        if (more) {
+          if (mbar_wait(&ctl->c_full[cs], ((it + 1) / kCS) & 1, abort_flag, deadline)) {
+            c0 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes);
+            c1 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes + 16);
+          } else {
+            good = false;
+          }
+        }
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->a_full[as]);
+        if (lane == 0) {
+          mbar_arrive(&ctl->a_full[as]);
+          if (more && good) mbar_arrive(&ctl->c_empty[cs]);
+        }
+        ++it;
+        return good;
+      };
+      if ((gpr & 7) == 0) {
+        // scales/biases 8 groups per 16-byte load, the next 8 prefetched a
+        // chunk ahead; each chunk is converted to fp16 (scale, bias) pairs
+        // once and its 8 stages are unrolled so the pairs stay in registers
+        uint4 sc = ldg_nc_v4(srow), bi = ldg_nc_v4(brow);
+        for (int k0 = 0; ok && k0 < num_k; k0 += 8) {
+          uint32_t sb[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const __half2 h = __floats2half2_rn(bf16_bits_to_f32(bf16_of(sc, g)), bf16_bits_to_f32(bf16_of(bi, g)));
+            sb[g] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          if (k0 + 8 < num_k) {
+            sc = ldg_nc_v4(srow + k0 + 8);
+            bi = ldg_nc_v4(brow + k0 + 8);
+          }
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const __half2 h = *reinterpret_cast<const __half2*>(&sb[g]);
+            if (!stage(__low2half2(h), __high2half2(h))) {
+              ok = false;
+              break;
+            }
+          }
+        }
+      } else {
+        for (int k = 0; ok && k < num_k; ++k)
+          ok = stage(bf16_to_h2(__ldg(srow + k)), bf16_to_h2(__ldg(brow + k)));
       }
     }
   } else {

@@ -48,11 +48,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same condition (no suspension).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete, sleeping 32 ns
 // between polls. Returns false once `*abort` is set or the deadline passes
-// (then it sets *abort).
+// (then it sets *abort). A phase that has already completed is seen by the
+// non-blocking test, which returns sooner than a potentially blocking wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t deadline) {
+  if (mbar_test_wait(bar, parity)) return true;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;

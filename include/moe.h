@@ -182,8 +182,9 @@ typedef enum moe_expert_path {
   MOE_PATH_AUTO = 0,        /* fused decode for T <= 4 when its conditions hold, tensor
                                cores for T >= 64 when the shape allows, else GEMV */
   MOE_PATH_GEMV = 1,        /* bandwidth-bound grouped GEMV (CUDA cores), any shape */
-  MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 256 == 0 and I % 128 == 0
-                               (else UNSUPPORTED_SHAPE) */
+  MOE_PATH_TENSOR_CORE = 2, /* tcgen05 grouped GEMM; needs H % 256 == 0, I % 128 == 0 and
+                               16-byte aligned codes, scales and biases (else
+                               UNSUPPORTED_SHAPE) */
   MOE_PATH_FUSED_DECODE = 3 /* a one-block prelude and one fused kernel for the router,
                                top-k, tables, expert products and combine; needs T <= 4,
                                H % 128 == 0, I % 128 == 0, H / 16 <= the SM count and

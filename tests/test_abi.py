@@ -44,6 +44,7 @@ def test_workspace_bytes_grows_with_tokens(moelib):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(H=100), 2), (dict(I=96), 2), (dict(top_k=9), 2), (dict(E=300), 2), (dict(block_m=48), 2),
+    (dict(block_m=256), 2),
     (dict(group_size=32), 2), (dict(T=-1), 1), (dict(E=4, top_k=8), 2)])
 def test_shape_rejected(moelib, kw, code):
     args = dict(T=4, H=512, I=128, E=256, top_k=8, shared=True, block_m=16, group_size=64)
