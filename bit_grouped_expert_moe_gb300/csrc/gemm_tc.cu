@@ -190,83 +190,93 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
   const uint32_t tmem = ctl->tmem;
   const uint64_t deadline = global_timer_ns() + (uint64_t)p.timeout_ns;
 
+  // Warps 0 and 1 run their loops with all 32 lanes, so loop values stay
+  // warp-uniform; every lane waits and one elected lane issues.
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, deadline)) != 0;
+  };
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tmap(&tm_codes);
       prefetch_tmap(&tm_s_codes);
       if (!kGateUp) prefetch_tmap(&tm_h);
-      int it = 0, issued_c = 0, issued_b = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; ok && w < items; w += G) {
-        const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
-        const int e = p.t.tile_expert[tile], row0 = p.t.tile_row0[tile];
-        const bool sh = e == p.E;
-        const CUtensorMap* map = sh ? &tm_s_codes : &tm_codes;
-        // first weight row of each half of the item (gate/up: gate and up rows)
-        int r_lo, r_hi;
-        if (kGateUp) {
-          r_lo = (sh ? 0 : e * 2 * I) + sub * 128;
-          r_hi = r_lo + I;
-        } else {
-          r_lo = (sh ? 0 : e * H) + sub * 256;
-          r_hi = r_lo + 128;
+    }
+    int it = 0, issued_c = 0, issued_b = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < items; w += G) {
+      const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
+      const int e = p.t.tile_expert[tile], row0 = p.t.tile_row0[tile];
+      const bool sh = e == p.E;
+      const CUtensorMap* map = sh ? &tm_s_codes : &tm_codes;
+      // first weight row of each half of the item (gate/up: gate and up rows)
+      int r_lo, r_hi;
+      if (kGateUp) {
+        r_lo = (sh ? 0 : e * 2 * I) + sub * 128;
+        r_hi = r_lo + I;
+      } else {
+        r_lo = (sh ? 0 : e * H) + sub * 256;
+        r_hi = r_lo + 128;
+      }
+      for (int k = 0; k < num_k; ++k, ++it) {
+        const int cs = it % kCS;
+        if (it >= kCS && !warp_wait(&ctl->c_empty[cs], ((it / kCS) - 1) & 1)) {
+          ok = false;
+          break;
         }
-        for (int k = 0; k < num_k; ++k, ++it) {
-          const int cs = it % kCS;
-          if (it >= kCS && !mbar_wait(&ctl->c_empty[cs], ((it / kCS) - 1) & 1, abort_flag, deadline)) {
-            ok = false;
-            break;
-          }
+        if (elect_one()) {
           mbar_arrive_expect_tx(&ctl->c_full[cs], kCBytes);
           tma_load_2d(sC + cs * kCBytes, map, k * 8, r_lo, &ctl->c_full[cs]);
           tma_load_2d(sC + cs * kCBytes + 4096, map, k * 8, r_hi, &ctl->c_full[cs]);
-          issued_c = it + 1;
-          if (!kGateUp) {
-            const int bs = it % kBS, j = it - kBS;  // the MMAs of stage j last read this slot
-            if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&ctl->b_full[bs], (uint32_t)(p.BM * 128));
-            tma_load_2d(sB + bs * kBBytes, &tm_h, k * 64, row0, &ctl->b_full[bs]);
-            issued_b = it + 1;
-          }
         }
-      }
-      if (*abort_flag) {  // let this block's own copies land before it exits
-        int dummy = 0;
-        const uint64_t dl = global_timer_ns() + 100000000ull;
-        for (int i = issued_c - kCS < 0 ? 0 : issued_c - kCS; i < issued_c; ++i)
-          mbar_wait(&ctl->c_full[i % kCS], (i / kCS) & 1, &dummy, dl);
-        for (int i = issued_b - kBS < 0 ? 0 : issued_b - kBS; i < issued_b; ++i)
-          mbar_wait(&ctl->b_full[i % kBS], (i / kBS) & 1, &dummy, dl);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int it = 0, ii = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; ok && w < items; w += G, ++ii) {
-        const int tile = w / p.per_tile;
-        const int N = (p.t.tile_rows[tile] + 15) & ~15;
-        const uint32_t idesc = idesc_f16_f32(128, N);
-        const int buf = ii & 1;
-        if (ii >= 2 && !mbar_wait(&ctl->acc_empty[buf], ((ii >> 1) - 1) & 1, abort_flag, deadline)) break;
-        const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
-        for (int k = 0; k < num_k; ++k, ++it) {
-          const int as = it % kAS, bs = it % kBS;
-          if (!mbar_wait(&ctl->a_full[as], (it / kAS) & 1, abort_flag, deadline) ||
-              !mbar_wait(&ctl->b_full[bs], (it / kBS) & 1, abort_flag, deadline)) {
+        __syncwarp();
+        issued_c = it + 1;
+        if (!kGateUp) {
+          const int bs = it % kBS, j = it - kBS;  // the MMAs of stage j last read this slot
+          if (j >= 0 && !warp_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          // descriptor start addresses count 16-byte units: 16 fp16 along K
-          // is +2, the second 128-row half of the A stage (+16384 B) is +1024
-          const uint64_t da = sw128_desc(smem_u32(sA + as * kABytes));
-          const uint64_t db = sw128_desc(smem_u32(sB + bs * kBBytes));
+          if (elect_one()) {
+            mbar_arrive_expect_tx(&ctl->b_full[bs], (uint32_t)(p.BM * 128));
+            tma_load_2d(sB + bs * kBBytes, &tm_h, k * 64, row0, &ctl->b_full[bs]);
+          }
+          __syncwarp();
+          issued_b = it + 1;
+        }
+      }
+    }
+    if (lane == 0 && *abort_flag) {  // let this block's own copies land before it exits
+      int dummy = 0;
+      const uint64_t dl = global_timer_ns() + 100000000ull;
+      for (int i = issued_c - kCS < 0 ? 0 : issued_c - kCS; i < issued_c; ++i)
+        mbar_wait(&ctl->c_full[i % kCS], (i / kCS) & 1, &dummy, dl);
+      for (int i = issued_b - kBS < 0 ? 0 : issued_b - kBS; i < issued_b; ++i)
+        mbar_wait(&ctl->b_full[i % kBS], (i / kBS) & 1, &dummy, dl);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    int it = 0, ii = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < items; w += G, ++ii) {
+      const int tile = w / p.per_tile;
+      const int N = (p.t.tile_rows[tile] + 15) & ~15;
+      const uint32_t idesc = idesc_f16_f32(128, N);
+      const int buf = ii & 1;
+      if (ii >= 2 && !warp_wait(&ctl->acc_empty[buf], ((ii >> 1) - 1) & 1)) break;
+      const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
+      for (int k = 0; k < num_k; ++k, ++it) {
+        const int as = it % kAS, bs = it % kBS;
+        if (!warp_wait(&ctl->a_full[as], (it / kAS) & 1) || !warp_wait(&ctl->b_full[bs], (it / kBS) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // descriptor start addresses count 16-byte units: 16 fp16 along K
+        // is +2, the second 128-row half of the A stage (+16384 B) is +1024
+        const uint64_t da = sw128_desc(smem_u32(sA + as * kABytes));
+        const uint64_t db = sw128_desc(smem_u32(sB + bs * kBBytes));
+        if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t acc = (k | kk) != 0;
@@ -275,10 +285,12 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           }
           mma_commit(&ctl->stage_done[it % kDone]);
         }
-        if (ok) mma_commit(&ctl->acc_full[buf]);
+        __syncwarp();
       }
-      mma_commit(&ctl->mma_done);  // arrives once every issued MMA has finished
+      if (ok && lane == 0) mma_commit(&ctl->acc_full[buf]);
+      __syncwarp();
     }
+    if (lane == 0) mma_commit(&ctl->mma_done);  // arrives once every issued MMA has finished
   } else if (warp < 6) {
     // ------------------------------------------ gather of x token rows
     if (kGateUp) {
