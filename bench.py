@@ -43,19 +43,19 @@ METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM 
 CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_expert_moe_gb300", "csrc")
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
-        bytes=17067264, profile="profiles/decode_layer_kernel_decode-t1.md",
-        sources={"decode.cu": "ef11f3fd1f7d2ca367faf5d274b014e6f0ad280922bf404b246f58caae7e0660",
-                 "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
+        bytes=17068032, profile="profiles/decode_layer_kernel_decode-t1.md",
+        sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
+                 "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("fused_decode_layer", "decode-t4"): dict(
-        bytes=56008448 + 532480, profile="profiles/decode_layer_kernel_decode-t4.md",
-        sources={"decode.cu": "ef11f3fd1f7d2ca367faf5d274b014e6f0ad280922bf404b246f58caae7e0660",
-                 "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
+        bytes=56009216 + 542208, profile="profiles/decode_layer_kernel_decode-t4.md",
+        sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
+                 "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=401553920 + 27580928, profile="profiles/expert_tc_kernel_prefill-4096.md",
-        sources={"gemm_tc.cu": "c9eebdfedfe44e74156d7963bce257c0937de3bb3b0356e1b36ed5449f7fee74",
-                 "tc_ptx.cuh": "80ce5ca42b9c2a30a425cf20d273b4e5195ae1f1c1ad4c84492d97ab78b4d0b6",
+        bytes=403497216 + 26766080, profile="profiles/expert_tc_kernel_prefill-4096.md",
+        sources={"gemm_tc.cu": "25cb9fa7dad9735a12b90bbcc35db1b6a1d1864a27f92b61b89a5c7b70f94b04",
+                 "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
 
