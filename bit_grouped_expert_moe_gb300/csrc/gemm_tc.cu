@@ -204,9 +204,15 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     }
     int it = 0, issued_c = 0, issued_b = 0;
     bool ok = true;
+    // the next item's tile is looked up a whole item ahead
+    int e_nx = p.t.tile_expert[blockIdx.x / p.per_tile], row0_nx = p.t.tile_row0[blockIdx.x / p.per_tile];
     for (int w = blockIdx.x; ok && w < items; w += G) {
       const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
-      const int e = p.t.tile_expert[tile], row0 = p.t.tile_row0[tile];
+      const int e = e_nx, row0 = row0_nx;
+      if (w + G < items) {
+        e_nx = p.t.tile_expert[(w + G) / p.per_tile];
+        row0_nx = p.t.tile_row0[(w + G) / p.per_tile];
+      }
       const bool sh = e == p.E;
       const CUtensorMap* map = sh ? &tm_s_codes : &tm_codes;
       // first weight row of each half of the item (gate/up: gate and up rows)
@@ -258,9 +264,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     // ------------------------------------------------------- MMA issuer
     int it = 0, ii = 0;
     bool ok = true;
+    int rows_nx = p.t.tile_rows[blockIdx.x / p.per_tile];  // looked up a whole item ahead
     for (int w = blockIdx.x; ok && w < items; w += G, ++ii) {
-      const int tile = w / p.per_tile;
-      const int N = (p.t.tile_rows[tile] + 15) & ~15;
+      const int N = (rows_nx + 15) & ~15;
+      if (w + G < items) rows_nx = p.t.tile_rows[(w + G) / p.per_tile];
       const uint32_t idesc = idesc_f16_f32(128, N);
       const int buf = ii & 1;
       if (ii >= 2 && !warp_wait(&ctl->acc_empty[buf], ((ii >> 1) - 1) & 1)) break;
@@ -357,16 +364,37 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     }
     __syncwarp();
     if (lane == 0 && ok) mbar_arrive(&ctl->c_empty[0]);
-    int it = 0;
-    for (int w = blockIdx.x; ok && w < items; w += G) {
+    // Scale and bias rows of this thread's weight row in item w; the first
+    // 8-group chunk of the next item is loaded a whole item ahead.
+    const bool chunked = (gpr & 7) == 0;
+    auto rows_of = [&](int w, const uint16_t*& srow, const uint16_t*& brow) {
       const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
       const int e = p.t.tile_expert[tile];
       const bool sh = e == p.E;
       size_t wrow;
       if (kGateUp) wrow = (size_t)(r < 128 ? 0 : I) + sub * 128 + (r & 127) + (sh ? 0 : (size_t)e * 2 * I);
       else wrow = (size_t)sub * 256 + r + (sh ? 0 : (size_t)e * H);
-      const uint16_t* srow = (sh ? p.s_scales : p.scales) + wrow * gpr;
-      const uint16_t* brow = (sh ? p.s_biases : p.biases) + wrow * gpr;
+      srow = (sh ? p.s_scales : p.scales) + wrow * gpr;
+      brow = (sh ? p.s_biases : p.biases) + wrow * gpr;
+    };
+    const uint16_t *srow, *brow;
+    rows_of(blockIdx.x, srow, brow);
+    uint4 sc_first = make_uint4(0, 0, 0, 0), bi_first = sc_first;
+    if (chunked) {
+      sc_first = ldg_nc_v4(srow);
+      bi_first = ldg_nc_v4(brow);
+    }
+    int it = 0;
+    for (int w = blockIdx.x; ok && w < items; w += G) {
+      const uint16_t *srow_n = srow, *brow_n = brow;
+      uint4 sc_nx = sc_first, bi_nx = bi_first;
+      if (w + G < items) {
+        rows_of(w + G, srow_n, brow_n);
+        if (chunked) {
+          sc_nx = ldg_nc_v4(srow_n);
+          bi_nx = ldg_nc_v4(brow_n);
+        }
+      }
       // One stage: wait until the MMAs that last read this A slot are done,
       // write the slot, read the next stage's codes while the stores drain,
       // then one lane releases the slot and the code slot.
@@ -406,11 +434,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
         ++it;
         return good;
       };
-      if ((gpr & 7) == 0) {
+      if (chunked) {
         // scales/biases 8 groups per 16-byte load, the next 8 prefetched a
         // chunk ahead; each chunk is converted to fp16 (scale, bias) pairs
         // once and its 8 stages are unrolled so the pairs stay in registers
-        uint4 sc = ldg_nc_v4(srow), bi = ldg_nc_v4(brow);
+        uint4 sc = sc_first, bi = bi_first;
         for (int k0 = 0; ok && k0 < num_k; k0 += 8) {
           uint32_t sb[8];
 #pragma unroll
@@ -435,6 +463,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
         for (int k = 0; ok && k < num_k; ++k)
           ok = stage(bf16_to_h2(__ldg(srow + k)), bf16_to_h2(__ldg(brow + k)));
       }
+      srow = srow_n;
+      brow = brow_n;
+      sc_first = sc_nx;
+      bi_first = bi_nx;
     }
   } else {
     // -------------------------------------------------------- epilogue

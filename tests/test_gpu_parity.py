@@ -244,6 +244,21 @@ def test_deterministic(moelib, cuda_dev):
         assert np.array_equal(r1[k], r2[k]), k
 
 
+@pytest.mark.parametrize("name,bm", [("prefill-4096", 128), ("prefill-zipf-512", 64)])
+def test_tensor_core_repeatable(moelib, cuda_dev, name, bm):
+    """The tensor-core path has no atomics, so repeated runs must agree bit
+    for bit; a ring-slot race between the dequantisation, gather and MMA
+    warps would show up as differing values (and does, in builds that let
+    the dequantisation run three stages ahead of the completed MMAs)."""
+    spec = synth.WORKLOADS[name]
+    L = parity.device_layer(spec, 0, cuda_dev)
+    x = synth.activations(spec, device=cuda_dev)
+    y0, _ = parity.gpu_forward(moelib, spec, L, x, bm, path=moelib.PATH_TENSOR_CORE)
+    for _ in range(5):
+        y1, _ = parity.gpu_forward(moelib, spec, L, x, bm, path=moelib.PATH_TENSOR_CORE)
+        assert np.array_equal(y0.view(np.uint32), y1.view(np.uint32))
+
+
 def test_zero_tokens_is_noop(moelib, cuda_dev):
     spec = synth.LayerSpec("z", T=0, H=512, I=128)
     shape = moelib.make_shape(0, 512, 128)
