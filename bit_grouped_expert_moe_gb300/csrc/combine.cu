@@ -18,21 +18,35 @@ combine_kernel(int H, int K, int A, int shared, const __half* __restrict__ o, co
   const int t = blockIdx.x;
   const int c = (blockIdx.y * kCombineThreads + threadIdx.x) * 8;
   if (c >= H) return;
+  // Every load of the token goes out before any is used: the K row
+  // indices and weights, then the K + 1 rows of o (the shared row last).
+  int rows[kMaxTopK + 1];
+  float wt[kMaxTopK + 1];
+#pragma unroll
+  for (int k = 0; k < kMaxTopK; ++k) {
+    rows[k] = k < K ? inv[(size_t)t * K + k] : 0;
+    wt[k] = k < K ? weights[(size_t)t * K + k] : 0.f;
+  }
+  rows[kMaxTopK] = A + t;
+  wt[kMaxTopK] = shared ? gate[t] : 0.f;
+  uint4 v[kMaxTopK + 1];
+#pragma unroll
+  for (int k = 0; k <= kMaxTopK; ++k)
+    if (k < K || (k == kMaxTopK && shared)) v[k] = *reinterpret_cast<const uint4*>(o + (size_t)rows[k] * H + c);
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  auto add = [&](int row, float w) {
-    const uint4 v = *reinterpret_cast<const uint4*>(o + (size_t)row * H + c);
-    const __half2* h2 = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+  for (int k = 0; k <= kMaxTopK; ++k) {
+    if (!(k < K || (k == kMaxTopK && shared))) continue;
+    const __half2* h2 = reinterpret_cast<const __half2*>(&v[k]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = __half22float2(h2[i]);
-      acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
-      acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+      acc[2 * i] = fmaf(wt[k], f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wt[k], f.y, acc[2 * i + 1]);
     }
-  };
-  for (int k = 0; k < K; ++k) add(inv[(size_t)t * K + k], weights[(size_t)t * K + k]);
-  if (shared) add(A + t, gate[t]);
+  }
   float4* yo = reinterpret_cast<float4*>(y + (size_t)t * H + c);
   yo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);

@@ -90,43 +90,53 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const uint32_t tmem = ctl->tmem;
   const uint64_t deadline = global_timer_ns() + (uint64_t)p.timeout_ns;
 
+  // Warps 0 and 1 run their loops with all 32 lanes (values stay
+  // warp-uniform): every lane waits, one elected lane issues.
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, deadline)) != 0;
+  };
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&tm_w);
       prefetch_tmap(&tm_x);
-      int issued = 0;
-      for (int it = 0; it < num_k; ++it) {
-        const int s = it % kRtStages;
-        if (it >= kRtStages && !mbar_wait(&ctl->empty[s], ((it / kRtStages) - 1) & 1, abort_flag, deadline)) break;
-        uint8_t* st = sm + s * kRtStage;
+    }
+    int issued = 0;
+    for (int it = 0; it < num_k; ++it) {
+      const int s = it % kRtStages;
+      if (it >= kRtStages && !warp_wait(&ctl->empty[s], ((it / kRtStages) - 1) & 1)) break;
+      uint8_t* st = sm + s * kRtStage;
+      if (elect_one()) {
         mbar_arrive_expect_tx(&ctl->full[s], kRtStage);
         tma_load_2d(st, &tm_w, it * 64, eb * 128, &ctl->full[s]);
         tma_load_2d(st + kRtA, &tm_x, it * 64, t0, &ctl->full[s]);
-        issued = it + 1;
       }
-      if (*abort_flag) {
-        int dummy = 0;
-        const uint64_t dl = global_timer_ns() + 100000000ull;
-        for (int it = issued - kRtStages < 0 ? 0 : issued - kRtStages; it < issued; ++it)
-          mbar_wait(&ctl->full[it % kRtStages], (it / kRtStages) & 1, &dummy, dl);
-      }
+      __syncwarp();
+      issued = it + 1;
+    }
+    if (lane == 0 && *abort_flag) {
+      int dummy = 0;
+      const uint64_t dl = global_timer_ns() + 100000000ull;
+      for (int it = issued - kRtStages < 0 ? 0 : issued - kRtStages; it < issued; ++it)
+        mbar_wait(&ctl->full[it % kRtStages], (it / kRtStages) & 1, &dummy, dl);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // kind::f16 with bf16 A and B (format 1), fp32 accumulator
-      const uint32_t idesc = idesc_f16_f32(128, kRtTok) | (1u << 7) | (1u << 10);
-      for (int it = 0; it < num_k; ++it) {
-        const int s = it % kRtStages;
-        if (!mbar_wait(&ctl->full[s], (it / kRtStages) & 1, abort_flag, deadline)) break;
-        tc_fence_after();
-        const uint32_t a = smem_u32(sm + s * kRtStage), b = a + kRtA;
+    // kind::f16 with bf16 A and B (format 1), fp32 accumulator
+    const uint32_t idesc = idesc_f16_f32(128, kRtTok) | (1u << 7) | (1u << 10);
+    for (int it = 0; it < num_k; ++it) {
+      const int s = it % kRtStages;
+      if (!warp_wait(&ctl->full[s], (it / kRtStages) & 1)) break;
+      tc_fence_after();
+      const uint64_t da = sw128_desc(smem_u32(sm + s * kRtStage));
+      const uint64_t db = sw128_desc(smem_u32(sm + s * kRtStage + kRtA));
+      if (elect_one()) {
+        // descriptor start addresses count 16-byte units: 16 bf16 along K is +2
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tmem, sw128_desc(a + kk * 32), sw128_desc(b + kk * 32), idesc, (it | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk) mma_f16(tmem, da + 2 * kk, db + 2 * kk, idesc, (it | kk) != 0);
         mma_commit(&ctl->empty[s]);
       }
-      mma_commit(&ctl->acc_full);
+      __syncwarp();
     }
+    if (lane == 0) mma_commit(&ctl->acc_full);
   }
   if (warp >= 2) {
     // Shared-gate logit and fp16 copy of x for this block's tokens, on warps
