@@ -167,9 +167,9 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
   if (threadIdx.x == 0) {
     for (int s = 0; s < kCS; ++s) {
       mbar_init(&ctl->c_full[s], 1);
-      mbar_init(&ctl->c_empty[s], 8);
+      mbar_init(&ctl->c_empty[s], 4);
     }
-    for (int s = 0; s < kAS; ++s) mbar_init(&ctl->a_full[s], 8);
+    for (int s = 0; s < kAS; ++s) mbar_init(&ctl->a_full[s], 4);
     for (int s = 0; s < kBS; ++s) mbar_init(&ctl->b_full[s], kGateUp ? 4 : 1);
     for (int s = 0; s < kDone; ++s) mbar_init(&ctl->stage_done[s], 1);
     for (int b = 0; b < 2; ++b) {
@@ -348,26 +348,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     }
   } else if (warp < 14) {
     // -------------------------------------------------- dequantisation
-    const int r = threadIdx.x - 192;  // weight row 0..255 of the item
-    const int gpr = kdim / 64;        // groups (scale, bias) per weight row
-    uint8_t* arow = sA + (r >> 7) * 16384 + (r & 127) * 128;
-    const uint8_t* crow = sC + (r >> 7) * 4096 + (r & 127) * 32;
-    // This block runs `total` stages; the codes of stage it + 1 are read
-    // while the stores of stage it drain, and one lane then releases both
-    // the A slot of stage it and the code slot of stage it + 1.
-    const int total = ((items - 1 - (int)blockIdx.x) / G + 1) * num_k;
-    uint4 c0, c1;
-    bool ok = mbar_wait(&ctl->c_full[0], 0, abort_flag, deadline);
-    if (ok) {
-      c0 = *reinterpret_cast<const uint4*>(crow);
-      c1 = *reinterpret_cast<const uint4*>(crow + 16);
-    }
-    __syncwarp();
-    if (lane == 0 && ok) mbar_arrive(&ctl->c_empty[0]);
-    // Scale and bias rows of this thread's weight row in item w; the first
-    // 8-group chunk of the next item is loaded a whole item ahead.
+    // Two groups of 4 warps take alternate stages (group g the stages with
+    // it % 2 == g; an item has an even number of stages). Thread gt of a
+    // group owns weight rows gt and gt + 128 of the item (gate/up: the gate
+    // and the up row of one h column), so each hand-off of a warp covers two
+    // rows while the other group works on the next stage.
+    const int grp = (warp - 6) >> 2;
+    const int gt = threadIdx.x - 192 - grp * 128;  // 0..127
+    const int gpr = kdim / 64;                     // groups (scale, bias) and stages per weight row
+    uint8_t* arow0 = sA + gt * 128;                // row gt in the first 128-row half of a stage
+    const uint8_t* crow0 = sC + gt * 32;
     const bool chunked = (gpr & 7) == 0;
-    auto rows_of = [&](int w, const uint16_t*& srow, const uint16_t*& brow) {
+    auto rows_of = [&](int w, int r, const uint16_t*& srow, const uint16_t*& brow) {
       const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
       const int e = p.t.tile_expert[tile];
       const bool sh = e == p.E;
@@ -377,96 +369,83 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       srow = (sh ? p.s_scales : p.scales) + wrow * gpr;
       brow = (sh ? p.s_biases : p.biases) + wrow * gpr;
     };
-    const uint16_t *srow, *brow;
-    rows_of(blockIdx.x, srow, brow);
-    uint4 sc_first = make_uint4(0, 0, 0, 0), bi_first = sc_first;
-    if (chunked) {
-      sc_first = ldg_nc_v4(srow);
-      bi_first = ldg_nc_v4(brow);
-    }
-    int it = 0;
-    for (int w = blockIdx.x; ok && w < items; w += G) {
-      const uint16_t *srow_n = srow, *brow_n = brow;
-      uint4 sc_nx = sc_first, bi_nx = bi_first;
-      if (w + G < items) {
-        rows_of(w + G, srow_n, brow_n);
-        if (chunked) {
-          sc_nx = ldg_nc_v4(srow_n);
-          bi_nx = ldg_nc_v4(brow_n);
-        }
+    bool ok = true;
+    int it = grp;
+    // One stage of this group: the codes of both rows, the wait for the
+    // MMAs that last read this A slot, both rows dequantised into the slot,
+    // then one lane releases the A slot and the code slot.
+    auto stage = [&](__half2 sa, __half2 ba, __half2 sb, __half2 bb) -> bool {
+      const int cs = it % kCS, as = it % kAS;
+      if (!mbar_wait(&ctl->c_full[cs], (it / kCS) & 1, abort_flag, deadline)) return false;
+      const uint4 a0 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes + 16);
+      const uint4 b0 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes + 4096);
+      const uint4 b1 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes + 4096 + 16);
+      {
+        const int j = it - kAS + kAMargin;  // the MMAs of stage j must be complete
+        if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) return false;
       }
-      // One stage: wait until the MMAs that last read this A slot are done,
-      // write the slot, read the next stage's codes while the stores drain,
-      // then one lane releases the slot and the code slot.
-      auto stage = [&](__half2 s2, __half2 b2) -> bool {
-        const int as = it % kAS;
-        {
-          const int j = it - kAS + kAMargin;  // the MMAs of stage j must be complete
-          if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) return false;
-        }
-        // the slot was last read by the tensor core (async proxy): order
-        // those reads before these generic-proxy stores
-        fence_proxy_async();
-        uint8_t* dst = arow + as * kABytes;
+      // the slot was last read by the tensor core (async proxy): order
+      // those reads before these generic-proxy stores
+      fence_proxy_async();
+      uint8_t* dst = arow0 + as * kABytes;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          uint32_t o[4];
-          dequant8_f16(q < 4 ? u4_get(c0, q) : u4_get(c1, q - 4), s2, b2, o);
-          *reinterpret_cast<uint4*>(dst + ((q ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        const bool more = it + 1 < total;
-        const int cs = (it + 1) % kCS;
-        bool good = true;
-        if (more) {
-          if (mbar_wait(&ctl->c_full[cs], ((it + 1) / kCS) & 1, abort_flag, deadline)) {
-            c0 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes);
-            c1 = *reinterpret_cast<const uint4*>(crow + cs * kCBytes + 16);
-          } else {
-            good = false;
-          }
-        }
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ctl->a_full[as]);
-          if (more && good) mbar_arrive(&ctl->c_empty[cs]);
-        }
-        ++it;
-        return good;
-      };
+      for (int q = 0; q < 8; ++q) {
+        uint32_t o[4], u[4];
+        dequant8_f16(q < 4 ? u4_get(a0, q) : u4_get(a1, q - 4), sa, ba, o);
+        dequant8_f16(q < 4 ? u4_get(b0, q) : u4_get(b1, q - 4), sb, bb, u);
+        *reinterpret_cast<uint4*>(dst + ((q ^ (gt & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + 16384 + ((q ^ (gt & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->a_full[as]);
+        mbar_arrive(&ctl->c_empty[cs]);
+      }
+      it += 2;
+      return true;
+    };
+    for (int w = blockIdx.x; ok && w < items; w += G) {
+      const uint16_t *srow0, *brow0, *srow1, *brow1;
+      rows_of(w, gt, srow0, brow0);
+      rows_of(w, gt + 128, srow1, brow1);
       if (chunked) {
-        // scales/biases 8 groups per 16-byte load, the next 8 prefetched a
-        // chunk ahead; each chunk is converted to fp16 (scale, bias) pairs
-        // once and its 8 stages are unrolled so the pairs stay in registers
-        uint4 sc = sc_first, bi = bi_first;
+        // scales/biases 8 groups per 16-byte load; this group's 4 (scale,
+        // bias) pairs of each row are converted to fp16 once per chunk and
+        // the next chunk is loaded while the 4 stages run
+        uint4 s0 = ldg_nc_v4(srow0), c0 = ldg_nc_v4(brow0), s1 = ldg_nc_v4(srow1), c1 = ldg_nc_v4(brow1);
         for (int k0 = 0; ok && k0 < num_k; k0 += 8) {
-          uint32_t sb[8];
+          uint32_t pa[4], pb[4];
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const __half2 h = __floats2half2_rn(bf16_bits_to_f32(bf16_of(sc, g)), bf16_bits_to_f32(bf16_of(bi, g)));
-            sb[g] = *reinterpret_cast<const uint32_t*>(&h);
+          for (int m = 0; m < 4; ++m) {
+            const int g = grp + 2 * m;
+            const __half2 ha = __floats2half2_rn(bf16_bits_to_f32(bf16_of(s0, g)), bf16_bits_to_f32(bf16_of(c0, g)));
+            const __half2 hb = __floats2half2_rn(bf16_bits_to_f32(bf16_of(s1, g)), bf16_bits_to_f32(bf16_of(c1, g)));
+            pa[m] = *reinterpret_cast<const uint32_t*>(&ha);
+            pb[m] = *reinterpret_cast<const uint32_t*>(&hb);
           }
           if (k0 + 8 < num_k) {
-            sc = ldg_nc_v4(srow + k0 + 8);
-            bi = ldg_nc_v4(brow + k0 + 8);
+            s0 = ldg_nc_v4(srow0 + k0 + 8);
+            c0 = ldg_nc_v4(brow0 + k0 + 8);
+            s1 = ldg_nc_v4(srow1 + k0 + 8);
+            c1 = ldg_nc_v4(brow1 + k0 + 8);
           }
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
-            const __half2 h = *reinterpret_cast<const __half2*>(&sb[g]);
-            if (!stage(__low2half2(h), __high2half2(h))) {
+          for (int m = 0; m < 4; ++m) {
+            const __half2 ha = *reinterpret_cast<const __half2*>(&pa[m]);
+            const __half2 hb = *reinterpret_cast<const __half2*>(&pb[m]);
+            if (!stage(__low2half2(ha), __high2half2(ha), __low2half2(hb), __high2half2(hb))) {
               ok = false;
               break;
             }
           }
         }
       } else {
-        for (int k = 0; ok && k < num_k; ++k)
-          ok = stage(bf16_to_h2(__ldg(srow + k)), bf16_to_h2(__ldg(brow + k)));
+        for (int k = grp; ok && k < num_k; k += 2)
+          ok = stage(bf16_to_h2(__ldg(srow0 + k)), bf16_to_h2(__ldg(brow0 + k)), bf16_to_h2(__ldg(srow1 + k)),
+                     bf16_to_h2(__ldg(brow1 + k)));
       }
-      srow = srow_n;
-      brow = brow_n;
-      sc_first = sc_nx;
-      bi_first = bi_nx;
     }
   } else {
     // -------------------------------------------------------- epilogue
