@@ -53,8 +53,8 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=403497216 + 26766080, profile="profiles/expert_tc_kernel_prefill-4096.md",
-        sources={"gemm_tc.cu": "25cb9fa7dad9735a12b90bbcc35db1b6a1d1864a27f92b61b89a5c7b70f94b04",
+        bytes=427410688 + 26764800, profile="profiles/expert_tc_kernel_prefill-4096.md",
+        sources={"gemm_tc.cu": "2e34a7dced4fb051f7b161f8f711bf342d03a5d3eaccd08d907196d7e4e042b3",
                  "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
