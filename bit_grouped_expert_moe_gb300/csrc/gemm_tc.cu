@@ -55,14 +55,10 @@ constexpr int kTcThreads = 576;
 #ifndef BGMOE_TC_BS
 #define BGMOE_TC_BS 5
 #endif
-#ifndef BGMOE_TC_LAG
-#define BGMOE_TC_LAG 2
-#endif
 #ifndef BGMOE_TC_A_MARGIN
 #define BGMOE_TC_A_MARGIN 1
 #endif
 constexpr int kCS = BGMOE_TC_CS, kAS = BGMOE_TC_AS, kBS = BGMOE_TC_BS;  // ring depths: codes, A, B
-constexpr int kGatherLag = BGMOE_TC_LAG;  // gather stages in flight before publishing (<= kBS - 2)
 // Generic-proxy stores into an A slot wait for the commit of the MMAs of
 // kAMargin stages AFTER the slot's previous use. Measured on GB300: rewriting
 // a slot as soon as the commit of the MMAs that read it had arrived corrupted
@@ -82,7 +78,7 @@ static_assert(kAS - kAMargin <= 2, "the dequant may wait for the MMAs at most tw
 #endif
 // The same rule for the gather's cp.async stores into a B slot.
 constexpr int kBMargin = BGMOE_TC_B_MARGIN;
-static_assert(kGatherLag + kBMargin <= kBS - 2, "the gather must keep a stage of slack");
+static_assert(kBMargin >= 0 && kBMargin < kBS, "B-slot margin must leave the gather a stage of lead");
 // One commit per stage: the MMAs of stage s arrive on stage_done[s % kDone],
 // which the dequantisation, the gather and the down kernel's B copies all
 // wait on. A waiter checks every stage in order, so it has seen the phase
@@ -170,7 +166,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       mbar_init(&ctl->c_empty[s], 4);
     }
     for (int s = 0; s < kAS; ++s) mbar_init(&ctl->a_full[s], 4);
-    for (int s = 0; s < kBS; ++s) mbar_init(&ctl->b_full[s], kGateUp ? 4 : 1);
+    for (int s = 0; s < kBS; ++s) mbar_init(&ctl->b_full[s], kGateUp ? 128 : 1);
     for (int s = 0; s < kDone; ++s) mbar_init(&ctl->stage_done[s], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&ctl->acc_full[b], 1);
@@ -278,6 +274,10 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           ok = false;
           break;
         }
+        // the gathered rows were written by cp.async (generic proxy): after
+        // the barrier made them visible to this warp, order them before the
+        // MMAs' async-proxy reads
+        if (kGateUp) fence_proxy_async();
         tc_fence_after();
         // descriptor start addresses count 16-byte units: 16 fp16 along K
         // is +2, the second 128-row half of the A stage (+16384 B) is +1024
@@ -331,20 +331,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
               cp_async_16(dst + j * 128 + ((c ^ (j & 7)) << 4), p.x16 + (size_t)tok[q] * H + k * 64 + c * 8,
                           j < rows ? 16u : 0u);
           }
-          cp_async_commit();
-          if (it >= kGatherLag) {
-            cp_async_wait<kGatherLag>();
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->b_full[(it - kGatherLag) % kBS]);
-          }
+          // the slot's barrier counts this thread's arrival once its copies land
+          cp_async_mbar_arrive_noinc(&ctl->b_full[bs]);
         }
       }
-      cp_async_wait<0>();
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0)
-        for (int j2 = (it - kGatherLag > 0 ? it - kGatherLag : 0); j2 < it; ++j2) mbar_arrive(&ctl->b_full[j2 % kBS]);
+      cp_async_wait_all();
     }
   } else if (warp < 14) {
     // -------------------------------------------------- dequantisation
