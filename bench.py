@@ -53,9 +53,9 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=427410688 + 26764800, profile="profiles/expert_tc_kernel_prefill-4096.md",
-        sources={"gemm_tc.cu": "2e34a7dced4fb051f7b161f8f711bf342d03a5d3eaccd08d907196d7e4e042b3",
-                 "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
+        bytes=429425408 + 27079680, profile="profiles/expert_tc_kernel_prefill-4096.md",
+        sources={"gemm_tc.cu": "4463adc553a106d32711705a3f8f29307090020e6e67c6d681ddb70f54a75c53",
+                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
 
