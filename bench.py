@@ -45,12 +45,12 @@ PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
         bytes=17068032, profile="profiles/decode_layer_kernel_decode-t1.md",
         sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
-                 "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
+                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("fused_decode_layer", "decode-t4"): dict(
-        bytes=56009216 + 542208, profile="profiles/decode_layer_kernel_decode-t4.md",
+        bytes=56009216 + 545280, profile="profiles/decode_layer_kernel_decode-t4.md",
         sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
-                 "tc_ptx.cuh": "2adaa17bbe8194c2a3474a3f096317ce11feafbd703c9cc13caacbc17bfcd3d4",
+                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
         bytes=429425408 + 27079680, profile="profiles/expert_tc_kernel_prefill-4096.md",
