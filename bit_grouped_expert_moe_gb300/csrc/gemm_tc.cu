@@ -67,11 +67,14 @@ constexpr int kCS = BGMOE_TC_CS, kAS = BGMOE_TC_AS, kBS = BGMOE_TC_BS;  // ring 
 // one-stage margin no corruption was seen in any repeated run.
 constexpr int kAMargin = BGMOE_TC_A_MARGIN;
 static_assert(kAMargin >= 0 && kAMargin < kAS, "A-slot margin must leave the dequant a stage of lead");
-// Measured too: with a 4-deep A ring and a one-stage margin (the dequant
-// waiting for the MMAs three iterations back) h came out wrong in every
-// repeated run; with a two-stage margin, or a 2- or 3-deep ring and a
-// one-stage margin, no run differed. So the dequant never runs more than two
-// iterations ahead of the completed MMAs.
+// Measured too, when every dequantisation warp wrote one row of every stage:
+// with a 4-deep A ring and a one-stage margin (the dequant waiting for the
+// MMAs three iterations back) h came out wrong in every repeated run, in the
+// rows of the warps that finished last; with a two-stage margin, or a 2- or
+// 3-deep ring and a one-stage margin, no run differed. With the two groups
+// below the 4-deep ring ran clean but no faster (the shared memory it takes
+// comes out of the code or B ring), so the dequant still never runs more
+// than two iterations ahead of the completed MMAs.
 static_assert(kAS - kAMargin <= 2, "the dequant may wait for the MMAs at most two iterations back");
 #ifndef BGMOE_TC_B_MARGIN
 #define BGMOE_TC_B_MARGIN 1
