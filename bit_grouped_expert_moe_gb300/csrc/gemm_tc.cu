@@ -400,15 +400,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       it += 2;
       return true;
     };
-    for (int w = blockIdx.x; ok && w < items; w += G) {
-      const uint16_t *srow0, *brow0, *srow1, *brow1;
-      rows_of(w, gt, srow0, brow0);
-      rows_of(w, gt + 128, srow1, brow1);
+    // One item, given its scale and bias rows and their first 8-group chunk.
+    auto run_item = [&](const uint16_t* srow0, const uint16_t* brow0, const uint16_t* srow1, const uint16_t* brow1,
+                        uint4 s0, uint4 c0, uint4 s1, uint4 c1) {
       if (chunked) {
         // scales/biases 8 groups per 16-byte load; this group's 4 (scale,
         // bias) pairs of each row are converted to fp16 once per chunk and
         // the next chunk is loaded while the 4 stages run
-        uint4 s0 = ldg_nc_v4(srow0), c0 = ldg_nc_v4(brow0), s1 = ldg_nc_v4(srow1), c1 = ldg_nc_v4(brow1);
         for (int k0 = 0; ok && k0 < num_k; k0 += 8) {
           uint32_t pa[4], pb[4];
 #pragma unroll
@@ -439,6 +437,47 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
         for (int k = grp; ok && k < num_k; k += 2)
           ok = stage(bf16_to_h2(__ldg(srow0 + k)), bf16_to_h2(__ldg(brow0 + k)), bf16_to_h2(__ldg(srow1 + k)),
                      bf16_to_h2(__ldg(brow1 + k)));
+      }
+    };
+    const uint4 z4 = make_uint4(0, 0, 0, 0);
+    if (kGateUp) {
+      // 32-stage items: the rows and the first chunk are loaded at the item start
+      for (int w = blockIdx.x; ok && w < items; w += G) {
+        const uint16_t *srow0, *brow0, *srow1, *brow1;
+        rows_of(w, gt, srow0, brow0);
+        rows_of(w, gt + 128, srow1, brow1);
+        if (chunked)
+          run_item(srow0, brow0, srow1, brow1, ldg_nc_v4(srow0), ldg_nc_v4(brow0), ldg_nc_v4(srow1), ldg_nc_v4(brow1));
+        else
+          run_item(srow0, brow0, srow1, brow1, z4, z4, z4, z4);
+      }
+    } else {
+      // 8-stage down items: the next item's rows and first chunk are looked
+      // up a whole item ahead
+      const uint16_t *srow0, *brow0, *srow1, *brow1;
+      rows_of(blockIdx.x, gt, srow0, brow0);
+      rows_of(blockIdx.x, gt + 128, srow1, brow1);
+      uint4 n0 = z4, n1 = z4, n2 = z4, n3 = z4;
+      if (chunked) {
+        n0 = ldg_nc_v4(srow0);
+        n1 = ldg_nc_v4(brow0);
+        n2 = ldg_nc_v4(srow1);
+        n3 = ldg_nc_v4(brow1);
+      }
+      for (int w = blockIdx.x; ok && w < items; w += G) {
+        const uint16_t *cs0 = srow0, *cb0 = brow0, *cs1 = srow1, *cb1 = brow1;
+        const uint4 s0 = n0, c0 = n1, s1 = n2, c1 = n3;
+        if (w + G < items) {
+          rows_of(w + G, gt, srow0, brow0);
+          rows_of(w + G, gt + 128, srow1, brow1);
+          if (chunked) {
+            n0 = ldg_nc_v4(srow0);
+            n1 = ldg_nc_v4(brow0);
+            n2 = ldg_nc_v4(srow1);
+            n3 = ldg_nc_v4(brow1);
+          }
+        }
+        run_item(cs0, cb0, cs1, cb1, s0, c0, s1, c1);
       }
     }
   } else {
