@@ -53,8 +53,8 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=429425408 + 27079680, profile="profiles/expert_tc_kernel_prefill-4096.md",
-        sources={"gemm_tc.cu": "57c5313ae8906d258838ebbb0165b8a731818359c4979d9b33dbeff6d1d89bc2",
+        bytes=428123904 + 27014400, profile="profiles/expert_tc_kernel_prefill-4096.md",
+        sources={"gemm_tc.cu": "b5977a6e1abc72896a48b429af781c9b95580b7b091780f707ca05b26b382596",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
