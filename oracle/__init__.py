@@ -27,3 +27,4 @@ from .moe import (  # noqa: F401
     moe_forward,
     topk_gap,
 )
+from .attention import gqa_decode_attention  # noqa: F401,E402

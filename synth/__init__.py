@@ -237,3 +237,80 @@ WORKLOADS = {
     "long-skew-16384": LayerSpec("long-skew-16384", T=16384, H=2048, I=512, bias="hot",
                                  hot_logit=1.65, seed=20260005, chunk=2048),
 }
+
+
+# ------------------------------------------------------- decode attention ---
+# Streams: kind * 2**32 + layer * 2**12 + (b * Hkv + g) for the cache,
+# kind * 2**32 + layer * 2**12 + b for the query.
+K_ATT_Q, K_ATT_K, K_ATT_V = 40, 41, 42
+
+
+@dataclass
+class AttnSpec:
+    """One decode-attention workload: B sequences with cache lengths `lens`,
+    Hq query heads sharing Hkv KV heads of size D ("Model specification" on
+    dothoosh.com: 16 query and 2 KV heads; D is not given there).
+
+    q ~ N(0, q_std^2), K ~ N(0, 1), V ~ N(0, 1), all bf16. With the default
+    scale 1/sqrt(D) the scores are then ~ N(0, q_std^2): q_std = 1 spreads the
+    weights over the whole context, larger values make them peak on a few
+    positions."""
+    name: str
+    lens: tuple
+    Hq: int = 16
+    Hkv: int = 2
+    D: int = 256
+    L_max: int = 0               # 0: max(lens)
+    q_std: float = 1.0
+    seed: int = 20260101
+    layers: int = 1
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def Lmax(self) -> int:
+        return self.L_max or max(self.lens)
+
+
+def attn_query(spec: AttnSpec, layer: int = 0, device="cpu"):
+    """q bf16 [B, Hq, D]."""
+    z = normal_f64(spec.seed, [stream_id(K_ATT_Q, layer, b) for b in range(spec.B)], spec.Hq * spec.D, device)
+    return to_bf16(z * spec.q_std).view(spec.B, spec.Hq, spec.D)
+
+
+def attn_cache(spec: AttnSpec, kind: int, layer: int = 0, device="cpu", pairs=None, rows=None):
+    """K (kind K_ATT_K) or V (K_ATT_V) cache rows 0..rows-1 (default L_max) of
+    the listed (b, g) pairs (default: all, in b-major order): bf16 [P, rows, D].
+    Every row, including those past a sequence's length, holds finite values."""
+    Hkv, D = spec.Hkv, spec.D
+    rows = spec.Lmax if rows is None else rows
+    if pairs is None:
+        pairs = [(b, g) for b in range(spec.B) for g in range(Hkv)]
+    out = torch.empty(len(pairs), rows, D, dtype=torch.bfloat16, device=device)
+    for i, (b, g) in enumerate(pairs):   # one stream per pair keeps the draws per call bounded
+        z = normal_f64(spec.seed, [stream_id(kind, layer, b * Hkv + g)], rows * D, device)
+        out[i] = to_bf16(z).view(rows, D)
+    return out
+
+
+def attn_inputs(spec: AttnSpec, layer: int = 0, device="cpu"):
+    """q [B, Hq, D], K and V [B, Hkv, L_max, D] (bf16) and lens int32 [B]."""
+    q = attn_query(spec, layer, device)
+    k = attn_cache(spec, K_ATT_K, layer, device).view(spec.B, spec.Hkv, spec.Lmax, spec.D)
+    v = attn_cache(spec, K_ATT_V, layer, device).view(spec.B, spec.Hkv, spec.Lmax, spec.D)
+    lens = torch.tensor(spec.lens, dtype=torch.int32, device=device)
+    return q, k, v, lens
+
+
+# Single-sequence decode at the context lengths the decode measurements on
+# the pages use (32K, 64K, 128K), with the model's 10 full-attention layers
+# per step; and a batch of ragged lengths.
+ATTN_WORKLOADS = {
+    "attn-decode-32k": AttnSpec("attn-decode-32k", lens=(32768,), layers=10, seed=20260111),
+    "attn-decode-64k": AttnSpec("attn-decode-64k", lens=(65536,), layers=10, seed=20260112),
+    "attn-decode-128k": AttnSpec("attn-decode-128k", lens=(131072,), layers=10, seed=20260113),
+    "attn-decode-batch8": AttnSpec("attn-decode-batch8", lens=(4096, 32768, 1, 17000, 65536, 8191, 777, 20000),
+                                   layers=10, seed=20260114),
+}

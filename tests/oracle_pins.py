@@ -13,6 +13,7 @@ import math
 
 import numpy as np
 
+import oracle.attention as A
 import oracle.moe as M
 from tests._util import bf16_from_f64, read_golden
 
@@ -384,6 +385,123 @@ def pin_layer_all_experts():
         c = fn(e)
         want += p[:, e:e + 1] * M.swiglu_expert(x, M.dequant(*c[:3]), M.dequant(*c[3:]))
     assert np.allclose(y, want, rtol=1e-10, atol=1e-12)
+
+
+# -------------------------------------------------------- decode attention ---
+
+def _attn(q, k, v, lens, scale=None):
+    return A.gqa_decode_attention(_bits(q), _bits(k), _bits(v), lens, scale)
+
+
+def pin_attn_single_position():
+    """One cached position: the softmax weight is 1 and o = v_0 for every
+    query head, whatever q is."""
+    B, Hq, Hkv, D, L = 2, 4, 2, 16, 5
+    q = RNG.standard_normal((B, Hq, D)) * 3
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    vb = M.bf16_bits_to_f64(_bits(v))
+    o = _attn(q, k, v, [1, 1])
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(o[b, h], vb[b, h // 2, 0]), (b, h)
+
+
+def pin_attn_two_positions_closed_form():
+    """Two positions whose scores differ by d = 1 (q = e_0, k_0 = 2 e_0,
+    k_1 = 0, D = 4, default scale 1/2): weights sigmoid(1) and 1 - sigmoid(1)."""
+    D = 4
+    q = np.zeros((1, 1, D)); q[0, 0, 0] = 1.0
+    k = np.zeros((1, 1, 2, D)); k[0, 0, 0, 0] = 2.0
+    v = np.zeros((1, 1, 2, D)); v[0, 0, 0, 0] = 1.0; v[0, 0, 1, 1] = 1.0
+    o = _attn(q, k, v, [2])
+    sig = 1.0 / (1.0 + math.exp(-1.0))
+    assert abs(o[0, 0, 0] - 0.7310585786300049) < 1e-15 and abs(sig - 0.7310585786300049) < 1e-15
+    assert abs(o[0, 0, 1] - 0.2689414213699951) < 1e-15
+    assert o[0, 0, 2] == 0 and o[0, 0, 3] == 0
+
+
+def pin_attn_equal_keys_mean():
+    """Identical keys (or q = 0) make every weight 1/n: o is the mean of the
+    first n value rows."""
+    B, Hq, Hkv, D, L = 1, 2, 1, 8, 9
+    row = RNG.standard_normal(D)
+    k = np.tile(row, (B, Hkv, L, 1))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    q = RNG.standard_normal((B, Hq, D))
+    vb = M.bf16_bits_to_f64(_bits(v))
+    for n in (1, 4, 9):
+        o = _attn(q, k, v, [n])
+        assert np.allclose(o[0, 0], vb[0, 0, :n].mean(axis=0), rtol=0, atol=1e-13), n
+    k2 = RNG.standard_normal((B, Hkv, L, D))
+    o = _attn(np.zeros((B, Hq, D)), k2, v, [L])
+    assert np.allclose(o[0, 1], vb[0, 0].mean(axis=0), rtol=0, atol=1e-13)
+
+
+def pin_attn_head_mapping():
+    """Query head h reads KV head h // (Hq/Hkv): with V of KV head g all equal
+    to g + 1, every output element of head h is h // (Hq/Hkv) + 1."""
+    B, Hq, Hkv, D, L = 1, 8, 2, 8, 6
+    q = RNG.standard_normal((B, Hq, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = np.zeros((B, Hkv, L, D))
+    for g in range(Hkv):
+        v[0, g] = g + 1
+    o = _attn(q, k, v, [L])
+    for h in range(Hq):
+        assert np.allclose(o[0, h], h // 4 + 1, rtol=0, atol=1e-14), h
+
+
+def pin_attn_masks_past_length():
+    """Rows at or past lens[b] do not matter: poisoning them (large values in K
+    and V) leaves o unchanged, and o equals the result on the truncated cache."""
+    B, Hq, Hkv, D, L = 3, 4, 2, 16, 12
+    q = RNG.standard_normal((B, Hq, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    lens = [5, 12, 0]
+    o = _attn(q, k, v, lens)
+    k2, v2 = k.copy(), v.copy()
+    for b, n in enumerate(lens):
+        k2[b, :, n:] = 1e4
+        v2[b, :, n:] = -3e4
+    assert np.array_equal(_attn(q, k2, v2, lens), o)
+    assert np.array_equal(_attn(q[:1], k[:1, :, :5], v[:1, :, :5], [5]), o[:1])
+    assert np.all(o[2] == 0)
+
+
+def pin_attn_invariances():
+    """Permuting cache positions (keys and values together) and adding one
+    vector to every key (every score shifts by the same q . c) leave o
+    unchanged; scaling every value by 2 doubles o."""
+    B, Hq, Hkv, D, L = 1, 4, 1, 8, 10
+    q = RNG.standard_normal((B, Hq, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    o = _attn(q, k, v, [L])
+    perm = RNG.permutation(L)
+    assert np.allclose(_attn(q, k[:, :, perm], v[:, :, perm], [L]), o, rtol=0, atol=1e-13)
+    c = np.round(RNG.standard_normal(D) * 4) / 4   # exact in bf16 sums with the keys below
+    kq = np.round(k * 8) / 8
+    assert np.allclose(_attn(q, kq + c, v, [L]), _attn(q, kq, v, [L]), rtol=0, atol=1e-12)
+    assert np.allclose(_attn(q, k, 2 * v, [L]), 2 * o, rtol=0, atol=1e-13)
+
+
+def pin_attn_matches_torch_sdpa():
+    """Full caches reduce the oracle to torch's scaled_dot_product_attention
+    (fp64, one query position, enable_gqa), an independent library routine, at
+    the default scale and at an explicit one."""
+    import torch
+    B, Hq, Hkv, D, L = 2, 8, 2, 32, 17
+    q = M.bf16_bits_to_f64(_bits(RNG.standard_normal((B, Hq, D)) * 2))
+    k = M.bf16_bits_to_f64(_bits(RNG.standard_normal((B, Hkv, L, D))))
+    v = M.bf16_bits_to_f64(_bits(RNG.standard_normal((B, Hkv, L, D))))
+    for scale in (None, 0.3):
+        want = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[:, :, None, :], torch.from_numpy(k), torch.from_numpy(v),
+            scale=scale, enable_gqa=True)[:, :, 0, :].numpy()
+        got = _attn(q, k, v, [L, L], scale)
+        assert np.allclose(got, want, rtol=0, atol=1e-12), scale
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -5,6 +5,7 @@ transposed operands, not only to crashes."""
 import numpy as np
 import pytest
 
+import oracle.attention as A
 import oracle.moe as M
 from tests.oracle_pins import PINS
 
@@ -121,6 +122,65 @@ MUTANTS = [
     ("swiglu_expert", gate_up_swapped), ("swiglu_expert", relu_instead_of_silu),
     ("swiglu_expert", down_transposed),
 ]
+
+
+def _attention_variant(label, mapping="div", scale_mode="rsqrt", len_shift=0, normalise=True, v_head=None):
+    """A copy of the decode-attention oracle with one plausible mistake."""
+    def attn(q_bits, k_bits, v_bits, lens, scale=None):
+        q, K, V = (M.bf16_bits_to_f64(t) for t in (q_bits, k_bits, v_bits))
+        B, Hq, D = q.shape
+        Hkv = K.shape[1]
+        r = Hq // Hkv
+        s = {"rsqrt": 1 / np.sqrt(D), "one": 1.0, "sqrt": np.sqrt(D)}[scale_mode] if scale is None else scale
+        o = np.zeros((B, Hq, D))
+        for b in range(B):
+            n = int(lens[b])
+            n = min(max(n + len_shift, 1), K.shape[2]) if n > 0 else 0
+            for h in range(Hq if n else 0):
+                g = h // r if mapping == "div" else h % Hkv
+                gv = g if v_head is None else v_head(h, Hkv)
+                lg = s * (K[b, g, :n] @ q[b, h])
+                w = np.exp(lg - lg.max())
+                if normalise:
+                    w /= w.sum()
+                o[b, h] = w @ V[b, gv, :n]
+        return o
+    attn.__name__ = label
+    return attn
+
+
+ATTN_MUTANTS = [
+    _attention_variant("kv_head_by_modulo", mapping="mod"),
+    _attention_variant("scale_missing", scale_mode="one"),
+    _attention_variant("scale_inverted", scale_mode="sqrt"),
+    _attention_variant("one_position_short", len_shift=-1),
+    _attention_variant("one_position_past_length", len_shift=1),
+    _attention_variant("weights_not_normalised", normalise=False),
+    _attention_variant("values_from_other_kv_head", v_head=lambda h, Hkv: (h + 1) % Hkv),
+]
+
+
+def _caught_by_some_pin():
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError):
+            caught.append(pin.__name__)
+    return caught
+
+
+@pytest.mark.parametrize("mutant", ATTN_MUTANTS, ids=[m.__name__ for m in ATTN_MUTANTS])
+def test_planted_attention_mistake_is_caught(monkeypatch, mutant):
+    monkeypatch.setattr(A, "gqa_decode_attention", mutant)
+    assert _caught_by_some_pin(), f"no pin caught the planted mistake {mutant.__name__}"
+
+
+def test_attention_variant_without_mistake_passes(monkeypatch):
+    """The mutant generator itself, with no mistake switched on, passes every
+    pin (so a caught mutant is caught for its mistake)."""
+    monkeypatch.setattr(A, "gqa_decode_attention", _attention_variant("faithful_copy"))
+    assert not _caught_by_some_pin()
 
 
 @pytest.mark.parametrize("name,mutant", MUTANTS, ids=[m.__name__ for _, m in MUTANTS])

@@ -39,3 +39,16 @@ def test_distributions():
     b = gu[2].float()
     assert (s >= 0).all() and abs(s.mean() - 0.02 * (2 / torch.pi) ** 0.5) < 1e-3
     assert abs((b + 8 * s).std() - 1e-3) < 2e-4
+
+
+def test_attention_inputs_subset_and_shape():
+    """A pair regenerated alone equals its slice of the whole cache; lengths
+    and shapes follow the spec."""
+    spec = synth.AttnSpec("t", lens=(3, 40, 0), Hq=8, Hkv=2, D=64)
+    q, k, v, lens = synth.attn_inputs(spec)
+    assert q.shape == (3, 8, 64) and k.shape == (3, 2, 40, 64) and v.shape == k.shape
+    assert lens.tolist() == [3, 40, 0]
+    one = synth.attn_cache(spec, synth.K_ATT_V, pairs=[(1, 1)])
+    assert torch.equal(one[0], v[1, 1])
+    assert not torch.equal(k, v)
+    assert torch.isfinite(k.float()).all() and torch.isfinite(v.float()).all()
