@@ -5,7 +5,9 @@ Default workload: decode, T = 1 token through 40 MoE layers with distinct
 weights (H = 2048, I = 512, E = 256 top-8 + shared, 4-bit group-64 weights,
 18.2 GB of weights, far larger than L2), one step = one pass over the 40
 layers; the metric is microseconds per layer. --workload picks another
-shape (prefill-zipf-512, prefill-4096, long-skew-16384, decode-t4, tiny).
+shape (prefill-zipf-512, prefill-4096, long-skew-16384, decode-t4, tiny),
+or decode attention over a bf16 KV cache (attn-decode-32k, -64k, -128k,
+attn-decode-batch8: 16 query heads on 2 KV heads, D = 256, 10 layers).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -55,6 +57,11 @@ PROFILED_TRAFFIC = {
     ("expert_gate_up", "prefill-4096"): dict(
         bytes=428123904 + 27014400, profile="profiles/expert_tc_kernel_prefill-4096.md",
         sources={"gemm_tc.cu": "b5977a6e1abc72896a48b429af781c9b95580b7b091780f707ca05b26b382596",
+                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
+                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
+    ("attn_block_kernel", "attn-decode-32k"): dict(
+        bytes=67159296 + 118528, profile="profiles/attn_block_kernel_attn-decode-32k.md",
+        sources={"attention.cu": "50552cacf493c737d614f8a534631a0b634f86bafb86d4f3d979dc229333245a",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
@@ -438,6 +445,199 @@ def run_ours(args, spec, rank, world, local_rank):
     return out
 
 
+# ------------------------------------------------------ decode attention --
+
+METRIC_ATTN = "decode-attention µs/layer (GQA, bf16 KV cache); % of HBM roofline"
+
+
+class AttnWorkload:
+    """Device-resident inputs of a decode-attention workload: one layer per
+    full-attention layer of the model, each with its own KV cache."""
+
+    def __init__(self, m, spec, device):
+        self.m, self.spec, self.dev = m, spec, device
+        self.layers = spec.layers
+        self.shape = m.attn_shape(spec.B, spec.Hq, spec.Hkv, spec.D, spec.Lmax)
+        self.q = torch.empty(self.layers, spec.B, spec.Hq, spec.D, dtype=torch.bfloat16, device=device)
+        self.kv = []
+        for li in range(self.layers):
+            q, k, v, lens = synth.attn_inputs(spec, layer=li, device=device)
+            self.q[li].copy_(q)
+            self.kv.append((k, v))
+            del q
+        self.lens = torch.tensor(spec.lens, dtype=torch.int32, device=device)
+        self.o = torch.empty(self.layers, spec.B, spec.Hq, spec.D, dtype=torch.float32, device=device)
+        self.ws = m.attn_alloc_workspace(self.shape, device)
+
+    def call(self, li, events=None):
+        k, v = self.kv[li]
+        if events is None:
+            self.m.attn_decode(self.shape, self.q[li], k, v, self.lens, self.o[li], self.ws)
+        else:
+            self.m.attn_decode_timed(self.shape, self.q[li], k, v, self.lens, self.o[li], self.ws, events)
+
+    def step(self):
+        for li in range(self.layers):
+            self.call(li)
+
+    def kv_bytes_per_layer(self):
+        s = self.spec
+        return sum(s.lens) * s.Hkv * s.D * 2 * 2
+
+
+def attn_stage_times(W, steps):
+    """Average block-kernel and merge-kernel times (ms) from event nodes
+    between the two kernels of every layer, in a graph of one step."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(W.layers)]
+    for e3 in ev:
+        for e in e3:
+            e.record()
+    torch.cuda.synchronize()
+
+    def timed_step():
+        for li in range(W.layers):
+            W.call(li, events=[e.cuda_event for e in ev[li]])
+    g = capture(timed_step)
+    blk = mrg = 0.0
+    for _ in range(steps):
+        g.replay()
+        torch.cuda.synchronize()
+        for e3 in ev:
+            blk += e3[0].elapsed_time(e3[1])
+            mrg += e3[1].elapsed_time(e3[2])
+    n = steps * W.layers
+    return blk / n, mrg / n
+
+
+def run_attention(args, spec, rank, world, local_rank):
+    import bit_grouped_expert_moe_gb300 as m
+    from bit_grouped_expert_moe_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    W = AttnWorkload(m, spec, dev)
+    stream = torch.cuda.current_stream()
+    graph = capture(W.step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert m.status_read(W.ws[:4].view(torch.int32)) == 0
+
+    barrier(world)
+    with ClockSampler(local_rank) as clk:
+        ms = time_region(graph.replay, args.steps, stream)
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    clocks = clk.summary()
+    blk_ms, mrg_ms = attn_stage_times(W, max(1, min(args.steps, 20)))
+
+    # End to end through the same C ABI with host buffers: every step copies
+    # each layer's query in from pinned memory and reads every output back.
+    q_host = W.q.cpu().pin_memory()
+    o_host = torch.empty(W.o.shape, dtype=W.o.dtype).pin_memory()
+
+    def e2e_step():
+        W.q.copy_(q_host, non_blocking=True)
+        graph.replay()
+        o_host.copy_(W.o, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(2, args.steps // 2)
+    e2e_ms = max_over_ranks(time_region(e2e_step, n_e2e, stream), world, dev) / n_e2e
+    assert m.status_read(W.ws[:4].view(torch.int32)) == 0
+
+    pk, pk_src = peaks()
+    peak = pk["hbm_gbs"]
+    kv = W.kv_bytes_per_layer()
+    blk_bytes = kv + spec.B * spec.Hq * spec.D * 2 + spec.B * 4
+    achieved = blk_bytes / (blk_ms / 1000.0) / 1e9
+    value = ms_step * 1000.0 / W.layers
+    out = {
+        "metric": METRIC_ATTN, "value": round(value, 3), "unit": "us/layer", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32", "data": "synthetic",
+        "config": {"workload": spec.name, "B": spec.B, "lens": list(spec.lens), "Hq": spec.Hq, "Hkv": spec.Hkv,
+                   "D": spec.D, "L_max": spec.Lmax, "layers": W.layers, "seed": spec.seed,
+                   "l2": f"inputs larger than L2: {W.layers} layers x {kv / 1e6:.0f} MB of KV cache per step",
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": {"kernel": "attn_block_kernel", "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic("attn_block_kernel", spec.name), "peak_source": pk_src,
+                     "algorithmic_bytes_per_launch": int(blk_bytes)},
+        "layer": {"us_per_layer": round(value, 3), "kv_bytes_per_layer": int(kv),
+                  "hbm_frac_per_layer": round(kv / (value / 1e6) / 1e9 / peak, 4)},
+        "kernels_us_per_call": {"attn_block_kernel": round(blk_ms * 1000.0, 3),
+                                "attn_merge_kernel": round(mrg_ms * 1000.0, 3)},
+        "e2e": {"value": round(e2e_ms * 1000.0 / W.layers, 3), "unit": "us/layer",
+                "h2d_bytes_per_step": q_host.numel() * 2, "d2h_bytes_per_step": o_host.numel() * 4},
+        "gpu_launches": 2 * W.layers * args.steps,
+        "launch": "one CUDA graph per step",
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = attn_cpu_baseline(spec, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out
+
+
+def _attn_oracle_inputs(spec):
+    from tests._util import bits16
+    q, k, v, lens = synth.attn_inputs(spec, layer=0)
+    return bits16(q), bits16(k), bits16(v), list(spec.lens)
+
+
+def attn_cpu_baseline(spec, seconds):
+    """The attention oracle, as it stands, timed on this host's cores on
+    layer 0 of the workload (inputs generated before the clock starts)."""
+    import oracle
+    args = _attn_oracle_inputs(spec)
+    spent, calls = 0.0, 0
+    while spent < seconds and calls < 50:
+        t0 = time.perf_counter()
+        oracle.gqa_decode_attention(*args)
+        spent += time.perf_counter() - t0
+        calls += 1
+    return {"value": round(spent / calls * 1e6, 3), "unit": "us/layer", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{calls} calls on layer 0 of the workload (numpy fp64, BLAS multithreaded)",
+            "seconds": round(spent, 2)}
+
+
+def run_attention_reference(args, spec, rank, world):
+    """The reference arm for attention workloads: the CPU oracle (rank 0)."""
+    if rank != 0:
+        return None
+    import oracle
+    a = _attn_oracle_inputs(spec)
+    times = []
+    t_start = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        if time.perf_counter() - t_start > 150.0 and times:
+            break
+        t0 = time.perf_counter()
+        oracle.gqa_decode_attention(*a)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    if not times:
+        times.append(dt)
+    value = sum(times) / len(times) * 1e6
+    return {"impl": "reference", "metric": METRIC_ATTN, "value": round(value, 3), "unit": "us/layer",
+            "n_gpus": world, "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(value / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "B": spec.B, "lens": list(spec.lens), "Hq": spec.Hq,
+                       "Hkv": spec.Hkv, "D": spec.D, "layers": spec.layers},
+            "cpu_baseline": {"value": round(value, 3), "unit": "us/layer", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": "one oracle call on layer 0 per step; capped at 150 s"},
+            "e2e": {"value": round(value, 3), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 # ----------------------------------------------------------- CPU oracle --
 
 def _oracle_layer_sample(spec, layer_idx, tokens):
@@ -538,7 +738,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode-t1", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default="decode-t1", choices=sorted(synth.WORKLOADS) + sorted(synth.ATTN_WORKLOADS))
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -547,6 +747,18 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = dist_env()
+    if args.workload in synth.ATTN_WORKLOADS:
+        spec = synth.ATTN_WORKLOADS[args.workload]
+        if args.layers:
+            import dataclasses
+            spec = dataclasses.replace(spec, layers=args.layers)
+        if args.impl == "reference":
+            out = run_attention_reference(args, spec, rank, world)
+        else:
+            out = run_attention(args, spec, rank, world, local_rank)
+        if rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+        return
     spec = synth.WORKLOADS[args.workload]
     if args.layers:
         import dataclasses

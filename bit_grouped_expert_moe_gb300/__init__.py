@@ -5,8 +5,9 @@ current CUDA stream is passed through; every step of the layer runs in the
 library's CUDA kernels. There is no fallback: if the library is not built,
 importing the entry points raises.
 
-Entry points mirror the C ABI in include/moe.h: workspace_bytes, max_tiles,
-route_blocks, route, forward, status_read, status_string, test_route_stall.
+Entry points mirror the C ABI in include/moe.h (workspace_bytes, max_tiles,
+route_blocks, route, forward, status_read, status_string, test_route_stall) and
+include/attention.h (attn_workspace_bytes, attn_decode, attn_decode_timed).
 """
 from __future__ import annotations
 
@@ -27,6 +28,10 @@ P = ctypes.c_void_p
 
 class Shape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("T", "H", "I", "I_shared", "E", "top_k", "group_size", "block_m")]
+
+
+class AttnShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "Hq", "Hkv", "D", "L_max")]
 
 
 class QMat(ctypes.Structure):
@@ -81,6 +86,12 @@ def lib() -> ctypes.CDLL:
         L.moe_test_route_stall.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P, sz, i32, ctypes.c_int64, P]
         L.moe_test_decode_stall.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                             ctypes.POINTER(RouteOutC), P, sz, i32, ctypes.c_int64, P]
+        ap = ctypes.POINTER(AttnShape)
+        L.moe_attn_workspace_bytes.argtypes = [ap, ctypes.POINTER(sz)]
+        L.moe_attn_decode.argtypes = [ap, P, P, P, P, ctypes.c_float, P, P, sz, P]
+        L.moe_attn_decode_timed.argtypes = [ap, P, P, P, P, ctypes.c_float, P, P, sz, ctypes.POINTER(P), P]
+        for f in ("moe_attn_workspace_bytes", "moe_attn_decode", "moe_attn_decode_timed"):
+            getattr(L, f).restype = i32
         for f in ("moe_workspace_bytes", "moe_max_tiles", "moe_route_blocks", "moe_route", "moe_forward",
                   "moe_forward_timed",
                   "moe_status_read", "moe_test_route_stall", "moe_test_decode_stall"):
@@ -233,3 +244,39 @@ def test_route_stall(shape, x, w_router, router_bias, w_shared_gate, out: dict, 
                                       _ptr(w_shared_gate), ctypes.byref(r), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), stalled_block, timeout_ns,
                                       _stream(stream)), "moe_test_route_stall")
+
+
+# ----------------------------------------------------- decode attention ---
+
+def attn_shape(B, Hq, Hkv, D, L_max) -> AttnShape:
+    return AttnShape(B, Hq, Hkv, D, L_max)
+
+
+def attn_workspace_bytes(shape: AttnShape) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_attn_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)), "moe_attn_workspace_bytes")
+    return n.value
+
+
+def attn_alloc_workspace(shape: AttnShape, device) -> torch.Tensor:
+    return torch.empty(max(attn_workspace_bytes(shape), 256), dtype=torch.uint8, device=device)
+
+
+def attn_decode(shape, q, k_cache, v_cache, lens, o, workspace, scale=None, stream=None):
+    """moe_attn_decode: q bf16 [B, Hq, D], caches bf16 [B, Hkv, L_max, D],
+    lens int32 [B], o fp32 [B, Hq, D] (all on the device). The workspace's
+    first int32 is the call's device status word."""
+    s = 1.0 / (shape.D ** 0.5) if scale is None else float(scale)
+    _check(lib().moe_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), s,
+                                 _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "moe_attn_decode")
+
+
+def attn_decode_timed(shape, q, k_cache, v_cache, lens, o, workspace, events, scale=None, stream=None):
+    """attn_decode recording three caller-created CUDA events (raw handles)
+    before the block kernel, between it and the merge kernel, and after."""
+    s = 1.0 / (shape.D ** 0.5) if scale is None else float(scale)
+    ev = (P * 3)(*events)
+    _check(lib().moe_attn_decode_timed(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), s,
+                                       _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(), ev,
+                                       _stream(stream)), "moe_attn_decode_timed")

@@ -8,13 +8,6 @@
 #include "kernels.h"
 
 namespace bgmoe {
-namespace {
-
-constexpr long long kDefaultTimeoutNs = 1000000000ll;  // 1 s per device-side wait
-constexpr int kMaxRouteBlocks = 128;
-constexpr int kMinTokensPerRouteBlock = 16;
-constexpr int kMaxTokens = 1 << 18;
-constexpr int kTensorCoreMinTokens = 64;
 
 thread_local char g_detail[256] = "";
 
@@ -22,6 +15,14 @@ moe_status cuda_fail(cudaError_t e, const char* where) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorString(e));
   return MOE_ERR_CUDA;
 }
+
+namespace {
+
+constexpr long long kDefaultTimeoutNs = 1000000000ll;  // 1 s per device-side wait
+constexpr int kMaxRouteBlocks = 128;
+constexpr int kMinTokensPerRouteBlock = 16;
+constexpr int kMaxTokens = 1 << 18;
+constexpr int kTensorCoreMinTokens = 64;
 
 moe_status check_shape(const moe_shape* s) {
   if (!s) return MOE_ERR_INVALID_ARG;

@@ -8,6 +8,11 @@
 
 namespace bgmoe {
 
+// Records "where: CUDA error text" for moe_last_error_detail() and returns
+// MOE_ERR_CUDA (every entry point of the library reports launch failures so).
+moe_status cuda_fail(cudaError_t e, const char* where);
+
+
 constexpr int kDecodeMaxTokens = 4;  // tokens per call handled by the fused decode kernel
 constexpr int kDecodeMaxStages = 8;  // shared-memory ring depth of the fused decode kernel
 

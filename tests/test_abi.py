@@ -109,3 +109,42 @@ def test_stall_hook_argument_checks(moelib):
     for blk, to in [(-1, 10**6), (nb, 10**6), (0, 0), (0, 10**10)]:
         assert L.moe_test_route_stall(ctypes.byref(sh), 0x100000, 0x200000, None, 0x300000, ctypes.byref(r),
                                       0x400000, 1 << 30, blk, to, None) == 1
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((0, 16, 2, 256, 64), 2), ((4097, 16, 2, 256, 64), 2), ((1, 16, 3, 256, 64), 2), ((1, 18, 2, 256, 64), 2),
+    ((1, 16, 2, 96, 64), 2), ((1, 16, 2, 512, 64), 2), ((1, 16, 2, 256, 0), 2), ((1, 16, 2, 256, (1 << 26) + 1), 2),
+    ((2048, 64, 64, 64, 8), 2), ((1, 16, 2, 256, 1 << 26), 0), ((4096, 8, 8, 64, 1), 0)])
+def test_attention_shape_checks(moelib, shape, code):
+    sh = moelib.attn_shape(*shape)
+    n = ctypes.c_size_t()
+    assert moelib.lib().moe_attn_workspace_bytes(ctypes.byref(sh), ctypes.byref(n)) == code
+
+
+def test_attention_workspace_formula(moelib):
+    """256 bytes of status, 256 per-block flags, then (256 + B*Hkv) partial
+    slots of 8 heads x (D + 2) floats."""
+    for B, Hkv, D in [(1, 2, 256), (8, 2, 256), (37, 4, 64)]:
+        sh = moelib.attn_shape(B, 4 * Hkv, Hkv, D, 1000)
+        assert moelib.attn_workspace_bytes(sh) == 256 + 1024 + (256 + B * Hkv) * 8 * (D + 2) * 4
+
+
+def test_attention_host_side_errors_before_any_cuda_call(moelib):
+    """Null or misaligned pointers, a short workspace and a bad scale are
+    rejected on the host; the fake device addresses are never dereferenced."""
+    L = moelib.lib()
+    sh = moelib.attn_shape(2, 16, 2, 256, 4096)
+    need = moelib.attn_workspace_bytes(sh)
+    q, k, v, lens, o, ws = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000
+    call = L.moe_attn_decode
+    assert call(ctypes.byref(sh), q, k, v, lens, 0.0625, o, ws, need - 1, None) == 3
+    assert call(ctypes.byref(sh), None, k, v, lens, 0.0625, o, ws, need, None) == 1
+    assert call(ctypes.byref(sh), q, k, None, lens, 0.0625, o, ws, need, None) == 1
+    assert call(ctypes.byref(sh), q, k, v, None, 0.0625, o, ws, need, None) == 1
+    assert call(ctypes.byref(sh), q + 8, k, v, lens, 0.0625, o, ws, need, None) == 1
+    assert call(ctypes.byref(sh), q, k + 2, v, lens, 0.0625, o, ws, need, None) == 1
+    assert call(ctypes.byref(sh), q, k, v, lens, 0.0625, o + 8, ws, need, None) == 1
+    assert call(ctypes.byref(sh), q, k, v, lens, 0.0625, o, ws + 16, need, None) == 1
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert call(ctypes.byref(sh), q, k, v, lens, bad, o, ws, need, None) == 1
+    assert L.moe_attn_decode_timed(ctypes.byref(sh), q, k, v, lens, 0.0625, o, ws, need, None, None) == 1
