@@ -64,18 +64,22 @@ template <int D>
 struct Smem {
   static constexpr int kSlabs = D / 64;
   static constexpr int kStageBytes = 2 * kSlabs * kSlab;  // K then V
-  static constexpr int kLd = D + 4;                       // merge rows padded against bank conflicts
-  static constexpr int kMergeBytes = kConsumers * kHeads * kLd * 4;
+  // A warp's softmax state as its lanes hold it: D/4 accumulators, then the
+  // maxima and sums of the lane's two heads; stored [value][lane].
+  static constexpr int kStateFloats = D / 4 + 4;
+  static constexpr int kStateBytes = kStateFloats * 32 * 4;
+  static constexpr int kMergeBytes = 3 * kStateBytes;     // warps 2, 3 (round 1) and warp 1 (round 2)
   static constexpr int kCtlOffset = kStages * kStageBytes + kMergeBytes;
-  static constexpr int kMergeMLOffset = kCtlOffset + 128;  // m, l of each warp and head
-  static constexpr int kBytes = kMergeMLOffset + kConsumers * kHeads * 2 * 4 + 1024;  // + alignment slack
+  static constexpr int kBytes = kCtlOffset + 128 + 1024;  // + alignment slack
 };
 
 struct Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t mrg_full;
-  uint64_t mrg_free;
+  uint64_t mrg_full;   // round 1: warps 2 and 3 have stored their states
+  uint64_t mrg_free;   // round 1: warps 0 and 1 have read them
+  uint64_t mrg2_full;  // round 2: warp 1 has stored its state
+  uint64_t mrg2_free;  // round 2: warp 0 has read it
   int abort;
 };
 
@@ -168,7 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + S::kCtlOffset);
   float* mrg = reinterpret_cast<float*>(smem + kStages * S::kStageBytes);
-  float* mrg_ml = reinterpret_cast<float*>(smem + S::kMergeMLOffset);
   __shared__ long long s_lo, s_hi;
   __shared__ int s_b, s_g, s_i, s_bad;
 
@@ -181,8 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->full[s], 1);
       mbar_init(&ctl->empty[s], kConsumers);
     }
-    mbar_init(&ctl->mrg_full, kConsumers);
-    mbar_init(&ctl->mrg_free, kConsumers);
+    mbar_init(&ctl->mrg_full, 2);
+    mbar_init(&ctl->mrg_free, 2);
+    mbar_init(&ctl->mrg2_full, 1);
+    mbar_init(&ctl->mrg2_free, 1);
     ctl->abort = 0;
     tc::fence_barrier_init();
   }
@@ -393,63 +398,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&ctl->empty[s]);
 
       if (cur.i == cur.nb - 1 || j == hi - 1) {
-        // ---- the run leaves this pair: merge the four warps' states
-        if (flushes > 0 && !warp_wait(&ctl->mrg_free, (flushes - 1) & 1)) {
-          ok = false;
-          break;
-        }
+        // ---- the run leaves this pair: merge the four warps' states. The
+        // warps hold their accumulators in the same lane layout, so a warp
+        // folds another's state in lane by lane: warps 2, 3 into 0, 1, then
+        // warp 1 into warp 0 (a fixed order), and warp 0 stores the result.
         float tA = lA, tB = lB;
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
           tA += __shfl_xor_sync(0xffffffffu, tA, o);
           tB += __shfl_xor_sync(0xffffffffu, tB, o);
         }
-        float* mw = mrg + warp * kHeads * S::kLd;
+        auto put = [&](float* st) {
 #pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-          const int d = 16 * mt + (lane >> 2);
-          mw[hA * S::kLd + d] = acc[mt][0];
-          mw[(hA + 1) * S::kLd + d] = acc[mt][1];
-          mw[hA * S::kLd + d + 8] = acc[mt][2];
-          mw[(hA + 1) * S::kLd + d + 8] = acc[mt][3];
+          for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) st[(4 * mt + k) * 32 + lane] = acc[mt][k];
+          st[(D / 4) * 32 + lane] = mA;
+          st[(D / 4 + 1) * 32 + lane] = mB;
+          st[(D / 4 + 2) * 32 + lane] = tA;
+          st[(D / 4 + 3) * 32 + lane] = tB;
+        };
+        auto take = [&](const float* st) {
+          const float m2A = st[(D / 4) * 32 + lane], m2B = st[(D / 4 + 1) * 32 + lane];
+          const float nA = fmaxf(mA, m2A), nB = fmaxf(mB, m2B);
+          const float a1A = exp2f(mA - nA), a2A = exp2f(m2A - nA);
+          const float a1B = exp2f(mB - nB), a2B = exp2f(m2B - nB);
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            acc[mt][0] = acc[mt][0] * a1A + st[(4 * mt + 0) * 32 + lane] * a2A;
+            acc[mt][1] = acc[mt][1] * a1B + st[(4 * mt + 1) * 32 + lane] * a2B;
+            acc[mt][2] = acc[mt][2] * a1A + st[(4 * mt + 2) * 32 + lane] * a2A;
+            acc[mt][3] = acc[mt][3] * a1B + st[(4 * mt + 3) * 32 + lane] * a2B;
+          }
+          tA = tA * a1A + st[(D / 4 + 2) * 32 + lane] * a2A;
+          tB = tB * a1B + st[(D / 4 + 3) * 32 + lane] * a2B;
+          mA = nA;
+          mB = nB;
+        };
+        float* st1 = mrg + (warp & 1) * S::kStateFloats * 32;  // round 1 slot of warp 2 / warp 3
+        float* st2 = mrg + 2 * S::kStateFloats * 32;           // round 2 slot
+        bool fail = false;
+        if (warp >= 2) {
+          fail = flushes > 0 && !warp_wait(&ctl->mrg_free, (flushes - 1) & 1);
+          if (!fail) {
+            put(st1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->mrg_full);
+          }
+        } else {
+          fail = !warp_wait(&ctl->mrg_full, flushes & 1);
+          if (!fail) {
+            take(st1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->mrg_free);
+            if (warp == 1) {
+              fail = flushes > 0 && !warp_wait(&ctl->mrg2_free, (flushes - 1) & 1);
+              if (!fail) {
+                put(st2);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->mrg2_full);
+              }
+            } else {
+              fail = !warp_wait(&ctl->mrg2_full, flushes & 1);
+              if (!fail) {
+                take(st2);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->mrg2_free);
+                const size_t slot = (size_t)c + cur.b * p.Hkv + cur.g;
+                float* po = p.part + (size_t)2 * p.slots * kHeads + slot * kHeads * D;
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                  const int d = 16 * mt + (lane >> 2);
+                  po[hA * D + d] = acc[mt][0];
+                  po[(hA + 1) * D + d] = acc[mt][1];
+                  po[hA * D + d + 8] = acc[mt][2];
+                  po[(hA + 1) * D + d + 8] = acc[mt][3];
+                }
+                if (lane < 4) {
+                  float* pm = p.part + slot * kHeads;
+                  float* pl = p.part + (size_t)p.slots * kHeads + slot * kHeads;
+                  pm[hA] = mA;
+                  pm[hA + 1] = mB;
+                  pl[hA] = tA;
+                  pl[hA + 1] = tB;
+                }
+              }
+            }
+          }
         }
-        if (lane < 4) {
-          mrg_ml[(warp * kHeads + hA) * 2] = mA;
-          mrg_ml[(warp * kHeads + hA) * 2 + 1] = tA;
-          mrg_ml[(warp * kHeads + hA + 1) * 2] = mB;
-          mrg_ml[(warp * kHeads + hA + 1) * 2 + 1] = tB;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->mrg_full);
-        if (!warp_wait(&ctl->mrg_full, flushes & 1)) {
+        if (fail) {
           ok = false;
           break;
         }
-        const int pair = cur.b * p.Hkv + cur.g;
-        const size_t slot = (size_t)c + pair;
-        float* pm = p.part;
-        float* pl = p.part + (size_t)p.slots * kHeads;
-        float* po = p.part + (size_t)2 * p.slots * kHeads;
-        for (int e = threadIdx.x; e < r * D; e += kConsumers * 32) {
-          const int h = e / D, d = e % D;
-          float M = kMinusBig;
-#pragma unroll
-          for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mrg_ml[(w * kHeads + h) * 2]);
-          float O = 0.f, L = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumers; ++w) {
-            const float f = exp2f(mrg_ml[(w * kHeads + h) * 2] - M);
-            O += f * mrg[(w * kHeads + h) * S::kLd + d];
-            L += f * mrg_ml[(w * kHeads + h) * 2 + 1];
-          }
-          po[(slot * kHeads + h) * D + d] = O;
-          if (d == 0) {
-            pm[slot * kHeads + h] = M;
-            pl[slot * kHeads + h] = L;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl->mrg_free);
         ++flushes;
         reset();
         if (j + 1 < hi) {
