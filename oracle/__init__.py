@@ -28,3 +28,4 @@ from .moe import (  # noqa: F401
     topk_gap,
 )
 from .attention import gqa_decode_attention  # noqa: F401,E402
+from .gated_deltanet import gated_delta_scan  # noqa: F401,E402

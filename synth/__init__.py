@@ -29,6 +29,7 @@ scale and bias per 64 weights from its "Prefill optimisations"):
 """
 from __future__ import annotations
 
+import itertools
 import math
 from dataclasses import dataclass, field
 
@@ -313,4 +314,63 @@ ATTN_WORKLOADS = {
     "attn-decode-128k": AttnSpec("attn-decode-128k", lens=(131072,), layers=10, seed=20260113),
     "attn-decode-batch8": AttnSpec("attn-decode-batch8", lens=(4096, 32768, 1, 17000, 65536, 8191, 777, 20000),
                                    layers=10, seed=20260114),
+}
+
+
+# --------------------------------------------------------- Gated DeltaNet ---
+# Streams: kind * 2**32 + layer * 2**12 + (0 for the token tensors, b for a
+# sequence's initial state).
+K_GDN_Q, K_GDN_K, K_GDN_V, K_GDN_GATE, K_GDN_BETA, K_GDN_STATE = 50, 51, 52, 53, 54, 55
+
+
+@dataclass
+class GdnSpec:
+    """One Gated DeltaNet workload: sequences of `lens` new tokens each, packed
+    end to end, through a layer of Hqk query/key heads and Hv value heads
+    ("Model specification" on dothoosh.com: 30 Gated DeltaNet layers; the
+    sizes are not given there).
+
+    q, k, v ~ N(0, 1) bf16; gate = log(alpha) = -|N(0, 0.05)| (alpha in about
+    0.9 .. 1); beta = sigmoid(N(0, 1)); initial state ~ N(0, 0.1^2) fp32."""
+    name: str
+    lens: tuple
+    Hqk: int = 16
+    Hv: int = 32
+    Dk: int = 128
+    Dv: int = 128
+    seed: int = 20260201
+    layers: int = 1
+
+    @property
+    def B(self) -> int:
+        return len(self.lens)
+
+    @property
+    def T(self) -> int:
+        return sum(self.lens)
+
+
+def gdn_inputs(spec: GdnSpec, layer: int = 0, device="cpu"):
+    """q, k bf16 [T, Hqk, Dk]; v bf16 [T, Hv, Dv]; gate, beta fp32 [T, Hv];
+    state0 fp32 [B, Hv, Dv, Dk]; offsets int32 [B+1]."""
+    T, Hqk, Hv, Dk, Dv = spec.T, spec.Hqk, spec.Hv, spec.Dk, spec.Dv
+    q = to_bf16(normal_f64(spec.seed, [stream_id(K_GDN_Q, layer)], T * Hqk * Dk, device)[0]).view(T, Hqk, Dk)
+    k = to_bf16(normal_f64(spec.seed, [stream_id(K_GDN_K, layer)], T * Hqk * Dk, device)[0]).view(T, Hqk, Dk)
+    v = to_bf16(normal_f64(spec.seed, [stream_id(K_GDN_V, layer)], T * Hv * Dv, device)[0]).view(T, Hv, Dv)
+    gate = (-0.05 * normal_f64(spec.seed, [stream_id(K_GDN_GATE, layer)], T * Hv, device)[0].abs())
+    beta = torch.sigmoid(normal_f64(spec.seed, [stream_id(K_GDN_BETA, layer)], T * Hv, device)[0])
+    state = torch.empty(spec.B, Hv, Dv, Dk, dtype=torch.float32, device=device)
+    for b in range(spec.B):
+        state[b] = (0.1 * normal_f64(spec.seed, [stream_id(K_GDN_STATE, layer, b)], Hv * Dv * Dk, device)[0]
+                    ).to(torch.float32).view(Hv, Dv, Dk)
+    offsets = torch.tensor([0] + list(itertools.accumulate(spec.lens)), dtype=torch.int32, device=device)
+    return (q, k, v, gate.to(torch.float32).view(T, Hv), beta.to(torch.float32).view(T, Hv), state, offsets)
+
+
+# Prefill of one 4096-token prompt (4 layers per step) and decode of 64
+# sequences one token each through the model's 30 Gated DeltaNet layers; a
+# ragged pack for the tests.
+GDN_WORKLOADS = {
+    "gdn-prefill-4096": GdnSpec("gdn-prefill-4096", lens=(4096,), layers=4, seed=20260211),
+    "gdn-decode-b64": GdnSpec("gdn-decode-b64", lens=(1,) * 64, layers=30, seed=20260212),
 }

@@ -14,6 +14,7 @@ import math
 import numpy as np
 
 import oracle.attention as A
+import oracle.gated_deltanet as G
 import oracle.moe as M
 from tests._util import bf16_from_f64, read_golden
 
@@ -502,6 +503,162 @@ def pin_attn_matches_torch_sdpa():
             scale=scale, enable_gqa=True)[:, :, 0, :].numpy()
         got = _attn(q, k, v, [L, L], scale)
         assert np.allclose(got, want, rtol=0, atol=1e-12), scale
+
+
+# ---------------------------------------------------------- Gated DeltaNet ---
+
+def _gdn(q, k, v, gate, beta, S0, offsets):
+    return G.gated_delta_scan(_bits(q), _bits(k), _bits(v), gate, beta, S0, offsets)
+
+
+def _gdn_case(T, Hqk=2, Hv=4, Dk=8, Dv=8, B=1):
+    q = RNG.standard_normal((T, Hqk, Dk))
+    k = RNG.standard_normal((T, Hqk, Dk))
+    v = RNG.standard_normal((T, Hv, Dv))
+    gate = -RNG.uniform(0.0, 0.5, (T, Hv))
+    beta = RNG.uniform(0.1, 0.9, (T, Hv))
+    S0 = RNG.standard_normal((B, Hv, Dv, Dk))
+    return q, k, v, gate, beta, S0
+
+
+def pin_gdn_full_write_is_retrieved():
+    """With beta = 1 and no decay, one step writes v under the unit key k^:
+    S_t k^ = v whatever S_{t-1} was, so q = k reads back v / sqrt(Dk)."""
+    T, Dk = 5, 16
+    q, k, v, gate, beta, S0 = _gdn_case(T, Dk=Dk, Dv=8)
+    gate[:] = 0.0
+    beta[:] = 1.0
+    o, _ = _gdn(k, k, v, gate, beta, S0, [0, T])
+    vb = M.bf16_bits_to_f64(_bits(v))
+    assert np.allclose(o, vb / math.sqrt(Dk), rtol=1e-5, atol=1e-6)
+
+
+def pin_gdn_orthonormal_keys_are_linear_attention():
+    """From S_0 = 0 with no decay and orthonormal keys e_t the writes do not
+    interfere: o_t = sum_{s<=t} beta_s v_s (q^_t)_s, q^ the unit q / sqrt(Dk)."""
+    T, Dk, Dv = 6, 8, 4
+    q, k, v, gate, beta, S0 = _gdn_case(T, Hqk=1, Hv=1, Dk=Dk, Dv=Dv)
+    k[:] = 0.0
+    for t in range(T):
+        k[t, 0, t] = 1.0
+    gate[:] = 0.0
+    S0[:] = 0.0
+    o, S = _gdn(q, k, v, gate, beta, S0, [0, T])
+    qb = M.bf16_bits_to_f64(_bits(q))[:, 0]
+    vb = M.bf16_bits_to_f64(_bits(v))[:, 0]
+    for t in range(T):
+        qh = qb[t] / np.linalg.norm(qb[t]) / math.sqrt(Dk)
+        want = sum(beta[s, 0] * vb[s] * qh[s] for s in range(t + 1))
+        assert np.allclose(o[t, 0], want, rtol=1e-5, atol=1e-7), t
+    assert np.allclose(S[0, 0][:, :T], (beta[:, 0][None, :] * vb.T), rtol=1e-5, atol=1e-7)
+
+
+def pin_gdn_orthonormal_keys_with_decay():
+    """Orthonormal keys e_t from S_0 = 0 with decay: each write decays from the
+    step after it, o_t = sum_{s<=t} (prod_{s<r<=t} alpha_r) beta_s v_s (q^_t)_s."""
+    T, Dk, Dv = 5, 8, 3
+    q, k, v, gate, beta, S0 = _gdn_case(T, Hqk=1, Hv=1, Dk=Dk, Dv=Dv)
+    k[:] = 0.0
+    for t in range(T):
+        k[t, 0, t] = 1.0
+    S0[:] = 0.0
+    o, _ = _gdn(q, k, v, gate, beta, S0, [0, T])
+    qb = M.bf16_bits_to_f64(_bits(q))[:, 0]
+    vb = M.bf16_bits_to_f64(_bits(v))[:, 0]
+    for t in range(T):
+        qh = qb[t] / np.linalg.norm(qb[t]) / math.sqrt(Dk)
+        want = sum(math.exp(gate[s + 1:t + 1, 0].sum()) * beta[s, 0] * vb[s] * qh[s] for s in range(t + 1))
+        assert np.allclose(o[t, 0], want, rtol=1e-5, atol=1e-7), t
+
+
+def pin_gdn_same_key_twice():
+    """Writing under the same unit key twice, from S_0 = 0: the second step's
+    delta is taken against the decayed state, so the memory then holds
+    alpha (1 - beta) v_0 + beta v_1 under that key (beta_0 = 1)."""
+    Dk, Dv = 8, 4
+    q, k, v, gate, beta, S0 = _gdn_case(2, Hqk=1, Hv=1, Dk=Dk, Dv=Dv)
+    k[:] = 0.0
+    k[:, 0, 3] = 1.0
+    q[:] = k
+    S0[:] = 0.0
+    gate[0, 0] = 0.0
+    beta[0, 0] = 1.0
+    o, S = _gdn(q, k, v, gate, beta, S0, [0, 2])
+    vb = M.bf16_bits_to_f64(_bits(v))[:, 0]
+    a, bt = math.exp(gate[1, 0]), beta[1, 0]
+    held = a * (1 - bt) * vb[0] + bt * vb[1]
+    assert np.allclose(S[0, 0][:, 3], held, rtol=1e-5, atol=1e-7)
+    assert np.allclose(o[1, 0], held / math.sqrt(Dk), rtol=1e-5, atol=1e-7)
+
+
+def pin_gdn_pure_decay():
+    """beta = 0: no writes, the state only decays: S_t = prod alpha_s S_0 and
+    o_t = (prod_{s<=t} alpha_s) S_0 q^_t."""
+    T, Dk = 4, 8
+    q, k, v, gate, beta, S0 = _gdn_case(T, Hqk=1, Hv=2, Dk=Dk, Dv=6)
+    beta[:] = 0.0
+    o, S = _gdn(q, k, v, gate, beta, S0, [0, T])
+    qb = M.bf16_bits_to_f64(_bits(q))[:, 0]
+    for h in range(2):
+        decay = np.exp(np.cumsum(gate[:, h]))
+        for t in range(T):
+            qh = qb[t] / np.linalg.norm(qb[t]) / math.sqrt(Dk)
+            assert np.allclose(o[t, h], decay[t] * (S0[0, h] @ qh), rtol=1e-6, atol=1e-9)
+        assert np.allclose(S[0, h], decay[-1] * S0[0, h], rtol=1e-12)
+
+
+def pin_gdn_head_grouping():
+    """Value head h reads query/key head h // (Hv/Hqk): key head 0 has q = k
+    (reads back v / sqrt(Dk) after a full write), key head 1 has q orthogonal
+    to k (reads 0); value heads 0, 1 follow key head 0, heads 2, 3 key head 1."""
+    Dk = 8
+    q, k, v, gate, beta, S0 = _gdn_case(1, Hqk=2, Hv=4, Dk=Dk, Dv=4)
+    k[0, 0] = 0.0
+    k[0, 0, 0] = 1.0
+    q[0, 0] = k[0, 0]
+    k[0, 1] = 0.0
+    k[0, 1, 1] = 1.0
+    q[0, 1] = 0.0
+    q[0, 1, 2] = 1.0
+    gate[:] = 0.0
+    beta[:] = 1.0
+    S0[:] = 0.0
+    o, _ = _gdn(q, k, v, gate, beta, S0, [0, 1])
+    vb = M.bf16_bits_to_f64(_bits(v))
+    for h in (0, 1):
+        assert np.allclose(o[0, h], vb[0, h] / math.sqrt(Dk), rtol=1e-5)
+    for h in (2, 3):
+        assert np.allclose(o[0, h], 0.0, atol=1e-12)
+
+
+def pin_gdn_scale_of_q_and_k_does_not_matter():
+    """q and k enter only through their directions (L2-normalised)."""
+    q, k, v, gate, beta, S0 = _gdn_case(7)
+    o, S = _gdn(q, k, v, gate, beta, S0, [0, 7])
+    o2, S2 = _gdn(4.0 * q, 0.25 * k, v, gate, beta, S0, [0, 7])
+    # equal up to the eps inside the normalisation (1e-6 against |k|^2 ~ 1)
+    assert np.allclose(o2, o, rtol=1e-5, atol=1e-5)
+    assert np.allclose(S2, S, rtol=1e-5, atol=1e-5)
+
+
+def pin_gdn_split_and_packing():
+    """A sequence run in one call equals the same tokens in two calls that
+    pass the state on; packing three sequences (one empty) in one call equals
+    three separate calls (no state leaks across a sequence boundary)."""
+    T = 9
+    q, k, v, gate, beta, S0 = _gdn_case(T, B=1)
+    o, S = _gdn(q, k, v, gate, beta, S0, [0, T])
+    o1, S1 = _gdn(q[:4], k[:4], v[:4], gate[:4], beta[:4], S0, [0, 4])
+    o2, S2 = _gdn(q[4:], k[4:], v[4:], gate[4:], beta[4:], S1, [0, T - 4])
+    assert np.array_equal(np.concatenate([o1, o2]), o) and np.array_equal(S2, S)
+    S03 = RNG.standard_normal((3, 4, 8, 8))
+    offs = [0, 3, 3, T]
+    op, Sp = _gdn(q, k, v, gate, beta, S03, offs)
+    for b in range(3):
+        lo, hi = offs[b], offs[b + 1]
+        ob, Sb = _gdn(q[lo:hi], k[lo:hi], v[lo:hi], gate[lo:hi], beta[lo:hi], S03[b:b + 1], [0, hi - lo])
+        assert np.array_equal(op[lo:hi], ob) and np.array_equal(Sp[b], Sb[0])
+    assert np.array_equal(Sp[1], S03[1])
 
 
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

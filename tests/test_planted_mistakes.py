@@ -6,6 +6,7 @@ import numpy as np
 import pytest
 
 import oracle.attention as A
+import oracle.gated_deltanet as G
 import oracle.moe as M
 from tests.oracle_pins import PINS
 
@@ -180,6 +181,63 @@ def test_attention_variant_without_mistake_passes(monkeypatch):
     """The mutant generator itself, with no mistake switched on, passes every
     pin (so a caught mutant is caught for its mistake)."""
     monkeypatch.setattr(A, "gqa_decode_attention", _attention_variant("faithful_copy"))
+    assert not _caught_by_some_pin()
+
+
+def _gdn_variant(label, order="decay_first", knorm=True, qscale=True, delta_from="decayed", mapping="div",
+                 read="after"):
+    """A copy of the Gated DeltaNet oracle with one plausible mistake."""
+    def scan(q_bits, k_bits, v_bits, gate, beta, state0, offsets):
+        q, k, v = (M.bf16_bits_to_f64(t) for t in (q_bits, k_bits, v_bits))
+        S_all = np.array(state0, dtype=np.float64, copy=True)
+        T, Hqk, Dk = q.shape
+        Hv = v.shape[1]
+        per = Hv // Hqk
+        o = np.zeros((T, Hv, v.shape[2]))
+        for b in range(len(offsets) - 1):
+            for h in range(Hv):
+                g = h // per if mapping == "div" else h % Hqk
+                S = S_all[b, h]
+                for t in range(int(offsets[b]), int(offsets[b + 1])):
+                    kh = k[t, g] / np.sqrt((k[t, g] ** 2).sum() + 1e-6) if knorm else k[t, g]
+                    qh = q[t, g] / np.sqrt((q[t, g] ** 2).sum() + 1e-6)
+                    if qscale:
+                        qh = qh / np.sqrt(Dk)
+                    a = np.exp(gate[t, h])
+                    if read == "before":
+                        o[t, h] = (a * S) @ qh
+                    if order == "decay_first":
+                        Sk = (S @ kh) if delta_from == "undecayed" else (a * S) @ kh
+                        S *= a
+                        S += np.outer(beta[t, h] * (v[t, h] - Sk), kh)
+                    else:
+                        S += np.outer(beta[t, h] * (v[t, h] - S @ kh), kh)
+                        S *= a
+                    if read == "after":
+                        o[t, h] = S @ qh
+        return o, S_all
+    scan.__name__ = label
+    return scan
+
+
+GDN_MUTANTS = [
+    _gdn_variant("decay_after_write", order="write_first"),
+    _gdn_variant("key_not_normalised", knorm=False),
+    _gdn_variant("query_not_scaled", qscale=False),
+    _gdn_variant("delta_against_undecayed_state", delta_from="undecayed"),
+    _gdn_variant("value_head_by_modulo", mapping="mod"),
+    _gdn_variant("output_read_before_write", read="before"),
+]
+
+
+@pytest.mark.parametrize("mutant", GDN_MUTANTS, ids=[m.__name__ for m in GDN_MUTANTS])
+def test_planted_gdn_mistake_is_caught(monkeypatch, mutant):
+    monkeypatch.setattr(G, "gated_delta_scan", mutant)
+    assert _caught_by_some_pin(), f"no pin caught the planted mistake {mutant.__name__}"
+
+
+def test_gdn_variant_without_mistake_passes(monkeypatch):
+    monkeypatch.setattr(G, "gated_delta_scan", _gdn_variant("faithful_copy"))
     assert not _caught_by_some_pin()
 
 

@@ -52,3 +52,13 @@ def test_attention_inputs_subset_and_shape():
     assert torch.equal(one[0], v[1, 1])
     assert not torch.equal(k, v)
     assert torch.isfinite(k.float()).all() and torch.isfinite(v.float()).all()
+
+
+def test_gdn_inputs_shapes_and_ranges():
+    spec = synth.GdnSpec("t", lens=(3, 0, 5), Hqk=2, Hv=4, Dk=8, Dv=8)
+    q, k, v, gate, beta, state, offsets = synth.gdn_inputs(spec)
+    assert q.shape == (8, 2, 8) and k.shape == q.shape and v.shape == (8, 4, 8)
+    assert gate.shape == (8, 4) and beta.shape == (8, 4) and state.shape == (3, 4, 8, 8)
+    assert offsets.tolist() == [0, 3, 3, 8]
+    assert bool((gate <= 0).all()) and bool(((beta > 0) & (beta < 1)).all())
+    assert not torch.equal(q, k)
