@@ -7,7 +7,8 @@ weights (H = 2048, I = 512, E = 256 top-8 + shared, 4-bit group-64 weights,
 layers; the metric is microseconds per layer. --workload picks another
 shape (prefill-zipf-512, prefill-4096, long-skew-16384, decode-t4, tiny),
 or decode attention over a bf16 KV cache (attn-decode-32k, -64k, -128k,
-attn-decode-batch8: 16 query heads on 2 KV heads, D = 256, 10 layers).
+attn-decode-batch8: 16 query heads on 2 KV heads, D = 256, 10 layers), or
+the Gated DeltaNet scan (gdn-prefill-4096, gdn-decode-b64).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -60,9 +61,17 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
-        bytes=67159296 + 118528, profile="profiles/attn_block_kernel_attn-decode-32k.md",
-        sources={"attention.cu": "50552cacf493c737d614f8a534631a0b634f86bafb86d4f3d979dc229333245a",
+        bytes=67168512 + 133120, profile="profiles/attn_block_kernel_attn-decode-32k.md",
+        sources={"attention.cu": "459908e5df635aef1646986b3d646fc1f74e811dbf8dffaeca363c987c0fc8f7",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
+                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
+    ("gdn_scan_kernel", "gdn-prefill-4096"): dict(
+        bytes=70285312 + 26173696, profile="profiles/gdn_scan_kernel_gdn-prefill-4096.md",
+        sources={"gdn.cu": "3d128b3587fd6d65c176086eff0449af4c6965844316f141c7afab279f923a23",
+                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
+    ("gdn_short_kernel", "gdn-decode-b64"): dict(
+        bytes=135300352 + 82013184, profile="profiles/gdn_short_kernel_gdn-decode-b64.md",
+        sources={"gdn.cu": "3d128b3587fd6d65c176086eff0449af4c6965844316f141c7afab279f923a23",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
 
@@ -638,6 +647,218 @@ def run_attention_reference(args, spec, rank, world):
             "e2e": {"value": round(value, 3), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# -------------------------------------------------------- Gated DeltaNet --
+
+METRIC_GDN = "Gated DeltaNet scan µs/layer (fp32 state in registers); % of ALU (prefill) / HBM (decode) roofline"
+# fp32 FMA peak: 152 SMs x 128 FP32 lanes x 2 flops x the SM clock (2070 MHz at most)
+FP32_LANES_PER_SM = 128
+
+
+class GdnWorkload:
+    """Device-resident inputs of a Gated DeltaNet workload: one set per layer,
+    each layer with its own initial state (read) and final state (written)."""
+
+    def __init__(self, m, spec, device):
+        self.m, self.spec, self.dev = m, spec, device
+        self.layers = spec.layers
+        self.shape = m.gdn_shape(spec.B, spec.T, spec.Hqk, spec.Hv, spec.Dk, spec.Dv)
+        self.inp = [list(synth.gdn_inputs(spec, layer=li, device=device)) for li in range(self.layers)]
+        self.state_out = [torch.empty_like(x[5]) for x in self.inp]
+        self.o = torch.empty(self.layers, spec.T, spec.Hv, spec.Dv, dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def call(self, li, events=None):
+        q, k, v, gate, beta, state, offsets = self.inp[li]
+        if events is None:
+            self.m.gdn_scan(self.shape, q, k, v, gate, beta, offsets, state, self.state_out[li], self.o[li],
+                            status=self.status)
+        else:
+            self.m.gdn_scan_timed(self.shape, q, k, v, gate, beta, offsets, state, self.state_out[li], self.o[li],
+                                  events, status=self.status)
+
+    def step(self):
+        for li in range(self.layers):
+            self.call(li)
+
+    def bytes_per_layer(self):
+        s = self.spec
+        state = s.B * s.Hv * s.Dv * s.Dk * 4 * 2
+        tok = s.T * (2 * s.Hqk * s.Dk * 2 + s.Hv * s.Dv * 2 + 2 * s.Hv * 4 + s.Hv * s.Dv * 4)
+        return state + tok + (s.B + 1) * 4
+
+    def flops_per_layer(self):
+        s = self.spec   # per token and state element: the two dot products and the update (3 FMAs)
+        return s.T * s.Hv * s.Dv * s.Dk * 6
+
+
+def gdn_kernel_time(W, steps):
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(W.layers)]
+    for e2 in ev:
+        for e in e2:
+            e.record()
+    torch.cuda.synchronize()
+
+    def timed_step():
+        for li in range(W.layers):
+            W.call(li, events=[e.cuda_event for e in ev[li]])
+    g = capture(timed_step)
+    t = 0.0
+    for _ in range(steps):
+        g.replay()
+        torch.cuda.synchronize()
+        for e2 in ev:
+            t += e2[0].elapsed_time(e2[1])
+    return t / (steps * W.layers)
+
+
+def run_gdn(args, spec, rank, world, local_rank):
+    import bit_grouped_expert_moe_gb300 as m
+    from bit_grouped_expert_moe_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    W = GdnWorkload(m, spec, dev)
+    stream = torch.cuda.current_stream()
+    graph = capture(W.step)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert m.status_read(W.status) == 0
+
+    barrier(world)
+    with ClockSampler(local_rank) as clk:
+        ms = time_region(graph.replay, args.steps, stream)
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    clocks = clk.summary()
+    k_ms = gdn_kernel_time(W, max(1, min(args.steps, 20)))
+
+    # End to end with host buffers: every step copies each layer's token
+    # inputs (q, k, v, gate, beta) in from pinned memory and reads every
+    # layer's output back; the recurrent state stays on the device.
+    host_in = [[x.cpu().pin_memory() for x in W.inp[li][:5]] for li in range(W.layers)]
+    o_host = torch.empty(W.o.shape, dtype=W.o.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for xs in host_in for x in xs)
+
+    def e2e_step():
+        for li in range(W.layers):
+            for dst, src in zip(W.inp[li][:5], host_in[li]):
+                dst.copy_(src, non_blocking=True)
+        graph.replay()
+        o_host.copy_(W.o, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = max(2, args.steps // 2)
+    e2e_ms = max_over_ranks(time_region(e2e_step, n_e2e, stream), world, dev) / n_e2e
+    assert m.status_read(W.status) == 0
+
+    pk, pk_src = peaks()
+    value = ms_step * 1000.0 / W.layers
+    decode = spec.T <= 2 * spec.B   # the library runs these on its short-sequence kernel
+    kname = "gdn_short_kernel" if decode else "gdn_scan_kernel"
+    if decode:
+        by = W.bytes_per_layer()
+        ach = by / (k_ms / 1000.0) / 1e9
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": profiled_traffic(kname, spec.name),
+                "peak_source": pk_src, "algorithmic_bytes_per_launch": int(by)}
+    else:
+        fl = W.flops_per_layer()
+        sm_mhz = pk.get("sm_max_mhz", 2070.0)
+        peak = 152 * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+        ach = fl / (k_ms / 1000.0) / 1e12
+        roof = {"kernel": kname, "bound": "alu", "achieved": round(ach, 2), "peak": round(peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": profiled_traffic(kname, spec.name),
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x max SM clock",
+                "algorithmic_flops_per_launch": int(fl)}
+    out = {
+        "metric": METRIC_GDN, "value": round(value, 3), "unit": "us/layer", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "inputs": "bf16 q, k, v; fp32 gate, beta, state", "data": "synthetic",
+        "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "Hqk": spec.Hqk, "Hv": spec.Hv, "Dk": spec.Dk,
+                   "Dv": spec.Dv, "layers": W.layers, "seed": spec.seed,
+                   "l2": f"{W.layers} layers x {W.bytes_per_layer() / 1e6:.0f} MB per step"
+                         + (" (larger than L2)" if W.layers * W.bytes_per_layer() > 129e6 else ""),
+                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "roofline": roof,
+        "kernels_us_per_call": {kname: round(k_ms * 1000.0, 3)},
+        "e2e": {"value": round(e2e_ms * 1000.0 / W.layers, 3), "unit": "us/layer", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": o_host.numel() * 4},
+        "gpu_launches": W.layers * args.steps,
+        "launch": "one CUDA graph per step",
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = gdn_cpu_baseline(spec, args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return out
+
+
+def _gdn_oracle_sample(spec, heads):
+    """One oracle call on layer 0 restricted to `heads` value heads (inputs
+    generated before the clock starts); returns seconds."""
+    import numpy as np
+    import oracle
+    from tests._util import bits16
+    q, k, v, gate, beta, state, offsets = synth.gdn_inputs(spec, layer=0)
+    per = spec.Hv // spec.Hqk
+    args = []
+    for h in heads:
+        g = h // per
+        args.append((bits16(q[:, g:g + 1]), bits16(k[:, g:g + 1]), bits16(v[:, h:h + 1]),
+                     gate[:, h:h + 1].double().numpy(), beta[:, h:h + 1].double().numpy(),
+                     state[:, h:h + 1].double().numpy(), offsets.numpy()))
+    t0 = time.perf_counter()
+    for a in args:
+        oracle.gated_delta_scan(*a)
+    return time.perf_counter() - t0
+
+
+def gdn_cpu_baseline(spec, seconds):
+    """The oracle, as it stands, on this host's cores: value heads of layer 0
+    timed one at a time until about `seconds`, scaled to a whole layer."""
+    spent, heads = 0.0, 0
+    while spent < seconds and heads < spec.Hv:
+        spent += _gdn_oracle_sample(spec, [heads])
+        heads += 1
+    per_layer = spent / heads * spec.Hv
+    return {"value": round(per_layer * 1e6, 3), "unit": "us/layer", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{heads} of the {spec.Hv} value heads of layer 0, scaled to the layer (numpy fp64)",
+            "seconds": round(spent, 2)}
+
+
+def run_gdn_reference(args, spec, rank, world):
+    if rank != 0:
+        return None
+    times = []
+    t_start = time.perf_counter()
+    for i in range(args.warmup + args.steps):
+        if time.perf_counter() - t_start > 150.0 and times:
+            break
+        dt = _gdn_oracle_sample(spec, [i % spec.Hv]) * spec.Hv
+        if i >= args.warmup:
+            times.append(dt)
+    if not times:
+        times.append(dt)
+    value = sum(times) / len(times) * 1e6
+    return {"impl": "reference", "metric": METRIC_GDN, "value": round(value, 3), "unit": "us/layer",
+            "n_gpus": world, "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(value / 1000.0, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "B": spec.B, "T": spec.T, "Hqk": spec.Hqk, "Hv": spec.Hv,
+                       "layers": spec.layers},
+            "cpu_baseline": {"value": round(value, 3), "unit": "us/layer", "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": "one value head of layer 0 per step, scaled to the layer; capped at 150 s"},
+            "e2e": {"value": round(value, 3), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
 # ----------------------------------------------------------- CPU oracle --
 
 def _oracle_layer_sample(spec, layer_idx, tokens):
@@ -738,7 +959,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode-t1", choices=sorted(synth.WORKLOADS) + sorted(synth.ATTN_WORKLOADS))
+    ap.add_argument("--workload", default="decode-t1",
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.ATTN_WORKLOADS) + sorted(synth.GDN_WORKLOADS))
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
@@ -747,6 +969,16 @@ def main(argv=None):
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = dist_env()
+    if args.workload in synth.GDN_WORKLOADS:
+        spec = synth.GDN_WORKLOADS[args.workload]
+        if args.layers:
+            import dataclasses
+            spec = dataclasses.replace(spec, layers=args.layers)
+        out = run_gdn_reference(args, spec, rank, world) if args.impl == "reference" else \
+            run_gdn(args, spec, rank, world, local_rank)
+        if rank == 0 and out is not None:
+            print(json.dumps(out), flush=True)
+        return
     if args.workload in synth.ATTN_WORKLOADS:
         spec = synth.ATTN_WORKLOADS[args.workload]
         if args.layers:

@@ -7,7 +7,8 @@ importing the entry points raises.
 
 Entry points mirror the C ABI in include/moe.h (workspace_bytes, max_tiles,
 route_blocks, route, forward, status_read, status_string, test_route_stall) and
-include/attention.h (attn_workspace_bytes, attn_decode, attn_decode_timed).
+include/attention.h (attn_workspace_bytes, attn_decode, attn_decode_timed) and
+include/gdn.h (gdn_scan, gdn_scan_timed).
 """
 from __future__ import annotations
 
@@ -32,6 +33,10 @@ class Shape(ctypes.Structure):
 
 class AttnShape(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("B", "Hq", "Hkv", "D", "L_max")]
+
+
+class GdnShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("B", "T", "Hqk", "Hv", "Dk", "Dv")]
 
 
 class QMat(ctypes.Structure):
@@ -92,6 +97,11 @@ def lib() -> ctypes.CDLL:
         L.moe_attn_decode_timed.argtypes = [ap, P, P, P, P, ctypes.c_float, P, P, sz, ctypes.POINTER(P), P]
         for f in ("moe_attn_workspace_bytes", "moe_attn_decode", "moe_attn_decode_timed"):
             getattr(L, f).restype = i32
+        gp = ctypes.POINTER(GdnShape)
+        L.moe_gdn_scan.argtypes = [gp, P, P, P, P, P, P, P, P, P, P, P]
+        L.moe_gdn_scan_timed.argtypes = [gp, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(P), P]
+        L.moe_gdn_scan.restype = i32
+        L.moe_gdn_scan_timed.restype = i32
         for f in ("moe_workspace_bytes", "moe_max_tiles", "moe_route_blocks", "moe_route", "moe_forward",
                   "moe_forward_timed",
                   "moe_status_read", "moe_test_route_stall", "moe_test_decode_stall"):
@@ -280,3 +290,25 @@ def attn_decode_timed(shape, q, k_cache, v_cache, lens, o, workspace, events, sc
     _check(lib().moe_attn_decode_timed(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), s,
                                        _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(), ev,
                                        _stream(stream)), "moe_attn_decode_timed")
+
+
+# ------------------------------------------------------- Gated DeltaNet ---
+
+def gdn_shape(B, T, Hqk, Hv, Dk=128, Dv=128) -> GdnShape:
+    return GdnShape(B, T, Hqk, Hv, Dk, Dv)
+
+
+def gdn_scan(shape, q, k, v, gate, beta, offsets, state_in, state_out, o, status=None, stream=None):
+    """moe_gdn_scan: q, k bf16 [T, Hqk, Dk]; v bf16 [T, Hv, Dv]; gate, beta
+    fp32 [T, Hv]; offsets int32 [B+1]; states fp32 [B, Hv, Dv, Dk] (state_out
+    may be state_in); o fp32 [T, Hv, Dv]; status an optional int32 device word."""
+    _check(lib().moe_gdn_scan(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta),
+                              _ptr(offsets), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(status),
+                              _stream(stream)), "moe_gdn_scan")
+
+
+def gdn_scan_timed(shape, q, k, v, gate, beta, offsets, state_in, state_out, o, events, status=None, stream=None):
+    ev = (P * 2)(*events)
+    _check(lib().moe_gdn_scan_timed(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(beta),
+                                    _ptr(offsets), _ptr(state_in), _ptr(state_out), _ptr(o), _ptr(status), ev,
+                                    _stream(stream)), "moe_gdn_scan_timed")

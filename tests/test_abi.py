@@ -148,3 +148,34 @@ def test_attention_host_side_errors_before_any_cuda_call(moelib):
     for bad in (0.0, -1.0, float("inf"), float("nan")):
         assert call(ctypes.byref(sh), q, k, v, lens, bad, o, ws, need, None) == 1
     assert L.moe_attn_decode_timed(ctypes.byref(sh), q, k, v, lens, 0.0625, o, ws, need, None, None) == 1
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((1, 1, 16, 32, 128, 128), 0), ((0, 1, 16, 32, 128, 128), 2), ((1, -1, 16, 32, 128, 128), 2),
+    ((1, 1, 16, 24, 128, 128), 2), ((1, 1, 32, 16, 128, 128), 2), ((1, 1, 16, 32, 64, 128), 2),
+    ((1, 1, 16, 32, 128, 64), 2), ((65536, 1, 1, 1, 128, 128), 2)])
+def test_gdn_shape_checks(moelib, shape, code):
+    """Shapes are checked on the host before any CUDA call (the fake device
+    addresses are never dereferenced)."""
+    sh = moelib.gdn_shape(*shape)
+    p = 0x100000
+    # offsets = NULL: a supported shape gets as far as the pointer checks (1),
+    # an unsupported one stops at the shape check (2); nothing is launched
+    got = moelib.lib().moe_gdn_scan(ctypes.byref(sh), p, p, p, p, p, None, p, p, p, None, None)
+    assert got == (code if code else 1)
+
+
+def test_gdn_host_side_errors_before_any_cuda_call(moelib):
+    L = moelib.lib()
+    sh = moelib.gdn_shape(2, 8, 16, 32)
+    a = [0x100000 * (i + 1) for i in range(9)]   # q k v gate beta offsets state_in state_out o
+    for i in range(9):
+        bad = list(a)
+        bad[i] = None
+        assert L.moe_gdn_scan(ctypes.byref(sh), *bad, None, None) == 1, i
+    for i, off in [(0, 8), (1, 4), (6, 4), (7, 8), (2, 2), (2, 8), (3, 2), (8, 2)]:
+        bad = list(a)
+        bad[i] += off
+        assert L.moe_gdn_scan(ctypes.byref(sh), *bad, None, None) == 1, (i, off)
+    ev = (ctypes.c_void_p * 2)(0x700000, None)
+    assert L.moe_gdn_scan_timed(ctypes.byref(sh), *a, None, ev, None) == 1
