@@ -62,7 +62,7 @@ PROFILED_TRAFFIC = {
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
         bytes=67168512 + 133120, profile="profiles/attn_block_kernel_attn-decode-32k.md",
-        sources={"attention.cu": "459908e5df635aef1646986b3d646fc1f74e811dbf8dffaeca363c987c0fc8f7",
+        sources={"attention.cu": "e8f852b2fde9ed15c26282ea26849de4a6a9042311d50698380afbe9442fe08b",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("gdn_scan_kernel", "gdn-prefill-4096"): dict(

@@ -68,7 +68,7 @@ struct Smem {
   // maxima and sums of the lane's two heads; stored [value][lane].
   static constexpr int kStateFloats = D / 4 + 4;
   static constexpr int kStateBytes = kStateFloats * 32 * 4;
-  static constexpr int kMergeBytes = 3 * kStateBytes;     // warps 2, 3 (round 1) and warp 1 (round 2)
+  static constexpr int kMergeBytes = 3 * kStateBytes;     // warps 2, 3 (first fold) and warp 1 (second fold)
   static constexpr int kCtlOffset = kStages * kStageBytes + kMergeBytes;
   static constexpr int kBytes = kCtlOffset + 128 + 1024;  // + alignment slack
 };
@@ -76,10 +76,10 @@ struct Smem {
 struct Ctl {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t mrg_full;   // round 1: warps 2 and 3 have stored their states
-  uint64_t mrg_free;   // round 1: warps 0 and 1 have read them
-  uint64_t mrg2_full;  // round 2: warp 1 has stored its state
-  uint64_t mrg2_free;  // round 2: warp 0 has read it
+  uint64_t mrg_full;   // first fold: warps 2 and 3 have stored their states
+  uint64_t mrg_free;   // first fold: warps 0 and 1 have read them
+  uint64_t mrg2_full;  // second fold: warp 1 has stored its state
+  uint64_t mrg2_free;  // second fold: warp 0 has read it
   int abort;
 };
 
@@ -435,8 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mA = nA;
           mB = nB;
         };
-        float* st1 = mrg + (warp & 1) * S::kStateFloats * 32;  // round 1 slot of warp 2 / warp 3
-        float* st2 = mrg + 2 * S::kStateFloats * 32;           // round 2 slot
+        float* st1 = mrg + (warp & 1) * S::kStateFloats * 32;  // first-fold slot of warp 2 / warp 3
+        float* st2 = mrg + 2 * S::kStateFloats * 32;           // second-fold slot
         bool fail = false;
         if (warp >= 2) {
           fail = flushes > 0 && !warp_wait(&ctl->mrg_free, (flushes - 1) & 1);
