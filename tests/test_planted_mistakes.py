@@ -125,7 +125,8 @@ MUTANTS = [
 ]
 
 
-def _attention_variant(label, mapping="div", scale_mode="rsqrt", len_shift=0, normalise=True, v_head=None):
+def _attention_variant(label, mapping="div", scale_mode="rsqrt", len_shift=0, normalise=True, v_head=None,
+                       shift=True):
     """A copy of the decode-attention oracle with one plausible mistake."""
     def attn(q_bits, k_bits, v_bits, lens, scale=None):
         q, K, V = (M.bf16_bits_to_f64(t) for t in (q_bits, k_bits, v_bits))
@@ -141,9 +142,11 @@ def _attention_variant(label, mapping="div", scale_mode="rsqrt", len_shift=0, no
                 g = h // r if mapping == "div" else h % Hkv
                 gv = g if v_head is None else v_head(h, Hkv)
                 lg = s * (K[b, g, :n] @ q[b, h])
-                w = np.exp(lg - lg.max())
+                with np.errstate(over="ignore", invalid="ignore"):
+                    w = np.exp(lg - lg.max()) if shift else np.exp(lg)
                 if normalise:
-                    w /= w.sum()
+                    with np.errstate(invalid="ignore"):
+                        w /= w.sum()
                 o[b, h] = w @ V[b, gv, :n]
         return o
     attn.__name__ = label
@@ -158,6 +161,7 @@ ATTN_MUTANTS = [
     _attention_variant("one_position_past_length", len_shift=1),
     _attention_variant("weights_not_normalised", normalise=False),
     _attention_variant("values_from_other_kv_head", v_head=lambda h, Hkv: (h + 1) % Hkv),
+    _attention_variant("softmax_without_max_shift", shift=False),
 ]
 
 
