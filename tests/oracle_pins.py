@@ -680,4 +680,47 @@ def pin_gdn_split_and_packing():
     assert np.array_equal(Sp[1], S03[1])
 
 
+def _gdn_chunkwise(q, k, v, gate, beta, S0, chunk):
+    """The same recurrence by the paper's chunkwise form, one value head with
+    its key head: within a chunk with cumulative decay g_i = prod_{j<=i} alpha_j
+    the state is S_i = g_i S_0 + sum_{l<=i} (g_i / g_l) u_l k^_l^T, where the
+    pseudo-values u solve the unit lower-triangular system
+        u_j + beta_j sum_{l<j} (g_j / g_l) (k^_l . k^_j) u_l = beta_j (v_j - g_j S_0 k^_j),
+    and o_i = S_i q^_i. A different algebra from the token loop (a triangular
+    solve and matrix products), written from the formula, not from the oracle."""
+    import scipy.linalg
+    T, Dk = k.shape
+    kh = k / np.sqrt((k * k).sum(axis=1, keepdims=True) + 1e-6)
+    qh = q / np.sqrt((q * q).sum(axis=1, keepdims=True) + 1e-6) / math.sqrt(Dk)
+    S = S0.copy()
+    o = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(T, c0 + chunk))
+        K, Q, V = kh[sl], qh[sl], v[sl]
+        g = np.exp(np.cumsum(gate[sl]))
+        ratio = g[:, None] / g[None, :]
+        n = K.shape[0]
+        low = np.tril(np.ones((n, n)), -1)
+        A = np.eye(n) + beta[sl][:, None] * ratio * (K @ K.T) * low
+        rhs = beta[sl][:, None] * (V - g[:, None] * (K @ S.T))
+        U = scipy.linalg.solve_triangular(A, rhs, lower=True, unit_diagonal=True)
+        incl = np.tril(np.ones((n, n)))
+        o[sl] = g[:, None] * (Q @ S.T) + ((ratio * incl) * (Q @ K.T)) @ U
+        S = g[-1] * S + (U * (g[-1] / g)[:, None]).T @ K
+    return o, S
+
+
+def pin_gdn_chunkwise_form_agrees():
+    """The token-by-token oracle equals the chunkwise (triangular-solve) form
+    of the gated delta rule, for chunks of 1, 4 and 7 tokens over 23 tokens."""
+    T = 23
+    q, k, v, gate, beta, S0 = _gdn_case(T, Hqk=1, Hv=1, Dk=8, Dv=6)
+    o, S = _gdn(q, k, v, gate, beta, S0, [0, T])
+    qb, kb, vb = (M.bf16_bits_to_f64(_bits(x)) for x in (q, k, v))
+    for chunk in (1, 4, 7):
+        oc, Sc = _gdn_chunkwise(qb[:, 0], kb[:, 0], vb[:, 0], gate[:, 0], beta[:, 0], S0[0, 0], chunk)
+        assert np.allclose(oc, o[:, 0], rtol=1e-9, atol=1e-11), chunk
+        assert np.allclose(Sc, S[0, 0], rtol=1e-9, atol=1e-11), chunk
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
