@@ -153,7 +153,9 @@ def test_attention_host_side_errors_before_any_cuda_call(moelib):
 @pytest.mark.parametrize("shape,code", [
     ((1, 1, 16, 32, 128, 128), 0), ((0, 1, 16, 32, 128, 128), 2), ((1, -1, 16, 32, 128, 128), 2),
     ((1, 1, 16, 24, 128, 128), 2), ((1, 1, 32, 16, 128, 128), 2), ((1, 1, 16, 32, 64, 128), 2),
-    ((1, 1, 16, 32, 128, 64), 2), ((65536, 1, 1, 1, 128, 128), 2)])
+    ((1, 1, 16, 32, 128, 64), 2), ((65536, 1, 1, 1, 128, 128), 2), ((1, 1, 1, 4097, 128, 128), 2),
+    # the largest supported grid, 65535 x 4096 x 8 = 2^31 - 32768 blocks, is accepted
+    ((65535, 1, 1, 4096, 128, 128), 0)])
 def test_gdn_shape_checks(moelib, shape, code):
     """Shapes are checked on the host before any CUDA call (the fake device
     addresses are never dereferenced)."""
