@@ -40,37 +40,37 @@ import synth  # noqa: E402
 METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM roofline"
 
 # DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum +
-# dram__bytes_write.sum from one ncu capture, summarised under profiles/),
-# with the SHA-256 of the kernel's sources at capture time: the figure is
-# reported only while the sources are unchanged, null otherwise.
+# dram__bytes_write.sum from one ncu capture), with the SHA-256 of the
+# kernel's sources at capture time: the figure is reported only while the
+# sources are unchanged, null otherwise.
 CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_expert_moe_gb300", "csrc")
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
-        bytes=17068032, profile="profiles/decode_layer_kernel_decode-t1.md",
+        bytes=17068032,
         sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("fused_decode_layer", "decode-t4"): dict(
-        bytes=56009216 + 545280, profile="profiles/decode_layer_kernel_decode-t4.md",
+        bytes=56009216 + 545280,
         sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=428123904 + 27014400, profile="profiles/expert_tc_kernel_prefill-4096.md",
+        bytes=428123904 + 27014400,
         sources={"gemm_tc.cu": "b5977a6e1abc72896a48b429af781c9b95580b7b091780f707ca05b26b382596",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
-        bytes=67168512 + 133120, profile="profiles/attn_block_kernel_attn-decode-32k.md",
+        bytes=67168512 + 133120,
         sources={"attention.cu": "e8f852b2fde9ed15c26282ea26849de4a6a9042311d50698380afbe9442fe08b",
                  "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("gdn_scan_kernel", "gdn-prefill-4096"): dict(
-        bytes=70285312 + 26173696, profile="profiles/gdn_scan_kernel_gdn-prefill-4096.md",
+        bytes=70285312 + 26173696,
         sources={"gdn.cu": "3d128b3587fd6d65c176086eff0449af4c6965844316f141c7afab279f923a23",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
     ("gdn_short_kernel", "gdn-decode-b64"): dict(
-        bytes=135300352 + 82013184, profile="profiles/gdn_short_kernel_gdn-decode-b64.md",
+        bytes=135300352 + 82013184,
         sources={"gdn.cu": "3d128b3587fd6d65c176086eff0449af4c6965844316f141c7afab279f923a23",
                  "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
 }
@@ -298,16 +298,10 @@ def stage_times(W, steps):
     return [s_ / n for s_ in sums]
 
 
-def run_ours(args, spec, rank, world, local_rank):
-    import bit_grouped_expert_moe_gb300 as m
-    from bit_grouped_expert_moe_gb300 import _build
-    _build.build()
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    block_m = args.block_m or (16 if spec.T <= 64 else 64 if spec.T <= 1024 else 128)
+def measure_moe(m, spec, args, dev, rank, world, block_m, steps, with_cpu_baseline):
+    """Times one MoE workload on this rank's GPU: the device-timed step, the
+    end-to-end step through the C ABI with host buffers, the per-kernel event
+    split and the roofline of the dominant kernel. Returns the record."""
     W = Workload(m, spec, dev, block_m, rank)
     stream = torch.cuda.current_stream()
     graph = capture(W.step)
@@ -319,14 +313,16 @@ def run_ours(args, spec, rank, world, local_rank):
     work = W.work()
 
     barrier(world)
-    with ClockSampler(local_rank) as clk:
-        ms = time_region(graph.replay, args.steps, stream)
+    with ClockSampler(dev.index or 0) as clk:
+        ms = time_region(graph.replay, steps, stream)
     ms = max_over_ranks(ms, world, dev)
-    ms_step = ms / args.steps
+    ms_step = ms / steps
     clocks = clk.summary()
 
-    # per-kernel breakdown (events between the kernels of every call)
-    prof_steps = max(1, min(args.steps, 20))
+    # per-kernel breakdown (events between the kernels of every call: event
+    # nodes serialise the launches, so programmatic-dependent-launch overlap
+    # between the fused decode layers is lost in this pass)
+    prof_steps = max(1, min(steps, 20))
     st = stage_times(W, prof_steps)
     names = ["router", "routing", "expert_gate_up", "expert_down", "combine"]
     per_call_ms = dict(zip(names, st))
@@ -369,7 +365,7 @@ def run_ours(args, spec, rank, world, local_rank):
 
     e2e_steps(2)
     torch.cuda.synchronize()
-    n_e2e = max(2, args.steps // 2)
+    n_e2e = max(2, steps // 2)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(s_in)
     e2e_steps(n_e2e)
@@ -393,37 +389,52 @@ def run_ours(args, spec, rank, world, local_rank):
         value = world * tokens_step / (ms_step / 1000.0)
         e2e_value = world * tokens_step / (e2e_ms / 1000.0)
         higher = True
-    if W.fused():
-        # events[2..3] bracket the fused decode kernel (top-k, tables, gate/up, down, combine)
-        names = ["router", "routing", "fused_decode_layer", "-", "-"]
-        per_call_ms = {k: v for k, v in zip(names, st) if k != "-"}
-        dom, dom_bytes = "fused_decode_layer", work["fused_bytes_per_step"] / layers_calls
-    else:
-        dom, dom_bytes = "expert_gate_up", work["gate_up_bytes_per_step"] / layers_calls
-    gu_ms = per_call_ms[dom]
-    gu_bytes_launch = dom_bytes
-    gu_flops_launch = work["gate_up_flops_per_step"] / layers_calls
+    layer_bytes = work["bytes_per_step"] / layers_calls
+    layer_ms = ms_step / layers_calls
     # A kernel timed inside a long step takes the sustained tensor peak; the
     # fp16 operands run at the bf16 rate.
     tensor_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    tensor_bound = (not W.fused()) and gu_flops_launch / gu_bytes_launch > tensor_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if tensor_bound:
-        achieved = gu_flops_launch / (gu_ms / 1000.0) / 1e12
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
-                    "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
-                    "traffic": profiled_traffic(dom, spec.name), "peak_source": pk_src + " (sustained bf16)",
-                    "algorithmic_flops_per_launch": int(gu_flops_launch),
-                    "algorithmic_bytes_per_launch": int(gu_bytes_launch)}
-    else:
-        achieved = gu_bytes_launch / (gu_ms / 1000.0) / 1e9
+    if W.fused():
+        # A decode layer is the prelude plus the fused decode kernel, chained
+        # to the next layer by programmatic dependent launch: its time is the
+        # timed step's share per layer, and every byte of the layer moves in
+        # the fused kernel.
+        names = ["router", "routing", "fused_decode_layer", "-", "-"]
+        per_call_ms = {k: v for k, v in zip(names, st) if k != "-"}
+        dom, dom_bytes = "fused_decode_layer", work["fused_bytes_per_step"] / layers_calls
+        achieved = dom_bytes / (layer_ms / 1000.0) / 1e9
         peak = pk["hbm_gbs"]
-        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                    "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom, spec.name),
-                    "peak_source": pk_src, "algorithmic_bytes_per_launch": int(gu_bytes_launch)}
-    peak = pk["hbm_gbs"]
-    layer_bytes = work["bytes_per_step"] / layers_calls
+        roofline = {"kernel": "decode_layer_kernel + prelude (one layer of the timed step)", "bound": "hbm",
+                    "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": profiled_traffic(dom, spec.name), "peak_source": pk_src,
+                    "algorithmic_bytes_per_launch": int(dom_bytes),
+                    "time_per_launch_us": round(layer_ms * 1000.0, 3),
+                    "time_source": "ms_per_step / layers (the timed graph, launches overlapped as in the step)"}
+    else:
+        dom, dom_bytes = "expert_gate_up", work["gate_up_bytes_per_step"] / layers_calls
+        gu_ms = per_call_ms[dom]
+        gu_flops_launch = work["gate_up_flops_per_step"] / layers_calls
+        tensor_bound = gu_flops_launch / dom_bytes > tensor_peak * 1e12 / (pk["hbm_gbs"] * 1e9)
+        if tensor_bound:
+            achieved = gu_flops_launch / (gu_ms / 1000.0) / 1e12
+            roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
+                        "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4),
+                        "traffic": profiled_traffic(dom, spec.name), "peak_source": pk_src + " (sustained bf16)",
+                        "algorithmic_flops_per_launch": int(gu_flops_launch),
+                        "algorithmic_bytes_per_launch": int(dom_bytes),
+                        "time_per_launch_us": round(gu_ms * 1000.0, 3),
+                        "time_source": "CUDA events around the launch inside the graph (no overlap to lose)"}
+        else:
+            achieved = dom_bytes / (gu_ms / 1000.0) / 1e9
+            peak = pk["hbm_gbs"]
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                        "unit": "GB/s", "frac": round(achieved / peak, 4),
+                        "traffic": profiled_traffic(dom, spec.name), "peak_source": pk_src,
+                        "algorithmic_bytes_per_launch": int(dom_bytes),
+                        "time_per_launch_us": round(gu_ms * 1000.0, 3),
+                        "time_source": "CUDA events around the launch inside the graph (no overlap to lose)"}
     out = {
-        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": higher, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "accumulate": "f32", "data": "synthetic",
         "config": {"workload": spec.name, "T": spec.T, "H": spec.H, "I": spec.I, "E": spec.E, "top_k": spec.top_k,
@@ -433,21 +444,61 @@ def run_ours(args, spec, rank, world, local_rank):
                    if W.layers > 1 else "weights 455.8 MB per layer, larger than the 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},
         "roofline": roofline,
-        "layer": {"us_per_layer": round(ms_step * 1000.0 / layers_calls, 3),
+        "layer": {"us_per_layer": round(layer_ms * 1000.0, 3),
                   "algorithmic_bytes_per_layer": int(layer_bytes),
-                  "hbm_frac_per_layer": round(layer_bytes / (ms_step / 1000.0 / layers_calls) / 1e9 / peak, 4),
+                  "hbm_frac_per_layer": round(layer_bytes / (layer_ms / 1000.0) / 1e9 / pk["hbm_gbs"], 4),
                   "distinct_experts_mean": work["distinct_experts_mean"],
                   "tflops": round(work["flops_per_step"] / (ms_step / 1000.0) / 1e12, 3)},
         "kernels_us_per_call": {k: round(v * 1000.0, 3) for k, v in per_call_ms.items()},
+        "kernels_timing": "CUDA events between the kernels of every call in a second graph pass; the event nodes "
+                          "break programmatic-dependent-launch overlap, so these are diagnostics, not the step",
         "e2e": {"value": round(e2e_value, 3), "unit": unit, "h2d_bytes_per_step": x_host.numel() * 2,
                 "d2h_bytes_per_step": y_host[0].numel() * 4,
                 "pipeline": "input copy, compute and output copy on three streams with two buffer sets"},
-        "gpu_launches": W.launches_per_step() * args.steps,
+        "gpu_launches": W.launches_per_step() * steps,
         "launch": "one CUDA graph per step",
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not W.fused():
+        gu_ms = per_call_ms["expert_gate_up"]
+        gu_tflops = work["gate_up_flops_per_step"] / layers_calls / (gu_ms / 1000.0) / 1e12
+        out["gate_up"] = {"us_per_launch": round(gu_ms * 1000.0, 3), "tflops": round(gu_tflops, 1),
+                          "frac_of_sustained_bf16": round(gu_tflops / tensor_peak, 4),
+                          "frac_of_burst_bf16": round(gu_tflops / pk["bf16_tflops"], 4),
+                          "hbm_gbs": round(dom_bytes / (gu_ms / 1000.0) / 1e9, 1)}
+    if with_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(spec, args.cpu_seconds)
+    del W, graph, g_cmp, xb, yb
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+# The prefill half of the metric, measured in the same run as a decode line.
+PREFILL_COMPANION = "prefill-4096"
+
+
+def run_ours(args, spec, rank, world, local_rank):
+    import bit_grouped_expert_moe_gb300 as m
+    from bit_grouped_expert_moe_gb300 import _build
+    _build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    block_m = args.block_m or (16 if spec.T <= 64 else 64 if spec.T <= 1024 else 128)
+    cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    out = measure_moe(m, spec, args, dev, rank, world, block_m, args.steps, cpu)
+    if spec.T <= 4 and not args.no_prefill:
+        # Prefill record of the same run: tokens/s on the device and end to
+        # end, the gate/up GEMM's tensor rate and fraction of the bf16 peak.
+        ps = synth.WORKLOADS[PREFILL_COMPANION]
+        rec = measure_moe(m, ps, args, dev, rank, world, 128, max(10, min(args.steps, 50)), False)
+        out["prefill"] = {k: rec[k] for k in ("value", "unit", "ms_per_step", "steps", "e2e", "gate_up", "roofline",
+                                               "layer", "kernels_us_per_call", "clocks", "gpu_launches")}
+        out["prefill"]["workload"] = ps.name
+        out["prefill"]["block_m"] = 128
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -965,6 +1016,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count (profiling only)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode workloads: skip the prefill-4096 record measured in the same run")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

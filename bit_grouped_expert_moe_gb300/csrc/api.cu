@@ -3,13 +3,44 @@
 // enqueued on the caller's stream with no host synchronisation.
 #include <cstdio>
 #include <cstring>
-#include <mutex>
+#include <cuda.h>
 
 #include "kernels.h"
 
 namespace bgmoe {
 
 thread_local char g_detail[256] = "";
+
+namespace {
+// Driver entry points for naming the current context (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+}  // namespace
+
+cudaError_t current_device_context(int* dev, unsigned long long* ctx) {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  *ctx = 0;
+  const cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  CUcontext c = nullptr;
+  if (get_current == nullptr || get_current(&c) != CUDA_SUCCESS || c == nullptr) return cudaSuccess;
+  unsigned long long id = 0;
+  // A context's identifier is unique for the life of the process; without
+  // it the handle stands in (a handle can be reused after a reset).
+  *ctx = (get_id != nullptr && get_id(c, &id) == CUDA_SUCCESS) ? id + 1 : reinterpret_cast<uintptr_t>(c);
+  return cudaSuccess;
+}
 
 moe_status cuda_fail(cudaError_t e, const char* where) {
   snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorString(e));
@@ -181,7 +212,11 @@ moe_status enqueue_routing_only(const Geometry& g, const float* router_bias, con
 moe_status enqueue_route(const Geometry& g, const void* x, const void* w_router, const float* router_bias,
                          const void* w_shared_gate, const moe_route_out& r, const Workspace& w,
                          int stalled_block, long long timeout_ns, cudaStream_t stream) {
-  cudaError_t e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, nullptr, stream);
+  // The call's status word starts at zero in stream order, before any kernel
+  // of the call can record a failure in it.
+  cudaError_t e = cudaMemsetAsync(r.status, 0, sizeof(int32_t), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status clear");
+  e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, nullptr, stream);
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   return enqueue_routing_only(g, router_bias, r, w, stalled_block, timeout_ns, stream);
 }
@@ -371,7 +406,11 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
     return MOE_OK;
   }
 
-  // Router logits, then the routing pipeline (two launches).
+  // Router logits, then the routing pipeline (two launches). The status word
+  // is cleared in stream order first, so no kernel of the call can have
+  // recorded a failure before it is cleared.
+  e = cudaMemsetAsync(r.status, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "status clear");
   e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, tc ? w.x16 : nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -457,26 +496,21 @@ namespace bgmoe {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = sizeof(g_noalloc_scratch);
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices];
+PointerMemo g_noalloc_memo;
 
 // Device address of the scratch array on the current device, looked up once
-// per device (the host-side name of a __device__ array is not its address).
+// per device and context with that device current (the host-side name of a
+// __device__ array is a stand-in, not its address; a new context, as after
+// cudaDeviceReset, reloads the module and may move the array, so its address
+// is looked up again there).
 cudaError_t noalloc_scratch(void** out) {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  unsigned long long ctx = 0;
+  cudaError_t e = current_device_context(&dev, &ctx);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
-  return cudaSuccess;
+  return static_cast<cudaError_t>(g_noalloc_memo.get(dev, ctx, out, [](void** p) {
+    return static_cast<int>(cudaGetSymbolAddress(p, g_noalloc_scratch));
+  }));
 }
 
 size_t align256(size_t n) { return (n + 255) & ~size_t(255); }

@@ -702,8 +702,8 @@ size_t workspace_bytes(const moe_attn_shape& s) {
 template <int D>
 cudaError_t launch(const moe_attn_shape& s, const CUtensorMap& tk, const CUtensorMap& tv, const Params& prm,
                    int grid, cudaStream_t stream) {
-  static int configured = 0;
-  cudaError_t e = ensure_smem(attn_block_kernel<D>, Smem<D>::kBytes, &configured);
+  static SmemLimitMemo smem_memo;
+  cudaError_t e = ensure_smem(attn_block_kernel<D>, Smem<D>::kBytes, &smem_memo);
   if (e != cudaSuccess) return e;
   attn_block_kernel<D><<<grid, kThreads, Smem<D>::kBytes, stream>>>(tk, tv, prm);
   return cudaGetLastError();

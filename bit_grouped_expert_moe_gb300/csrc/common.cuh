@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "host_memo.h"
 #include "moe.h"
 
 namespace bgmoe {
@@ -132,17 +133,25 @@ __device__ __forceinline__ bool device_failed(const int32_t* status) {
   return *reinterpret_cast<const volatile int32_t*>(status) != 0;
 }
 
+// The current device and an identifier of its current CUDA context (0 when
+// no context is current or the driver cannot name it). Defined in api.cu.
+cudaError_t current_device_context(int* dev, unsigned long long* ctx);
+
 // Raises a kernel's dynamic shared-memory limit to `bytes` the first time a
-// launch needs it (the value is cached, so launches inside a CUDA-graph
-// capture make no attribute call once a first, uncaptured call has run). The
-// default limit is 48 KB minus the kernel's static shared memory, so even a
-// small request is raised once.
+// launch on this device and context needs it (memoised per device and
+// context, so launches inside a CUDA-graph capture make no attribute call
+// once a first, uncaptured call has run there). The default limit is 48 KB
+// minus the kernel's static shared memory, so even a small request is raised
+// once.
 template <typename Kernel>
-inline cudaError_t ensure_smem(Kernel k, size_t bytes, int* configured) {
-  if (bytes == 0 || (int)bytes <= *configured) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) *configured = (int)bytes;
-  return e;
+inline cudaError_t ensure_smem(Kernel k, size_t bytes, SmemLimitMemo* memo) {
+  int dev = 0;
+  unsigned long long ctx = 0;
+  cudaError_t e = current_device_context(&dev, &ctx);
+  if (e != cudaSuccess) return e;
+  return static_cast<cudaError_t>(memo->ensure(dev, ctx, (int)bytes, [&](int b) {
+    return static_cast<int>(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, b));
+  }));
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {

@@ -707,8 +707,8 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
   args.per_item = L.per_item;
   args.stage_bytes = (long long)L.stage_bytes;
   args.ring_offset = (long long)L.ring_offset;
-  static int configured = 0;
-  e = ensure_smem(decode_layer_kernel, L.total, &configured);
+  static SmemLimitMemo smem_memo;
+  e = ensure_smem(decode_layer_kernel, L.total, &smem_memo);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);

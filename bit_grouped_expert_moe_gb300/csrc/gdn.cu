@@ -414,8 +414,8 @@ moe_status scan(const moe_gdn_shape* shape, const void* q, const void* k, const 
   if (s.T <= 2 * s.B) {  // a token or two per sequence on average: decode
     gdn_short_kernel<<<grid, kThreads, 0, stream>>>(prm);
   } else {
-    static int configured = 0;
-    if ((e = ensure_smem(gdn_scan_kernel, sizeof(Smem), &configured)) != cudaSuccess)
+    static SmemLimitMemo smem_memo;
+    if ((e = ensure_smem(gdn_scan_kernel, sizeof(Smem), &smem_memo)) != cudaSuccess)
       return cuda_fail(e, "shared-memory limit");
     gdn_scan_kernel<<<grid, kThreads, sizeof(Smem), stream>>>(prm);
   }

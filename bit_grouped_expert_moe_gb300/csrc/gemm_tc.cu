@@ -584,8 +584,8 @@ int tc_sm_count() {
 template <bool kGateUp>
 cudaError_t launch_tc(const Geometry& g, const CUtensorMap& tm, const CUtensorMap& tms, const CUtensorMap& tmh,
                       const TcParams& p, cudaStream_t stream) {
-  static int configured = 0;
-  cudaError_t e = ensure_smem(expert_tc_kernel<kGateUp>, kSmemBytes, &configured);
+  static SmemLimitMemo smem_memo;
+  cudaError_t e = ensure_smem(expert_tc_kernel<kGateUp>, kSmemBytes, &smem_memo);
   if (e != cudaSuccess) return e;
   const int sms = tc_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;

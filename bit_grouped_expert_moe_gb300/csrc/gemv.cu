@@ -210,8 +210,8 @@ gemv_down_kernel(int H, int I, int E, int rows_per_block, const __half* __restri
 template <int kIt>
 static cudaError_t launch_gate_up_it(const Geometry& g, const uint16_t* x, const ExpertArgs& w, const TileArgs& t,
                                      __half* h, size_t smem, cudaStream_t stream) {
-  static int configured = 0;
-  cudaError_t e = ensure_smem(gemv_gate_up_kernel<kIt>, smem, &configured);
+  static SmemLimitMemo smem_memo;
+  cudaError_t e = ensure_smem(gemv_gate_up_kernel<kIt>, smem, &smem_memo);
   if (e != cudaSuccess) return e;
   dim3 grid(g.max_tiles, g.I / kGemvWarps);
   gemv_gate_up_kernel<kIt><<<grid, kGemvWarps * 32, smem, stream>>>(g.H, g.I, g.E, g.K, g.A, x, w, t, h);
@@ -234,8 +234,8 @@ cudaError_t launch_gemv_down(const Geometry& g, const __half* h, const ExpertArg
   const int R = 32 / L;
   const int rows_per_block = (kGemvWarps * R > 64) ? kGemvWarps * R : 64;
   const size_t smem = (size_t)kTokChunk * g.I * kPad / 32 * sizeof(float);
-  static int configured = 0;
-  cudaError_t e = ensure_smem(gemv_down_kernel, smem, &configured);
+  static SmemLimitMemo smem_memo;
+  cudaError_t e = ensure_smem(gemv_down_kernel, smem, &smem_memo);
   if (e != cudaSuccess) return e;
   dim3 grid(g.max_tiles, (g.H + rows_per_block - 1) / rows_per_block);
   gemv_down_kernel<<<grid, kGemvWarps * 32, smem, stream>>>(g.H, g.I, g.E, rows_per_block, h, w, t, o);

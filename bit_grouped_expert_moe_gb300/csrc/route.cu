@@ -246,8 +246,8 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t stream) {
   g.K = a.K;
   g.E = a.E;
   const size_t smem = route_smem_bytes(g);
-  static int configured = 0;
-  cudaError_t err = ensure_smem(route_kernel, smem, &configured);
+  static SmemLimitMemo smem_memo;
+  cudaError_t err = ensure_smem(route_kernel, smem, &smem_memo);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.P);

@@ -5,9 +5,10 @@
 //
 // One warp owns one weight row (expert e, or the gate row); a block covers
 // kRouterTokens tokens whose bf16 rows sit in shared memory, so each 16-byte
-// weight load feeds 8 x kRouterTokens FMAs. The block also clears the routing
-// kernel's look-back words and the call's status word (the routing kernel runs
-// after this one on the same stream).
+// weight load feeds 8 x kRouterTokens FMAs. The blocks also clear the routing
+// kernel's look-back words (the routing kernel runs after this one on the same
+// stream; the call's status word is cleared in stream order before this
+// kernel).
 #include "common.cuh"
 
 namespace bgmoe {
@@ -31,16 +32,13 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
   // anything this kernel writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // Clear the look-back words, the status word and the decode kernel's
-  // grid-barrier counter for this call.
+  // Clear the look-back words and (when given) a grid-barrier counter for
+  // this call.
   {
     const int nblocks = gridDim.x * gridDim.y;
     const int b = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = b * blockDim.x + threadIdx.x; i < n_state; i += nblocks * blockDim.x) state[i] = 0ull;
-    if (b == 0 && threadIdx.x == 0) {
-      *status = 0;
-      if (bar != nullptr) *bar = 0u;
-    }
+    if (b == 0 && threadIdx.x == 0 && bar != nullptr) *bar = 0u;
   }
 
   const int vec_per_row = H / 8;
@@ -137,8 +135,8 @@ cudaError_t launch_router_logits(const Geometry& g, const void* x, const void* w
   const int rows = g.E + (wsg ? 1 : 0);
   dim3 grid((rows + kRouterWarps - 1) / kRouterWarps, (g.T + kRouterTokens - 1) / kRouterTokens);
   const size_t smem = (size_t)kRouterTokens * g.H * sizeof(uint16_t);
-  static int configured = 0;
-  cudaError_t e = ensure_smem(router_logits_kernel, smem, &configured);
+  static SmemLimitMemo smem_memo;
+  cudaError_t e = ensure_smem(router_logits_kernel, smem, &smem_memo);
   if (e != cudaSuccess) return e;
   router_logits_kernel<<<grid, kRouterWarps * 32, smem, stream>>>(
       static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wr), static_cast<const uint16_t*>(wsg),

@@ -65,11 +65,11 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
   const int t0 = blockIdx.x * kRtTok, eb = blockIdx.y;
   const int num_k = p.H / 64;
 
-  {  // clear the look-back words and the status word of this call
+  {  // clear the look-back words of this call (the status word was cleared
+     // in stream order before this kernel)
     const int nblocks = gridDim.x * gridDim.y;
     const int b = blockIdx.y * gridDim.x + blockIdx.x;
     for (int i = b * blockDim.x + threadIdx.x; i < p.n_state; i += nblocks * blockDim.x) p.state[i] = 0ull;
-    if (b == 0 && threadIdx.x == 0) *p.status = 0;
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRtStages; ++s) {
@@ -269,8 +269,8 @@ cudaError_t launch_router_tc(const Geometry& g, const void* x, const void* wr, c
   RouterTcParams p{g.T, g.H, g.E, static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(wsg), logits, x16,
                    state, n_state, status, timeout_ns};
   const size_t smem = kRtStages * kRtStage + sizeof(RtCtl) + 1024;
-  static int configured = 0;
-  e = ensure_smem(router_tc_kernel, smem, &configured);
+  static SmemLimitMemo smem_memo;
+  e = ensure_smem(router_tc_kernel, smem, &smem_memo);
   if (e != cudaSuccess) return e;
   dim3 grid((g.T + kRtTok - 1) / kRtTok, (g.E + 127) / 128);
   router_tc_kernel<<<grid, kRtThreads, smem, stream>>>(tw, tx, p);

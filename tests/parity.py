@@ -1,10 +1,11 @@
 """Helpers for the GPU parity tests: run the library through its C ABI on
 seeded inputs, run the CPU oracle on the same inputs, compare.
 
-The bar (from the layer's acceptance criteria): routing ids identical except
-on near-tie tokens; routing tables bit-exact given identical ids; y within
-rel-L2 <= 3e-3 and max-abs <= 1e-2 * RMS(oracle y) over the compared tokens;
-tokens left out (ids differ on a near tie) at most 0.1 % of the tokens."""
+The bar (from the layer's acceptance criteria): each token's set of routed
+experts identical except on tokens whose 8th/9th router-logit gap is below
+1e-4; routing tables bit-exact given identical ids; y within rel-L2 <= 3e-3
+and max-abs <= 1e-2 * RMS(oracle y) over every other token; tokens left out
+(expert sets differ across a near tie) at most 0.1 % of the tokens."""
 from __future__ import annotations
 
 import numpy as np
@@ -79,23 +80,44 @@ def oracle_forward(spec, L, x, tokens=None):
     return oracle.moe_forward(bits16(x), bits16(L.wr), bias, wsg, spec.top_k, fn, tokens=tokens)
 
 
-def near_tie(logits, top_k):
-    """Tokens with any two of their top_k + 1 largest fp32 logits closer than
-    NEAR_TIE (the only tokens whose selection may differ by rounding)."""
-    l32 = np.sort(np.asarray(logits).astype(np.float32).astype(np.float64), axis=1)[:, ::-1]
-    k1 = min(top_k + 1, l32.shape[1])
-    return np.any(np.diff(l32[:, :k1], axis=1) > -NEAR_TIE, axis=1)
+def topk_gap(logits, top_k):
+    """l_(top_k) - l_(top_k + 1) per token on the oracle's fp64 logits (inf
+    when every expert is selected): the margin between the last expert chosen
+    and the first one left out."""
+    l = np.sort(np.asarray(logits, dtype=np.float64), axis=1)[:, ::-1]
+    if top_k >= l.shape[1]:
+        return np.full(l.shape[0], np.inf)
+    return l[:, top_k - 1] - l[:, top_k]
 
 
 def check_ids(ids_gpu, ids_ref, logits, top_k):
-    """Returns the mask of excluded tokens; asserts the rest match exactly."""
+    """Routing ids of the GPU against the oracle's, compared as sets per token
+    (an order swap inside the selection leaves y unchanged, so such tokens are
+    still compared). A token may differ only if its 8th/9th logit gap (the
+    top_k-th / (top_k+1)-th) is below NEAR_TIE; those tokens are left out of
+    the y comparison and must number at most MAX_EXCLUDED of the tokens.
+    Returns the mask of excluded tokens."""
+    ids_ref = np.asarray(ids_ref)
     ids_gpu = np.asarray(ids_gpu).reshape(ids_ref.shape)
-    mism = np.any(ids_gpu != ids_ref, axis=1)
-    near = near_tie(logits, top_k)
-    assert not np.any(mism & ~near), f"ids differ on {np.sum(mism & ~near)} tokens with a clear margin"
-    excl = mism & near
+    differ = np.any(np.sort(ids_gpu, axis=1) != np.sort(ids_ref, axis=1), axis=1)
+    near = topk_gap(logits, top_k) < NEAR_TIE
+    assert not np.any(differ & ~near), f"expert sets differ on {np.sum(differ & ~near)} tokens with a clear 8th/9th gap"
+    excl = differ & near
     assert excl.sum() <= MAX_EXCLUDED * len(excl), f"{excl.sum()} near-tie tokens of {len(excl)} differ"
     return excl
+
+
+def check_weights(ids_gpu, w_gpu, ids_ref, w_ref, keep, rtol=2e-5, atol=1e-6):
+    """Routing weights per (token, expert): each token's weights are put in
+    expert-id order on both sides before comparing, so an order swap inside
+    the selection compares like with like."""
+    ids_ref = np.asarray(ids_ref)
+    ids_gpu = np.asarray(ids_gpu).reshape(ids_ref.shape)
+    w_gpu = np.asarray(w_gpu).reshape(ids_ref.shape)
+    og, orf = np.argsort(ids_gpu, axis=1), np.argsort(ids_ref, axis=1)
+    wg = np.take_along_axis(w_gpu, og, axis=1)[keep]
+    wr = np.take_along_axis(np.asarray(w_ref), orf, axis=1)[keep]
+    assert np.allclose(wg, wr, rtol=rtol, atol=atol), float(np.max(np.abs(wg - wr)))
 
 
 def check_y(y_gpu, y_ref, excl=None):
