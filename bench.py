@@ -1,10 +1,11 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 MoE layer (one JSON line on stdout).
 
-Default workload: decode, T = 1 token through 40 MoE layers with distinct
-weights (H = 2048, I = 512, E = 256 top-8 + shared, 4-bit group-64 weights,
-18.2 GB of weights, far larger than L2), one step = one pass over the 40
-layers; the metric is microseconds per layer. --workload picks another
+Default workload: decode, T = 1 token through 40 chained MoE layers with
+distinct weights (H = 2048, I = 512, E = 256 top-8 + shared, 4-bit group-64
+weights, 18.2 GB of weights, far larger than L2; layer l+1 reads layer l's
+x + y), one step = one pass over the 40 layers; the metric is microseconds
+per layer. The same run adds a prefill-4096 record (tokens/s). --workload picks another
 shape (prefill-zipf-512, prefill-4096, long-skew-16384, decode-t4, tiny),
 or decode attention over a bf16 KV cache (attn-decode-32k, -64k, -128k,
 attn-decode-batch8: 16 query heads on 2 KV heads, D = 256, 10 layers), or
@@ -195,22 +196,34 @@ class Workload:
         self.ws = m.alloc_workspace(self.shape, device)
         self.y = torch.empty(self.layers, self.calls, self.T, spec.H, dtype=torch.float32, device=device)
         self.route = [m.alloc_route_out(self.shape, device) for _ in range(self.layers)]
+        # Decode chains its layers: layer l reads the x_next that layer l-1
+        # wrote (bf16(x + y), through moe_forward_residual), as a model's
+        # stack of layers does; x is layer 0's input.
+        self.chain = torch.empty(self.layers, self.T, spec.H, dtype=torch.bfloat16, device=device) \
+            if self.fused() else None
 
     def fused(self):
-        return self.T <= 4  # the library runs decode-sized calls as router + fused decode kernel
+        return self.T <= 4  # the library runs decode-sized calls as a prelude + the fused decode kernel
 
     def launches_per_step(self):
         return (2 if self.fused() else 5) * self.layers * self.calls
 
+    def layer_input(self, li, c):
+        return self.x[c] if (self.chain is None or li == 0) else self.chain[li - 1]
+
     def call(self, li, c, events=None):
         L = self.L[li]
         routed, shared = self.experts[li]
-        if events is None:
+        if events is None and self.chain is not None:
+            self.m.forward_residual(self.shape, self.layer_input(li, c), L.wr, L.bias, routed, shared, L.wsg,
+                                    self.y[li, c], self.chain[li], self.ws, route_out=self.route[li])
+        elif events is None:
             self.m.forward(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg, self.y[li, c], self.ws,
                            route_out=self.route[li])
         else:
-            self.m.forward_timed(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg, self.y[li, c], self.ws,
-                                 events=events, route_out=self.route[li])
+            # the event pass reads the chain as the timed step left it
+            self.m.forward_timed(self.shape, self.layer_input(li, c), L.wr, L.bias, routed, shared, L.wsg,
+                                 self.y[li, c], self.ws, events=events, route_out=self.route[li])
 
     def step(self):
         for c in range(self.calls):

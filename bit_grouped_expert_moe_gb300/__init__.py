@@ -6,7 +6,8 @@ library's CUDA kernels. There is no fallback: if the library is not built,
 importing the entry points raises.
 
 Entry points mirror the C ABI in include/moe.h (workspace_bytes, max_tiles,
-route_blocks, route, forward, status_read, status_string, test_route_stall) and
+route_blocks, route, forward, forward_residual, forward_timed, route_noalloc,
+status_read, status_string, test_route_stall, test_decode_stall) and
 include/attention.h (attn_workspace_bytes, attn_decode, attn_decode_timed) and
 include/gdn.h (gdn_scan, gdn_scan_timed).
 """
@@ -21,7 +22,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbgmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE = 0, 1, 2
-MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT = 3, 4, 5
+MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_RANGE = 3, 4, 5, 6
 PATH_AUTO, PATH_GEMV, PATH_TENSOR_CORE, PATH_FUSED_DECODE = 0, 1, 2, 3
 
 P = ctypes.c_void_p
@@ -83,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.moe_route.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P, sz, P]
         L.moe_forward.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                   ctypes.POINTER(RouteOutC), P, sz, P]
+        L.moe_forward_residual.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
+                                           P, ctypes.POINTER(RouteOutC), P, sz, P]
         L.moe_forward_timed.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                         ctypes.POINTER(RouteOutC), P, sz, ctypes.POINTER(P), i32, P]
         L.moe_route_noalloc.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P]
@@ -103,7 +106,7 @@ def lib() -> ctypes.CDLL:
         L.moe_gdn_scan.restype = i32
         L.moe_gdn_scan_timed.restype = i32
         for f in ("moe_workspace_bytes", "moe_max_tiles", "moe_route_blocks", "moe_route", "moe_forward",
-                  "moe_forward_timed",
+                  "moe_forward_timed", "moe_forward_residual",
                   "moe_status_read", "moe_test_route_stall", "moe_test_decode_stall"):
             getattr(L, f).restype = i32
         _lib = L
@@ -208,6 +211,21 @@ def forward(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, 
                              ctypes.byref(sc) if sc is not None else None, _ptr(w_shared_gate), _ptr(y),
                              ctypes.byref(r) if r is not None else None, _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)), "moe_forward")
+
+
+def forward_residual(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, x_next, workspace,
+                     route_out=None, stream=None):
+    """moe_forward_residual: forward() that also writes x_next = bf16(x + y),
+    the next layer's input (bf16 [T, H], distinct from x)."""
+    ec = _experts_c(experts)
+    sc = _experts_c(shared)
+    r = _route_c(route_out) if route_out is not None else None
+    _check(lib().moe_forward_residual(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(router_bias),
+                                      ctypes.byref(ec), ctypes.byref(sc) if sc is not None else None,
+                                      _ptr(w_shared_gate), _ptr(y), _ptr(x_next),
+                                      ctypes.byref(r) if r is not None else None, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(stream)),
+           "moe_forward_residual")
 
 
 def forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, workspace, events=None,

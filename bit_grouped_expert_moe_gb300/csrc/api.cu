@@ -108,7 +108,8 @@ struct Workspace {
   int32_t* tile_rows;
   int32_t* num_tiles;
   uint16_t* x16;              // [T][H] fp16 activations for the tensor-core path
-  unsigned int* bar;          // grid-barrier counter of the fused decode kernel
+  unsigned int* bar;          // arrival counter of the fused decode kernel
+  float* partial;             // [kMaxDecodeBlocks][T][H] block sums of the fused decode kernel (T <= 4 only)
   __half* h;                  // [rows][I]
   __half* o;                  // [rows][H]
   size_t bytes;
@@ -139,6 +140,8 @@ Workspace carve(const Geometry& g, void* base) {
   w.num_tiles = static_cast<int32_t*>(take(sizeof(int32_t)));
   w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)g.T * g.H));
   w.bar = static_cast<unsigned int*>(take(2 * sizeof(unsigned int)));
+  w.partial = static_cast<float*>(
+      take(g.T <= kDecodeMaxTokens ? sizeof(float) * (size_t)kMaxDecodeBlocks * g.T * g.H : 0));
   w.h = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.I));
   w.o = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.H));
   w.bytes = off;
@@ -254,6 +257,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_RANGE: return "a value left the fp16 operand range";
   }
   return "unknown status";
 }
@@ -311,7 +315,8 @@ namespace {
 moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,
                         const moe_experts* experts, const moe_experts* shared, const void* w_shared_gate, float* y,
                         const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* const* events,
-                        int32_t expert_path, void* stream, int32_t stall_block, int64_t timeout_ns) {
+                        int32_t expert_path, void* stream, int32_t stall_block, int64_t timeout_ns,
+                        void* x_next = nullptr) {
   moe_status st = check_shape(shape);
   if (expert_path < MOE_PATH_AUTO || expert_path > MOE_PATH_FUSED_DECODE) return MOE_ERR_INVALID_ARG;
   if (st != MOE_OK) return st;
@@ -394,8 +399,9 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
     d.tile_rows = r.tile_rows;
     d.num_tiles = r.num_tiles;
     d.status = r.status;
-    d.h = w.h;
+    d.partial = w.partial;
     d.y = y;
+    d.x_next = static_cast<uint16_t*>(x_next);
     d.bar = w.bar;
     d.timeout_ns = timeout_ns;
     d.stall_block = stall_block;
@@ -432,7 +438,8 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
   e = tc ? launch_down_tc(g, w.h, dn, t, w.o, r.status, kDefaultTimeoutNs, s) : launch_gemv_down(g, w.h, dn, t, w.o, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
   if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, s);
+  e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, static_cast<const uint16_t*>(x),
+                     static_cast<uint16_t*>(x_next), s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if ((e = mark(5)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;
@@ -456,6 +463,17 @@ moe_status moe_test_decode_stall(const moe_shape* shape, const void* x, const vo
   if (stalled_block < 0 || timeout_ns <= 0 || timeout_ns > kDefaultTimeoutNs) return MOE_ERR_INVALID_ARG;
   return forward_impl(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out, workspace,
                       ws_bytes, nullptr, MOE_PATH_FUSED_DECODE, stream, stalled_block, timeout_ns);
+}
+
+moe_status moe_forward_residual(const moe_shape* shape, const void* x, const void* w_router,
+                                const float* router_bias, const moe_experts* experts, const moe_experts* shared,
+                                const void* w_shared_gate, float* y, void* x_next, const moe_route_out* route_out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  if (!x_next) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x_next) & 15) || (reinterpret_cast<uintptr_t>(x) & 15)) return MOE_ERR_INVALID_ARG;
+  if (x_next == x) return MOE_ERR_INVALID_ARG;
+  return forward_impl(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out, workspace,
+                      ws_bytes, nullptr, MOE_PATH_AUTO, stream, -1, kDefaultTimeoutNs, x_next);
 }
 
 moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,

@@ -1,6 +1,7 @@
 // Device helpers shared by the kernels of the MoE layer (sm_103a).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -43,20 +44,19 @@ __device__ __forceinline__ float order_key_to_float(uint32_t k) {
   return __uint_as_float(u);
 }
 
-// Top-k of one token by one warp over lrow[0..E) (+ bias), with ties to the
-// lower expert index, and the renormalised softmax weight of each pick:
-// lane k < K returns pick k in *e_out and its weight in *w_out; every lane
-// returns sigmoid(lrow[E]) in *gate_out when `shared`.
-// Every logit load is issued before any is used (one L2 round trip); keys
-// are fp32 order keys (0 marks an empty or taken entry: a finite logit never
-// maps to 0). Each lane keeps the best of its own entries; a round takes the
-// warp maximum and, among the lanes holding it, the lowest expert index.
-__device__ __forceinline__ void warp_topk(const float* lrow, const float* bias, int E, int K, bool shared, int lane,
-                                          int* e_out, float* w_out, float* gate_out) {
-  float lv[kMaxExperts / 32], bv[kMaxExperts / 32];
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) lv[j] = __ldcg(lrow + min(lane + 32 * j, E - 1));
-  const float gate_logit = __ldcg(lrow + (shared ? E : 0));
+// Top-k of one token by one warp, given the logits: lane l holds
+// lv[j] = logit of expert l + 32 j (entries past E ignored) and every lane the
+// shared-gate logit. Ties go to the lower expert index, and each pick gets its
+// renormalised softmax weight: lane k < K returns pick k in *e_out and its
+// weight in *w_out; every lane returns sigmoid(gate_logit) in *gate_out when
+// `shared`. Keys are fp32 order keys (0 marks an empty or taken entry: a
+// finite logit never maps to 0). Each lane keeps the best of its own entries;
+// a round takes the warp maximum and, among the lanes holding it, the lowest
+// expert index.
+__device__ __forceinline__ void warp_topk_select(const float (&lv)[kMaxExperts / 32], float gate_logit,
+                                                 const float* bias, int E, int K, bool shared, int lane,
+                                                 int* e_out, float* w_out, float* gate_out) {
+  float bv[kMaxExperts / 32];
 #pragma unroll
   for (int j = 0; j < kMaxExperts / 32; ++j) bv[j] = bias ? __ldg(bias + min(lane + 32 * j, E - 1)) : 0.f;
   uint32_t key[kMaxExperts / 32];
@@ -102,6 +102,17 @@ __device__ __forceinline__ void warp_topk(const float* lrow, const float* bias, 
   *e_out = my_e;
   *w_out = z / sum;
   *gate_out = shared ? 1.f / (1.f + expf(-gate_logit)) : 0.f;
+}
+
+// warp_topk_select over lrow[0..E) (+ bias) read from global memory: every
+// logit load is issued before any is used (one L2 round trip).
+__device__ __forceinline__ void warp_topk(const float* lrow, const float* bias, int E, int K, bool shared, int lane,
+                                          int* e_out, float* w_out, float* gate_out) {
+  float lv[kMaxExperts / 32];
+#pragma unroll
+  for (int j = 0; j < kMaxExperts / 32; ++j) lv[j] = __ldcg(lrow + min(lane + 32 * j, E - 1));
+  const float gate_logit = __ldcg(lrow + (shared ? E : 0));
+  warp_topk_select(lv, gate_logit, bias, E, K, shared, lane, e_out, w_out, gate_out);
 }
 
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const unsigned long long* p) {

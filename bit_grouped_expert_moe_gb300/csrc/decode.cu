@@ -1,91 +1,90 @@
-// Fused decode MoE layer (T <= 4 tokens): top-k, routing tables, gate/up with
-// fused dequantisation and SiLU, down projection and the weighted combine in
-// one kernel that follows the router kernel.
+// Fused decode MoE layer (T <= 4 tokens): router, top-k, routing tables,
+// gate/up with fused dequantisation and SiLU, down projection and the
+// weighted combine in one kernel, after a one-block prelude.
 // [droneth.or.th Lily article, "Decode is bound by bandwidth more than
 // compute": at batch 1 weights are barely reused, so the bound is the bytes
 // moved; dothoosh.com "Perplexity Lily: 1.35x faster decode for Qwen3.6 on
 // Apple silicon", "Decode optimisations", kernel fusion: chains of kernels
 // fused so intermediates stay on chip.]
 //
-// Weights stream through a ring of shared-memory stages filled by bulk async
-// copies (cp.async.bulk, completion counted on an mbarrier), so a block keeps
-// up to `stages` tiles in flight whatever the compute between them does. One
-// ring item is either
-//   a gate/up item: expert slot s, h columns n0..n0+15 -> gate rows
-//     n0..n0+15 and up rows I+n0..I+n0+15 with their scales and biases
-//     (18H bytes; two MMA units of 8 columns), or
-//   a down item: rows m0..m0+15 of W_down for up to `per_item` slots.
-// The products run on mma.sync.m16n8k16 (fp16 operands, fp32 accumulation):
-// 16 weight rows x 8 token columns per instruction. In a gate/up unit the 16
-// MMA rows are 8 gate rows then the matching 8 up rows, so the lane that
-// holds gate(n, j) also holds up(n, j). Each lane dequantises whole code words into
-// A fragments; one word unpacks as the pairs (k0,k4), (k1,k5), (k2,k6),
-// (k3,k7), so the activations are kept in that K order inside every group of
-// 8 (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte shared-memory load.
+// Work split. An item is (expert slot s, 32 h columns n0..n0+31). The block
+// that computes those h columns also computes their share of the down
+// projection, W_down[:, n0..n0+31] h[n0..n0+31] for every output row, so h
+// never leaves the block; each warp keeps its output rows' sums in registers
+// across the block's items, and the blocks' sums meet once, at the end, in a
+// fixed-order reduction. Slot 0 is the shared expert (every token; it needs
+// no routing), slots 1.. the distinct routed experts in increasing index;
+// item i goes to block i mod G, so blocks 0..I/32-1 start with a shared item.
 //
-// One block per SM, every block resident: 16 consumer warps and one producer
-// warp whose lane 0 issues the bulk copies (kept out of the consumer warps: a
-// lane issuing while its warp-mates wait on an mbarrier is held up by them).
-// A one-block prelude kernel clears the two grid-barrier counters and the
-// status word. Both kernels use programmatic dependent launch: the prelude
-// starts while the previous layer's kernel finishes (after that kernel's
-// barrier B) and waits for it before clearing; this kernel starts at once,
-// loads weights, and waits for the prelude before it reads x. Phases:
-//   0  the router's first weight loads and, in a block whose first item
-//      belongs to the shared expert (which every token uses), that item's
-//      copies go out; after the wait x is staged (fp16 in the permuted K
-//      order for the experts, bf16 for the router);
-//   R  router logits: block b, warp w computes rows b + G*w, G*16 apart, and
-//      writes l[t][r] to global memory; grid barrier A;
-//   1  every block selects the top-k experts of the T tokens itself (reading
-//      the logits through L2) and derives the expert slots; from here the
-//      producer fills the ring as the consumers release stages (one "empty"
-//      mbarrier per stage);
-//   2  gate/up items: the 16 warps split K, the partial sums of each 8-column
-//      unit are added in a fixed order by one warp while the others go on,
-//      and h = w * silu(gate) * up (the token's routing weight, or the shared
-//      gate, folded in) goes to global memory as fp16;
-//   3  grid barrier B;
-//   4  block b owns output rows 16b..16b+15: with the weights folded into h,
-//      y[t][m] = sum over slots of W_down[m] . h_slot,t, so every warp keeps one
-//      accumulator over its (slot, K block) tasks and the 16 accumulators are
-//      added in a fixed order at the end. The last block writes the routing
-//      tables.
-// Reading, right after a programmatic-dependent-launch wait, values another
-// kernel wrote just before it finished proved slow (about 2.8 us for the
-// logits row on GB300, against 1.5 us for a DRAM miss of unrelated data),
-// which is why the router runs inside this kernel.
+// Phases of one block:
+//   0  (before the programmatic-dependent-launch wait: weights only) the
+//      warps load their router rows into registers; a block whose first item
+//      is a shared one issues that item's weight copies;
+//   R  x is staged (fp16 in the permuted K order for the MMAs, bf16 for the
+//      router); the router rows b + G*w give logits, stored straight to
+//      global memory; a block with a shared item computes the shared gate;
+//   1  blocks with routed items poll the T logit rows until no entry holds
+//      the sentinel the prelude wrote (no grid barrier: the wait is on the
+//      data itself), select the top-k and build the slot table;
+//   2  items: gate/up (the 16 warps split K), one block barrier, four warps
+//      add the partial sums in a fixed order and form h = w silu(gate) up in
+//      shared memory (the routing weight, or the shared gate, folded in),
+//      another barrier, then every warp adds its W_down rows times h into its
+//      register sums;
+//   3  every block stores its sums and arrives on one counter; blocks owning
+//      16 output rows wait for every arrival and add the blocks' sums in
+//      block order: y (fp32), and x_next = bf16(x + y) when asked for.
+//
+// Weights reach shared memory by cp.async, each warp loading exactly the
+// bytes it will use into a two-slot ring of its own (an item's gate/up part
+// and its down part), so copies of the next part overlap the current part's
+// arithmetic and no warp waits on another warp's copies.
+//
+// Products on mma.sync.m16n8k16 (fp16 operands, fp32 accumulation): 16
+// weight rows x 8 token columns per instruction. Gate/up: the 16 MMA rows are
+// 8 gate rows then the matching 8 up rows, so the lane holding gate(n, t)
+// also holds up(n, t). Each lane dequantises whole code words into A
+// fragments; one word unpacks as the pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7),
+// so x and h are kept in that K order inside every group of 8
+// (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte shared-memory load.
+#include <atomic>
+
 #include "kernels.h"
 #include "tc_ptx.cuh"
 
 namespace bgmoe {
 
-constexpr int kDecWarps = 16;                        // consumer warps
-constexpr int kDecConsumers = kDecWarps * 32;
-constexpr int kDecThreads = kDecConsumers + 32;      // + the producer warp
+constexpr int kDecWarps = 16;
+constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecMaxA = kDecodeMaxTokens * kMaxTopK;
 constexpr int kDecMaxSlots = kDecMaxA + 1;
+constexpr int kItemCols = 32;                   // h columns per item
+constexpr int kUnits = kItemCols / 8;           // MMA units of 8 h columns (8 gate + 8 up rows)
+constexpr int kGuTaskBytes = 16 * 64 + 16 * 8;  // 16 code rows x 128 K, and their scale and bias pairs
+constexpr int kDnTileBytes = 16 * 16 + 16 * 8;  // 16 W_down rows x 32 K, and their scale and bias pairs
+constexpr int kMaxDnTiles = 8;                  // W_down tiles of 16 rows per warp (H <= 2048)
+constexpr int kDecMaxH = kDecWarps * 16 * kMaxDnTiles;
+constexpr int kGateWarp = kDecWarps - 1;        // computes the shared gate in blocks with a shared item
+// The prelude fills the logits with this pattern; fp32 arithmetic never
+// produces it (a NaN result is 0x7FFFFFFF), so a reader that sees any other
+// value sees the router's output.
+constexpr uint32_t kLogitSentinel = 0xFFFFFFFFu;
 
 struct DecodeSmall {
   int ids[kDecMaxA];
   float w[kDecMaxA];
-  float g[kDecodeMaxTokens];
-  int pos[kDecMaxA];                             // expert-sorted position of assignment a
-  int slot_e[kDecMaxSlots];                      // expert of each slot (slot 0 = shared when present)
-  int slot_n[kDecMaxSlots];                      // rows (tokens) of the slot
+  float g[kDecodeMaxTokens];                   // shared gate per token
+  int pos[kDecMaxA];                           // expert-sorted position of assignment a
+  int slot_e[kDecMaxSlots];                    // expert of each slot (slot 0 = shared when present)
+  int slot_n[kDecMaxSlots];                    // rows (tokens) of the slot
   int slot_row[kDecMaxSlots][kDecodeMaxTokens];
-  int slot_tok[kDecMaxSlots][kDecodeMaxTokens];
-  float slot_w[kDecMaxSlots][kDecodeMaxTokens];  // routing weight (shared slot: gate) of each slot row
-  int tok_row[kDecMaxSlots][kDecodeMaxTokens];   // h row of (slot, token), -1 if the token skips it
-  const uint8_t* slot_src[kDecMaxSlots][6];     // gate/up codes, scales, biases; down codes, scales, biases
+  float slot_wt[kDecMaxSlots][kDecodeMaxTokens];  // weight of token t in the slot (0: not routed there)
+  const uint8_t* slot_src[kDecMaxSlots][6];    // gate/up codes, scales, biases; down codes, scales, biases
   int nslots;
-  int failed;    // consumer abort flag (a stage or grid-barrier wait ran out)
-  int pfail;     // producer abort flag (kept apart: consumers branch on `failed` only)
-  uint64_t full[kDecodeMaxStages];               // stage filled (bulk-copy bytes landed)
-  uint64_t empty[kDecodeMaxStages];              // stage released by all consumer warps
-  float part[2][2][kDecWarps][4][32];            // per-warp MMA partials: [item parity][sub-unit][warp][reg][lane]
+  int failed;        // a logit poll or the final wait ran out
+  int range;         // an fp16 operand (x or h) left the fp16 range
+  unsigned nb;       // blocks holding down-projection sums
 };
-
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -95,37 +94,27 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Bulk async copy global -> this CTA's shared memory, completion counted in
-// bytes on `bar` (both addresses and the size multiples of 16 bytes).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   tc::smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Waits for the mbarrier phase with the given parity, sleeping between polls
-// (up to 256 ns) so that waiting warps leave the issue slots to the warps
-// doing work. Returns false once *abort is set or the deadline passes (then
-// it sets *abort).
-__device__ __forceinline__ bool ring_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint64_t deadline) {
-  unsigned ns = 32;
-  while (!tc::mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if (global_timer_ns() > deadline) {
-      *abort = 1;
-      return false;
-    }
-    __nanosleep(ns);
-    ns = ns < 256 ? 2 * ns : 256;
-  }
-  return true;
+__device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-// Arrival on a grid barrier: release orders the block's earlier writes (made
+// Arrival on a counter: release orders the block's earlier writes (made
 // visible to this thread by the preceding block barrier) before the add.
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
 }
 
 // d += A * B with A 16x16 (row), B 16x8 (col), fp16 in, fp32 accumulate.
@@ -161,125 +150,144 @@ __device__ __forceinline__ void mma_chunk(float (&d)[4], const uint4& r0, const 
   }
 }
 
-__device__ __forceinline__ void load_b(uint4 (&xb)[4], const __half* row, bool live) {
+// x[t] . row for the router: lane l holds bf16 elements 8 (l + 32 q) .. +7 of
+// the row in w4[q]; the activations are bf16 in shared memory; fp32 sums in
+// lane order, then a butterfly over the warp (every lane gets the result).
+__device__ __forceinline__ float row_dot(const uint4 (&w4)[8], const uint16_t* xrow, int rvec, int lane) {
+  float acc = 0.f;
 #pragma unroll
-  for (int w = 0; w < 4; ++w)
-    xb[w] = live ? *reinterpret_cast<const uint4*>(row + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+  for (int q = 0; q < 8; ++q) {
+    const int v = lane + 32 * q;
+    if (v < rvec) {
+      const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
+      const uint4 x4 = *reinterpret_cast<const uint4*>(xrow + (size_t)v * 8);
+      const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        acc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), bf16_bits_to_f32(xv[m] & 0xFFFFu), acc);
+        acc = fmaf(bf16_bits_to_f32(ww[m] >> 16), bf16_bits_to_f32(xv[m] >> 16), acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
 }
 
-
-// Named barrier of the 16 consumer warps (the producer warp never joins it).
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kDecConsumers) : "memory");
+__device__ __forceinline__ void load_row(uint4 (&w4)[8], const uint16_t* row, int rvec, int lane) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (lane + 32 * q < rvec) w4[q] = ldg_nc_v4(row + (size_t)(lane + 32 * q) * 8);
 }
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t dsm_raw[];
   __shared__ DecodeSmall S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool producer = warp == kDecWarps;
   const int g8 = lane >> 2, c4 = lane & 3;  // fragment coordinates
   const int T = a.T, H = a.H, I = a.I, E = a.E, K = a.K;
   const int A = T * K;
+  const int sh = a.shared ? 1 : 0;
   const int G = gridDim.x, b = blockIdx.x;
   const int gpr = H / kGroup, igpr = I / kGroup;
-  const int NST = a.stages;
-  const int cpb = I / 16;            // gate/up items per slot (16 h columns each)
-  const int mblocks = H / 16;        // blocks with output rows
-  const int m0 = b * 16;
-  const int kbs = I / 128, nkb = H / 128;
-  const int per_item = a.per_item;   // down slots per ring item
-  const size_t stage_bytes = (size_t)a.stage_bytes;
-  __half* xs = reinterpret_cast<__half*>(dsm_raw);  // phases 0-2: x16 [T][H]; phase 4: h [R][I]
-  uint16_t* xraw = reinterpret_cast<uint16_t*>(xs + (size_t)T * H);  // phases 0-R: x bf16 [T][H]
-  uint8_t* ring = dsm_raw + a.ring_offset;
-  const uint64_t deadline0 = global_timer_ns() + (uint64_t)a.timeout_ns;
+  const int cpi = I / kItemCols;     // items per slot
+  const int nkb = H / 128;           // gate/up K blocks of 128
+  const int mtiles = H / 16;         // W_down tiles of 16 output rows
+  const size_t slot_bytes = (size_t)a.slot_bytes;
+  uint8_t* ring = dsm_raw + (size_t)warp * 2 * slot_bytes;          // this warp's two slots
+  __half* x16 = reinterpret_cast<__half*>(dsm_raw + a.x16_offset);   // [T][H] fp16, K-permuted
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(dsm_raw + a.xraw_offset);  // [T][H] bf16
+  float* part = reinterpret_cast<float*>(dsm_raw + a.part_offset);   // [16 warps][4][32]
+  __half* hs = reinterpret_cast<__half*>(dsm_raw + a.hs_offset);     // [8 tokens][32 columns]
+  const uint64_t deadline = global_timer_ns() + (uint64_t)a.timeout_ns;
 
-  // ---- ring producer (the producer warp): item i -> stage i % NST. Every
-  // part of an item is one bulk copy, each posted by its own lane in a single
-  // instruction; the producer shares its scheduler with busy consumer warps,
-  // so it keeps its own instruction count per item small.
-  int n2 = 0;  // gate/up items of this block (known after routing); down items follow them
-  const uint32_t gcb = 16u * (H / 2), gsb = 16u * gpr * 2;     // gate/up item: 16 code rows / scale rows
-  const uint32_t dcb = 16u * (I / 2), dsb = 16u * igpr * 2;    // down item, per slot: 16 code rows / scale rows
-  auto issue = [&](int i, int nslots) {  // called by all 32 lanes of the producer warp
-    const int st = i % NST;
-    uint8_t* dst = ring + (size_t)st * stage_bytes;
-    uint64_t* bar = &S.full[st];
-    if (nslots < 0 || i < n2) {  // gate/up item (nslots < 0: the shared item issued before routing)
-      const int u = b + i * G;
-      const int s = u / cpb, n0 = (u - s * cpb) * 16;
-      if (lane == 0) tc::mbar_arrive_expect_tx(bar, 2 * gcb + 4 * gsb);
-      __syncwarp();
-      if (lane < 6) {
-        // lane: 0 gate codes, 1 up codes, 2 gate scales, 3 up scales, 4 gate biases, 5 up biases
-        const int kind = lane >> 1, up = lane & 1;
-        const uint8_t* base = nslots >= 0 ? S.slot_src[s][kind]
-                              : reinterpret_cast<const uint8_t*>(kind == 0 ? (const void*)a.gu.s_codes
-                                                                 : kind == 1 ? (const void*)a.gu.s_scales
-                                                                             : (const void*)a.gu.s_biases);
-        const size_t row = up ? (size_t)(I + n0) : (size_t)n0;
-        const uint32_t rb = kind == 0 ? (uint32_t)(H / 2) : (uint32_t)gpr * 2;
-        const uint32_t off = kind == 0 ? up * gcb : 2 * gcb + (uint32_t)(lane - 2) * gsb;
-        bulk_g2s(dst + off, base + row * rb, kind == 0 ? gcb : gsb, bar);
-      }
-    } else {  // down item: rows m0..m0+15 of slots p0..p0+np-1
-      const int p0 = (i - n2) * per_item;
-      const int np = min(per_item, nslots - p0);
-      if (lane == 0) tc::mbar_arrive_expect_tx(bar, (uint32_t)np * (dcb + 2 * dsb));
-      __syncwarp();
-      for (int c = lane; c < 3 * np; c += 32) {  // lane: slot c / 3, part c % 3 (codes, scales, biases)
-        const int p = c / 3, kind = c - 3 * p;
-        const uint32_t rb = kind == 0 ? (uint32_t)(I / 2) : (uint32_t)igpr * 2;
-        const uint32_t off = (uint32_t)p * (dcb + 2 * dsb) + (kind == 0 ? 0u : dcb + (uint32_t)(kind - 1) * dsb);
-        bulk_g2s(dst + off, S.slot_src[p0 + p][3 + kind] + (size_t)m0 * rb, kind == 0 ? dcb : dsb, bar);
-      }
-    }
-  };
-  int issued = 0;  // items issued so far (producer warp)
-  // Waits (bounded) until the last copy of every stage has landed, so the
-  // block never exits with copies into its shared memory in flight.
-  auto drain = [&]() {
-    for (int i = issued > NST ? issued - NST : 0; i < issued; ++i) {
-      const uint64_t dl = global_timer_ns() + (uint64_t)a.timeout_ns;
-      while (!tc::mbar_try_wait(&S.full[i % NST], (uint32_t)((i / NST) & 1)))
-        if (global_timer_ns() > dl) break;
-    }
-  };
-
-  // ---- phase 0: barriers, x as fp16 in the permuted K order, the shared unit
-  if (producer) {
-    if (lane == 0) {
-      for (int st = 0; st < NST; ++st) {
-        tc::mbar_init(&S.full[st], 1);
-        tc::mbar_init(&S.empty[st], kDecWarps);
-      }
-      tc::fence_barrier_init();
-      S.failed = 0;
-      S.pfail = 0;
-    }
-    __syncwarp();
-    if (a.shared && b < cpb) {  // this block's first unit belongs to the shared expert
-      issue(0, -1);
-      issued = 1;
+  if (tid == 0) {
+    S.failed = 0;
+    S.range = 0;
+    S.nslots = sh;
+    if (sh) {
+      S.slot_e[0] = E;
+      S.slot_n[0] = T;
+      S.slot_src[0][0] = reinterpret_cast<const uint8_t*>(a.gu.s_codes);
+      S.slot_src[0][1] = reinterpret_cast<const uint8_t*>(a.gu.s_scales);
+      S.slot_src[0][2] = reinterpret_cast<const uint8_t*>(a.gu.s_biases);
+      S.slot_src[0][3] = reinterpret_cast<const uint8_t*>(a.dn.s_codes);
+      S.slot_src[0][4] = reinterpret_cast<const uint8_t*>(a.dn.s_scales);
+      S.slot_src[0][5] = reinterpret_cast<const uint8_t*>(a.dn.s_biases);
     }
   }
-  for (int i = tid; i < kDecMaxSlots * kDecodeMaxTokens; i += kDecThreads) (&S.tok_row[0][0])[i] = -1;
-  // The router warps' first weight loads go out before x is staged (they do
-  // not depend on it).
-  const int rrows = E + (a.shared ? 1 : 0), rvec = H / 8;
-  const int r0 = b + G * warp;
-  const bool router_warp = warp < kDecWarps && r0 < rrows;
-  uint4 w4[8];
-  if (router_warp) {
-    const uint16_t* wrow = r0 < E ? a.wr + (size_t)r0 * H : a.wsg;
+  for (int i = tid; i < kDecMaxSlots * kDecodeMaxTokens; i += kDecThreads) (&S.slot_wt[0][0])[i] = 0.f;
+  for (int i = tid; i < 8 * kItemCols / 2; i += kDecThreads) reinterpret_cast<uint32_t*>(hs)[i] = 0u;
+  __syncthreads();
+
+  // ---- weight copies of one part of an item into a slot of this warp's ring
+  // gate/up part: this warp's unit u = warp % 4 (h columns n0 + 8u .. +7, as
+  // gate rows and up rows) for K blocks kb = warp / 4 + 4 j.
+  auto issue_gu = [&](int item, uint8_t* dst) {
+    const int s = item / cpi, n0 = (item - s * cpi) * kItemCols;
+    const uint8_t* codes = S.slot_src[s][0];
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(S.slot_src[s][1]);
+    const uint16_t* bi = reinterpret_cast<const uint16_t*>(S.slot_src[s][2]);
+    const int u = warp & 3;
+    for (int j = 0, kb = warp >> 2; kb < nkb; ++j, kb += 4) {
+      uint8_t* td = dst + j * kGuTaskBytes;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (lane + 32 * q < rvec) w4[q] = ldg_nc_v4(wrow + (size_t)(lane + 32 * q) * 8);
+      for (int q0 = 0; q0 < 64; q0 += 32) {  // 16 rows x 4 pieces of 16 bytes
+        const int q = q0 + lane, r = q >> 2, piece = q & 3;
+        const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
+        cp_async16(td + r * 64 + piece * 16, codes + (size_t)row * (H / 2) + kb * 64 + piece * 16);
+      }
+      {  // scale and bias pairs of groups 2kb, 2kb+1 of the 16 rows
+        const int r = lane >> 1, kind = lane & 1;
+        const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
+        cp_async4(td + 1024 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)row * gpr + 2 * kb);
+      }
+    }
+  };
+  // down part: W_down rows of this warp's tiles (16 tile + r, tile = warp +
+  // 16 i), columns n0..n0+31 (16 bytes of codes per row, one scale group).
+  auto issue_dn = [&](int item, uint8_t* dst) {
+    const int s = item / cpi, c = item - s * cpi;
+    const uint8_t* codes = S.slot_src[s][3];
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(S.slot_src[s][4]);
+    const uint16_t* bi = reinterpret_cast<const uint16_t*>(S.slot_src[s][5]);
+    const int gp = (c >> 1) & ~1;  // the aligned pair of groups holding this item's group
+#pragma unroll
+    for (int q0 = 0; q0 < 16 * kMaxDnTiles; q0 += 32) {
+      const int q = q0 + lane, i = q >> 4, r = q & 15, tile = warp + 16 * i;
+      if (tile < mtiles) cp_async16(dst + i * kDnTileBytes + r * 16, codes + (size_t)(16 * tile + r) * (I / 2) + c * 16);
+    }
+#pragma unroll
+    for (int q0 = 0; q0 < 32 * kMaxDnTiles; q0 += 32) {
+      const int q = q0 + lane, i = q >> 5, r = (q & 31) >> 1, kind = q & 1, tile = warp + 16 * i;
+      if (tile < mtiles)
+        cp_async4(dst + i * kDnTileBytes + 256 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)(16 * tile + r) * igpr + gp);
+    }
+  };
+  int issued = 0;  // parts issued by this warp: part 2j = gate/up of item j, 2j+1 = its down part
+  auto issue_part = [&](int p) {
+    const int item = b + G * (p >> 1);
+    if (p & 1) issue_dn(item, ring + slot_bytes);
+    else issue_gu(item, ring);
+    tc::cp_async_commit();
+  };
+
+  // ---- phase 0: weights only (they do not depend on the previous kernel)
+  const bool shared_first = sh && b < cpi;
+  if (shared_first) {
+    issue_part(0);
+    issue_part(1);
+    issued = 2;
   }
-  // Everything above reads only weights. x (and this call's workspace) may be
-  // the previous kernel's output: wait for the prelude, which itself waits
-  // for the previous layer's kernels to finish.
+  const int rrows = E + sh, rvec = H / 8;
+  const int rrow = b + G * warp;
+  const bool router_warp = rrow < rrows && warp != kGateWarp;
+  uint4 w4[8];
+  if (router_warp) load_row(w4, rrow < E ? a.wr + (size_t)rrow * H : a.wsg, rvec, lane);
+  if (shared_first && warp == kGateWarp) load_row(w4, a.wsg, rvec, lane);
+
+  // x (and this call's workspace) may be the previous kernel's output: wait
+  // for the prelude, which itself waits for the previous layer's kernels.
   grid_dep_wait();
   for (int i = tid; i < T * H / 8; i += kDecThreads) {
     const uint4 v = ldg_nc_v4(a.x + (size_t)i * 8);
@@ -290,6 +298,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       f[2 * q] = bf16_bits_to_f32(wv[q] & 0xFFFFu);
       f[2 * q + 1] = bf16_bits_to_f32(wv[q] >> 16);
     }
+    bool big = false;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) big |= fabsf(f[q]) >= 65520.f;  // becomes inf in fp16
+    if (big) S.range = 1;
     const __half2 p0 = __floats2half2_rn(f[0], f[4]), p1 = __floats2half2_rn(f[1], f[5]);
     const __half2 p2 = __floats2half2_rn(f[2], f[6]), p3 = __floats2half2_rn(f[3], f[7]);
     uint4 o;
@@ -297,252 +309,128 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     o.y = *reinterpret_cast<const uint32_t*>(&p1);
     o.z = *reinterpret_cast<const uint32_t*>(&p2);
     o.w = *reinterpret_cast<const uint32_t*>(&p3);
-    reinterpret_cast<uint4*>(xs)[i] = o;
-    reinterpret_cast<uint4*>(xraw)[i] = v;  // bf16 as given, for the router
+    reinterpret_cast<uint4*>(x16)[i] = o;
+    reinterpret_cast<uint4*>(xraw)[i] = v;
   }
   __syncthreads();
 
-  // ---- phase R: router logits l[t][r] = x[t] . W_r[r] (r = E: the shared
-  // expert's gate row), fp32, rows r = b + G * warp (+ G * 16 ...)
-  for (int r = r0; router_warp && r < rrows; r += G * kDecWarps) {
-    const uint16_t* wrow = r < E ? a.wr + (size_t)r * H : a.wsg;
-    float acc[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-    for (int v0 = lane; v0 < rvec; v0 += 32 * 8) {
-      if (r != r0 || v0 != lane) {  // the first batch was loaded before the x staging
-#pragma unroll
-        for (int q = 0; q < 8; ++q)  // every load of the batch before any use
-          if (v0 + 32 * q < rvec) w4[q] = ldg_nc_v4(wrow + (size_t)(v0 + 32 * q) * 8);
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int v = v0 + 32 * q;
-        if (v < rvec) {
-          const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
-#pragma unroll
-          for (int t = 0; t < kDecodeMaxTokens; ++t)
-            if (t < T) {
-              const uint4 x4 = *reinterpret_cast<const uint4*>(xraw + (size_t)t * H + (size_t)v * 8);
-              const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
-              float sacc = acc[t];
-#pragma unroll
-              for (int m = 0; m < 4; ++m) {
-                sacc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), bf16_bits_to_f32(xv[m] & 0xFFFFu), sacc);
-                sacc = fmaf(bf16_bits_to_f32(ww[m] >> 16), bf16_bits_to_f32(xv[m] >> 16), sacc);
-              }
-              acc[t] = sacc;
-            }
-        }
+  // ---- phase R: router logits l[t][r] (r = E: the shared gate row), stored
+  // for the other blocks; the shared gate itself where a shared item is here
+  if (router_warp)
+    for (int t = 0; t < T; ++t) {
+      const float l = row_dot(w4, xraw + (size_t)t * H, rvec, lane);
+      if (lane == 0) st_relaxed_f32(a.logits + (size_t)t * (E + 1) + rrow, l);
+    }
+  if (shared_first && warp == kGateWarp)
+    for (int t = 0; t < T; ++t) {
+      const float l = row_dot(w4, xraw + (size_t)t * H, rvec, lane);
+      if (lane == 0) {
+        S.g[t] = 1.f / (1.f + expf(-l));
+        S.slot_wt[0][t] = S.g[t];
       }
     }
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], o);
-      if (lane == 0 && t < T) a.logits[(size_t)t * (E + 1) + r] = acc[t];
-    }
-  }
+  // The next call's prelude may launch now: it waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- grid barrier A: every logit written (the prelude kernel cleared the
-  // counters before this grid's wait returned)
-  __syncthreads();
-  if (tid == 0) {
-    red_release_add(a.bar, 1u);
-    while (ld_acquire_u32(a.bar) < (unsigned)G) {
-      if (global_timer_ns() > deadline0) {
-        S.failed = 1;
-        atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
-        break;
-      }
-      __nanosleep(20);
-    }
-  }
-  __syncthreads();
-
-  // ---- phase 1a: top-k, renormalised weights, shared gate (warp per token)
-  if (warp < T) {
-    int e;
-    float w, g;
-    warp_topk(a.logits + (size_t)warp * (E + 1), a.bias, E, K, a.shared, lane, &e, &w, &g);
-    if (lane < K) {
-      S.ids[warp * K + lane] = e;
-      S.w[warp * K + lane] = w;
-    }
-    if (lane == 0) S.g[warp] = g;
-  }
-  __syncthreads();
-  if (S.failed) {  // grid barrier A ran out
-    if (producer && lane == 0) drain();
-    return;
-  }
-
-  // ---- phase 1b: expert-sorted positions and slots (one lane per assignment)
-  if (warp == 0) {
-    const bool live = lane < A;
-    const int e = live ? S.ids[lane] : kMaxExperts + 1;
-    const unsigned same = __match_any_sync(0xffffffffu, e) & __ballot_sync(0xffffffffu, live);
-    const int before = __popc(same & lanemask_lt());  // earlier assignments of the same expert
-    const bool first = live && before == 0;
-    int lt = 0, dlt = 0;  // assignments / distinct experts with a lower index
-    for (int q = 0; q < A; ++q) {
-      const int vq = __shfl_sync(0xffffffffu, 2 * e + (first ? 1 : 0), q);
-      const int lower = (vq >> 1) < e;
-      lt += lower;
-      dlt += lower & vq;
-    }
-    const int sh = a.shared ? 1 : 0;
-    if (live) {
-      const int slot = dlt + sh, tok = lane / K;
-      S.pos[lane] = lt + before;
-      S.slot_row[slot][before] = lt + before;
-      S.slot_tok[slot][before] = tok;
-      S.slot_w[slot][before] = S.w[lane];
-      S.tok_row[slot][tok] = lt + before;
-      if (first) {
-        S.slot_e[slot] = e;
-        S.slot_n[slot] = __popc(same);
-      }
-    }
-    const int d = __popc(__ballot_sync(0xffffffffu, first));
-    if (lane == 0) {
-      S.nslots = d + sh;
-      if (sh) {
-        S.slot_e[0] = E;
-        S.slot_n[0] = T;
-      }
-    }
-    if (sh && lane < T) {
-      S.slot_row[0][lane] = A + lane;
-      S.slot_tok[0][lane] = lane;
-      S.slot_w[0][lane] = S.g[lane];
-      S.tok_row[0][lane] = A + lane;
-    }
-    __syncwarp();
-    // weight addresses of every slot, for the producer
-    const int ns = d + sh;
-    for (int q = lane; q < ns; q += 32) {
-      const int ex = S.slot_e[q];
-      const bool shq = ex == E;
-      S.slot_src[q][0] = reinterpret_cast<const uint8_t*>(shq ? a.gu.s_codes : a.gu.codes + (size_t)ex * 2 * I * (H / 8));
-      S.slot_src[q][1] = reinterpret_cast<const uint8_t*>(shq ? a.gu.s_scales : a.gu.scales + (size_t)ex * 2 * I * gpr);
-      S.slot_src[q][2] = reinterpret_cast<const uint8_t*>(shq ? a.gu.s_biases : a.gu.biases + (size_t)ex * 2 * I * gpr);
-      S.slot_src[q][3] = reinterpret_cast<const uint8_t*>(shq ? a.dn.s_codes : a.dn.codes + (size_t)ex * H * (I / 8));
-      S.slot_src[q][4] = reinterpret_cast<const uint8_t*>(shq ? a.dn.s_scales : a.dn.scales + (size_t)ex * H * igpr);
-      S.slot_src[q][5] = reinterpret_cast<const uint8_t*>(shq ? a.dn.s_biases : a.dn.biases + (size_t)ex * H * igpr);
-    }
-  }
-  __syncthreads();  // the last block-wide barrier: from here on the producer runs on its own
-  const int nslots = S.nslots;
-  const int units = nslots * cpb;
-  n2 = units > b ? (units - b + G - 1) / G : 0;
-  const int n4 = b < mblocks ? (nslots + per_item - 1) / per_item : 0;
-  const int items = n2 + n4;
-
-  if (producer) {
-    for (int i = issued; i < items; ++i) {
-      // stage i % NST is free once every consumer warp released item i - NST
-      if (i >= NST && !ring_wait(&S.empty[i % NST], (uint32_t)((i / NST - 1) & 1), &S.pfail, deadline0))
-        break;
-      issue(i, nslots);
-      issued = i + 1;
-    }
-    if (lane == 0) drain();
-    return;
-  }
-
-  // ---- phase 2: gate/up items (consumer warps). An item is two 8-column
-  // units: unit q takes gate rows 8q..8q+7 and up rows 8q..8q+7 of the stage
-  // as its 16 MMA rows.
-  const int R = A + (a.shared ? T : 0);
-  for (int i = 0; i < n2; ++i) {
-    // On a timeout every consumer still runs every iteration (skipping the
-    // math), so all of them pass the same named barriers.
-    const int st = i % NST;
-    const uint8_t* sp = ring + (size_t)st * stage_bytes;
-    const bool ok = ring_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0);
-    const int u = b + i * G;
-    const int s = u / cpb, n0 = (u - s * cpb) * 16;
-    const int nr = S.slot_n[s];
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-    if (ok) {
-      const bool col_live = g8 < nr;
-      const __half* xrow = xs + (size_t)(col_live ? S.slot_tok[s][g8] : 0) * H;
-      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sp + 2 * gcb);  // gate sc, up sc, gate bi, up bi
-      const int q16 = gsb / 2;  // uint16 entries per run
-      for (int kb = warp; kb < nkb; kb += kDecWarps) {
-        const int koff = kb * 64 + 16 * c4;  // byte offset of this lane's 32 K inside a code row
-        const int gi = g8 * gpr + 2 * kb + (c4 >> 1), gi8 = gi + 8 * gpr;
-        uint4 xb[4];
-        load_b(xb, xrow + kb * 128 + 32 * c4, col_live);
-        const uint4 cg0 = *reinterpret_cast<const uint4*>(sp + g8 * (H / 2) + koff);
-        const uint4 cu0 = *reinterpret_cast<const uint4*>(sp + gcb + g8 * (H / 2) + koff);
-        const uint4 cg1 = *reinterpret_cast<const uint4*>(sp + (g8 + 8) * (H / 2) + koff);
-        const uint4 cu1 = *reinterpret_cast<const uint4*>(sp + gcb + (g8 + 8) * (H / 2) + koff);
-        mma_chunk(d0, cg0, cu0, bf16_h2(s16[gi]), bf16_h2(s16[2 * q16 + gi]), bf16_h2(s16[q16 + gi]),
-                  bf16_h2(s16[3 * q16 + gi]), xb);
-        mma_chunk(d1, cg1, cu1, bf16_h2(s16[gi8]), bf16_h2(s16[2 * q16 + gi8]), bf16_h2(s16[q16 + gi8]),
-                  bf16_h2(s16[3 * q16 + gi8]), xb);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&S.empty[st]);  // this warp is done with the stage
+  // ---- phase 1: top-k and slots, where this block may hold routed items.
+  // A block whose only item is its shared one skips it (every item index
+  // past its first is beyond the largest possible item count).
+  const int max_items = ((A < E ? A : E) + sh) * cpi;
+  const bool need_topk = !(shared_first && b + G >= max_items && b != G - 1);
+  if (need_topk) {
+    if (warp < T) {
+      const float* lrow = a.logits + (size_t)warp * (E + 1);
+      float lv[kMaxExperts / 32];
+      float gl = 0.f;
+      bool ok = false;
+      while (true) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      S.part[i & 1][0][warp][r][lane] = d0[r];
-      S.part[i & 1][1][warp][r][lane] = d1[r];
-    }
-    consumer_sync();
+        for (int j = 0; j < kMaxExperts / 32; ++j)
+          lv[j] = __uint_as_float(ld_relaxed_u32(lrow + min(lane + 32 * j, E - 1)));
+        gl = __uint_as_float(ld_relaxed_u32(lrow + (sh ? E : 0)));
+        bool mine = __float_as_uint(gl) != kLogitSentinel;
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if (ok && warp == (2 * i + q) % kDecWarps) {
-        // d0, d1: gate(n0+8q+g, slot rows 2c, 2c+1); d2, d3: up of the same
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = 0; w < kDecWarps; ++w)  // fixed order: the same bits on every run
-#pragma unroll
-          for (int r = 0; r < 4; ++r) v[r] += S.part[i & 1][q][w][r][lane];
-        const int pn = tc::perm8_pos(n0 + 8 * q + g8);
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const int j = 2 * c4 + jj;
-          if (j < nr)
-            a.h[(size_t)S.slot_row[s][j] * I + pn] = __float2half_rn(silu_f32(v[jj]) * v[2 + jj] * S.slot_w[s][j]);
-        }
-      }
-  }
-
-  // ---- phase 3: grid barrier (every block resident; bounded wait)
-  consumer_sync();
-  if (tid == 0) {
-    if (!S.failed) {
-      if (b != a.stall_block) red_release_add(a.bar + 1, 1u);
-      while (ld_acquire_u32(a.bar + 1) < (unsigned)G) {
-        if (global_timer_ns() > deadline0) {
-          S.failed = 1;
+        for (int j = 0; j < kMaxExperts / 32; ++j) mine &= __float_as_uint(lv[j]) != kLogitSentinel;
+        if (__all_sync(0xffffffffu, mine)) {
+          ok = true;
           break;
         }
-        __nanosleep(20);
+        if (global_timer_ns() > deadline) break;
+        __nanosleep(32);
+      }
+      if (ok) {
+        int e;
+        float w, g;
+        warp_topk_select(lv, gl, a.bias, E, K, a.shared, lane, &e, &w, &g);
+        if (lane < K) {
+          S.ids[warp * K + lane] = e;
+          S.w[warp * K + lane] = w;
+        }
+        if (lane == 0 && !shared_first) S.g[warp] = g;  // a shared-item block keeps its own (same bits)
+      } else if (lane == 0) {
+        S.failed = 1;
       }
     }
-    if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+    __syncthreads();
+    if (!S.failed && warp == 0) {
+      // expert-sorted positions and slots (one lane per assignment)
+      const bool live = lane < A;
+      const int e = live ? S.ids[lane] : kMaxExperts + 1;
+      const unsigned same = __match_any_sync(0xffffffffu, e) & __ballot_sync(0xffffffffu, live);
+      const int before = __popc(same & lanemask_lt());  // earlier assignments of the same expert
+      const bool first = live && before == 0;
+      int lt = 0, dlt = 0;  // assignments / distinct experts with a lower index
+      for (int q = 0; q < A; ++q) {
+        const int vq = __shfl_sync(0xffffffffu, 2 * e + (first ? 1 : 0), q);
+        const int lower = (vq >> 1) < e;
+        lt += lower;
+        dlt += lower & vq;
+      }
+      if (live) {
+        const int slot = dlt + sh, tok = lane / K;
+        S.pos[lane] = lt + before;
+        S.slot_row[slot][before] = lt + before;
+        S.slot_wt[slot][tok] = S.w[lane];
+        if (first) {
+          S.slot_e[slot] = e;
+          S.slot_n[slot] = __popc(same);
+        }
+      }
+      const int d = __popc(__ballot_sync(0xffffffffu, first));
+      if (lane == 0) S.nslots = d + sh;
+      if (sh && lane < T) {
+        S.slot_row[0][lane] = A + lane;
+        if (!shared_first) S.slot_wt[0][lane] = S.g[lane];
+      }
+      __syncwarp();
+      for (int q = lane + sh; q < d + sh; q += 32) {  // weight addresses of the routed slots
+        const int ex = S.slot_e[q];
+        S.slot_src[q][0] = reinterpret_cast<const uint8_t*>(a.gu.codes + (size_t)ex * 2 * I * (H / 8));
+        S.slot_src[q][1] = reinterpret_cast<const uint8_t*>(a.gu.scales + (size_t)ex * 2 * I * gpr);
+        S.slot_src[q][2] = reinterpret_cast<const uint8_t*>(a.gu.biases + (size_t)ex * 2 * I * gpr);
+        S.slot_src[q][3] = reinterpret_cast<const uint8_t*>(a.dn.codes + (size_t)ex * H * (I / 8));
+        S.slot_src[q][4] = reinterpret_cast<const uint8_t*>(a.dn.scales + (size_t)ex * H * igpr);
+        S.slot_src[q][5] = reinterpret_cast<const uint8_t*>(a.dn.biases + (size_t)ex * H * igpr);
+      }
+    }
+    __syncthreads();
+    if (S.failed && tid == 0) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
   }
-  consumer_sync();
-  // The next call's prelude may now be scheduled; it waits for this grid to
-  // finish before it clears the counters.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (S.failed) return;  // the producer drains the copies in flight
+  const int items = S.failed ? 0 : S.nslots * cpi;
+  const int nitems = b < items ? (items - b + G - 1) / G : 0;
 
   // The routing outputs (same definitions as moe_route), written by the last
-  // block: it has no output rows when H / 16 < gridDim.x, so this costs the
-  // layer nothing.
-  if (b == G - 1) {
-    for (int i = tid; i < A; i += kDecConsumers) {
+  // block, which holds no item at T = 1.
+  if (b == G - 1 && !S.failed) {
+    for (int i = tid; i < A; i += kDecThreads) {
       a.ids[i] = S.ids[i];
       a.weights[i] = S.w[i];
       a.sorted[S.pos[i]] = i;
       a.inv[i] = S.pos[i];
     }
     if (a.shared)
-      for (int t = tid; t < T; t += kDecConsumers) a.gate[t] = S.g[t];
-    for (int e = tid; e <= E + 1; e += kDecConsumers) {
+      for (int t = tid; t < T; t += kDecThreads) a.gate[t] = S.g[t];
+    for (int e = tid; e <= E + 1; e += kDecThreads) {
       int lt = 0, eq = 0;
       for (int q = 0; q < A; ++q) {
         lt += S.ids[q] < e;
@@ -552,12 +440,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       a.offsets[e] = e <= E ? lt : A + (a.shared ? T : 0);
     }
     // one tile per expert in use (counts <= T <= 4 < block_m), then the shared tile
-    const int d = nslots - (a.shared ? 1 : 0);
-    for (int s = tid; s < d; s += kDecConsumers) {
-      const int slot = s + (a.shared ? 1 : 0);
-      a.tile_expert[s] = S.slot_e[slot];
-      a.tile_row0[s] = S.slot_row[slot][0];
-      a.tile_rows[s] = S.slot_n[slot];
+    const int d = S.nslots - sh;
+    for (int s = tid; s < d; s += kDecThreads) {
+      a.tile_expert[s] = S.slot_e[s + sh];
+      a.tile_row0[s] = S.slot_row[s + sh][0];
+      a.tile_rows[s] = S.slot_n[s + sh];
     }
     if (tid == 0) {
       if (a.shared) {
@@ -565,151 +452,266 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
         a.tile_row0[d] = A;
         a.tile_rows[d] = T;
       }
-      *a.num_tiles = nslots;
+      *a.num_tiles = S.nslots;
     }
   }
-  if (n4 == 0) return;
 
-  // ---- phase 4: W_down rows m0..m0+15 of every slot against the weighted h
-  __half* hs = xs;  // [R][I] (x is no longer needed)
-  for (int i = tid; i < R * I / 8; i += kDecConsumers)
-    reinterpret_cast<uint4*>(hs)[i] = __ldcg(reinterpret_cast<const uint4*>(a.h) + i);
-  consumer_sync();
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows g, g+8 x tokens 2c, 2c+1 over this warp's tasks
-  for (int i = n2; i < items; ++i) {
-    const int st = i % NST;
-    const uint8_t* sp = ring + (size_t)st * stage_bytes;
-    if (ring_wait(&S.full[st], (uint32_t)((i / NST) & 1), &S.failed, deadline0)) {
-      const int p0 = (i - n2) * per_item;
-      const int np = min(per_item, nslots - p0);
-      for (int task = warp; task < np * kbs; task += kDecWarps) {
-        const int p = task / kbs, kb = task - p * kbs;
-        const int s = p0 + p;
-        const uint8_t* dp = sp + (size_t)p * (dcb + 2 * dsb);
-        const int koff = kb * 64 + 16 * c4;
-        const int gi = g8 * igpr + 2 * kb + (c4 >> 1), gi8 = gi + 8 * igpr;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(dp + g8 * (I / 2) + koff);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(dp + (g8 + 8) * (I / 2) + koff);
-        const uint16_t* s16 = reinterpret_cast<const uint16_t*>(dp + dcb);  // scales, then biases
-        const __half2 s0 = bf16_h2(s16[gi]), s1 = bf16_h2(s16[gi8]);
-        const __half2 b0 = bf16_h2(s16[dsb / 2 + gi]), b1 = bf16_h2(s16[dsb / 2 + gi8]);
-        const int row = g8 < T ? S.tok_row[s][g8] : -1;  // B column = token
-        uint4 xb[4];
-        load_b(xb, hs + (size_t)(row < 0 ? 0 : row) * I + kb * 128 + 32 * c4, row >= 0);
-        mma_chunk(acc, c0, c1, s0, b0, s1, b1, xb);
-      }
+  // ---- phase 2: this block's items b, b + G, ...
+  float acc[kMaxDnTiles][4];
+#pragma unroll
+  for (int i = 0; i < kMaxDnTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  while (issued < 2 && issued < 2 * nitems) issue_part(issued++);
+  const uint8_t* slot_gu = ring;
+  const uint8_t* slot_dn = ring + slot_bytes;
+  for (int j = 0; j < nitems; ++j) {
+    const int item = b + G * j;
+    const int s = item / cpi;
+    // gate/up part (ring slot 0): part 2j must have landed
+    if (issued > 2 * j + 1) tc::cp_async_wait<1>();
+    else tc::cp_async_wait<0>();
+    __syncwarp();
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int jj = 0, kb = warp >> 2; kb < nkb; ++jj, kb += 4) {
+      const uint8_t* t = slot_gu + jj * kGuTaskBytes;
+      uint4 xb[4];
+      const __half* xrow = x16 + (size_t)(g8 < T ? g8 : 0) * H + kb * 128 + 32 * c4;
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(xrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 cg = *reinterpret_cast<const uint4*>(t + g8 * 64 + c4 * 16);
+      const uint4 cu = *reinterpret_cast<const uint4*>(t + (8 + g8) * 64 + c4 * 16);
+      const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 1024);  // per row: scale pair, bias pair
+      const int gs = c4 >> 1;  // this lane's 32 K lie in group 2kb + gs
+      mma_chunk(d, cg, cu, bf16_h2(sb[g8 * 4 + gs]), bf16_h2(sb[g8 * 4 + 2 + gs]), bf16_h2(sb[(8 + g8) * 4 + gs]),
+                bf16_h2(sb[(8 + g8) * 4 + 2 + gs]), xb);
     }
     __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&S.empty[st]);
-  }
+    if (2 * j + 2 < 2 * nitems) issue_part(issued++);  // next item's gate/up part into slot 0
 #pragma unroll
-  for (int r = 0; r < 4; ++r) S.part[0][0][warp][r][lane] = acc[r];
-  consumer_sync();
-  if (S.failed) {
-    if (tid == 0) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
-    return;
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r];
+    __syncthreads();
+    if (warp < kUnits) {
+      // unit u = warp: warps u, u+4, u+8, u+12 hold its partial sums (fixed
+      // order). d0, d1: gate(column 8u + g, tokens 2c, 2c+1); d2, d3: up.
+      float v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        v[r] = ((part[(warp * 4 + r) * 32 + lane] + part[((warp + 4) * 4 + r) * 32 + lane]) +
+                part[((warp + 8) * 4 + r) * 32 + lane]) +
+               part[((warp + 12) * 4 + r) * 32 + lane];
+      const int pc = tc::perm8_pos(8 * warp + g8);
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int t = 2 * c4 + jj;
+        if (t < T) {
+          const __half hv = __float2half_rn(silu_f32(v[jj]) * v[2 + jj] * S.slot_wt[s][t]);
+          if (__hisinf(hv)) S.range = 1;
+          hs[t * kItemCols + pc] = hv;
+        }
+      }
+    }
+    __syncthreads();
+    // down part (ring slot 1): part 2j + 1 must have landed
+    if (issued > 2 * j + 2) tc::cp_async_wait<1>();
+    else tc::cp_async_wait<0>();
+    __syncwarp();
+    {
+      const uint4 hb = *reinterpret_cast<const uint4*>(hs + g8 * kItemCols + 8 * c4);  // token g (zero if >= T)
+      const int gs = ((item - s * cpi) >> 1) & 1;  // this item's group within the loaded pair
+#pragma unroll
+      for (int i = 0; i < kMaxDnTiles; ++i)
+        if (warp + 16 * i < mtiles) {
+          const uint8_t* t = slot_dn + i * kDnTileBytes;
+          const uint32_t c0 = *reinterpret_cast<const uint32_t*>(t + g8 * 16 + c4 * 4);
+          const uint32_t c1 = *reinterpret_cast<const uint32_t*>(t + (8 + g8) * 16 + c4 * 4);
+          const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 256);
+          uint32_t p0[4], p1[4];
+          tc::dequant8_f16(c0, bf16_h2(sb[g8 * 4 + gs]), bf16_h2(sb[g8 * 4 + 2 + gs]), p0);
+          tc::dequant8_f16(c1, bf16_h2(sb[(8 + g8) * 4 + gs]), bf16_h2(sb[(8 + g8) * 4 + 2 + gs]), p1);
+          mma_16816(acc[i], p0[0], p1[0], p0[1], p1[1], hb.x, hb.y);
+          mma_16816(acc[i], p0[2], p1[2], p0[3], p1[3], hb.z, hb.w);
+        }
+    }
+    __syncwarp();
+    if (2 * j + 3 < 2 * nitems) issue_part(issued++);  // next item's down part into slot 1
   }
-  for (int i = tid; i < T * 16; i += kDecConsumers) {
-    const int t = i >> 4, row = i & 15;
-    const int ln = (row & 7) * 4 + (t >> 1), r = (t & 1) + ((row >> 3) << 1);
-    float v = 0.f;
-    for (int w = 0; w < kDecWarps; ++w) v += S.part[0][0][w][r][ln];  // fixed order
-    a.y[(size_t)t * H + m0 + row] = v;
+  tc::cp_async_wait_all();  // no copy into this block's shared memory outlives it
+
+  // ---- phase 3: this block's sums, one arrival, the fixed-order reduction
+  if (nitems > 0) {
+    float* P = a.partial + (size_t)b * T * H;
+#pragma unroll
+    for (int i = 0; i < kMaxDnTiles; ++i) {
+      const int tile = warp + 16 * i;
+      if (tile < mtiles) {
+        const int m0 = 16 * tile + g8, t0 = 2 * c4;
+        if (t0 < T) {
+          P[(size_t)t0 * H + m0] = acc[i][0];
+          P[(size_t)t0 * H + m0 + 8] = acc[i][2];
+        }
+        if (t0 + 1 < T) {
+          P[(size_t)(t0 + 1) * H + m0] = acc[i][1];
+          P[(size_t)(t0 + 1) * H + m0 + 8] = acc[i][3];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    if (S.range) atomicCAS(a.status, 0, (int32_t)MOE_ERR_RANGE);
+    if (b != a.stall_block) red_release_add(a.bar, 1u + (nitems > 0 ? (1u << 16) : 0u));
+  }
+  if (b >= mtiles) return;  // no output rows here
+  if (tid == 0) {
+    unsigned v = 0;
+    while (((v = ld_acquire_u32(a.bar)) & 0xFFFFu) < (unsigned)G) {
+      if (global_timer_ns() > deadline) {
+        S.failed = 1;
+        break;
+      }
+      __nanosleep(32);
+    }
+    S.nb = v >> 16;
+    if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+  }
+  __syncthreads();
+  if (S.failed) return;
+  const int nb = (int)S.nb;
+  float* red = reinterpret_cast<float*>(dsm_raw);  // [32][T][16] (the ring is no longer in use)
+  const int ml = tid & 15, bl = tid >> 4;
+  for (int slice = b; slice < mtiles; slice += G) {
+    const int m = 16 * slice + ml;
+    float v[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int kMaxPer = (kMaxDecodeBlocks + 31) / 32;
+    float pv[kMaxPer][kDecodeMaxTokens];
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k)  // every load before any use
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxTokens; ++t)
+        pv[k][t] = (bl + 32 * k < nb && t < T) ? __ldcg(a.partial + ((size_t)(bl + 32 * k) * T + t) * H + m) : 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxPer; ++k)
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxTokens; ++t) v[t] += pv[k][t];
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxTokens; ++t)
+      if (t < T) red[(bl * T + t) * 16 + ml] = v[t];
+    __syncthreads();
+    if (tid < 16 * T) {
+      const int t = tid >> 4;
+      float y = 0.f;
+      for (int q = 0; q < 32; ++q) y += red[(q * T + t) * 16 + ml];  // fixed order
+      a.y[(size_t)t * H + m] = y;
+      if (a.x_next) {
+        const float xv = bf16_bits_to_f32(a.x[(size_t)t * H + m]);
+        a.x_next[(size_t)t * H + m] = __bfloat16_as_ushort(__float2bfloat16_rn(xv + y));
+      }
+    }
+    __syncthreads();
   }
 }
 
 namespace {
 int sm_count(int dev) {
-  static int sms[64] = {0};
-  if (dev < 0 || dev >= 64) return 0;
-  if (sms[dev] == 0 && cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms[dev] = 0;
-  return sms[dev];
+  static std::atomic<int> sms[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    sms[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
 }
 
-constexpr size_t kDecDynamicLimit = 186 * 1024;  // 227 KB per block minus the static part (about 38 KB)
+constexpr size_t kDecDynamicLimit = 220 * 1024;  // 227 KB per block minus the static part
 
-// Dynamic shared memory: x16 [T][H] and x bf16 [T][H] (phases 0-2) / h [R][I]
-// (phase 4), then
-// the ring. A stage holds one gate/up item (18H bytes: 32 code rows of H/2,
-// 32 scale rows and 32 bias rows of H/32) or W_down rows of `per_item` slots
-// (9I bytes each).
+// Dynamic shared memory: 16 warps x 2 ring slots, x16 and x bf16 [T][H],
+// the partial sums of the gate/up reduction, h of one item.
 struct DecodeLayout {
-  size_t ring_offset, stage_bytes, total;
-  int stages, per_item;
+  size_t slot_bytes, x16_offset, xraw_offset, part_offset, hs_offset, total;
 };
 
 DecodeLayout decode_layout(const Geometry& g) {
   DecodeLayout L{};
-  const int R = g.A + (g.shared ? g.T : 0);
-  const size_t xs = 2 * (size_t)g.T * g.H * 2, hs = (size_t)R * g.I * 2;  // x16 + x bf16, or h
-  L.ring_offset = ((xs > hs ? xs : hs) + 127) & ~size_t(127);
-  const int big = g.H > g.I ? g.H : g.I;
-  L.stage_bytes = 18 * (size_t)big;
-  L.per_item = 2 * big / g.I;
-  const size_t room = kDecDynamicLimit > L.ring_offset ? kDecDynamicLimit - L.ring_offset : 0;
-  const size_t fit = room / L.stage_bytes;
-  L.stages = (int)(fit < (size_t)kDecodeMaxStages ? fit : kDecodeMaxStages);
-  L.total = L.ring_offset + (size_t)L.stages * L.stage_bytes;
+  const size_t gu = (size_t)((g.H + 511) / 512) * kGuTaskBytes;
+  const size_t dn = (size_t)((g.H / 16 + kDecWarps - 1) / kDecWarps) * kDnTileBytes;
+  L.slot_bytes = ((gu > dn ? gu : dn) + 127) & ~size_t(127);
+  const size_t xb = ((size_t)g.T * g.H * 2 + 127) & ~size_t(127);
+  L.x16_offset = (size_t)kDecWarps * 2 * L.slot_bytes;
+  L.xraw_offset = L.x16_offset + xb;
+  L.part_offset = L.xraw_offset + xb;
+  L.hs_offset = L.part_offset + (size_t)kDecWarps * 4 * 32 * 4;
+  L.total = L.hs_offset + 8 * kItemCols * 2;
+  const size_t red = (size_t)32 * kDecodeMaxTokens * 16 * 4;  // the final reduction reuses the ring
+  if (L.total < red) L.total = red;
   return L;
 }
 }  // namespace
 
-// One block per SM, all resident (the grid barrier needs that); 16 output
-// rows per block; K in whole 128-wide blocks on both projections; at least
-// two ring stages.
+// One block per SM, every block resident (blocks wait for each other's
+// logits and sums); K of gate/up in whole 128-wide blocks, H at most 2048
+// (each warp keeps at most 8 tiles of output sums in registers), I in whole
+// 128-wide blocks, enough router warps for E + 1 rows.
 bool decode_supported(const Geometry& g) {
   int dev = 0;
-  if (g.T < 1 || g.T > kDecodeMaxTokens || g.H % 128 || g.I % 128 || cudaGetDevice(&dev) != cudaSuccess)
+  if (g.T < 1 || g.T > kDecodeMaxTokens || g.H % 128 || g.H > kDecMaxH || g.I % 128 ||
+      cudaGetDevice(&dev) != cudaSuccess)
     return false;
   const int sms = sm_count(dev);
-  return sms > 0 && g.H / 16 <= sms && decode_layout(g).stages >= 2;
+  if (sms <= 0 || sms > kMaxDecodeBlocks || g.E + 1 > sms * (kDecWarps - 1)) return false;
+  return decode_layout(g).total <= kDecDynamicLimit;
 }
 
-// Clears the decode kernel's two grid-barrier counters and the call's status
-// word. Launched with programmatic dependent launch, it starts while the
-// previous kernel on the stream (often the previous layer's decode kernel) is
-// finishing, lets the decode kernel start at once, and waits for the previous
-// kernel to complete before it touches the counters; the decode kernel waits
-// for this grid before it reads x or the counters.
-__global__ void decode_prelude_kernel(unsigned int* bar, int32_t* status) {
+// Fills the call's logits with the sentinel and clears the arrival counter
+// and the status word. Launched with programmatic dependent launch, it starts
+// while the previous kernel on the stream (often the previous layer's decode
+// kernel) is finishing, lets the decode kernel start at once, and waits for
+// the previous kernel to complete before it writes; the decode kernel waits
+// for this grid before it reads x, the logits or the counter.
+__global__ void decode_prelude_kernel(float* logits, int n_logits, unsigned int* bar, int32_t* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int i = threadIdx.x; i < n_logits; i += blockDim.x) reinterpret_cast<uint32_t*>(logits)[i] = kLogitSentinel;
   if (threadIdx.x == 0) {
     bar[0] = 0u;
-    bar[1] = 0u;
     *status = 0;
   }
 }
 
 cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int grid = sm_count(dev);
+  if (grid <= 0 || grid > kMaxDecodeBlocks) return cudaErrorInvalidDevice;
+  const DecodeLayout L = decode_layout(g);
+  static SmemLimitMemo smem_memo;
+  e = ensure_smem(decode_layer_kernel, L.total, &smem_memo);
+  if (e != cudaSuccess) return e;
+  // Every block must be resident at once: one block per SM must fit.
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, L.total);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   {
     cudaLaunchConfig_t pc{};
     pc.gridDim = dim3(1);
-    pc.blockDim = dim3(32);
+    pc.blockDim = dim3(256);
     pc.stream = stream;
     cudaLaunchAttribute pa[1];
     pa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pa[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    const cudaError_t pe = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.bar, args_in.status);
-    if (pe != cudaSuccess) return pe;
+    e = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.logits, g.T * (g.E + 1), args_in.bar, args_in.status);
+    if (e != cudaSuccess) return e;
   }
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const int grid = sm_count(dev);
-  if (grid <= 0) return cudaErrorInvalidDevice;
-  const DecodeLayout L = decode_layout(g);
   DecodeArgs args = args_in;
-  args.stages = L.stages;
-  args.per_item = L.per_item;
-  args.stage_bytes = (long long)L.stage_bytes;
-  args.ring_offset = (long long)L.ring_offset;
-  static SmemLimitMemo smem_memo;
-  e = ensure_smem(decode_layer_kernel, L.total, &smem_memo);
-  if (e != cudaSuccess) return e;
+  args.slot_bytes = (long long)L.slot_bytes;
+  args.x16_offset = (long long)L.x16_offset;
+  args.xraw_offset = (long long)L.xraw_offset;
+  args.part_offset = (long long)L.part_offset;
+  args.hs_offset = (long long)L.hs_offset;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);

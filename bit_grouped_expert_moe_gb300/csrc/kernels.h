@@ -81,15 +81,17 @@ cudaError_t launch_gate_up_tc(const Geometry& g, const uint16_t* x16, const Expe
 cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs& w, const TileArgs& t, __half* o,
                            int32_t* status, long long timeout_ns, cudaStream_t stream);
 
-// Fused decode layer (decode.cu): top-k, tables, gate/up, down and combine
-// after the router kernel, for T <= kDecodeMaxTokens.
+// Fused decode layer (decode.cu): router, top-k, tables, gate/up, down and
+// combine in one kernel after a one-block prelude, for T <= kDecodeMaxTokens.
+constexpr int kMaxDecodeBlocks = 160;  // largest grid (one block per SM) the workspace's sums cover
 struct DecodeArgs {
   int T, H, I, E, K, shared;
   const uint16_t* x;     // bf16 [T][H]
   const uint16_t* wr;    // bf16 [E][H] router weights
   const uint16_t* wsg;   // bf16 [H] shared-expert gate row, or null
-  float* logits;         // [T][E+1] written and read by the decode kernel
+  float* logits;         // [T][E+1], filled with a sentinel by the prelude, then written by the router rows
   const float* bias;     // [E] or null
+  float* partial;        // [kMaxDecodeBlocks][T][H] per-block sums of the down projection
   ExpertArgs gu, dn;
   int32_t* ids;
   float* weights;
@@ -103,21 +105,23 @@ struct DecodeArgs {
   int32_t* tile_rows;
   int32_t* num_tiles;
   int32_t* status;
-  __half* h;             // fp16 [A+T][I], K order permuted within groups of 8
   float* y;              // fp32 [T][H]
-  unsigned int* bar;     // two grid-barrier counters, cleared by launch_decode's prelude kernel
+  uint16_t* x_next;      // bf16 [T][H] = bf16(x + y), or null
+  unsigned int* bar;     // arrival counter, cleared by launch_decode's prelude kernel
   long long timeout_ns;
-  int stall_block;       // test only: this block never arrives at grid barrier B (-1: none)
-  // ring geometry, filled in by launch_decode
-  int stages, per_item;
-  long long stage_bytes, ring_offset;
+  int stall_block;       // test only: this block never arrives on the counter (-1: none)
+  // shared-memory layout, filled in by launch_decode
+  long long slot_bytes, x16_offset, xraw_offset, part_offset, hs_offset;
 };
 bool decode_supported(const Geometry& g);
-// Launches the prelude (clears the grid-barrier counters and the status
-// word) and then the decode kernel with programmatic dependent launch.
+// Launches the prelude (sentinel logits, cleared counter and status word) and
+// then the decode kernel with programmatic dependent launch.
 cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);
 
+// y = the weighted sum of the expert rows; x_next = bf16(x + y) when x_next is
+// not null.
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,
-                           const float* gate, const int32_t* status, float* y, cudaStream_t stream);
+                           const float* gate, const int32_t* status, float* y, const uint16_t* x,
+                           uint16_t* x_next, cudaStream_t stream);
 
 }  // namespace bgmoe

@@ -68,7 +68,9 @@ typedef enum moe_status {
   MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* shape outside the supported set below */
   MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_bytes() */
   MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
-  MOE_ERR_DEVICE_TIMEOUT = 5       /* a bounded device-side wait expired */
+  MOE_ERR_DEVICE_TIMEOUT = 5,      /* a bounded device-side wait expired */
+  MOE_ERR_RANGE = 6                /* a value left the fp16 range of the expert path's operands
+                                      (|x|, |h| or |o| >= 65520); the outputs are not valid */
 } moe_status;
 
 /* Shape of one call. Supported: T >= 0; H and I multiples of 64 with
@@ -177,6 +179,24 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_rout
                        float* y, const moe_route_out* route_out,
                        void* workspace, size_t ws_bytes, void* stream);
 
+/* moe_forward whose output also joins the residual stream, so a stack of
+ * layers can run back to back with each call's x_next as the next call's x:
+ *   x_next bf16 [T][H] = bf16_rn(x + y)     (y fp32 [T][H] as in moe_forward)
+ * The pages' decode path writes each step's result straight into the
+ * device-resident input slot of the next step [dothoosh.com "Perplexity
+ * Lily: 1.35x faster decode for Qwen3.6 on Apple silicon", "Decode
+ * optimisations", kernel-fusion item]; the residual add is a reading (the
+ * pages do not say what joins consecutive MoE layers), the one transformer
+ * layers use around their feed-forward block. x and x_next must be distinct,
+ * 16-byte aligned device buffers (else INVALID_ARG). The fused decode kernel
+ * writes x_next in the same pass as y; the other paths in the combine kernel.
+ * Other arguments and errors as moe_forward. */
+moe_status moe_forward_residual(const moe_shape* shape, const void* x, const void* w_router,
+                                const float* router_bias, const moe_experts* experts,
+                                const moe_experts* shared, const void* w_shared_gate, float* y,
+                                void* x_next, const moe_route_out* route_out, void* workspace,
+                                size_t ws_bytes, void* stream);
+
 /* Expert-GEMM implementations selectable through moe_forward_timed. */
 typedef enum moe_expert_path {
   MOE_PATH_AUTO = 0,        /* fused decode for T <= 4 when its conditions hold, tensor
@@ -187,10 +207,14 @@ typedef enum moe_expert_path {
                                UNSUPPORTED_SHAPE) */
   MOE_PATH_FUSED_DECODE = 3 /* a one-block prelude and one fused kernel for the router,
                                top-k, tables, expert products and combine; needs T <= 4,
-                               H % 128 == 0, I % 128 == 0, H / 16 <= the SM count and
-                               16-byte aligned codes, scales and biases (else
-                               UNSUPPORTED_SHAPE). Its events[1] and events[2] follow
-                               events[0] at once and events[4..5] == events[3] */
+                               H % 128 == 0, H <= 2048, I % 128 == 0, E + 1 <= 15 x the
+                               SM count, at most 160 SMs, one 512-thread block of about
+                               190 KB of shared memory resident on every SM (no other
+                               kernel may hold SMs while it runs: its blocks wait for one
+                               another, with a 1 s limit) and 16-byte aligned codes,
+                               scales and biases (else UNSUPPORTED_SHAPE). Its events[1]
+                               and events[2] follow events[0] at once and
+                               events[4..5] == events[3] */
 } moe_expert_path;
 
 /* moe_forward with a chosen expert path that also records caller-owned CUDA

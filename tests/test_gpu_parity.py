@@ -8,6 +8,10 @@ import oracle
 import synth
 from tests import parity
 from tests._util import bits16, bf16_from_f64, read_golden
+
+
+def bits16_to_f64(b):
+    return oracle.bf16_bits_to_f64(b)
 from tests.oracle_pins import check_routing_invariants
 
 pytestmark = pytest.mark.gpu
@@ -160,11 +164,50 @@ def test_fused_decode(moelib, cuda_dev, T, E, K, shared, H, I):
     _run_and_check(moelib, cuda_dev, spec, path=moelib.PATH_FUSED_DECODE)
 
 
+@pytest.mark.parametrize("T,path", [(1, "fused"), (4, "fused"), (2, "gemv"), (100, "auto")])
+def test_residual_chain_of_three_layers(moelib, cuda_dev, T, path):
+    """Three layers run back to back through moe_forward_residual, each call's
+    x_next feeding the next call, against the oracle applied three times with
+    the same residual join (x_{l+1} = bf16(x_l + y_l)): every layer's y meets
+    the bar, and x_next is exactly the bf16 rounding of x + y."""
+    if path == "gemv":  # a shape the fused kernel refuses (H > 2048): the combine kernel joins
+        spec = synth.LayerSpec("chain", T=T, H=2304, I=256, E=64, top_k=4, seed=20260041)
+    else:
+        spec = synth.LayerSpec("chain", T=T, H=2048, I=512, seed=20260041, layers=3)
+    layers = [parity.device_layer(spec, li, cuda_dev) for li in range(3)]
+    x0 = synth.activations(spec, device=cuda_dev)
+    shape = moelib.make_shape(T, spec.H, spec.I, spec.E, spec.top_k, spec.shared, 16)
+    ws = moelib.alloc_workspace(shape, cuda_dev)
+    xs = [x0] + [torch.empty_like(x0) for _ in range(3)]
+    ys = [torch.empty(T, spec.H, dtype=torch.float32, device=cuda_dev) for _ in range(3)]
+    ros = [moelib.alloc_route_out(shape, cuda_dev) for _ in range(3)]
+    for li, L in enumerate(layers):
+        routed, shared = parity.experts_arg(L)
+        moelib.forward_residual(shape, xs[li], L.wr, L.bias, routed, shared, L.wsg, ys[li], xs[li + 1], ws,
+                                route_out=ros[li])
+    torch.cuda.synchronize()
+    x_ref = bits16(x0)
+    for li, L in enumerate(layers):
+        assert moelib.status_read(ros[li]["status"]) == 0
+        y_gpu = ys[li].cpu().numpy()
+        # x_next is the kernel's own y joined to its own input, rounded once to bf16
+        want = bf16_from_f64(bits16_to_f64(bits16(xs[li])) + y_gpu.astype(np.float32).astype(np.float64))
+        assert np.array_equal(bits16(xs[li + 1]), want)
+        # the oracle's chain: its own y, its own join
+        y_ref, ids_ref, w_ref, g_ref, logits = oracle.moe_forward(x_ref, bits16(L.wr), None, bits16(L.wsg),
+                                                                  spec.top_k, parity.layer_expert_fn(L, spec.E))
+        ids_gpu = ros[li]["ids"].cpu().numpy()[: T * spec.top_k].reshape(T, spec.top_k)
+        excl = parity.check_ids(ids_gpu, ids_ref, logits, spec.top_k)
+        parity.check_y(y_gpu, y_ref, excl)
+        x_ref = bf16_from_f64(bits16_to_f64(x_ref) + y_ref.astype(np.float32).astype(np.float64))
+
+
 @pytest.mark.parametrize("H,I", [(128, 64), (320, 128), (4096, 512)])
 def test_fused_decode_shape_limits(moelib, cuda_dev, H, I):
-    """K of both projections must come in whole 128-wide blocks and the
-    output rows 16 per SM: other decode shapes are refused on the fused path
-    and served by the GEMV path under the automatic choice."""
+    """K of gate/up must come in whole 128-wide blocks, I too, and H is at
+    most 2048 (16 warps x 8 register tiles of 16 output rows): other decode
+    shapes are refused on the fused path and served by the GEMV path under
+    the automatic choice."""
     spec = synth.LayerSpec("fused-limits", T=2, H=H, I=I, E=16, top_k=2, seed=20260021)
     L = parity.device_layer(spec, 0, cuda_dev)
     x = synth.activations(spec, device=cuda_dev)
@@ -293,10 +336,11 @@ def test_device_timeout_is_reported_not_hung(moelib, cuda_dev):
 
 
 def test_fused_decode_timeout_is_reported_not_hung(moelib, cuda_dev):
-    """One block of the fused decode kernel never arrives at its second grid
-    barrier: every block gives up after a 20 ms limit, lets its own copies
-    land and returns, the call reports MOE_ERR_DEVICE_TIMEOUT, and the next
-    normal call on the same context and workspace is correct."""
+    """One block of the fused decode kernel never arrives on the counter that
+    gates the final reduction: the blocks waiting on it give up after a 20 ms
+    limit and return (every block lets its own copies land first), the call
+    reports MOE_ERR_DEVICE_TIMEOUT, and the next normal call on the same
+    context and workspace is correct."""
     spec = synth.WORKLOADS["decode-t1"]
     L = parity.device_layer(spec, 0, cuda_dev)
     x = synth.activations(spec, device=cuda_dev)
