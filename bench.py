@@ -196,9 +196,10 @@ class Workload:
         self.ws = m.alloc_workspace(self.shape, device)
         self.y = torch.empty(self.layers, self.calls, self.T, spec.H, dtype=torch.float32, device=device)
         self.route = [m.alloc_route_out(self.shape, device) for _ in range(self.layers)]
-        # Decode chains its layers: layer l reads the x_next that layer l-1
-        # wrote (bf16(x + y), through moe_forward_residual), as a model's
-        # stack of layers does; x is layer 0's input.
+        # Decode chains its layers as pre-norm blocks (moe_forward_residual):
+        # layer l reads the residual row r_l that layer l-1 wrote
+        # (r_l = bf16(r_{l-1} + y_{l-1})) and runs on RMSNorm(r_l), as a
+        # model's stack of layers does; x is layer 0's residual row.
         self.chain = torch.empty(self.layers, self.T, spec.H, dtype=torch.bfloat16, device=device) \
             if self.fused() else None
 
@@ -221,8 +222,9 @@ class Workload:
             self.m.forward(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg, self.y[li, c], self.ws,
                            route_out=self.route[li])
         else:
-            # the event pass reads the chain as the timed step left it
-            self.m.forward_timed(self.shape, self.layer_input(li, c), L.wr, L.bias, routed, shared, L.wsg,
+            # the diagnostic event pass runs every layer on the workload's own
+            # input (plain moe_forward semantics)
+            self.m.forward_timed(self.shape, self.x[c], L.wr, L.bias, routed, shared, L.wsg,
                                  self.y[li, c], self.ws, events=events, route_out=self.route[li])
 
     def step(self):
@@ -453,6 +455,8 @@ def measure_moe(m, spec, args, dev, rank, world, block_m, steps, with_cpu_baseli
         "config": {"workload": spec.name, "T": spec.T, "H": spec.H, "I": spec.I, "E": spec.E, "top_k": spec.top_k,
                    "shared_expert": spec.shared, "layers": W.layers, "tokens_per_call": W.T, "block_m": block_m,
                    "router_bias": spec.bias, "seed": spec.seed,
+                   "layer_chain": "pre-norm residual blocks: x = RMSNorm(r) (eps 1e-6, gain 1), "
+                                  "r_next = bf16(r + y) feeds the next layer" if W.fused() else "independent calls",
                    "l2": f"inputs larger than L2: {W.layers} layers x {layer_bytes / 1e6:.0f} MB touched per step"
                    if W.layers > 1 else "weights 455.8 MB per layer, larger than the 129 MB L2",
                    "parallelism": "replicas" if world > 1 else "1 GPU"},

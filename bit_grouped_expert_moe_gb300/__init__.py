@@ -84,8 +84,8 @@ def lib() -> ctypes.CDLL:
         L.moe_route.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P, sz, P]
         L.moe_forward.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                   ctypes.POINTER(RouteOutC), P, sz, P]
-        L.moe_forward_residual.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
-                                           P, ctypes.POINTER(RouteOutC), P, sz, P]
+        L.moe_forward_residual.argtypes = [sp, P, P, ctypes.c_float, P, P, ctypes.POINTER(ExpertsC),
+                                           ctypes.POINTER(ExpertsC), P, P, P, ctypes.POINTER(RouteOutC), P, sz, P]
         L.moe_forward_timed.argtypes = [sp, P, P, P, ctypes.POINTER(ExpertsC), ctypes.POINTER(ExpertsC), P, P,
                                         ctypes.POINTER(RouteOutC), P, sz, ctypes.POINTER(P), i32, P]
         L.moe_route_noalloc.argtypes = [sp, P, P, P, P, ctypes.POINTER(RouteOutC), P]
@@ -213,17 +213,19 @@ def forward(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, 
                              workspace.numel() * workspace.element_size(), _stream(stream)), "moe_forward")
 
 
-def forward_residual(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, x_next, workspace,
-                     route_out=None, stream=None):
-    """moe_forward_residual: forward() that also writes x_next = bf16(x + y),
-    the next layer's input (bf16 [T, H], distinct from x)."""
+def forward_residual(shape, r, w_router, router_bias, experts, shared, w_shared_gate, y, r_next, workspace,
+                     norm_weight=None, norm_eps=1e-6, route_out=None, stream=None):
+    """moe_forward_residual: one pre-norm MoE block. The layer runs on
+    x = RMSNorm(r) (gain norm_weight, or 1), y is its output and
+    r_next = bf16(r + y) the next layer's residual row (bf16 [T, H],
+    distinct from r). Fused decode shapes only."""
     ec = _experts_c(experts)
     sc = _experts_c(shared)
-    r = _route_c(route_out) if route_out is not None else None
-    _check(lib().moe_forward_residual(ctypes.byref(shape), _ptr(x), _ptr(w_router), _ptr(router_bias),
-                                      ctypes.byref(ec), ctypes.byref(sc) if sc is not None else None,
-                                      _ptr(w_shared_gate), _ptr(y), _ptr(x_next),
-                                      ctypes.byref(r) if r is not None else None, _ptr(workspace),
+    rc = _route_c(route_out) if route_out is not None else None
+    _check(lib().moe_forward_residual(ctypes.byref(shape), _ptr(r), _ptr(norm_weight), float(norm_eps),
+                                      _ptr(w_router), _ptr(router_bias), ctypes.byref(ec),
+                                      ctypes.byref(sc) if sc is not None else None, _ptr(w_shared_gate), _ptr(y),
+                                      _ptr(r_next), ctypes.byref(rc) if rc is not None else None, _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(stream)),
            "moe_forward_residual")
 

@@ -316,7 +316,7 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
                         const moe_experts* experts, const moe_experts* shared, const void* w_shared_gate, float* y,
                         const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* const* events,
                         int32_t expert_path, void* stream, int32_t stall_block, int64_t timeout_ns,
-                        void* x_next = nullptr) {
+                        void* x_next = nullptr, const void* norm_w = nullptr, float norm_eps = 0.f) {
   moe_status st = check_shape(shape);
   if (expert_path < MOE_PATH_AUTO || expert_path > MOE_PATH_FUSED_DECODE) return MOE_ERR_INVALID_ARG;
   if (st != MOE_OK) return st;
@@ -360,6 +360,11 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
   const bool dec_ok = decode_supported(g) && aligned;
   if (expert_path == MOE_PATH_FUSED_DECODE && !dec_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   const bool fused = expert_path == MOE_PATH_FUSED_DECODE || (expert_path == MOE_PATH_AUTO && dec_ok);
+  // The pre-norm residual join is part of the fused decode kernel only.
+  if (x_next != nullptr && !fused) {
+    snprintf(g_detail, sizeof(g_detail), "the residual entry point runs on the fused decode path only");
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  }
   const bool tc_ok = tc_path_supported(g) && aligned;
   if (expert_path == MOE_PATH_TENSOR_CORE && !tc_ok) return MOE_ERR_UNSUPPORTED_SHAPE;
   const bool tc = expert_path == MOE_PATH_TENSOR_CORE ||
@@ -379,6 +384,9 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
     d.K = g.K;
     d.shared = g.shared;
     d.x = static_cast<const uint16_t*>(x);
+    d.norm = x_next != nullptr ? 1 : 0;
+    d.norm_w = static_cast<const uint16_t*>(norm_w);
+    d.norm_eps = norm_eps;
     d.logits = w.logits;
     d.bias = router_bias;
     d.gu = ExpertArgs{experts->gate_up.codes, experts->gate_up.scales, experts->gate_up.biases,
@@ -438,8 +446,7 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
   e = tc ? launch_down_tc(g, w.h, dn, t, w.o, r.status, kDefaultTimeoutNs, s) : launch_gemv_down(g, w.h, dn, t, w.o, s);
   if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
   if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, static_cast<const uint16_t*>(x),
-                     static_cast<uint16_t*>(x_next), s);
+  e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if ((e = mark(5)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;
@@ -465,15 +472,16 @@ moe_status moe_test_decode_stall(const moe_shape* shape, const void* x, const vo
                       ws_bytes, nullptr, MOE_PATH_FUSED_DECODE, stream, stalled_block, timeout_ns);
 }
 
-moe_status moe_forward_residual(const moe_shape* shape, const void* x, const void* w_router,
-                                const float* router_bias, const moe_experts* experts, const moe_experts* shared,
-                                const void* w_shared_gate, float* y, void* x_next, const moe_route_out* route_out,
-                                void* workspace, size_t ws_bytes, void* stream) {
-  if (!x_next) return MOE_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(x_next) & 15) || (reinterpret_cast<uintptr_t>(x) & 15)) return MOE_ERR_INVALID_ARG;
-  if (x_next == x) return MOE_ERR_INVALID_ARG;
-  return forward_impl(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, route_out, workspace,
-                      ws_bytes, nullptr, MOE_PATH_AUTO, stream, -1, kDefaultTimeoutNs, x_next);
+moe_status moe_forward_residual(const moe_shape* shape, const void* r, const void* norm_weight, float norm_eps,
+                                const void* w_router, const float* router_bias, const moe_experts* experts,
+                                const moe_experts* shared, const void* w_shared_gate, float* y, void* r_next,
+                                const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* stream) {
+  if (!r || !r_next || r_next == r || !(norm_eps > 0.f)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(r) & 15) || (reinterpret_cast<uintptr_t>(r_next) & 15) ||
+      (reinterpret_cast<uintptr_t>(norm_weight) & 15))
+    return MOE_ERR_INVALID_ARG;
+  return forward_impl(shape, r, w_router, router_bias, experts, shared, w_shared_gate, y, route_out, workspace,
+                      ws_bytes, nullptr, MOE_PATH_AUTO, stream, -1, kDefaultTimeoutNs, r_next, norm_weight, norm_eps);
 }
 
 moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,

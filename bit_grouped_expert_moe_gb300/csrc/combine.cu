@@ -1,8 +1,7 @@
 // Gather + weighted combine + shared-expert add:
 //   y[t, :] = sum_{k=0..K-1} w[t, k] * o[inv[t*K + k], :] + g[t] * o[A + t, :]
 // summed in that fixed order in fp32 (no atomics, so the result is the same
-// on every run), and, when asked for, x_next[t, :] = bf16(x[t, :] + y[t, :])
-// (the layer's output joined to the residual stream, the next layer's input). [dothoosh.com "Perplexity Lily: 1.35x faster decode for
+// on every run). [dothoosh.com "Perplexity Lily: 1.35x faster decode for
 // Qwen3.6 on Apple silicon", "Model specification": each token's output mixes
 // its 8 chosen experts with the shared expert that processes every token.]
 #include "kernels.h"
@@ -14,8 +13,7 @@ constexpr int kCombineThreads = 64;
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(int H, int K, int A, int shared, const __half* __restrict__ o, const int32_t* __restrict__ inv,
                const float* __restrict__ weights, const float* __restrict__ gate,
-               const int32_t* __restrict__ status, float* __restrict__ y, const uint16_t* __restrict__ x,
-               uint16_t* __restrict__ x_next) {
+               const int32_t* __restrict__ status, float* __restrict__ y) {
   if (device_failed(status)) return;
   const int t = blockIdx.x;
   const int c = (blockIdx.y * kCombineThreads + threadIdx.x) * 8;
@@ -52,26 +50,12 @@ combine_kernel(int H, int K, int A, int shared, const __half* __restrict__ o, co
   float4* yo = reinterpret_cast<float4*>(y + (size_t)t * H + c);
   yo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
   yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  if (x_next != nullptr) {
-    const uint4 xv = *reinterpret_cast<const uint4*>(x + (size_t)t * H + c);
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-    uint32_t nw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_f32(xw[i] & 0xFFFFu) + acc[2 * i]));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(bf16_bits_to_f32(xw[i] >> 16) + acc[2 * i + 1]));
-      nw[i] = lo | (hi << 16);
-    }
-    *reinterpret_cast<uint4*>(x_next + (size_t)t * H + c) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
-  }
 }
 
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,
-                           const float* gate, const int32_t* status, float* y, const uint16_t* x,
-                           uint16_t* x_next, cudaStream_t stream) {
+                           const float* gate, const int32_t* status, float* y, cudaStream_t stream) {
   dim3 grid(g.T, (g.H / 8 + kCombineThreads - 1) / kCombineThreads);
-  combine_kernel<<<grid, kCombineThreads, 0, stream>>>(g.H, g.K, g.A, g.shared, o, inv, weights, gate, status, y, x,
-                                                       x_next);
+  combine_kernel<<<grid, kCombineThreads, 0, stream>>>(g.H, g.K, g.A, g.shared, o, inv, weights, gate, status, y);
   return cudaGetLastError();
 }
 

@@ -20,9 +20,11 @@
 //   0  (before the programmatic-dependent-launch wait: weights only) the
 //      warps load their router rows into registers; a block whose first item
 //      is a shared one issues that item's weight copies;
-//   R  x is staged (fp16 in the permuted K order for the MMAs, bf16 for the
-//      router); the router rows b + G*w give logits, stored straight to
-//      global memory; a block with a shared item computes the shared gate;
+//   R  the layer input is staged (fp32 for the router, fp16 in the permuted
+//      K order for the MMAs; with the pre-norm join it is RMSNorm of the
+//      residual row, never rounded to bf16); the router rows b + G*w give
+//      logits, stored straight to global memory; a block with a shared item
+//      computes the shared gate;
 //   1  blocks with routed items poll the T logit rows until no entry holds
 //      the sentinel the prelude wrote (no grid barrier: the wait is on the
 //      data itself), select the top-k and build the slot table;
@@ -33,7 +35,8 @@
 //      register sums;
 //   3  every block stores its sums and arrives on one counter; blocks owning
 //      16 output rows wait for every arrival and add the blocks' sums in
-//      block order: y (fp32), and x_next = bf16(x + y) when asked for.
+//      block order: y (fp32), and the next residual row bf16(r + y) when
+//      asked for.
 //
 // Weights reach shared memory by cp.async, each warp loading exactly the
 // bytes it will use into a two-slot ring of its own (an item's gate/up part
@@ -74,6 +77,7 @@ struct DecodeSmall {
   int ids[kDecMaxA];
   float w[kDecMaxA];
   float g[kDecodeMaxTokens];                   // shared gate per token
+  float inv_rms[kDecodeMaxTokens];             // 1 / rms of each token's residual row (pre-norm join)
   int pos[kDecMaxA];                           // expert-sorted position of assignment a
   int slot_e[kDecMaxSlots];                    // expert of each slot (slot 0 = shared when present)
   int slot_n[kDecMaxSlots];                    // rows (tokens) of the slot
@@ -151,21 +155,22 @@ __device__ __forceinline__ void mma_chunk(float (&d)[4], const uint4& r0, const 
 }
 
 // x[t] . row for the router: lane l holds bf16 elements 8 (l + 32 q) .. +7 of
-// the row in w4[q]; the activations are bf16 in shared memory; fp32 sums in
+// the row in w4[q]; the activations are fp32 in shared memory; fp32 sums in
 // lane order, then a butterfly over the warp (every lane gets the result).
-__device__ __forceinline__ float row_dot(const uint4 (&w4)[8], const uint16_t* xrow, int rvec, int lane) {
+__device__ __forceinline__ float row_dot(const uint4 (&w4)[8], const float* xrow, int rvec, int lane) {
   float acc = 0.f;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int v = lane + 32 * q;
     if (v < rvec) {
       const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
-      const uint4 x4 = *reinterpret_cast<const uint4*>(xrow + (size_t)v * 8);
-      const uint32_t xv[4] = {x4.x, x4.y, x4.z, x4.w};
+      const float4 xa = *reinterpret_cast<const float4*>(xrow + (size_t)v * 8);
+      const float4 xc = *reinterpret_cast<const float4*>(xrow + (size_t)v * 8 + 4);
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        acc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), bf16_bits_to_f32(xv[m] & 0xFFFFu), acc);
-        acc = fmaf(bf16_bits_to_f32(ww[m] >> 16), bf16_bits_to_f32(xv[m] >> 16), acc);
+        acc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), xv[2 * m], acc);
+        acc = fmaf(bf16_bits_to_f32(ww[m] >> 16), xv[2 * m + 1], acc);
       }
     }
   }
@@ -196,7 +201,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const size_t slot_bytes = (size_t)a.slot_bytes;
   uint8_t* ring = dsm_raw + (size_t)warp * 2 * slot_bytes;          // this warp's two slots
   __half* x16 = reinterpret_cast<__half*>(dsm_raw + a.x16_offset);   // [T][H] fp16, K-permuted
-  uint16_t* xraw = reinterpret_cast<uint16_t*>(dsm_raw + a.xraw_offset);  // [T][H] bf16
+  float* xf = reinterpret_cast<float*>(dsm_raw + a.xf_offset);      // [T][H] fp32 layer input
   float* part = reinterpret_cast<float*>(dsm_raw + a.part_offset);   // [16 warps][4][32]
   __half* hs = reinterpret_cast<__half*>(dsm_raw + a.hs_offset);     // [8 tokens][32 columns]
   const uint64_t deadline = global_timer_ns() + (uint64_t)a.timeout_ns;
@@ -289,14 +294,63 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   // x (and this call's workspace) may be the previous kernel's output: wait
   // for the prelude, which itself waits for the previous layer's kernels.
   grid_dep_wait();
-  for (int i = tid; i < T * H / 8; i += kDecThreads) {
-    const uint4 v = ldg_nc_v4(a.x + (size_t)i * 8);
-    const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-    float f[8];
+  // x as fp32 (exact from bf16); with the pre-norm join, the sum of squares
+  // of each token's residual row as well (fixed order: per thread, then the
+  // warp butterfly, then the warps in order)
+  float ss[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      f[2 * q] = bf16_bits_to_f32(wv[q] & 0xFFFFu);
-      f[2 * q + 1] = bf16_bits_to_f32(wv[q] >> 16);
+  for (int t = 0; t < kDecodeMaxTokens; ++t)
+    if (t < T)
+      for (int v = tid; v < H / 8; v += kDecThreads) {
+        const uint4 u = ldg_nc_v4(a.x + (size_t)t * H + (size_t)v * 8);
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+        float f[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          f[2 * q] = bf16_bits_to_f32(wv[q] & 0xFFFFu);
+          f[2 * q + 1] = bf16_bits_to_f32(wv[q] >> 16);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ss[t] = fmaf(f[q], f[q], ss[t]);
+        float4* dst = reinterpret_cast<float4*>(xf + (size_t)t * H + (size_t)v * 8);
+        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+      }
+  if (a.norm) {
+#pragma unroll
+    for (int t = 0; t < kDecodeMaxTokens; ++t) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+      if (lane == 0) part[warp * kDecodeMaxTokens + t] = ss[t];
+    }
+  }
+  __syncthreads();
+  if (a.norm && tid < T) {
+    float tot = 0.f;
+    for (int w = 0; w < kDecWarps; ++w) tot += part[w * kDecodeMaxTokens + tid];
+    S.inv_rms[tid] = 1.f / sqrtf(tot / (float)H + a.norm_eps);
+  }
+  __syncthreads();
+  // the layer input: x (or RMSNorm(r) = r / rms(r) * gain, kept in fp32 for
+  // the router), and its fp16 copy in the permuted K order for the MMAs
+  for (int i = tid; i < T * H / 8; i += kDecThreads) {
+    const int t = i / (H / 8);
+    float4* src = reinterpret_cast<float4*>(xf + (size_t)i * 8);
+    float f[8];
+    const float4 fa = src[0], fc = src[1];
+    f[0] = fa.x, f[1] = fa.y, f[2] = fa.z, f[3] = fa.w, f[4] = fc.x, f[5] = fc.y, f[6] = fc.z, f[7] = fc.w;
+    if (a.norm) {
+      const float s = S.inv_rms[t];
+      uint4 gw = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0 pairs
+      if (a.norm_w) gw = ldg_nc_v4(a.norm_w + (size_t)(i - t * (H / 8)) * 8);
+      const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        f[2 * q] = f[2 * q] * s * bf16_bits_to_f32(gv[q] & 0xFFFFu);
+        f[2 * q + 1] = f[2 * q + 1] * s * bf16_bits_to_f32(gv[q] >> 16);
+      }
+      src[0] = make_float4(f[0], f[1], f[2], f[3]);
+      src[1] = make_float4(f[4], f[5], f[6], f[7]);
     }
     bool big = false;
 #pragma unroll
@@ -310,7 +364,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     o.z = *reinterpret_cast<const uint32_t*>(&p2);
     o.w = *reinterpret_cast<const uint32_t*>(&p3);
     reinterpret_cast<uint4*>(x16)[i] = o;
-    reinterpret_cast<uint4*>(xraw)[i] = v;
   }
   __syncthreads();
 
@@ -318,12 +371,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   // for the other blocks; the shared gate itself where a shared item is here
   if (router_warp)
     for (int t = 0; t < T; ++t) {
-      const float l = row_dot(w4, xraw + (size_t)t * H, rvec, lane);
+      const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
       if (lane == 0) st_relaxed_f32(a.logits + (size_t)t * (E + 1) + rrow, l);
     }
   if (shared_first && warp == kGateWarp)
     for (int t = 0; t < T; ++t) {
-      const float l = row_dot(w4, xraw + (size_t)t * H, rvec, lane);
+      const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
       if (lane == 0) {
         S.g[t] = 1.f / (1.f + expf(-l));
         S.slot_wt[0][t] = S.g[t];
@@ -625,10 +678,10 @@ int sm_count(int dev) {
 
 constexpr size_t kDecDynamicLimit = 220 * 1024;  // 227 KB per block minus the static part
 
-// Dynamic shared memory: 16 warps x 2 ring slots, x16 and x bf16 [T][H],
-// the partial sums of the gate/up reduction, h of one item.
+// Dynamic shared memory: 16 warps x 2 ring slots, x16 fp16 and x fp32
+// [T][H], the partial sums of the gate/up reduction, h of one item.
 struct DecodeLayout {
-  size_t slot_bytes, x16_offset, xraw_offset, part_offset, hs_offset, total;
+  size_t slot_bytes, x16_offset, xf_offset, part_offset, hs_offset, total;
 };
 
 DecodeLayout decode_layout(const Geometry& g) {
@@ -638,8 +691,8 @@ DecodeLayout decode_layout(const Geometry& g) {
   L.slot_bytes = ((gu > dn ? gu : dn) + 127) & ~size_t(127);
   const size_t xb = ((size_t)g.T * g.H * 2 + 127) & ~size_t(127);
   L.x16_offset = (size_t)kDecWarps * 2 * L.slot_bytes;
-  L.xraw_offset = L.x16_offset + xb;
-  L.part_offset = L.xraw_offset + xb;
+  L.xf_offset = L.x16_offset + xb;
+  L.part_offset = L.xf_offset + 2 * xb;
   L.hs_offset = L.part_offset + (size_t)kDecWarps * 4 * 32 * 4;
   L.total = L.hs_offset + 8 * kItemCols * 2;
   const size_t red = (size_t)32 * kDecodeMaxTokens * 16 * 4;  // the final reduction reuses the ring
@@ -709,7 +762,7 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
   DecodeArgs args = args_in;
   args.slot_bytes = (long long)L.slot_bytes;
   args.x16_offset = (long long)L.x16_offset;
-  args.xraw_offset = (long long)L.xraw_offset;
+  args.xf_offset = (long long)L.xf_offset;
   args.part_offset = (long long)L.part_offset;
   args.hs_offset = (long long)L.hs_offset;
   cudaLaunchConfig_t cfg{};

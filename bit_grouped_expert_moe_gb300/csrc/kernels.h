@@ -86,7 +86,10 @@ cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs&
 constexpr int kMaxDecodeBlocks = 160;  // largest grid (one block per SM) the workspace's sums cover
 struct DecodeArgs {
   int T, H, I, E, K, shared;
-  const uint16_t* x;     // bf16 [T][H]
+  const uint16_t* x;     // bf16 [T][H]: the layer input, or (norm) the residual stream r
+  int norm;              // 1: the layer input is RMSNorm(r) (fp32, not rounded), r = x
+  const uint16_t* norm_w;  // bf16 [H] RMSNorm gain, or null (gain 1)
+  float norm_eps;
   const uint16_t* wr;    // bf16 [E][H] router weights
   const uint16_t* wsg;   // bf16 [H] shared-expert gate row, or null
   float* logits;         // [T][E+1], filled with a sentinel by the prelude, then written by the router rows
@@ -106,22 +109,19 @@ struct DecodeArgs {
   int32_t* num_tiles;
   int32_t* status;
   float* y;              // fp32 [T][H]
-  uint16_t* x_next;      // bf16 [T][H] = bf16(x + y), or null
+  uint16_t* x_next;      // bf16 [T][H] = bf16(r + y) (the next layer's residual stream), or null
   unsigned int* bar;     // arrival counter, cleared by launch_decode's prelude kernel
   long long timeout_ns;
   int stall_block;       // test only: this block never arrives on the counter (-1: none)
   // shared-memory layout, filled in by launch_decode
-  long long slot_bytes, x16_offset, xraw_offset, part_offset, hs_offset;
+  long long slot_bytes, x16_offset, xf_offset, part_offset, hs_offset;
 };
 bool decode_supported(const Geometry& g);
 // Launches the prelude (sentinel logits, cleared counter and status word) and
 // then the decode kernel with programmatic dependent launch.
 cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);
 
-// y = the weighted sum of the expert rows; x_next = bf16(x + y) when x_next is
-// not null.
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,
-                           const float* gate, const int32_t* status, float* y, const uint16_t* x,
-                           uint16_t* x_next, cudaStream_t stream);
+                           const float* gate, const int32_t* status, float* y, cudaStream_t stream);
 
 }  // namespace bgmoe

@@ -179,23 +179,32 @@ moe_status moe_forward(const moe_shape* shape, const void* x, const void* w_rout
                        float* y, const moe_route_out* route_out,
                        void* workspace, size_t ws_bytes, void* stream);
 
-/* moe_forward whose output also joins the residual stream, so a stack of
- * layers can run back to back with each call's x_next as the next call's x:
- *   x_next bf16 [T][H] = bf16_rn(x + y)     (y fp32 [T][H] as in moe_forward)
+/* One pre-norm MoE block, for stacks of layers run back to back: the layer's
+ * input is the RMS-normalised residual row and its output joins the
+ * residual stream, which is the next call's r:
+ *   x[t]      = r[t] / sqrt(mean_h r[t,h]^2 + norm_eps) * norm_weight   (fp32)
+ *   y         = the layer of moe_forward applied to x                   (fp32 [T][H])
+ *   r_next[t] = bf16_rn(r[t] + y[t])                                     (bf16 [T][H])
  * The pages' decode path writes each step's result straight into the
  * device-resident input slot of the next step [dothoosh.com "Perplexity
  * Lily: 1.35x faster decode for Qwen3.6 on Apple silicon", "Decode
- * optimisations", kernel-fusion item]; the residual add is a reading (the
- * pages do not say what joins consecutive MoE layers), the one transformer
- * layers use around their feed-forward block. x and x_next must be distinct,
- * 16-byte aligned device buffers (else INVALID_ARG). The fused decode kernel
- * writes x_next in the same pass as y; the other paths in the combine kernel.
- * Other arguments and errors as moe_forward. */
-moe_status moe_forward_residual(const moe_shape* shape, const void* x, const void* w_router,
-                                const float* router_bias, const moe_experts* experts,
-                                const moe_experts* shared, const void* w_shared_gate, float* y,
-                                void* x_next, const moe_route_out* route_out, void* workspace,
-                                size_t ws_bytes, void* stream);
+ * optimisations", kernel-fusion item]. What joins two MoE layers is not on
+ * the pages: the reading taken is the transformer's pre-norm residual block
+ * (without a normalisation the synthetic weights' gain makes a stack of
+ * layers overflow within three layers). x stays fp32 for the router and is
+ * rounded once to fp16 for the expert products.
+ *   r            bf16 [T][H], 16-byte aligned; r_next distinct from r, 16-byte aligned
+ *   norm_weight  bf16 [H] gain, or NULL for a gain of 1 (16-byte aligned)
+ *   norm_eps     > 0 (1e-6 in the workloads)
+ * Runs on the fused decode path only (the shapes MOE_PATH_FUSED_DECODE
+ * accepts; else UNSUPPORTED_SHAPE); y and r_next come out of the same
+ * kernel. Other arguments and errors as moe_forward. */
+moe_status moe_forward_residual(const moe_shape* shape, const void* r, const void* norm_weight,
+                                float norm_eps, const void* w_router, const float* router_bias,
+                                const moe_experts* experts, const moe_experts* shared,
+                                const void* w_shared_gate, float* y, void* r_next,
+                                const moe_route_out* route_out, void* workspace, size_t ws_bytes,
+                                void* stream);
 
 /* Expert-GEMM implementations selectable through moe_forward_timed. */
 typedef enum moe_expert_path {

@@ -26,6 +26,7 @@ from .moe import (  # noqa: F401
     swiglu_expert,
     moe_forward,
     topk_gap,
+    rms_norm,
 )
 from .attention import gqa_decode_attention  # noqa: F401,E402
 from .gated_deltanet import gated_delta_scan  # noqa: F401,E402

@@ -88,7 +88,30 @@ def topk_gap(logits, top_k: int) -> np.ndarray:
     return l32[:, top_k - 1] - l32[:, top_k]
 
 
-def route(x_bits, wr_bits, bias, wsg_bits, top_k: int):
+def rms_norm(r_bits, eps: float, gain_bits=None) -> np.ndarray:
+    """The input of a pre-norm MoE block, fp64 [T, H]:
+    x[t] = r[t] / sqrt(mean_h r[t, h]^2 + eps) * gain.
+
+    The pages do not say what joins two consecutive MoE layers. The reading
+    taken for running layers back to back is the transformer's pre-norm
+    residual block: each layer reads the RMS-normalised residual row and adds
+    its output back to that row. `gain` (bf16 [H]) is the normalisation's
+    per-channel scale, 1 when absent."""
+    r = bf16_bits_to_f64(r_bits)
+    x = r / np.sqrt(np.mean(r * r, axis=1, keepdims=True) + eps)
+    if gain_bits is not None:
+        x = x * bf16_bits_to_f64(gain_bits)[None, :]
+    return x
+
+
+def _logits_f64(x, wr_bits, bias):
+    l = x @ bf16_bits_to_f64(wr_bits).T
+    if bias is not None:
+        l = l + np.asarray(bias, dtype=np.float32).astype(np.float64)[None, :]
+    return l
+
+
+def route(x_bits, wr_bits, bias, wsg_bits, top_k: int, x_f64=None):
     """Router + top-k + renormalised softmax weights + shared-expert gate.
 
     Returns (ids int32 [T, k], weights fp64 [T, k], gate fp64 [T] or None,
@@ -97,15 +120,18 @@ def route(x_bits, wr_bits, bias, wsg_bits, top_k: int):
     experts renormalised over the selected ones, which equals
     exp(l_k - l_max) / sum_j exp(l_j - l_max) over the selected j; the shared
     expert (which processes every token, [dothoosh "Model specification"]) is
-    scaled by the gate sigmoid(sum_h x[t, h] * w_sg[h])."""
-    l = router_logits(x_bits, wr_bits, bias)
+    scaled by the gate sigmoid(sum_h x[t, h] * w_sg[h]). `x_f64`, when given,
+    is the input itself in fp64 (a normalised residual row) and x_bits is
+    ignored."""
+    l = router_logits(x_bits, wr_bits, bias) if x_f64 is None else _logits_f64(x_f64, wr_bits, bias)
     ids = select_top_k(l, top_k)
     sel = np.take_along_axis(l, ids.astype(np.int64), axis=1)
     z = np.exp(sel - sel[:, :1])
     w = z / z.sum(axis=1, keepdims=True)
     gate = None
     if wsg_bits is not None:
-        s = bf16_bits_to_f64(x_bits) @ bf16_bits_to_f64(wsg_bits)
+        xs = bf16_bits_to_f64(x_bits) if x_f64 is None else x_f64
+        s = xs @ bf16_bits_to_f64(wsg_bits)
         gate = 1.0 / (1.0 + np.exp(-s))
     return ids, w, gate, l
 
@@ -174,7 +200,7 @@ def swiglu_expert(xrows, w_gu, w_dn) -> np.ndarray:
     return h @ w_dn.T
 
 
-def moe_forward(x_bits, wr_bits, bias, wsg_bits, top_k: int, expert_fn, tokens=None):
+def moe_forward(x_bits, wr_bits, bias, wsg_bits, top_k: int, expert_fn, tokens=None, x_f64=None):
     """The whole layer for the tokens listed (all tokens by default).
 
     y[t] = sum_k w[t, k] * Expert_{ids[t, k]}(x_t) + g_t * Shared(x_t)
@@ -186,14 +212,18 @@ def moe_forward(x_bits, wr_bits, bias, wsg_bits, top_k: int, expert_fn, tokens=N
     way the pages' grouped GEMM groups them, but the arithmetic is the plain
     definition (fp64 sums make the order of the additions immaterial at any
     tolerance the tests use).
+    `x_f64`, when given, is the input in fp64 (a normalised residual row,
+    see rms_norm) and x_bits is ignored.
     Returns (y fp64 [n, H], ids, weights, gate, logits) for the n tokens."""
-    x_bits = np.asarray(x_bits)
-    if tokens is None:
-        tokens = np.arange(x_bits.shape[0])
-    tokens = np.asarray(tokens)
-    xs = x_bits[tokens]
-    ids, w, gate, logits = route(xs, wr_bits, bias, wsg_bits, top_k)
-    x = bf16_bits_to_f64(xs)
+    n_all = (np.asarray(x_f64) if x_f64 is not None else np.asarray(x_bits)).shape[0]
+    tokens = np.arange(n_all) if tokens is None else np.asarray(tokens)
+    if x_f64 is None:
+        xs = np.asarray(x_bits)[tokens]
+        ids, w, gate, logits = route(xs, wr_bits, bias, wsg_bits, top_k)
+        x = bf16_bits_to_f64(xs)
+    else:
+        x = np.asarray(x_f64, dtype=np.float64)[tokens]
+        ids, w, gate, logits = route(None, wr_bits, bias, wsg_bits, top_k, x_f64=x)
     n, H = x.shape
     E = np.asarray(wr_bits).shape[0]
     y = np.zeros((n, H), dtype=np.float64)

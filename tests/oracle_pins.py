@@ -388,6 +388,31 @@ def pin_layer_all_experts():
     assert np.allclose(y, want, rtol=1e-10, atol=1e-12)
 
 
+# ------------------------------------------------------ pre-norm residual ---
+
+def pin_rms_norm_handworked():
+    """Hand-worked rows: [1, 7] has mean square 25, so its RMS is 5 and the
+    normalised row [0.2, 1.4]; a row of ones with eps = 3 divides by
+    sqrt(1 + 3) = 2; a row of +-2 becomes +-1 (eps negligible)."""
+    x = M.rms_norm(_bits([[1.0, 7.0]]), 1e-30)
+    assert np.allclose(x, [[0.2, 1.4]], rtol=1e-14, atol=0)
+    x = M.rms_norm(_bits([[1.0, 1.0, 1.0, 1.0]]), 3.0)
+    assert np.allclose(x, [[0.5] * 4], rtol=1e-14, atol=0)
+    r = np.array([[-2.0, 2.0, 2.0, -2.0, 2.0, 2.0, 2.0, 2.0]])
+    assert np.allclose(M.rms_norm(_bits(r), 1e-30), r / 2, rtol=1e-14, atol=0)
+
+
+def pin_rms_norm_invariants():
+    """The output's mean square is 1 (eps negligible), scaling the row by a
+    power of two changes nothing, and the gain multiplies each channel."""
+    r = RNG.standard_normal((5, 96)) * 3
+    x = M.rms_norm(_bits(r), 1e-30)
+    assert np.allclose(np.mean(x * x, axis=1), 1.0, rtol=1e-12)
+    assert np.allclose(M.rms_norm(_bits(r * 8), 1e-30), x, rtol=1e-12)
+    gain = np.where(np.arange(96) % 2 == 0, 2.0, 0.5)
+    assert np.allclose(M.rms_norm(_bits(r), 1e-30, _bits(gain)), x * gain[None, :], rtol=1e-12)
+
+
 # -------------------------------------------------------- decode attention ---
 
 def _attn(q, k, v, lens, scale=None):

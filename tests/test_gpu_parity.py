@@ -164,42 +164,60 @@ def test_fused_decode(moelib, cuda_dev, T, E, K, shared, H, I):
     _run_and_check(moelib, cuda_dev, spec, path=moelib.PATH_FUSED_DECODE)
 
 
-@pytest.mark.parametrize("T,path", [(1, "fused"), (4, "fused"), (2, "gemv"), (100, "auto")])
-def test_residual_chain_of_three_layers(moelib, cuda_dev, T, path):
-    """Three layers run back to back through moe_forward_residual, each call's
-    x_next feeding the next call, against the oracle applied three times with
-    the same residual join (x_{l+1} = bf16(x_l + y_l)): every layer's y meets
-    the bar, and x_next is exactly the bf16 rounding of x + y."""
-    if path == "gemv":  # a shape the fused kernel refuses (H > 2048): the combine kernel joins
-        spec = synth.LayerSpec("chain", T=T, H=2304, I=256, E=64, top_k=4, seed=20260041)
-    else:
-        spec = synth.LayerSpec("chain", T=T, H=2048, I=512, seed=20260041, layers=3)
+@pytest.mark.parametrize("T,gain", [(1, False), (4, True), (3, False)])
+def test_prenorm_chain_of_three_layers(moelib, cuda_dev, T, gain):
+    """Three pre-norm MoE blocks run back to back through moe_forward_residual,
+    each call's r_next feeding the next call: every layer's y meets the bar
+    against the oracle applied to that layer's residual row (x = RMSNorm(r),
+    then the layer), and r_next is exactly bf16(r + y) of the kernel's own y."""
+    spec = synth.LayerSpec("chain", T=T, H=2048, I=512, seed=20260041, layers=3)
     layers = [parity.device_layer(spec, li, cuda_dev) for li in range(3)]
-    x0 = synth.activations(spec, device=cuda_dev)
+    r0 = synth.activations(spec, device=cuda_dev)
+    g = None
+    if gain:  # a gain row of 0.5 .. 1.5 in bf16
+        g = (0.5 + torch.arange(spec.H, device=cuda_dev, dtype=torch.float32) / spec.H).to(torch.bfloat16)
+    eps = 1e-6
     shape = moelib.make_shape(T, spec.H, spec.I, spec.E, spec.top_k, spec.shared, 16)
     ws = moelib.alloc_workspace(shape, cuda_dev)
-    xs = [x0] + [torch.empty_like(x0) for _ in range(3)]
+    rs = [r0] + [torch.empty_like(r0) for _ in range(3)]
     ys = [torch.empty(T, spec.H, dtype=torch.float32, device=cuda_dev) for _ in range(3)]
     ros = [moelib.alloc_route_out(shape, cuda_dev) for _ in range(3)]
     for li, L in enumerate(layers):
         routed, shared = parity.experts_arg(L)
-        moelib.forward_residual(shape, xs[li], L.wr, L.bias, routed, shared, L.wsg, ys[li], xs[li + 1], ws,
-                                route_out=ros[li])
+        moelib.forward_residual(shape, rs[li], L.wr, L.bias, routed, shared, L.wsg, ys[li], rs[li + 1], ws,
+                                norm_weight=g, norm_eps=eps, route_out=ros[li])
     torch.cuda.synchronize()
-    x_ref = bits16(x0)
     for li, L in enumerate(layers):
         assert moelib.status_read(ros[li]["status"]) == 0
         y_gpu = ys[li].cpu().numpy()
-        # x_next is the kernel's own y joined to its own input, rounded once to bf16
-        want = bf16_from_f64(bits16_to_f64(bits16(xs[li])) + y_gpu.astype(np.float32).astype(np.float64))
-        assert np.array_equal(bits16(xs[li + 1]), want)
-        # the oracle's chain: its own y, its own join
-        y_ref, ids_ref, w_ref, g_ref, logits = oracle.moe_forward(x_ref, bits16(L.wr), None, bits16(L.wsg),
-                                                                  spec.top_k, parity.layer_expert_fn(L, spec.E))
+        r_bits = bits16(rs[li])
+        # the join: the kernel's own y added to its own input row, rounded once to bf16
+        want = bf16_from_f64(bits16_to_f64(r_bits) + y_gpu.astype(np.float64))
+        assert np.array_equal(bits16(rs[li + 1]), want)
+        x = oracle.rms_norm(r_bits, eps, None if g is None else bits16(g))
+        y_ref, ids_ref, w_ref, g_ref, logits = oracle.moe_forward(None, bits16(L.wr), None, bits16(L.wsg),
+                                                                  spec.top_k, parity.layer_expert_fn(L, spec.E),
+                                                                  x_f64=x)
         ids_gpu = ros[li]["ids"].cpu().numpy()[: T * spec.top_k].reshape(T, spec.top_k)
         excl = parity.check_ids(ids_gpu, ids_ref, logits, spec.top_k)
         parity.check_y(y_gpu, y_ref, excl)
-        x_ref = bf16_from_f64(bits16_to_f64(x_ref) + y_ref.astype(np.float32).astype(np.float64))
+    # the stream stays in range over the three layers (the reason for the norm)
+    assert torch.isfinite(rs[3].float()).all()
+
+
+def test_prenorm_block_needs_the_fused_path(moelib, cuda_dev):
+    """moe_forward_residual runs on the fused decode kernel only: a shape the
+    fused kernel refuses (H > 2048) is refused, with nothing launched."""
+    spec = synth.LayerSpec("chain-big", T=2, H=2304, I=256, E=64, top_k=4, seed=20260042)
+    L = parity.device_layer(spec, 0, cuda_dev)
+    r = synth.activations(spec, device=cuda_dev)
+    shape = moelib.make_shape(2, spec.H, spec.I, spec.E, spec.top_k, spec.shared, 16)
+    ws = moelib.alloc_workspace(shape, cuda_dev)
+    y = torch.empty(2, spec.H, device=cuda_dev)
+    routed, shared = parity.experts_arg(L)
+    with pytest.raises(moelib.MoeError) as ei:
+        moelib.forward_residual(shape, r, L.wr, L.bias, routed, shared, L.wsg, y, torch.empty_like(r), ws)
+    assert ei.value.status == moelib.MOE_ERR_UNSUPPORTED_SHAPE
 
 
 @pytest.mark.parametrize("H,I", [(128, 64), (320, 128), (4096, 512)])

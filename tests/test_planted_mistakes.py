@@ -16,6 +16,7 @@ _routing = M.routing_tables
 _swiglu = M.swiglu_expert
 _select = M.select_top_k
 _logits = M.router_logits
+_rms = M.rms_norm
 
 
 def nibble_order_reversed(codes, scales, biases, group=64):
@@ -61,15 +62,15 @@ def logits_transposed_bias(x, wr, bias=None):
     return l
 
 
-def no_renormalisation(x, wr, bias, wsg, top_k):
-    ids, w, g, l = _route(x, wr, bias, wsg, top_k)
+def no_renormalisation(x, wr, bias, wsg, top_k, **kw):
+    ids, w, g, l = _route(x, wr, bias, wsg, top_k, **kw)
     p = np.exp(l - l.max(axis=1, keepdims=True))
     p /= p.sum(axis=1, keepdims=True)
     return ids, np.take_along_axis(p, ids.astype(np.int64), axis=1), g, l
 
 
-def gate_is_one_minus_sigmoid(x, wr, bias, wsg, top_k):
-    ids, w, g, l = _route(x, wr, bias, wsg, top_k)
+def gate_is_one_minus_sigmoid(x, wr, bias, wsg, top_k, **kw):
+    ids, w, g, l = _route(x, wr, bias, wsg, top_k, **kw)
     return ids, w, (None if g is None else 1.0 - g), l
 
 
@@ -114,6 +115,29 @@ def down_transposed(xrows, w_gu, w_dn):
     return h @ (w_dn if H == I else w_dn.reshape(I, H))
 
 
+def rms_sum_not_mean(r_bits, eps, gain_bits=None):
+    r = M.bf16_bits_to_f64(r_bits)
+    x = r / np.sqrt(np.sum(r * r, axis=1, keepdims=True) + eps)
+    return x if gain_bits is None else x * M.bf16_bits_to_f64(gain_bits)[None, :]
+
+
+def rms_without_sqrt(r_bits, eps, gain_bits=None):
+    r = M.bf16_bits_to_f64(r_bits)
+    x = r / (np.mean(r * r, axis=1, keepdims=True) + eps)
+    return x if gain_bits is None else x * M.bf16_bits_to_f64(gain_bits)[None, :]
+
+
+def rms_eps_outside_sqrt(r_bits, eps, gain_bits=None):
+    r = M.bf16_bits_to_f64(r_bits)
+    x = r / (np.sqrt(np.mean(r * r, axis=1, keepdims=True)) + eps)
+    return x if gain_bits is None else x * M.bf16_bits_to_f64(gain_bits)[None, :]
+
+
+def rms_gain_divides(r_bits, eps, gain_bits=None):
+    x = _rms(r_bits, eps)
+    return x if gain_bits is None else x / M.bf16_bits_to_f64(gain_bits)[None, :]
+
+
 MUTANTS = [
     ("dequant", nibble_order_reversed), ("dequant", bias_subtracted), ("dequant", signed_codes),
     ("dequant", scale_per_group_of_32), ("select_top_k", ties_to_higher_index),
@@ -121,7 +145,8 @@ MUTANTS = [
     ("route", gate_is_one_minus_sigmoid), ("routing_tables", scatter_reversed_within_expert),
     ("routing_tables", tiles_off_by_one), ("routing_tables", offsets_inclusive),
     ("swiglu_expert", gate_up_swapped), ("swiglu_expert", relu_instead_of_silu),
-    ("swiglu_expert", down_transposed),
+    ("swiglu_expert", down_transposed), ("rms_norm", rms_sum_not_mean), ("rms_norm", rms_without_sqrt),
+    ("rms_norm", rms_eps_outside_sqrt), ("rms_norm", rms_gain_divides),
 ]
 
 
