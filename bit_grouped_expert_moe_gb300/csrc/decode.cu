@@ -66,6 +66,10 @@ constexpr int kUnits = kItemCols / 8;           // MMA units of 8 h columns (8 g
 constexpr int kGuTaskBytes = 16 * 64 + 16 * 8;  // 16 code rows x 128 K, and their scale and bias pairs
 constexpr int kDnTileBytes = 16 * 16 + 16 * 8;  // 16 W_down rows x 32 K, and their scale and bias pairs
 constexpr int kMaxDnTiles = 8;                  // W_down tiles of 16 rows per warp (H <= 2048)
+constexpr int kDnTilesPerTask = 4;              // W_down tiles per down task (two down tasks per item)
+constexpr int kTaskBytes = kDnTilesPerTask * kDnTileBytes;  // one ring slot (>= kGuTaskBytes)
+constexpr int kSlots = 6;                       // ring slots per warp: a whole item at H = 2048
+static_assert(kGuTaskBytes <= kTaskBytes, "a gate/up task must fit a ring slot");
 constexpr int kDecMaxH = kDecWarps * 16 * kMaxDnTiles;
 constexpr int kGateWarp = kDecWarps - 1;        // computes the shared gate in blocks with a shared item
 // The prelude fills the logits with this pattern; fp32 arithmetic never
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const int nkb = H / 128;           // gate/up K blocks of 128
   const int mtiles = H / 16;         // W_down tiles of 16 output rows
   const size_t slot_bytes = (size_t)a.slot_bytes;
-  uint8_t* ring = dsm_raw + (size_t)warp * 2 * slot_bytes;          // this warp's two slots
+  uint8_t* ring = dsm_raw + (size_t)warp * slot_bytes;              // this warp's ring of kSlots tasks
   __half* x16 = reinterpret_cast<__half*>(dsm_raw + a.x16_offset);   // [T][H] fp16, K-permuted
   float* xf = reinterpret_cast<float*>(dsm_raw + a.xf_offset);      // [T][H] fp32 layer input
   float* part = reinterpret_cast<float*>(dsm_raw + a.part_offset);   // [16 warps][4][32]
@@ -225,68 +229,84 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   for (int i = tid; i < 8 * kItemCols / 2; i += kDecThreads) reinterpret_cast<uint32_t*>(hs)[i] = 0u;
   __syncthreads();
 
-  // ---- weight copies of one part of an item into a slot of this warp's ring
-  // gate/up part: this warp's unit u = warp % 4 (h columns n0 + 8u .. +7, as
-  // gate rows and up rows) for K blocks kb = warp / 4 + 4 j.
-  auto issue_gu = [&](int item, uint8_t* dst) {
+  // ---- this warp's tasks, in order: for each of the block's items, its
+  // gate/up tasks (unit u = warp % 4, i.e. h columns n0 + 8u .. +7 as gate
+  // rows and up rows, one K block kb = warp / 4 + 4 jj each), then two down
+  // tasks (W_down tiles 16 (warp + 16 i) .. +15, i = 4 d .. 4 d + 3, columns
+  // n0 .. n0 + 31). Each task's bytes are one cp.async group in one slot of
+  // the warp's ring, so a task is computed as soon as its own bytes land.
+  const int ngu = (warp >> 2) < nkb ? (nkb - (warp >> 2) + 3) / 4 : 0;  // gate/up tasks per item
+  const int tpi = ngu + 2;                                                 // tasks per item
+  auto issue_gu = [&](int item, int jj, uint8_t* td) {
     const int s = item / cpi, n0 = (item - s * cpi) * kItemCols;
     const uint8_t* codes = S.slot_src[s][0];
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(S.slot_src[s][1]);
     const uint16_t* bi = reinterpret_cast<const uint16_t*>(S.slot_src[s][2]);
-    const int u = warp & 3;
-    for (int j = 0, kb = warp >> 2; kb < nkb; ++j, kb += 4) {
-      uint8_t* td = dst + j * kGuTaskBytes;
+    const int u = warp & 3, kb = (warp >> 2) + 4 * jj;
 #pragma unroll
-      for (int q0 = 0; q0 < 64; q0 += 32) {  // 16 rows x 4 pieces of 16 bytes
-        const int q = q0 + lane, r = q >> 2, piece = q & 3;
-        const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
-        cp_async16(td + r * 64 + piece * 16, codes + (size_t)row * (H / 2) + kb * 64 + piece * 16);
-      }
-      {  // scale and bias pairs of groups 2kb, 2kb+1 of the 16 rows
-        const int r = lane >> 1, kind = lane & 1;
-        const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
-        cp_async4(td + 1024 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)row * gpr + 2 * kb);
-      }
+    for (int q0 = 0; q0 < 64; q0 += 32) {  // 16 rows x 4 pieces of 16 bytes
+      const int q = q0 + lane, r = q >> 2, piece = q & 3;
+      const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
+      cp_async16(td + r * 64 + piece * 16, codes + (size_t)row * (H / 2) + kb * 64 + piece * 16);
+    }
+    {  // scale and bias pairs of groups 2kb, 2kb+1 of the 16 rows
+      const int r = lane >> 1, kind = lane & 1;
+      const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
+      cp_async4(td + 1024 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)row * gpr + 2 * kb);
     }
   };
-  // down part: W_down rows of this warp's tiles (16 tile + r, tile = warp +
-  // 16 i), columns n0..n0+31 (16 bytes of codes per row, one scale group).
-  auto issue_dn = [&](int item, uint8_t* dst) {
+  auto issue_dn = [&](int item, int dt, uint8_t* td) {
     const int s = item / cpi, c = item - s * cpi;
     const uint8_t* codes = S.slot_src[s][3];
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(S.slot_src[s][4]);
     const uint16_t* bi = reinterpret_cast<const uint16_t*>(S.slot_src[s][5]);
     const int gp = (c >> 1) & ~1;  // the aligned pair of groups holding this item's group
 #pragma unroll
-    for (int q0 = 0; q0 < 16 * kMaxDnTiles; q0 += 32) {
-      const int q = q0 + lane, i = q >> 4, r = q & 15, tile = warp + 16 * i;
-      if (tile < mtiles) cp_async16(dst + i * kDnTileBytes + r * 16, codes + (size_t)(16 * tile + r) * (I / 2) + c * 16);
+    for (int q0 = 0; q0 < 16 * kDnTilesPerTask; q0 += 32) {  // 16 bytes of codes per row
+      const int q = q0 + lane, i = q >> 4, r = q & 15, tile = warp + 16 * (kDnTilesPerTask * dt + i);
+      if (tile < mtiles) cp_async16(td + i * kDnTileBytes + r * 16, codes + (size_t)(16 * tile + r) * (I / 2) + c * 16);
     }
 #pragma unroll
-    for (int q0 = 0; q0 < 32 * kMaxDnTiles; q0 += 32) {
-      const int q = q0 + lane, i = q >> 5, r = (q & 31) >> 1, kind = q & 1, tile = warp + 16 * i;
+    for (int q0 = 0; q0 < 32 * kDnTilesPerTask; q0 += 32) {  // scale and bias pairs
+      const int q = q0 + lane, i = q >> 5, r = (q & 31) >> 1, kind = q & 1;
+      const int tile = warp + 16 * (kDnTilesPerTask * dt + i);
       if (tile < mtiles)
-        cp_async4(dst + i * kDnTileBytes + 256 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)(16 * tile + r) * igpr + gp);
+        cp_async4(td + i * kDnTileBytes + 256 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)(16 * tile + r) * igpr + gp);
     }
   };
-  int issued = 0;  // parts issued by this warp: part 2j = gate/up of item j, 2j+1 = its down part
-  auto issue_part = [&](int p) {
-    const int item = b + G * (p >> 1);
-    if (p & 1) issue_dn(item, ring + slot_bytes);
-    else issue_gu(item, ring);
+  int issued = 0;  // tasks issued by this warp (one cp.async group each)
+  auto issue_task = [&](int k) {
+    const int j = k / tpi, t = k - j * tpi;
+    uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
+    if (t < ngu) issue_gu(b + G * j, t, td);
+    else issue_dn(b + G * j, t - ngu, td);
     tc::cp_async_commit();
   };
+  // Task k's bytes have landed (every later group may still be in flight),
+  // and every lane of the warp sees them.
+  auto wait_task = [&](int k) {
+    switch (issued - k - 1) {
+      case 0: tc::cp_async_wait<0>(); break;
+      case 1: tc::cp_async_wait<1>(); break;
+      case 2: tc::cp_async_wait<2>(); break;
+      case 3: tc::cp_async_wait<3>(); break;
+      case 4: tc::cp_async_wait<4>(); break;
+      default: tc::cp_async_wait<kSlots - 1>(); break;
+    }
+    __syncwarp();
+  };
 
-  // ---- phase 0: weights only (they do not depend on the previous kernel)
+  // ---- phase 0: weights only (they do not depend on the previous kernel).
+  // Blocks with a shared item start its copies; the router rows go to the
+  // other blocks (their x arrives without queueing behind those copies).
   const bool shared_first = sh && b < cpi;
-  if (shared_first) {
-    issue_part(0);
-    issue_part(1);
-    issued = 2;
-  }
+  if (shared_first)
+    for (; issued < tpi && issued < kSlots; ++issued) issue_task(issued);
+  const int sfb = sh ? (cpi < G ? cpi : 0) : 0;  // blocks with a shared item (none hold router rows)
+  const int RG = G - sfb;                        // router blocks
   const int rrows = E + sh, rvec = H / 8;
-  const int rrow = b + G * warp;
-  const bool router_warp = rrow < rrows && warp != kGateWarp;
+  const int rrow = b - sfb + RG * warp;
+  const bool router_warp = b >= sfb && rrow < rrows && warp != kGateWarp;
   uint4 w4[8];
   if (router_warp) load_row(w4, rrow < E ? a.wr + (size_t)rrow * H : a.wsg, rvec, lane);
   if (shared_first && warp == kGateWarp) load_row(w4, a.wsg, rvec, lane);
@@ -509,23 +529,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     }
   }
 
-  // ---- phase 2: this block's items b, b + G, ...
+  // ---- phase 2: this block's items b, b + G, ..., task by task
   float acc[kMaxDnTiles][4];
 #pragma unroll
   for (int i = 0; i < kMaxDnTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  while (issued < 2 && issued < 2 * nitems) issue_part(issued++);
-  const uint8_t* slot_gu = ring;
-  const uint8_t* slot_dn = ring + slot_bytes;
+  const int ntasks = nitems * tpi;
+  for (; issued < ntasks && issued < kSlots; ++issued) issue_task(issued);
+  int k = 0;  // next task of this warp
   for (int j = 0; j < nitems; ++j) {
     const int item = b + G * j;
     const int s = item / cpi;
-    // gate/up part (ring slot 0): part 2j must have landed
-    if (issued > 2 * j + 1) tc::cp_async_wait<1>();
-    else tc::cp_async_wait<0>();
-    __syncwarp();
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int jj = 0, kb = warp >> 2; kb < nkb; ++jj, kb += 4) {
-      const uint8_t* t = slot_gu + jj * kGuTaskBytes;
+    for (int jj = 0; jj < ngu; ++jj, ++k) {
+      wait_task(k);
+      const uint8_t* t = ring + (size_t)(k % kSlots) * kTaskBytes;
+      const int kb = (warp >> 2) + 4 * jj;
       uint4 xb[4];
       const __half* xrow = x16 + (size_t)(g8 < T ? g8 : 0) * H + kb * 128 + 32 * c4;
 #pragma unroll
@@ -537,9 +555,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       const int gs = c4 >> 1;  // this lane's 32 K lie in group 2kb + gs
       mma_chunk(d, cg, cu, bf16_h2(sb[g8 * 4 + gs]), bf16_h2(sb[g8 * 4 + 2 + gs]), bf16_h2(sb[(8 + g8) * 4 + gs]),
                 bf16_h2(sb[(8 + g8) * 4 + 2 + gs]), xb);
+      __syncwarp();  // the slot is read: refill it
+      if (issued < ntasks) issue_task(issued++);
     }
-    __syncwarp();
-    if (2 * j + 2 < 2 * nitems) issue_part(issued++);  // next item's gate/up part into slot 0
 #pragma unroll
     for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r];
     __syncthreads();
@@ -564,29 +582,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       }
     }
     __syncthreads();
-    // down part (ring slot 1): part 2j + 1 must have landed
-    if (issued > 2 * j + 2) tc::cp_async_wait<1>();
-    else tc::cp_async_wait<0>();
-    __syncwarp();
-    {
-      const uint4 hb = *reinterpret_cast<const uint4*>(hs + g8 * kItemCols + 8 * c4);  // token g (zero if >= T)
-      const int gs = ((item - s * cpi) >> 1) & 1;  // this item's group within the loaded pair
+    const uint4 hb = *reinterpret_cast<const uint4*>(hs + g8 * kItemCols + 8 * c4);  // token g (zero if >= T)
+    const int gs = ((item - s * cpi) >> 1) & 1;  // this item's group within the loaded pair
 #pragma unroll
-      for (int i = 0; i < kMaxDnTiles; ++i)
-        if (warp + 16 * i < mtiles) {
-          const uint8_t* t = slot_dn + i * kDnTileBytes;
+    for (int dt = 0; dt < kMaxDnTiles / kDnTilesPerTask; ++dt, ++k) {
+      wait_task(k);
+      const uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
+#pragma unroll
+      for (int i = 0; i < kDnTilesPerTask; ++i)
+        if (warp + 16 * (kDnTilesPerTask * dt + i) < mtiles) {
+          const uint8_t* t = td + i * kDnTileBytes;
           const uint32_t c0 = *reinterpret_cast<const uint32_t*>(t + g8 * 16 + c4 * 4);
           const uint32_t c1 = *reinterpret_cast<const uint32_t*>(t + (8 + g8) * 16 + c4 * 4);
           const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 256);
           uint32_t p0[4], p1[4];
           tc::dequant8_f16(c0, bf16_h2(sb[g8 * 4 + gs]), bf16_h2(sb[g8 * 4 + 2 + gs]), p0);
           tc::dequant8_f16(c1, bf16_h2(sb[(8 + g8) * 4 + gs]), bf16_h2(sb[(8 + g8) * 4 + 2 + gs]), p1);
-          mma_16816(acc[i], p0[0], p1[0], p0[1], p1[1], hb.x, hb.y);
-          mma_16816(acc[i], p0[2], p1[2], p0[3], p1[3], hb.z, hb.w);
+          float (&ac)[4] = acc[kDnTilesPerTask * dt + i];
+          mma_16816(ac, p0[0], p1[0], p0[1], p1[1], hb.x, hb.y);
+          mma_16816(ac, p0[2], p1[2], p0[3], p1[3], hb.z, hb.w);
         }
+      __syncwarp();
+      if (issued < ntasks) issue_task(issued++);
     }
-    __syncwarp();
-    if (2 * j + 3 < 2 * nitems) issue_part(issued++);  // next item's down part into slot 1
   }
   tc::cp_async_wait_all();  // no copy into this block's shared memory outlives it
 
@@ -609,15 +627,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       }
     }
   }
+  // Each warp arrives once its own sums are stored (warp 0 also counts the
+  // block among those holding sums); no block barrier on this path.
+  __syncwarp();
+  if (lane == 0 && b != a.stall_block)
+    red_release_add(a.bar, 1u + (warp == 0 && nitems > 0 ? (1u << 16) : 0u));
   __syncthreads();
-  if (tid == 0) {
-    if (S.range) atomicCAS(a.status, 0, (int32_t)MOE_ERR_RANGE);
-    if (b != a.stall_block) red_release_add(a.bar, 1u + (nitems > 0 ? (1u << 16) : 0u));
-  }
+  if (tid == 0 && S.range) atomicCAS(a.status, 0, (int32_t)MOE_ERR_RANGE);
   if (b >= mtiles) return;  // no output rows here
   if (tid == 0) {
     unsigned v = 0;
-    while (((v = ld_acquire_u32(a.bar)) & 0xFFFFu) < (unsigned)G) {
+    while (((v = ld_acquire_u32(a.bar)) & 0xFFFFu) < (unsigned)(G * kDecWarps)) {
       if (global_timer_ns() > deadline) {
         S.failed = 1;
         break;
@@ -678,7 +698,7 @@ int sm_count(int dev) {
 
 constexpr size_t kDecDynamicLimit = 220 * 1024;  // 227 KB per block minus the static part
 
-// Dynamic shared memory: 16 warps x 2 ring slots, x16 fp16 and x fp32
+// Dynamic shared memory: 16 warps x kSlots task slots, x16 fp16 and x fp32
 // [T][H], the partial sums of the gate/up reduction, h of one item.
 struct DecodeLayout {
   size_t slot_bytes, x16_offset, xf_offset, part_offset, hs_offset, total;
@@ -686,11 +706,9 @@ struct DecodeLayout {
 
 DecodeLayout decode_layout(const Geometry& g) {
   DecodeLayout L{};
-  const size_t gu = (size_t)((g.H + 511) / 512) * kGuTaskBytes;
-  const size_t dn = (size_t)((g.H / 16 + kDecWarps - 1) / kDecWarps) * kDnTileBytes;
-  L.slot_bytes = ((gu > dn ? gu : dn) + 127) & ~size_t(127);
+  L.slot_bytes = (size_t)kSlots * kTaskBytes;  // one warp's ring
   const size_t xb = ((size_t)g.T * g.H * 2 + 127) & ~size_t(127);
-  L.x16_offset = (size_t)kDecWarps * 2 * L.slot_bytes;
+  L.x16_offset = (size_t)kDecWarps * L.slot_bytes;
   L.xf_offset = L.x16_offset + xb;
   L.part_offset = L.xf_offset + 2 * xb;
   L.hs_offset = L.part_offset + (size_t)kDecWarps * 4 * 32 * 4;
@@ -704,14 +722,18 @@ DecodeLayout decode_layout(const Geometry& g) {
 // One block per SM, every block resident (blocks wait for each other's
 // logits and sums); K of gate/up in whole 128-wide blocks, H at most 2048
 // (each warp keeps at most 8 tiles of output sums in registers), I in whole
-// 128-wide blocks, enough router warps for E + 1 rows.
+// 128-wide blocks, enough router warps (15 per block without a shared item)
+// for the E (+ 1) router rows.
 bool decode_supported(const Geometry& g) {
   int dev = 0;
   if (g.T < 1 || g.T > kDecodeMaxTokens || g.H % 128 || g.H > kDecMaxH || g.I % 128 ||
       cudaGetDevice(&dev) != cudaSuccess)
     return false;
   const int sms = sm_count(dev);
-  if (sms <= 0 || sms > kMaxDecodeBlocks || g.E + 1 > sms * (kDecWarps - 1)) return false;
+  if (sms <= 0 || sms > kMaxDecodeBlocks) return false;
+  // router rows live on the blocks without a shared item, 15 warps each
+  const int cpi = g.I / kItemCols, sfb = g.shared ? (cpi < sms ? cpi : 0) : 0;
+  if (g.E + g.shared > (sms - sfb) * (kDecWarps - 1)) return false;
   return decode_layout(g).total <= kDecDynamicLimit;
 }
 
