@@ -7,49 +7,52 @@
 // Apple silicon", "Decode optimisations", kernel fusion: chains of kernels
 // fused so intermediates stay on chip.]
 //
-// Work split. An item is (expert slot s, 32 h columns n0..n0+31). The block
-// that computes those h columns also computes their share of the down
-// projection, W_down[:, n0..n0+31] h[n0..n0+31] for every output row, so h
-// never leaves the block; each warp keeps its output rows' sums in registers
-// across the block's items, and the blocks' sums meet once, at the end, in a
-// fixed-order reduction. Slot 0 is the shared expert (every token; it needs
-// no routing), slots 1.. the distinct routed experts in increasing index;
-// item i goes to block i mod G, so blocks 0..I/32-1 start with a shared item.
+// Work split. Slot 0 is the shared expert (every token; it needs no
+// routing), slots 1.. the distinct routed experts in increasing index.
+//   gate/up: an item is (slot s, 32 h columns n0..n0+31); item i goes to
+//     block i mod G, so blocks 0..I/32-1 start with a shared item. The block
+//     forms h = w silu(gate) up for its columns (the routing weight, or the
+//     shared gate, folded in), stores it to the workspace and counts the
+//     item on the slot's counter (a release).
+//   down: block b owns output rows 16b..16b+15 (W_down rows of every slot:
+//     4 KB of codes per slot, contiguous). It waits for each slot's counter
+//     to reach I/32 (an acquire), reads that slot's h and adds its products
+//     into per-warp sums; the 16 warps' sums are added in a fixed order into
+//     y, so results are bit-identical run to run.
+// No grid-wide barrier: the router's logits are exchanged through a
+// sentinel the prelude writes (a reader polls the data itself), and h
+// through the per-slot counters.
+//
+// Tasks. Every unit of work is 16 weight rows x 128 K: a gate/up task (8
+// gate rows and the matching 8 up rows of one 8-column unit, one K block)
+// or a down task (16 W_down rows, one 128-wide block of h columns). Each
+// warp streams its tasks through a ring of kSlots shared-memory slots, one
+// cp.async group per task, and computes a task as soon as its bytes land;
+// the copies of the next tasks overlap the arithmetic. The shared expert's
+// down tasks are copied into a buffer of their own before the kernel waits
+// for its predecessor (their weights need no routing).
 //
 // Phases of one block:
-//   0  (before the programmatic-dependent-launch wait: weights only) the
-//      warps load their router rows into registers; a block whose first item
-//      is a shared one issues that item's weight copies;
+//   0  (before the programmatic-dependent-launch wait: weights only) router
+//      rows into registers on the blocks without a shared item; the shared
+//      item's gate/up tasks and the shared down tasks go out;
 //   R  the layer input is staged (fp32 for the router, fp16 in the permuted
 //      K order for the MMAs; with the pre-norm join it is RMSNorm of the
-//      residual row, never rounded to bf16); the router rows b + G*w give
-//      logits, stored straight to global memory; a block with a shared item
-//      computes the shared gate;
-//   1  blocks with routed items poll the T logit rows until no entry holds
-//      the sentinel the prelude wrote (no grid barrier: the wait is on the
-//      data itself), select the top-k and build the slot table;
-//   2  items: gate/up (the 16 warps split K), one block barrier, four warps
-//      add the partial sums in a fixed order and form h = w silu(gate) up in
-//      shared memory (the routing weight, or the shared gate, folded in),
-//      another barrier, then every warp adds its W_down rows times h into its
-//      register sums;
-//   3  every block stores its sums and arrives on one counter; blocks owning
-//      16 output rows wait for every arrival and add the blocks' sums in
-//      block order: y (fp32), and the next residual row bf16(r + y) when
-//      asked for.
-//
-// Weights reach shared memory by cp.async, each warp loading exactly the
-// bytes it will use into a two-slot ring of its own (an item's gate/up part
-// and its down part), so copies of the next part overlap the current part's
-// arithmetic and no warp waits on another warp's copies.
+//      residual row, never rounded to bf16); logits are stored straight to
+//      global memory; a block with a shared item computes the shared gate
+//      and its shared item;
+//   1  blocks with routed work poll the T logit rows until no entry holds
+//      the sentinel, select the top-k and build the slot table;
+//   2  routed gate/up items;
+//   3  down: slot by slot as the counters complete (h staged in shared
+//      memory in batches), then the fixed-order sum into y and the next
+//      residual row bf16(r + y) when asked for.
 //
 // Products on mma.sync.m16n8k16 (fp16 operands, fp32 accumulation): 16
-// weight rows x 8 token columns per instruction. Gate/up: the 16 MMA rows are
-// 8 gate rows then the matching 8 up rows, so the lane holding gate(n, t)
-// also holds up(n, t). Each lane dequantises whole code words into A
-// fragments; one word unpacks as the pairs (k0,k4), (k1,k5), (k2,k6), (k3,k7),
-// so x and h are kept in that K order inside every group of 8
-// (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte shared-memory load.
+// weight rows x 8 token columns per instruction. Each lane dequantises whole
+// code words into A fragments; one word unpacks as the pairs (k0,k4),
+// (k1,k5), (k2,k6), (k3,k7), so x and h are kept in that K order inside every
+// group of 8 (0,4,1,5,2,6,3,7) and a B fragment is one 16-byte load.
 #include <atomic>
 
 #include "kernels.h"
@@ -60,22 +63,17 @@ namespace bgmoe {
 constexpr int kDecWarps = 16;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kDecMaxA = kDecodeMaxTokens * kMaxTopK;
-constexpr int kDecMaxSlots = kDecMaxA + 1;
-constexpr int kItemCols = 32;                   // h columns per item
-constexpr int kUnits = kItemCols / 8;           // MMA units of 8 h columns (8 gate + 8 up rows)
-constexpr int kGuTaskBytes = 16 * 64 + 16 * 8;  // 16 code rows x 128 K, and their scale and bias pairs
-constexpr int kDnTileBytes = 16 * 16 + 16 * 8;  // 16 W_down rows x 32 K, and their scale and bias pairs
-constexpr int kMaxDnTiles = 8;                  // W_down tiles of 16 rows per warp (H <= 2048)
-constexpr int kDnTilesPerTask = 4;              // W_down tiles per down task (two down tasks per item)
-constexpr int kTaskBytes = kDnTilesPerTask * kDnTileBytes;  // one ring slot (>= kGuTaskBytes)
-constexpr int kSlots = 6;                       // ring slots per warp: a whole item at H = 2048
-static_assert(kGuTaskBytes <= kTaskBytes, "a gate/up task must fit a ring slot");
-constexpr int kDecMaxH = kDecWarps * 16 * kMaxDnTiles;
-constexpr int kGateWarp = kDecWarps - 1;        // computes the shared gate in blocks with a shared item
+constexpr int kItemCols = 32;                 // h columns per gate/up item
+constexpr int kUnits = kItemCols / 8;         // MMA units of 8 h columns (8 gate + 8 up rows)
+constexpr int kTaskBytes = 16 * 64 + 16 * 8;  // 16 code rows x 128 K, their scale and bias pairs
+constexpr int kSlots = 6;                     // ring slots per warp
+constexpr int kDecMaxI = 1024;                // shared down tasks: one per warp at most (I / 128 <= 8)
+constexpr int kGateWarp = kDecWarps - 1;      // computes the shared gate in blocks with a shared item
 // The prelude fills the logits with this pattern; fp32 arithmetic never
 // produces it (a NaN result is 0x7FFFFFFF), so a reader that sees any other
 // value sees the router's output.
 constexpr uint32_t kLogitSentinel = 0xFFFFFFFFu;
+static_assert(kDecodeMaxSlots >= kDecMaxA + 1, "slot counters");
 
 struct DecodeSmall {
   int ids[kDecMaxA];
@@ -83,15 +81,14 @@ struct DecodeSmall {
   float g[kDecodeMaxTokens];                   // shared gate per token
   float inv_rms[kDecodeMaxTokens];             // 1 / rms of each token's residual row (pre-norm join)
   int pos[kDecMaxA];                           // expert-sorted position of assignment a
-  int slot_e[kDecMaxSlots];                    // expert of each slot (slot 0 = shared when present)
-  int slot_n[kDecMaxSlots];                    // rows (tokens) of the slot
-  int slot_row[kDecMaxSlots][kDecodeMaxTokens];
-  float slot_wt[kDecMaxSlots][kDecodeMaxTokens];  // weight of token t in the slot (0: not routed there)
-  const uint8_t* slot_src[kDecMaxSlots][6];    // gate/up codes, scales, biases; down codes, scales, biases
+  int slot_e[kDecodeMaxSlots];                 // expert of each slot (slot 0 = shared when present)
+  int slot_n[kDecodeMaxSlots];                 // rows (tokens) of the slot
+  int slot_row[kDecodeMaxSlots][kDecodeMaxTokens];
+  float slot_wt[kDecodeMaxSlots][kDecodeMaxTokens];  // weight of token t in the slot (0: not routed there)
+  const uint8_t* slot_src[kDecodeMaxSlots][6];  // gate/up codes, scales, biases; down codes, scales, biases
   int nslots;
-  int failed;        // a logit poll or the final wait ran out
+  int failed;        // a logit poll or a counter wait ran out
   int range;         // an fp16 operand (x or h) left the fp16 range
-  unsigned nb;       // blocks holding down-projection sums
 };
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -112,7 +109,7 @@ __device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
   asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-// Arrival on a counter: release orders the block's earlier writes (made
+// Counts on a counter: release orders the block's earlier writes (made
 // visible to this thread by the preceding block barrier) before the add.
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -123,6 +120,20 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(tc::smem_u32(dst)), "l"(src) : "memory");
+}
+
+// Waits until at most n of this thread's most recent cp.async groups are
+// pending (every older group has landed).
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n <= 0 ? 0 : n) {
+    case 0: tc::cp_async_wait<0>(); break;
+    case 1: tc::cp_async_wait<1>(); break;
+    case 2: tc::cp_async_wait<2>(); break;
+    case 3: tc::cp_async_wait<3>(); break;
+    case 4: tc::cp_async_wait<4>(); break;
+    case 5: tc::cp_async_wait<5>(); break;
+    default: tc::cp_async_wait<6>(); break;
+  }
 }
 
 // d += A * B with A 16x16 (row), B 16x8 (col), fp16 in, fp32 accumulate.
@@ -140,13 +151,20 @@ __device__ __forceinline__ __half2 bf16_h2(uint16_t bits16) {
   return __halves2half2(h, h);
 }
 
-// The 32 K of one lane's 16-byte code chunk for its two rows (fragment rows g
-// and g+8) against the matching B fragments xb[w] (permuted activations,
-// 8 K per 16-byte word): 8 MMAs. With g = lane / 4 and c = lane % 4, MMA k
-// slots 2c, 2c+1, 2c+8, 2c+9 of word w hold K offsets 8w + {0,4}, {1,5} (first
-// MMA) and 8w + {2,6}, {3,7} (second), on A and B alike.
-__device__ __forceinline__ void mma_chunk(float (&d)[4], const uint4& r0, const uint4& r1, __half2 s0, __half2 b0,
-                                          __half2 s1, __half2 b1, const uint4 (&xb)[4]) {
+// One task's products: this lane's 32 K of fragment rows g and g+8 (16-byte
+// code chunks at c * 16 of rows g and g + 8 of the slot, their scale and
+// bias from the slot's pair of groups) against the B fragments xb[w]
+// (permuted activations, 8 K per 16-byte word): 8 MMAs. With g = lane / 4
+// and c = lane % 4, MMA k slots 2c, 2c+1, 2c+8, 2c+9 of word w hold K
+// offsets 8w + {0,4}, {1,5} (first MMA) and 8w + {2,6}, {3,7} (second), on A
+// and B alike.
+__device__ __forceinline__ void task_mma(float (&d)[4], const uint8_t* t, int g8, int c4, const uint4 (&xb)[4]) {
+  const uint4 r0 = *reinterpret_cast<const uint4*>(t + g8 * 64 + c4 * 16);
+  const uint4 r1 = *reinterpret_cast<const uint4*>(t + (8 + g8) * 64 + c4 * 16);
+  const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 1024);  // per row: scale pair, bias pair
+  const int gs = c4 >> 1;  // this lane's 32 K lie in the second group of the pair when c >= 2
+  const __half2 s0 = bf16_h2(sb[g8 * 4 + gs]), b0 = bf16_h2(sb[g8 * 4 + 2 + gs]);
+  const __half2 s1 = bf16_h2(sb[(8 + g8) * 4 + gs]), b1 = bf16_h2(sb[(8 + g8) * 4 + 2 + gs]);
   const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -156,6 +174,22 @@ __device__ __forceinline__ void mma_chunk(float (&d)[4], const uint4& r0, const 
     mma_16816(d, p0[0], p1[0], p0[1], p1[1], xb[w].x, xb[w].y);
     mma_16816(d, p0[2], p1[2], p0[3], p1[3], xb[w].z, xb[w].w);
   }
+}
+
+// Copies of one task: 16 rows of a packed matrix (rows lo .. lo + 7, then
+// hi .. hi + 7), K block kb (64 bytes of codes per row), and the scale and
+// bias pairs of groups 2kb, 2kb+1 of each row.
+__device__ __forceinline__ void task_copy(uint8_t* td, const uint8_t* codes, const uint16_t* sc, const uint16_t* bi,
+                                          int lo, int hi, int row_bytes, int gpr, int kb, int lane) {
+#pragma unroll
+  for (int q0 = 0; q0 < 64; q0 += 32) {  // 16 rows x 4 pieces of 16 bytes
+    const int q = q0 + lane, r = q >> 2, piece = q & 3;
+    const int row = (r < 8 ? lo : hi) + (r & 7);
+    cp_async16(td + r * 64 + piece * 16, codes + (size_t)row * row_bytes + kb * 64 + piece * 16);
+  }
+  const int r = lane >> 1, kind = lane & 1;
+  const int row = (r < 8 ? lo : hi) + (r & 7);
+  cp_async4(td + 1024 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)row * gpr + 2 * kb);
 }
 
 // x[t] . row for the router: lane l holds bf16 elements 8 (l + 32 q) .. +7 of
@@ -199,15 +233,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   const int sh = a.shared ? 1 : 0;
   const int G = gridDim.x, b = blockIdx.x;
   const int gpr = H / kGroup, igpr = I / kGroup;
-  const int cpi = I / kItemCols;     // items per slot
-  const int nkb = H / 128;           // gate/up K blocks of 128
-  const int mtiles = H / 16;         // W_down tiles of 16 output rows
-  const size_t slot_bytes = (size_t)a.slot_bytes;
-  uint8_t* ring = dsm_raw + (size_t)warp * slot_bytes;              // this warp's ring of kSlots tasks
-  __half* x16 = reinterpret_cast<__half*>(dsm_raw + a.x16_offset);   // [T][H] fp16, K-permuted
-  float* xf = reinterpret_cast<float*>(dsm_raw + a.xf_offset);      // [T][H] fp32 layer input
-  float* part = reinterpret_cast<float*>(dsm_raw + a.part_offset);   // [16 warps][4][32]
-  __half* hs = reinterpret_cast<__half*>(dsm_raw + a.hs_offset);     // [8 tokens][32 columns]
+  const int cpi = I / kItemCols;     // gate/up items per slot
+  const int nkb = H / 128;           // gate/up K blocks of 128 (4 per item and warp at H = 2048)
+  const int dkb = I / 128;           // down K blocks of 128 per slot
+  const int tpw = nkb / 4;           // gate/up tasks per item and warp (H % 512 == 0)
+  const bool has_rows = b < H / 16;  // this block owns output rows 16b .. 16b + 15
+  uint8_t* ring = dsm_raw + (size_t)warp * kSlots * kTaskBytes;        // this warp's ring
+  uint8_t* sdn = dsm_raw + a.sdn_offset;                                // shared down tasks [dkb][kTaskBytes]
+  __half* x16 = reinterpret_cast<__half*>(dsm_raw + a.x16_offset);     // [T][H] fp16, K-permuted
+  float* xf = reinterpret_cast<float*>(dsm_raw + a.xf_offset);         // [T][H] fp32 layer input
+  __half* hst = reinterpret_cast<__half*>(dsm_raw + a.x16_offset);     // down phase: h of a batch of slots
+  float* part = reinterpret_cast<float*>(dsm_raw + a.part_offset);     // [16 warps][4][32]
   const uint64_t deadline = global_timer_ns() + (uint64_t)a.timeout_ns;
 
   if (tid == 0) {
@@ -225,85 +261,53 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       S.slot_src[0][5] = reinterpret_cast<const uint8_t*>(a.dn.s_biases);
     }
   }
-  for (int i = tid; i < kDecMaxSlots * kDecodeMaxTokens; i += kDecThreads) (&S.slot_wt[0][0])[i] = 0.f;
-  for (int i = tid; i < 8 * kItemCols / 2; i += kDecThreads) reinterpret_cast<uint32_t*>(hs)[i] = 0u;
+  for (int i = tid; i < kDecodeMaxSlots * kDecodeMaxTokens; i += kDecThreads) (&S.slot_wt[0][0])[i] = 0.f;
   __syncthreads();
 
-  // ---- this warp's tasks, in order: for each of the block's items, its
-  // gate/up tasks (unit u = warp % 4, i.e. h columns n0 + 8u .. +7 as gate
-  // rows and up rows, one K block kb = warp / 4 + 4 jj each), then two down
-  // tasks (W_down tiles 16 (warp + 16 i) .. +15, i = 4 d .. 4 d + 3, columns
-  // n0 .. n0 + 31). Each task's bytes are one cp.async group in one slot of
-  // the warp's ring, so a task is computed as soon as its own bytes land.
-  const int ngu = (warp >> 2) < nkb ? (nkb - (warp >> 2) + 3) / 4 : 0;  // gate/up tasks per item
-  const int tpi = ngu + 2;                                                 // tasks per item
-  auto issue_gu = [&](int item, int jj, uint8_t* td) {
-    const int s = item / cpi, n0 = (item - s * cpi) * kItemCols;
-    const uint8_t* codes = S.slot_src[s][0];
-    const uint16_t* sc = reinterpret_cast<const uint16_t*>(S.slot_src[s][1]);
-    const uint16_t* bi = reinterpret_cast<const uint16_t*>(S.slot_src[s][2]);
-    const int u = warp & 3, kb = (warp >> 2) + 4 * jj;
-#pragma unroll
-    for (int q0 = 0; q0 < 64; q0 += 32) {  // 16 rows x 4 pieces of 16 bytes
-      const int q = q0 + lane, r = q >> 2, piece = q & 3;
-      const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
-      cp_async16(td + r * 64 + piece * 16, codes + (size_t)row * (H / 2) + kb * 64 + piece * 16);
-    }
-    {  // scale and bias pairs of groups 2kb, 2kb+1 of the 16 rows
-      const int r = lane >> 1, kind = lane & 1;
-      const int row = r < 8 ? n0 + 8 * u + r : I + n0 + 8 * u + r - 8;
-      cp_async4(td + 1024 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)row * gpr + 2 * kb);
-    }
-  };
-  auto issue_dn = [&](int item, int dt, uint8_t* td) {
-    const int s = item / cpi, c = item - s * cpi;
-    const uint8_t* codes = S.slot_src[s][3];
-    const uint16_t* sc = reinterpret_cast<const uint16_t*>(S.slot_src[s][4]);
-    const uint16_t* bi = reinterpret_cast<const uint16_t*>(S.slot_src[s][5]);
-    const int gp = (c >> 1) & ~1;  // the aligned pair of groups holding this item's group
-#pragma unroll
-    for (int q0 = 0; q0 < 16 * kDnTilesPerTask; q0 += 32) {  // 16 bytes of codes per row
-      const int q = q0 + lane, i = q >> 4, r = q & 15, tile = warp + 16 * (kDnTilesPerTask * dt + i);
-      if (tile < mtiles) cp_async16(td + i * kDnTileBytes + r * 16, codes + (size_t)(16 * tile + r) * (I / 2) + c * 16);
-    }
-#pragma unroll
-    for (int q0 = 0; q0 < 32 * kDnTilesPerTask; q0 += 32) {  // scale and bias pairs
-      const int q = q0 + lane, i = q >> 5, r = (q & 31) >> 1, kind = q & 1;
-      const int tile = warp + 16 * (kDnTilesPerTask * dt + i);
-      if (tile < mtiles)
-        cp_async4(td + i * kDnTileBytes + 256 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)(16 * tile + r) * igpr + gp);
-    }
-  };
-  int issued = 0;  // tasks issued by this warp (one cp.async group each)
+  // ---- this warp's ring of tasks, in order: for each of the block's gate/up
+  // items, its tasks (unit u = warp % 4: gate rows n0 + 8u .. +7 and the up
+  // rows I + n0 + 8u .. +7; K blocks kb = (warp / 4) tpw + jj), then its
+  // routed down tasks (slot s >= sh, K block kc, task number
+  // q = (s - sh) dkb + kc taken by warp q % 16).
+  int n_items = 0, n_dn = 0;  // set once the slots are known
   auto issue_task = [&](int k) {
-    const int j = k / tpi, t = k - j * tpi;
     uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
-    if (t < ngu) issue_gu(b + G * j, t, td);
-    else issue_dn(b + G * j, t - ngu, td);
+    if (k < n_items * tpw) {
+      const int j = k / tpw, jj = k - j * tpw;
+      const int item = b + G * j, s = item / cpi, n0 = (item - s * cpi) * kItemCols;
+      const int u = warp & 3, kb = (warp >> 2) * tpw + jj;
+      task_copy(td, S.slot_src[s][0], reinterpret_cast<const uint16_t*>(S.slot_src[s][1]),
+                reinterpret_cast<const uint16_t*>(S.slot_src[s][2]), n0 + 8 * u, I + n0 + 8 * u, H / 2, gpr, kb,
+                lane);
+    } else {
+      const int q = warp + kDecWarps * (k - n_items * tpw);
+      const int s = sh + q / dkb, kc = q - (s - sh) * dkb;
+      task_copy(td, S.slot_src[s][3], reinterpret_cast<const uint16_t*>(S.slot_src[s][4]),
+                reinterpret_cast<const uint16_t*>(S.slot_src[s][5]), 16 * b, 16 * b + 8, I / 2, igpr, kc, lane);
+    }
     tc::cp_async_commit();
   };
-  // Task k's bytes have landed (every later group may still be in flight),
-  // and every lane of the warp sees them.
-  auto wait_task = [&](int k) {
-    switch (issued - k - 1) {
-      case 0: tc::cp_async_wait<0>(); break;
-      case 1: tc::cp_async_wait<1>(); break;
-      case 2: tc::cp_async_wait<2>(); break;
-      case 3: tc::cp_async_wait<3>(); break;
-      case 4: tc::cp_async_wait<4>(); break;
-      default: tc::cp_async_wait<kSlots - 1>(); break;
-    }
+  int issued = 0;  // tasks issued by this warp (one cp.async group each)
+  auto wait_task = [&](int k) {  // task k's bytes have landed, for every lane
+    cp_async_wait_dyn(issued - k - 1);
     __syncwarp();
   };
 
-  // ---- phase 0: weights only (they do not depend on the previous kernel).
-  // Blocks with a shared item start its copies; the router rows go to the
-  // other blocks (their x arrives without queueing behind those copies).
+  // ---- phase 0: weights only (they do not depend on the previous kernel)
   const bool shared_first = sh && b < cpi;
-  if (shared_first)
-    for (; issued < tpi && issued < kSlots; ++issued) issue_task(issued);
-  const int sfb = sh ? (cpi < G ? cpi : 0) : 0;  // blocks with a shared item (none hold router rows)
-  const int RG = G - sfb;                        // router blocks
+  if (sh && has_rows && warp < dkb) {  // the shared down task of K block `warp`
+    task_copy(sdn + (size_t)warp * kTaskBytes, S.slot_src[0][3], reinterpret_cast<const uint16_t*>(S.slot_src[0][4]),
+              reinterpret_cast<const uint16_t*>(S.slot_src[0][5]), 16 * b, 16 * b + 8, I / 2, igpr, warp, lane);
+    tc::cp_async_commit();
+  }
+  if (shared_first) {
+    n_items = 1;  // the shared item (more items, if any, are counted after routing)
+    for (; issued < tpw && issued < kSlots; ++issued) issue_task(issued);
+  }
+  // router rows on the blocks without a shared item (their x loads then do
+  // not queue behind those copies)
+  const int sfb = sh ? (cpi < G ? cpi : 0) : 0;
+  const int RG = G - sfb;
   const int rrows = E + sh, rvec = H / 8;
   const int rrow = b - sfb + RG * warp;
   const bool router_warp = b >= sfb && rrow < rrows && warp != kGateWarp;
@@ -405,11 +409,63 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   // The next call's prelude may launch now: it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // ---- phase 1: top-k and slots, where this block may hold routed items.
-  // A block whose only item is its shared one skips it (every item index
-  // past its first is beyond the largest possible item count).
+  // One gate/up item: tasks k0 .. k0 + tpw - 1 of this warp's ring; then h
+  // to the workspace and the item counted on its slot's counter.
+  auto run_item = [&](int j, int k0) {
+    const int item = b + G * j, s = item / cpi, n0 = (item - s * cpi) * kItemCols;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int jj = 0; jj < tpw; ++jj) {
+      const int k = k0 + jj;
+      wait_task(k);
+      const int kb = (warp >> 2) * tpw + jj;
+      uint4 xb[4];
+      const __half* xrow = x16 + (size_t)(g8 < T ? g8 : 0) * H + kb * 128 + 32 * c4;
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(xrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+      task_mma(d, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb);
+      __syncwarp();  // the slot is read: refill it
+      if (issued < n_items * tpw + n_dn) issue_task(issued++);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r];
+    __syncthreads();
+    if (warp < kUnits) {
+      // unit u = warp: warps u, u+4, u+8, u+12 hold its partial sums (fixed
+      // order). d0, d1: gate(column 8u + g, tokens 2c, 2c+1); d2, d3: up.
+      float v[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        v[r] = ((part[(warp * 4 + r) * 32 + lane] + part[((warp + 4) * 4 + r) * 32 + lane]) +
+                part[((warp + 8) * 4 + r) * 32 + lane]) +
+               part[((warp + 12) * 4 + r) * 32 + lane];
+      const int pc = tc::perm8_pos(n0 + 8 * warp + g8);
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int t = 2 * c4 + jj;
+        if (t < T) {
+          const __half hv = __float2half_rn(silu_f32(v[jj]) * v[2 + jj] * S.slot_wt[s][t]);
+          if (__hisinf(hv)) S.range = 1;
+          a.h[((size_t)s * T + t) * I + pc] = hv;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && b != a.stall_block) red_release_add(a.cnt + s, 1u);
+  };
+
+  int k = 0;  // next task of this warp's ring
+  if (shared_first) {
+    run_item(0, 0);
+    k = tpw;
+  }
+
+  // ---- phase 1: top-k and slots, where this block has routed work: routed
+  // items (past its shared one) or output rows. A block with neither skips
+  // it, except the last block, which writes the routing outputs.
   const int max_items = ((A < E ? A : E) + sh) * cpi;
-  const bool need_topk = !(shared_first && b + G >= max_items && b != G - 1);
+  const bool routed_items = b + (shared_first ? G : 0) < max_items;
+  const bool need_topk = routed_items || has_rows || b == G - 1;
   if (need_topk) {
     if (warp < T) {
       const float* lrow = a.logits + (size_t)warp * (E + 1);
@@ -489,12 +545,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     __syncthreads();
     if (S.failed && tid == 0) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
   }
-  const int items = S.failed ? 0 : S.nslots * cpi;
-  const int nitems = b < items ? (items - b + G - 1) / G : 0;
+  const bool routed = need_topk && !S.failed;
+  const int nslots = routed ? S.nslots : sh;
+  const int items = nslots * cpi;
+  n_items = b < items ? (items - b + G - 1) / G : 0;
+  // routed down tasks of this warp: q = warp, warp + 16, ... < (nslots - sh) dkb
+  const int nq = has_rows && routed ? (nslots - sh) * dkb : 0;
+  n_dn = nq > warp ? (nq - warp + kDecWarps - 1) / kDecWarps : 0;
 
   // The routing outputs (same definitions as moe_route), written by the last
-  // block, which holds no item at T = 1.
-  if (b == G - 1 && !S.failed) {
+  // block.
+  if (b == G - 1 && routed) {
     for (int i = tid; i < A; i += kDecThreads) {
       a.ids[i] = S.ids[i];
       a.weights[i] = S.w[i];
@@ -529,158 +590,88 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     }
   }
 
-  // ---- phase 2: this block's items b, b + G, ..., task by task
-  float acc[kMaxDnTiles][4];
-#pragma unroll
-  for (int i = 0; i < kMaxDnTiles; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-  const int ntasks = nitems * tpi;
-  for (; issued < ntasks && issued < kSlots; ++issued) issue_task(issued);
-  int k = 0;  // next task of this warp
-  for (int j = 0; j < nitems; ++j) {
-    const int item = b + G * j;
-    const int s = item / cpi;
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int jj = 0; jj < ngu; ++jj, ++k) {
-      wait_task(k);
-      const uint8_t* t = ring + (size_t)(k % kSlots) * kTaskBytes;
-      const int kb = (warp >> 2) + 4 * jj;
-      uint4 xb[4];
-      const __half* xrow = x16 + (size_t)(g8 < T ? g8 : 0) * H + kb * 128 + 32 * c4;
-#pragma unroll
-      for (int w = 0; w < 4; ++w)
-        xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(xrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-      const uint4 cg = *reinterpret_cast<const uint4*>(t + g8 * 64 + c4 * 16);
-      const uint4 cu = *reinterpret_cast<const uint4*>(t + (8 + g8) * 64 + c4 * 16);
-      const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 1024);  // per row: scale pair, bias pair
-      const int gs = c4 >> 1;  // this lane's 32 K lie in group 2kb + gs
-      mma_chunk(d, cg, cu, bf16_h2(sb[g8 * 4 + gs]), bf16_h2(sb[g8 * 4 + 2 + gs]), bf16_h2(sb[(8 + g8) * 4 + gs]),
-                bf16_h2(sb[(8 + g8) * 4 + 2 + gs]), xb);
-      __syncwarp();  // the slot is read: refill it
-      if (issued < ntasks) issue_task(issued++);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r];
-    __syncthreads();
-    if (warp < kUnits) {
-      // unit u = warp: warps u, u+4, u+8, u+12 hold its partial sums (fixed
-      // order). d0, d1: gate(column 8u + g, tokens 2c, 2c+1); d2, d3: up.
-      float v[4];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        v[r] = ((part[(warp * 4 + r) * 32 + lane] + part[((warp + 4) * 4 + r) * 32 + lane]) +
-                part[((warp + 8) * 4 + r) * 32 + lane]) +
-               part[((warp + 12) * 4 + r) * 32 + lane];
-      const int pc = tc::perm8_pos(8 * warp + g8);
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int t = 2 * c4 + jj;
-        if (t < T) {
-          const __half hv = __float2half_rn(silu_f32(v[jj]) * v[2 + jj] * S.slot_wt[s][t]);
-          if (__hisinf(hv)) S.range = 1;
-          hs[t * kItemCols + pc] = hv;
-        }
-      }
-    }
-    __syncthreads();
-    const uint4 hb = *reinterpret_cast<const uint4*>(hs + g8 * kItemCols + 8 * c4);  // token g (zero if >= T)
-    const int gs = ((item - s * cpi) >> 1) & 1;  // this item's group within the loaded pair
-#pragma unroll
-    for (int dt = 0; dt < kMaxDnTiles / kDnTilesPerTask; ++dt, ++k) {
-      wait_task(k);
-      const uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
-#pragma unroll
-      for (int i = 0; i < kDnTilesPerTask; ++i)
-        if (warp + 16 * (kDnTilesPerTask * dt + i) < mtiles) {
-          const uint8_t* t = td + i * kDnTileBytes;
-          const uint32_t c0 = *reinterpret_cast<const uint32_t*>(t + g8 * 16 + c4 * 4);
-          const uint32_t c1 = *reinterpret_cast<const uint32_t*>(t + (8 + g8) * 16 + c4 * 4);
-          const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 256);
-          uint32_t p0[4], p1[4];
-          tc::dequant8_f16(c0, bf16_h2(sb[g8 * 4 + gs]), bf16_h2(sb[g8 * 4 + 2 + gs]), p0);
-          tc::dequant8_f16(c1, bf16_h2(sb[(8 + g8) * 4 + gs]), bf16_h2(sb[(8 + g8) * 4 + 2 + gs]), p1);
-          float (&ac)[4] = acc[kDnTilesPerTask * dt + i];
-          mma_16816(ac, p0[0], p1[0], p0[1], p1[1], hb.x, hb.y);
-          mma_16816(ac, p0[2], p1[2], p0[3], p1[3], hb.z, hb.w);
-        }
-      __syncwarp();
-      if (issued < ntasks) issue_task(issued++);
-    }
+  // ---- phase 2: the routed gate/up items
+  const int ntasks = n_items * tpw + n_dn;
+  for (; issued < ntasks && issued - k < kSlots; ++issued) issue_task(issued);
+  for (int j = shared_first ? 1 : 0; j < n_items; ++j) {
+    run_item(j, k);
+    k += tpw;
   }
-  tc::cp_async_wait_all();  // no copy into this block's shared memory outlives it
 
-  // ---- phase 3: this block's sums, one arrival, the fixed-order reduction
-  if (nitems > 0) {
-    float* P = a.partial + (size_t)b * T * H;
-#pragma unroll
-    for (int i = 0; i < kMaxDnTiles; ++i) {
-      const int tile = warp + 16 * i;
-      if (tile < mtiles) {
-        const int m0 = 16 * tile + g8, t0 = 2 * c4;
-        if (t0 < T) {
-          P[(size_t)t0 * H + m0] = acc[i][0];
-          P[(size_t)t0 * H + m0 + 8] = acc[i][2];
-        }
-        if (t0 + 1 < T) {
-          P[(size_t)(t0 + 1) * H + m0] = acc[i][1];
-          P[(size_t)(t0 + 1) * H + m0 + 8] = acc[i][3];
+  // ---- phase 3: down, for the blocks with output rows
+  if (has_rows && routed) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows g, g+8 x tokens 2c, 2c+1, over this warp's down tasks
+    const int hb_bytes = T * I * 2;
+    const int batch = (int)(a.hst_bytes / hb_bytes);  // slots whose h fits in shared memory at once
+    for (int s0 = 0; s0 < nslots; s0 += batch) {
+      const int s1 = min(nslots, s0 + batch);
+      // every item of these slots counted (one thread per slot)
+      if (tid >= s0 && tid < s1) {
+        const unsigned want = (unsigned)cpi;
+        while (ld_acquire_u32(a.cnt + tid) < want) {
+          if (global_timer_ns() > deadline) {
+            S.failed = 1;
+            break;
+          }
+          __nanosleep(32);
         }
       }
-    }
-  }
-  // Each warp arrives once its own sums are stored (warp 0 also counts the
-  // block among those holding sums); no block barrier on this path.
-  __syncwarp();
-  if (lane == 0 && b != a.stall_block)
-    red_release_add(a.bar, 1u + (warp == 0 && nitems > 0 ? (1u << 16) : 0u));
-  __syncthreads();
-  if (tid == 0 && S.range) atomicCAS(a.status, 0, (int32_t)MOE_ERR_RANGE);
-  if (b >= mtiles) return;  // no output rows here
-  if (tid == 0) {
-    unsigned v = 0;
-    while (((v = ld_acquire_u32(a.bar)) & 0xFFFFu) < (unsigned)(G * kDecWarps)) {
-      if (global_timer_ns() > deadline) {
-        S.failed = 1;
-        break;
+      __syncthreads();
+      if (S.failed) break;
+      // h of the batch (fp16 [slot][T][I], K-permuted), read past L1
+      for (int i = tid; i < (s1 - s0) * hb_bytes / 16; i += kDecThreads)
+        reinterpret_cast<uint4*>(hst)[i] = __ldcg(reinterpret_cast<const uint4*>(a.h + (size_t)s0 * T * I) + i);
+      __syncthreads();
+      // the shared slot's tasks from their own buffer
+      if (s0 == 0 && sh && warp < dkb) {
+        cp_async_wait_dyn(issued);  // the oldest group: the shared down task
+        __syncwarp();
+        uint4 xb[4];
+        const __half* hrow = hst + (size_t)(g8 < T ? g8 : 0) * I + warp * 128 + 32 * c4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+        task_mma(acc, sdn + (size_t)warp * kTaskBytes, g8, c4, xb);
       }
-      __nanosleep(32);
+      // the routed slots' tasks of this batch, in ring order
+      for (; k < ntasks; ++k) {
+        const int q = warp + kDecWarps * (k - n_items * tpw);
+        const int s = sh + q / dkb, kc = q - (s - sh) * dkb;
+        if (s >= s1) break;
+        wait_task(k);
+        uint4 xb[4];
+        const __half* hrow = hst + ((size_t)(s - s0) * T + (g8 < T ? g8 : 0)) * I + kc * 128 + 32 * c4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+        task_mma(acc, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb);
+        __syncwarp();
+        if (issued < ntasks) issue_task(issued++);
+      }
+      __syncthreads();  // the batch's h is read
     }
-    S.nb = v >> 16;
-    if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
-  }
-  __syncthreads();
-  if (S.failed) return;
-  const int nb = (int)S.nb;
-  float* red = reinterpret_cast<float*>(dsm_raw);  // [32][T][16] (the ring is no longer in use)
-  const int ml = tid & 15, bl = tid >> 4;
-  for (int slice = b; slice < mtiles; slice += G) {
-    const int m = 16 * slice + ml;
-    float v[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
-    constexpr int kMaxPer = (kMaxDecodeBlocks + 31) / 32;
-    float pv[kMaxPer][kDecodeMaxTokens];
+    // the 16 warps' sums in a fixed order: y and the next residual row
 #pragma unroll
-    for (int k = 0; k < kMaxPer; ++k)  // every load before any use
-#pragma unroll
-      for (int t = 0; t < kDecodeMaxTokens; ++t)
-        pv[k][t] = (bl + 32 * k < nb && t < T) ? __ldcg(a.partial + ((size_t)(bl + 32 * k) * T + t) * H + m) : 0.f;
-#pragma unroll
-    for (int k = 0; k < kMaxPer; ++k)
-#pragma unroll
-      for (int t = 0; t < kDecodeMaxTokens; ++t) v[t] += pv[k][t];
-#pragma unroll
-    for (int t = 0; t < kDecodeMaxTokens; ++t)
-      if (t < T) red[(bl * T + t) * 16 + ml] = v[t];
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = acc[r];
     __syncthreads();
-    if (tid < 16 * T) {
-      const int t = tid >> 4;
+    if (!S.failed && tid < 16 * T) {
+      const int t = tid >> 4, row = tid & 15;
+      const int ln = (row & 7) * 4 + (t >> 1), r = (t & 1) + ((row >> 3) << 1);
       float y = 0.f;
-      for (int q = 0; q < 32; ++q) y += red[(q * T + t) * 16 + ml];  // fixed order
+      for (int w = 0; w < kDecWarps; ++w) y += part[(w * 4 + r) * 32 + ln];
+      const int m = 16 * b + row;
       a.y[(size_t)t * H + m] = y;
       if (a.x_next) {
         const float xv = bf16_bits_to_f32(a.x[(size_t)t * H + m]);
         a.x_next[(size_t)t * H + m] = __bfloat16_as_ushort(__float2bfloat16_rn(xv + y));
       }
     }
-    __syncthreads();
+  }
+  tc::cp_async_wait_all();  // no copy into this block's shared memory outlives it
+  __syncthreads();
+  if (tid == 0) {
+    if (S.failed) atomicExch(a.status, (int32_t)MOE_ERR_DEVICE_TIMEOUT);
+    else if (S.range) atomicCAS(a.status, 0, (int32_t)MOE_ERR_RANGE);
   }
 }
 
@@ -698,59 +689,57 @@ int sm_count(int dev) {
 
 constexpr size_t kDecDynamicLimit = 220 * 1024;  // 227 KB per block minus the static part
 
-// Dynamic shared memory: 16 warps x kSlots task slots, x16 fp16 and x fp32
-// [T][H], the partial sums of the gate/up reduction, h of one item.
+// Dynamic shared memory: 16 warps x kSlots task slots, the shared down
+// tasks, x16 fp16 and x fp32 [T][H] (in the down phase: h of a batch of
+// slots), the partial sums of the gate/up reduction and of the final sum.
 struct DecodeLayout {
-  size_t slot_bytes, x16_offset, xf_offset, part_offset, hs_offset, total;
+  size_t sdn_offset, x16_offset, xf_offset, part_offset, hst_bytes, total;
 };
 
 DecodeLayout decode_layout(const Geometry& g) {
   DecodeLayout L{};
-  L.slot_bytes = (size_t)kSlots * kTaskBytes;  // one warp's ring
+  L.sdn_offset = (size_t)kDecWarps * kSlots * kTaskBytes;
+  L.x16_offset = L.sdn_offset + (size_t)(g.I / 128) * kTaskBytes;
   const size_t xb = ((size_t)g.T * g.H * 2 + 127) & ~size_t(127);
-  L.x16_offset = (size_t)kDecWarps * L.slot_bytes;
   L.xf_offset = L.x16_offset + xb;
   L.part_offset = L.xf_offset + 2 * xb;
-  L.hs_offset = L.part_offset + (size_t)kDecWarps * 4 * 32 * 4;
-  L.total = L.hs_offset + 8 * kItemCols * 2;
-  const size_t red = (size_t)32 * kDecodeMaxTokens * 16 * 4;  // the final reduction reuses the ring
-  if (L.total < red) L.total = red;
+  L.hst_bytes = 3 * xb;  // x16 and xf, reused for h
+  L.total = L.part_offset + (size_t)kDecWarps * 4 * 32 * 4;
   return L;
 }
 }  // namespace
 
 // One block per SM, every block resident (blocks wait for each other's
-// logits and sums); K of gate/up in whole 128-wide blocks, H at most 2048
-// (each warp keeps at most 8 tiles of output sums in registers), I in whole
-// 128-wide blocks, enough router warps (15 per block without a shared item)
-// for the E (+ 1) router rows.
+// logits and h); H a multiple of 512 up to 2048 (each warp takes a quarter of
+// K in whole 128-wide blocks; 16-row output tiles on at most the SM count),
+// I a multiple of 128 up to 1024, enough router warps (15 per block without a
+// shared item) for the E (+ 1) router rows, h of a slot within the staging
+// area.
 bool decode_supported(const Geometry& g) {
   int dev = 0;
-  if (g.T < 1 || g.T > kDecodeMaxTokens || g.H % 128 || g.H > kDecMaxH || g.I % 128 ||
+  if (g.T < 1 || g.T > kDecodeMaxTokens || g.H % 512 || g.H > 2048 || g.I % 128 || g.I > kDecMaxI ||
       cudaGetDevice(&dev) != cudaSuccess)
     return false;
   const int sms = sm_count(dev);
-  if (sms <= 0 || sms > kMaxDecodeBlocks) return false;
-  // router rows live on the blocks without a shared item, 15 warps each
+  if (sms <= 0 || g.H / 16 > sms) return false;
   const int cpi = g.I / kItemCols, sfb = g.shared ? (cpi < sms ? cpi : 0) : 0;
   if (g.E + g.shared > (sms - sfb) * (kDecWarps - 1)) return false;
-  return decode_layout(g).total <= kDecDynamicLimit;
+  const DecodeLayout L = decode_layout(g);
+  return L.total <= kDecDynamicLimit && L.hst_bytes >= (size_t)g.T * g.I * 2;
 }
 
-// Fills the call's logits with the sentinel and clears the arrival counter
-// and the status word. Launched with programmatic dependent launch, it starts
+// Fills the call's logits with the sentinel and clears the slot counters and
+// the status word. Launched with programmatic dependent launch, it starts
 // while the previous kernel on the stream (often the previous layer's decode
 // kernel) is finishing, lets the decode kernel start at once, and waits for
 // the previous kernel to complete before it writes; the decode kernel waits
-// for this grid before it reads x, the logits or the counter.
-__global__ void decode_prelude_kernel(float* logits, int n_logits, unsigned int* bar, int32_t* status) {
+// for this grid before it reads x, the logits or the counters.
+__global__ void decode_prelude_kernel(float* logits, int n_logits, unsigned int* cnt, int32_t* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int i = threadIdx.x; i < n_logits; i += blockDim.x) reinterpret_cast<uint32_t*>(logits)[i] = kLogitSentinel;
-  if (threadIdx.x == 0) {
-    bar[0] = 0u;
-    *status = 0;
-  }
+  for (int i = threadIdx.x; i < kDecodeMaxSlots; i += blockDim.x) cnt[i] = 0u;
+  if (threadIdx.x == 0) *status = 0;
 }
 
 cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStream_t stream) {
@@ -758,7 +747,7 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int grid = sm_count(dev);
-  if (grid <= 0 || grid > kMaxDecodeBlocks) return cudaErrorInvalidDevice;
+  if (grid <= 0) return cudaErrorInvalidDevice;
   const DecodeLayout L = decode_layout(g);
   static SmemLimitMemo smem_memo;
   e = ensure_smem(decode_layer_kernel, L.total, &smem_memo);
@@ -778,15 +767,15 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
     pa[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.logits, g.T * (g.E + 1), args_in.bar, args_in.status);
+    e = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.logits, g.T * (g.E + 1), args_in.cnt, args_in.status);
     if (e != cudaSuccess) return e;
   }
   DecodeArgs args = args_in;
-  args.slot_bytes = (long long)L.slot_bytes;
+  args.sdn_offset = (long long)L.sdn_offset;
   args.x16_offset = (long long)L.x16_offset;
   args.xf_offset = (long long)L.xf_offset;
   args.part_offset = (long long)L.part_offset;
-  args.hs_offset = (long long)L.hs_offset;
+  args.hst_bytes = (long long)L.hst_bytes;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecThreads);

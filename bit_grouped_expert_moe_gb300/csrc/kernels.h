@@ -83,7 +83,7 @@ cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs&
 
 // Fused decode layer (decode.cu): router, top-k, tables, gate/up, down and
 // combine in one kernel after a one-block prelude, for T <= kDecodeMaxTokens.
-constexpr int kMaxDecodeBlocks = 160;  // largest grid (one block per SM) the workspace's sums cover
+constexpr int kDecodeMaxSlots = kDecodeMaxTokens * kMaxTopK + 1;  // distinct routed experts + the shared one
 struct DecodeArgs {
   int T, H, I, E, K, shared;
   const uint16_t* x;     // bf16 [T][H]: the layer input, or (norm) the residual stream r
@@ -94,7 +94,8 @@ struct DecodeArgs {
   const uint16_t* wsg;   // bf16 [H] shared-expert gate row, or null
   float* logits;         // [T][E+1], filled with a sentinel by the prelude, then written by the router rows
   const float* bias;     // [E] or null
-  float* partial;        // [kMaxDecodeBlocks][T][H] per-block sums of the down projection
+  __half* h;             // fp16 [kDecodeMaxSlots][T][I] h of every slot (K order permuted within groups of 8)
+  unsigned int* cnt;     // [kDecodeMaxSlots] gate/up items done per slot, cleared by the prelude
   ExpertArgs gu, dn;
   int32_t* ids;
   float* weights;
@@ -110,15 +111,14 @@ struct DecodeArgs {
   int32_t* status;
   float* y;              // fp32 [T][H]
   uint16_t* x_next;      // bf16 [T][H] = bf16(r + y) (the next layer's residual stream), or null
-  unsigned int* bar;     // arrival counter, cleared by launch_decode's prelude kernel
   long long timeout_ns;
-  int stall_block;       // test only: this block never arrives on the counter (-1: none)
+  int stall_block;       // test only: this block never counts its gate/up items (-1: none)
   // shared-memory layout, filled in by launch_decode
-  long long slot_bytes, x16_offset, xf_offset, part_offset, hs_offset;
+  long long sdn_offset, x16_offset, xf_offset, part_offset, hst_bytes;
 };
 bool decode_supported(const Geometry& g);
-// Launches the prelude (sentinel logits, cleared counter and status word) and
-// then the decode kernel with programmatic dependent launch.
+// Launches the prelude (sentinel logits, cleared slot counters and status
+// word) and then the decode kernel with programmatic dependent launch.
 cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);
 
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,

@@ -216,14 +216,15 @@ typedef enum moe_expert_path {
                                UNSUPPORTED_SHAPE) */
   MOE_PATH_FUSED_DECODE = 3 /* a one-block prelude and one fused kernel for the router,
                                top-k, tables, expert products and combine; needs T <= 4,
-                               H % 128 == 0, H <= 2048, I % 128 == 0, E + 1 <= 15 x the
-                               SM count, at most 160 SMs, one 512-thread block of about
-                               190 KB of shared memory resident on every SM (no other
-                               kernel may hold SMs while it runs: its blocks wait for one
-                               another, with a 1 s limit) and 16-byte aligned codes,
-                               scales and biases (else UNSUPPORTED_SHAPE). Its events[1]
-                               and events[2] follow events[0] at once and
-                               events[4..5] == events[3] */
+                               H % 512 == 0, H <= 2048, H / 16 <= the SM count,
+                               I % 128 == 0, I <= 1024, E (+1 with a shared expert)
+                               <= 15 x (SM count - I / 32), one 512-thread block of
+                               about 170 KB of shared memory resident on every SM (no
+                               other kernel may hold SMs while it runs: its blocks wait
+                               for one another's data, with a 1 s limit) and 16-byte
+                               aligned codes, scales and biases (else
+                               UNSUPPORTED_SHAPE). Its events[1] and events[2] follow
+                               events[0] at once and events[4..5] == events[3] */
 } moe_expert_path;
 
 /* moe_forward with a chosen expert path that also records caller-owned CUDA
@@ -278,13 +279,14 @@ moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const voi
 
 /* Test hook for the fused decode kernel's failure path: moe_forward_timed
  * with MOE_PATH_FUSED_DECODE, except that block `stalled_block` of the
- * decode kernel never arrives at its second grid barrier and every device
- * wait gives up after `timeout_ns` (0 < timeout_ns <= 1 s). The call's status
- * word then reads MOE_ERR_DEVICE_TIMEOUT, every block has returned (having
- * let its own copies land) and the context stays usable. Same arguments as
- * moe_forward; UNSUPPORTED_SHAPE where the fused path is refused;
- * INVALID_ARG for a negative block or a timeout out of range (a block index
- * past the grid stalls nothing). */
+ * decode kernel never counts its gate/up items as done, so the blocks that
+ * need those items' h wait out `timeout_ns` (0 < timeout_ns <= 1 s; every
+ * device wait of the call gives up after it). The call's status word then
+ * reads MOE_ERR_DEVICE_TIMEOUT, every block has returned (having let its own
+ * copies land) and the context stays usable. Same arguments as moe_forward;
+ * UNSUPPORTED_SHAPE where the fused path is refused; INVALID_ARG for a
+ * negative block or a timeout out of range (a block index past the grid
+ * stalls nothing). */
 moe_status moe_test_decode_stall(const moe_shape* shape, const void* x, const void* w_router,
                                  const float* router_bias, const moe_experts* experts, const moe_experts* shared,
                                  const void* w_shared_gate, float* y, const moe_route_out* route_out,

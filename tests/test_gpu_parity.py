@@ -156,9 +156,10 @@ def test_tensor_core_unsupported_shape_is_refused(moelib, cuda_dev):
 
 
 @pytest.mark.parametrize("T,E,K,shared,H,I", [(1, 256, 8, True, 2048, 512), (4, 256, 8, True, 2048, 512),
-                                               (3, 64, 8, True, 256, 128), (2, 16, 2, False, 128, 128),
+                                               (3, 64, 8, True, 512, 128), (2, 16, 2, False, 512, 256),
                                                (4, 8, 1, True, 512, 256), (1, 32, 4, False, 1024, 384),
-                                               (4, 4, 4, True, 2048, 128), (2, 256, 8, True, 1536, 640)])
+                                               (4, 4, 4, True, 2048, 128), (2, 256, 8, True, 1536, 640),
+                                               (3, 256, 8, True, 2048, 1024)])
 def test_fused_decode(moelib, cuda_dev, T, E, K, shared, H, I):
     spec = synth.LayerSpec("fused", T=T, H=H, I=I, E=E, top_k=K, shared=shared, seed=20260019)
     _run_and_check(moelib, cuda_dev, spec, path=moelib.PATH_FUSED_DECODE)
@@ -220,12 +221,12 @@ def test_prenorm_block_needs_the_fused_path(moelib, cuda_dev):
     assert ei.value.status == moelib.MOE_ERR_UNSUPPORTED_SHAPE
 
 
-@pytest.mark.parametrize("H,I", [(128, 64), (320, 128), (4096, 512)])
+@pytest.mark.parametrize("H,I", [(128, 64), (320, 128), (256, 128), (4096, 512), (512, 1152)])
 def test_fused_decode_shape_limits(moelib, cuda_dev, H, I):
-    """K of gate/up must come in whole 128-wide blocks, I too, and H is at
-    most 2048 (16 warps x 8 register tiles of 16 output rows): other decode
-    shapes are refused on the fused path and served by the GEMV path under
-    the automatic choice."""
+    """The fused path takes H a multiple of 512 up to 2048 (each warp a
+    quarter of K in whole 128-wide blocks, 16-row output tiles on at most the
+    SM count) and I a multiple of 128 up to 1024: other decode shapes are
+    refused on it and served by the GEMV path under the automatic choice."""
     spec = synth.LayerSpec("fused-limits", T=2, H=H, I=I, E=16, top_k=2, seed=20260021)
     L = parity.device_layer(spec, 0, cuda_dev)
     x = synth.activations(spec, device=cuda_dev)
@@ -354,11 +355,11 @@ def test_device_timeout_is_reported_not_hung(moelib, cuda_dev):
 
 
 def test_fused_decode_timeout_is_reported_not_hung(moelib, cuda_dev):
-    """One block of the fused decode kernel never arrives on the counter that
-    gates the final reduction: the blocks waiting on it give up after a 20 ms
-    limit and return (every block lets its own copies land first), the call
-    reports MOE_ERR_DEVICE_TIMEOUT, and the next normal call on the same
-    context and workspace is correct."""
+    """One block of the fused decode kernel never counts its gate/up items as
+    done: the blocks that need those items' h give up after a 20 ms limit and
+    return (every block lets its own copies land first), the call reports
+    MOE_ERR_DEVICE_TIMEOUT, and the next normal call on the same context and
+    workspace is correct."""
     spec = synth.WORKLOADS["decode-t1"]
     L = parity.device_layer(spec, 0, cuda_dev)
     x = synth.activations(spec, device=cuda_dev)
