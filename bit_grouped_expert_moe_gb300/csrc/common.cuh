@@ -50,49 +50,50 @@ __device__ __forceinline__ float order_key_to_float(uint32_t k) {
 // renormalised softmax weight: lane k < K returns pick k in *e_out and its
 // weight in *w_out; every lane returns sigmoid(gate_logit) in *gate_out when
 // `shared`. Keys are fp32 order keys (0 marks an empty or taken entry: a
-// finite logit never maps to 0). Each lane keeps the best of its own entries;
-// a round takes the warp maximum and, among the lanes holding it, the lowest
-// expert index.
+// finite logit never maps to 0).
+//
+// Each lane first sorts its 8 entries once (a 19-comparator network on
+// (key, lower j first) packed into 64 bits, no branches). A round then takes
+// the warp maximum of the lanes' heads and, among the lanes holding it, the
+// lowest expert index; the winning lane pops its head. Every lane runs the
+// same instructions, and a round is two warp reductions and a few selects.
 __device__ __forceinline__ void warp_topk_select(const float (&lv)[kMaxExperts / 32], float gate_logit,
                                                  const float* bias, int E, int K, bool shared, int lane,
                                                  int* e_out, float* w_out, float* gate_out) {
-  float bv[kMaxExperts / 32];
+  constexpr int kN = kMaxExperts / 32;
+  static_assert(kN == 8, "the sorting network below sorts 8 entries per lane");
+  uint64_t v[kN];
 #pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) bv[j] = bias ? __ldg(bias + min(lane + 32 * j, E - 1)) : 0.f;
-  uint32_t key[kMaxExperts / 32];
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j) key[j] = lane + 32 * j < E ? float_order_key(lv[j] + bv[j]) : 0u;
-  uint32_t lb = 0u;
-  int lbj = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxExperts / 32; ++j)
-    if (key[j] > lb) {
-      lb = key[j];
-      lbj = j;
-    }
+  for (int j = 0; j < kN; ++j) {
+    const float b = bias ? __ldg(bias + min(lane + 32 * j, E - 1)) : 0.f;
+    const uint32_t key = lane + 32 * j < E ? float_order_key(lv[j] + b) : 0u;
+    v[j] = ((uint64_t)key << 32) | (uint32_t)(kN - 1 - j);  // equal keys: the lower j sorts first
+  }
+  auto cx = [&](int a, int b) {  // larger value to position a
+    const uint64_t hi = v[a] > v[b] ? v[a] : v[b], lo = v[a] > v[b] ? v[b] : v[a];
+    v[a] = hi;
+    v[b] = lo;
+  };
+  cx(0, 2), cx(1, 3), cx(4, 6), cx(5, 7);
+  cx(0, 4), cx(1, 5), cx(2, 6), cx(3, 7);
+  cx(0, 1), cx(2, 3), cx(4, 5), cx(6, 7);
+  cx(2, 4), cx(3, 5);
+  cx(1, 4), cx(3, 6);
+  cx(1, 2), cx(3, 4), cx(5, 6);
   uint32_t my_key = 0u, top_key = 0u;
   int my_e = 0;
   for (int k = 0; k < K; ++k) {
-    const uint32_t M = __reduce_max_sync(0xffffffffu, lb);
-    const uint32_t ew = __reduce_min_sync(0xffffffffu, lb == M ? (uint32_t)(lane + 32 * lbj) : 0xFFFFFFFFu);
-    if (k == 0) top_key = M;
-    if (lane == k) {
-      my_key = M;
-      my_e = (int)ew;
-    }
-    if (lane == (int)(ew & 31u)) {
-      const int jr = (int)(ew >> 5);
-      lb = 0u;
-      lbj = 0;
+    const uint32_t hk = (uint32_t)(v[0] >> 32);
+    const uint32_t he = (uint32_t)lane + 32u * (uint32_t)(kN - 1 - (int)(v[0] & 0xFFFFFFFFu));
+    const uint32_t M = __reduce_max_sync(0xffffffffu, hk);
+    const uint32_t ew = __reduce_min_sync(0xffffffffu, hk == M ? he : 0xFFFFFFFFu);
+    top_key = k == 0 ? M : top_key;
+    my_key = lane == k ? M : my_key;
+    my_e = lane == k ? (int)ew : my_e;
+    const bool won = lane == (int)(ew & 31u);
 #pragma unroll
-      for (int j = 0; j < kMaxExperts / 32; ++j) {
-        if (j == jr) key[j] = 0u;
-        if (key[j] > lb) {
-          lb = key[j];
-          lbj = j;
-        }
-      }
-    }
+    for (int j = 0; j < kN - 1; ++j) v[j] = won ? v[j + 1] : v[j];
+    v[kN - 1] = won ? 0ull : v[kN - 1];
   }
   // weights: exp(v_k - v_0) / sum over the selected (lanes k < K in parallel)
   const float z = lane < K ? expf(order_key_to_float(my_key) - order_key_to_float(top_key)) : 0.f;

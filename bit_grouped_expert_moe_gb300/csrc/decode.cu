@@ -38,8 +38,8 @@
 //      item's gate/up tasks and the shared down tasks go out;
 //   R  the layer input is staged (fp32 for the router, fp16 in the permuted
 //      K order for the MMAs; with the pre-norm join it is RMSNorm of the
-//      residual row, never rounded to bf16); logits are stored straight to
-//      global memory; a block with a shared item computes the shared gate
+//      residual row, never rounded to bf16); logits are written to L2 by
+//      atomic exchange; a block with a shared item computes the shared gate
 //      and its shared item;
 //   1  blocks with routed work poll the T logit rows until no entry holds
 //      the sentinel, select the top-k and build the slot table;
@@ -103,10 +103,6 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-__device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
-  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // Counts on a counter: release orders the block's earlier writes (made
@@ -396,7 +392,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   if (router_warp)
     for (int t = 0; t < T; ++t) {
       const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
-      if (lane == 0) st_relaxed_f32(a.logits + (size_t)t * (E + 1) + rrow, l);
+      // an atomic exchange is performed at L2, where the polling blocks read
+      // (a plain store could sit in this SM's L1 for microseconds)
+      if (lane == 0) atomicExch(a.logits + (size_t)t * (E + 1) + rrow, l);
     }
   if (shared_first && warp == kGateWarp)
     for (int t = 0; t < T; ++t) {
