@@ -470,6 +470,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       float lv[kMaxExperts / 32];
       float gl = 0.f;
       bool ok = false;
+      // Measured on GB300: the selection's eight rounds took about 5000
+      // cycles when they followed this poll directly and about 780 when a
+      // warp reduction ran in every poll round just before the exit test
+      // (the reductions themselves cost 28 cycles each).
+      uint32_t warm = (uint32_t)lane;
       while (true) {
 #pragma unroll
         for (int j = 0; j < kMaxExperts / 32; ++j)
@@ -478,6 +483,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
         bool mine = __float_as_uint(gl) != kLogitSentinel;
 #pragma unroll
         for (int j = 0; j < kMaxExperts / 32; ++j) mine &= __float_as_uint(lv[j]) != kLogitSentinel;
+        warm = __reduce_max_sync(0xffffffffu, warm + (uint32_t)lane);
         if (__all_sync(0xffffffffu, mine)) {
           ok = true;
           break;
@@ -485,6 +491,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
         if (global_timer_ns() > deadline) break;
         __nanosleep(32);
       }
+      if (warm == 0xFFFFFFFFu) S.range = 1;  // keeps the reduction (never true: warm grows by at most 62 a round)
       if (ok) {
         int e;
         float w, g;
