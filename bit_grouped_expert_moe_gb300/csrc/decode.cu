@@ -147,17 +147,14 @@ __device__ __forceinline__ __half2 bf16_h2(uint16_t bits16) {
   return __halves2half2(h, h);
 }
 
-// One task's products (one out-of-line copy: the kernel's code is fetched
-// from memory at every launch, and the weight stream keeps evicting it from
-// L2): this lane's 32 K of fragment rows g and g+8 (16-byte
+// One task's products: this lane's 32 K of fragment rows g and g+8 (16-byte
 // code chunks at c * 16 of rows g and g + 8 of the slot, their scale and
 // bias from the slot's pair of groups) against the B fragments xb[w]
 // (permuted activations, 8 K per 16-byte word): 8 MMAs. With g = lane / 4
 // and c = lane % 4, MMA k slots 2c, 2c+1, 2c+8, 2c+9 of word w hold K
 // offsets 8w + {0,4}, {1,5} (first MMA) and 8w + {2,6}, {3,7} (second), on A
 // and B alike.
-__device__ __noinline__ float4 task_mma(float4 acc, const uint8_t* t, int g8, int c4, uint4 x0, uint4 x1, uint4 x2,
-                                        uint4 x3) {
+__device__ __forceinline__ void task_mma(float (&d)[4], const uint8_t* t, int g8, int c4, const uint4 (&xb)[4]) {
   const uint4 r0 = *reinterpret_cast<const uint4*>(t + g8 * 64 + c4 * 16);
   const uint4 r1 = *reinterpret_cast<const uint4*>(t + (8 + g8) * 64 + c4 * 16);
   const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 1024);  // per row: scale pair, bias pair
@@ -165,8 +162,6 @@ __device__ __noinline__ float4 task_mma(float4 acc, const uint8_t* t, int g8, in
   const __half2 s0 = bf16_h2(sb[g8 * 4 + gs]), b0 = bf16_h2(sb[g8 * 4 + 2 + gs]);
   const __half2 s1 = bf16_h2(sb[(8 + g8) * 4 + gs]), b1 = bf16_h2(sb[(8 + g8) * 4 + 2 + gs]);
   const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
-  const uint4 xb[4] = {x0, x1, x2, x3};
-  float d[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t p0[4], p1[4];
@@ -175,22 +170,12 @@ __device__ __noinline__ float4 task_mma(float4 acc, const uint8_t* t, int g8, in
     mma_16816(d, p0[0], p1[0], p0[1], p1[1], xb[w].x, xb[w].y);
     mma_16816(d, p0[2], p1[2], p0[3], p1[3], xb[w].z, xb[w].w);
   }
-  return make_float4(d[0], d[1], d[2], d[3]);
-}
-
-// The four 16-byte B fragments of token g (zero past the T tokens) at this
-// lane's 32 K: row + 32 c, permuted activations.
-__device__ __forceinline__ float4 task_mma_row(float4 acc, const uint8_t* t, int g8, int c4, const __half* row,
-                                               bool live) {
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  const uint4* r = reinterpret_cast<const uint4*>(row + 32 * c4);
-  return task_mma(acc, t, g8, c4, live ? r[0] : z, live ? r[1] : z, live ? r[2] : z, live ? r[3] : z);
 }
 
 // Copies of one task: 16 rows of a packed matrix (rows lo .. lo + 7, then
 // hi .. hi + 7), K block kb (64 bytes of codes per row), and the scale and
 // bias pairs of groups 2kb, 2kb+1 of each row.
-__device__ __noinline__ void task_copy(uint8_t* td, const uint8_t* codes, const uint16_t* sc, const uint16_t* bi,
+__device__ __forceinline__ void task_copy(uint8_t* td, const uint8_t* codes, const uint16_t* sc, const uint16_t* bi,
                                           int lo, int hi, int row_bytes, int gpr, int kb, int lane) {
 #pragma unroll
   for (int q0 = 0; q0 < 64; q0 += 32) {  // 16 rows x 4 pieces of 16 bytes
@@ -404,19 +389,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 
   // ---- phase R: router logits l[t][r] (r = E: the shared gate row), stored
   // for the other blocks; the shared gate itself where a shared item is here
-  const bool gate_warp = shared_first && warp == kGateWarp;
-  if (router_warp || gate_warp)
+  if (router_warp)
+    for (int t = 0; t < T; ++t) {
+      const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
+      // an atomic exchange is performed at L2, where the polling blocks read
+      // (a plain store could sit in this SM's L1 for microseconds)
+      if (lane == 0) atomicExch(a.logits + (size_t)t * (E + 1) + rrow, l);
+    }
+  if (shared_first && warp == kGateWarp)
     for (int t = 0; t < T; ++t) {
       const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
       if (lane == 0) {
-        if (router_warp) {
-          // an atomic exchange is performed at L2, where the polling blocks
-          // read (a plain store could sit in this SM's L1 for microseconds)
-          atomicExch(a.logits + (size_t)t * (E + 1) + rrow, l);
-        } else {
-          S.g[t] = 1.f / (1.f + expf(-l));
-          S.slot_wt[0][t] = S.g[t];
-        }
+        S.g[t] = 1.f / (1.f + expf(-l));
+        S.slot_wt[0][t] = S.g[t];
       }
     }
   // The next call's prelude may launch now: it waits for this grid to finish.
@@ -426,20 +411,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   // to the workspace and the item counted on its slot's counter.
   auto run_item = [&](int j, int k0) {
     const int item = b + G * j, s = item / cpi, n0 = (item - s * cpi) * kItemCols;
-    float4 d = make_float4(0.f, 0.f, 0.f, 0.f);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
     for (int jj = 0; jj < tpw; ++jj) {
       const int k = k0 + jj;
       wait_task(k);
       const int kb = (warp >> 2) * tpw + jj;
-      d = task_mma_row(d, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4,
-                       x16 + (size_t)(g8 < T ? g8 : 0) * H + kb * 128, g8 < T);
+      uint4 xb[4];
+      const __half* xrow = x16 + (size_t)(g8 < T ? g8 : 0) * H + kb * 128 + 32 * c4;
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(xrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+      task_mma(d, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb);
       __syncwarp();  // the slot is read: refill it
       if (issued < n_items * tpw + n_dn) issue_task(issued++);
     }
-    part[(warp * 4 + 0) * 32 + lane] = d.x;
-    part[(warp * 4 + 1) * 32 + lane] = d.y;
-    part[(warp * 4 + 2) * 32 + lane] = d.z;
-    part[(warp * 4 + 3) * 32 + lane] = d.w;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r];
     __syncthreads();
     if (warp < kUnits) {
       // unit u = warp: warps u, u+4, u+8, u+12 hold its partial sums (fixed
@@ -618,7 +605,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 
   // ---- phase 3: down, for the blocks with output rows
   if (has_rows && routed) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);  // rows g, g+8 x tokens 2c, 2c+1, over this warp's down tasks
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows g, g+8 x tokens 2c, 2c+1, over this warp's down tasks
     const int hb_bytes = T * I * 2;
     const int batch = (int)(a.hst_bytes / hb_bytes);  // slots whose h fits in shared memory at once
     for (int s0 = 0; s0 < nslots; s0 += batch) {
@@ -644,8 +631,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       if (s0 == 0 && sh && warp < dkb) {
         cp_async_wait_dyn(issued);  // the oldest group: the shared down task
         __syncwarp();
-        acc = task_mma_row(acc, sdn + (size_t)warp * kTaskBytes, g8, c4,
-                           hst + (size_t)(g8 < T ? g8 : 0) * I + warp * 128, g8 < T);
+        uint4 xb[4];
+        const __half* hrow = hst + (size_t)(g8 < T ? g8 : 0) * I + warp * 128 + 32 * c4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+        task_mma(acc, sdn + (size_t)warp * kTaskBytes, g8, c4, xb);
       }
       // the routed slots' tasks of this batch, in ring order
       for (; k < ntasks; ++k) {
@@ -653,18 +644,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
         const int s = sh + q / dkb, kc = q - (s - sh) * dkb;
         if (s >= s1) break;
         wait_task(k);
-        acc = task_mma_row(acc, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4,
-                           hst + ((size_t)(s - s0) * T + (g8 < T ? g8 : 0)) * I + kc * 128, g8 < T);
+        uint4 xb[4];
+        const __half* hrow = hst + ((size_t)(s - s0) * T + (g8 < T ? g8 : 0)) * I + kc * 128 + 32 * c4;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
+        task_mma(acc, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb);
         __syncwarp();
         if (issued < ntasks) issue_task(issued++);
       }
       __syncthreads();  // the batch's h is read
     }
     // the 16 warps' sums in a fixed order: y and the next residual row
-    part[(warp * 4 + 0) * 32 + lane] = acc.x;
-    part[(warp * 4 + 1) * 32 + lane] = acc.y;
-    part[(warp * 4 + 2) * 32 + lane] = acc.z;
-    part[(warp * 4 + 3) * 32 + lane] = acc.w;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = acc[r];
     __syncthreads();
     if (!S.failed && tid < 16 * T) {
       const int t = tid >> 4, row = tid & 15;
