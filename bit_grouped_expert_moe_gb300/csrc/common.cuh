@@ -140,9 +140,35 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 
 __device__ __forceinline__ float silu_f32(float a) { return a / (1.0f + __expf(-a)); }
 
+// Records MOE_ERR_RANGE in the call's status word, unless a failure is
+// already recorded there: a value written as an fp16 operand of the expert
+// path (x, h or o) left the range where fp16 holds it to the layer's
+// tolerance (see fp16_overflows and kFp16Floor).
+__device__ __forceinline__ void flag_range(const int32_t* status) {
+  atomicCAS(const_cast<int32_t*>(status), 0, (int32_t)MOE_ERR_RANGE);
+}
+
+// A bf16 value that becomes inf in fp16 (|v| >= 65520 rounds past 65504).
+__device__ __forceinline__ bool fp16_overflows(float v) { return fabsf(v) >= 65520.f; }
+
+// Below 2^-14 fp16 keeps a fixed absolute step of 2^-24. A slice of h or o
+// whose largest magnitude is under 2^-16 is therefore rounded with an error
+// above 2^-9 of its largest value: the kernels report such a slice (unless it
+// is all zero) as MOE_ERR_RANGE instead of returning a result that has lost
+// the precision the rest of the path keeps.
+constexpr float kFp16Floor = 1.52587890625e-05f;  // 2^-16
+
 // A kernel after the routing kernel does nothing once a device error is set.
 __device__ __forceinline__ bool device_failed(const int32_t* status) {
   return *reinterpret_cast<const volatile int32_t*>(status) != 0;
+}
+
+// device_failed, decided once for the whole block (every thread must call
+// it): thread 0 reads the status word and all threads get its answer, so a
+// word set meanwhile by another block (a range report) cannot split the
+// block into threads that return and threads that wait at a barrier.
+__device__ __forceinline__ bool block_failed(const int32_t* status) {
+  return __syncthreads_or(threadIdx.x == 0 && device_failed(status)) != 0;
 }
 
 // The current device and an identifier of its current CUDA context (0 when

@@ -142,25 +142,24 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ __half2 bf16_h2(uint16_t bits16) {
-  const __half h = __float2half_rn(bf16_bits_to_f32(bits16));
-  return __halves2half2(h, h);
-}
-
 // One task's products: this lane's 32 K of fragment rows g and g+8 (16-byte
 // code chunks at c * 16 of rows g and g + 8 of the slot, their scale and
 // bias from the slot's pair of groups) against the B fragments xb[w]
 // (permuted activations, 8 K per 16-byte word): 8 MMAs. With g = lane / 4
 // and c = lane % 4, MMA k slots 2c, 2c+1, 2c+8, 2c+9 of word w hold K
 // offsets 8w + {0,4}, {1,5} (first MMA) and 8w + {2,6}, {3,7} (second), on A
-// and B alike.
-__device__ __forceinline__ void task_mma(float (&d)[4], const uint8_t* t, int g8, int c4, const uint4 (&xb)[4]) {
+// and B alike. Returns false when a scale of 4 or more (scale * 2^14 past
+// fp16) was met.
+__device__ __forceinline__ bool task_mma(float (&d)[4], const uint8_t* t, int g8, int c4, const uint4 (&xb)[4]) {
   const uint4 r0 = *reinterpret_cast<const uint4*>(t + g8 * 64 + c4 * 16);
   const uint4 r1 = *reinterpret_cast<const uint4*>(t + (8 + g8) * 64 + c4 * 16);
   const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 1024);  // per row: scale pair, bias pair
   const int gs = c4 >> 1;  // this lane's 32 K lie in the second group of the pair when c >= 2
-  const __half2 s0 = bf16_h2(sb[g8 * 4 + gs]), b0 = bf16_h2(sb[g8 * 4 + 2 + gs]);
-  const __half2 s1 = bf16_h2(sb[(8 + g8) * 4 + gs]), b1 = bf16_h2(sb[(8 + g8) * 4 + 2 + gs]);
+  // scale * 2^14 and bias per row (tc::dequant8_f16)
+  const __half2 s0 = __float2half2_rn(bf16_bits_to_f32(sb[g8 * 4 + gs]) * 16384.f);
+  const __half2 b0 = __float2half2_rn(bf16_bits_to_f32(sb[g8 * 4 + 2 + gs]));
+  const __half2 s1 = __float2half2_rn(bf16_bits_to_f32(sb[(8 + g8) * 4 + gs]) * 16384.f);
+  const __half2 b1 = __float2half2_rn(bf16_bits_to_f32(sb[(8 + g8) * 4 + 2 + gs]));
   const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -170,6 +169,7 @@ __device__ __forceinline__ void task_mma(float (&d)[4], const uint8_t* t, int g8
     mma_16816(d, p0[0], p1[0], p0[1], p1[1], xb[w].x, xb[w].y);
     mma_16816(d, p0[2], p1[2], p0[3], p1[3], xb[w].z, xb[w].w);
   }
+  return !(__hisinf(__low2half(s0)) | __hisinf(__low2half(s1)));
 }
 
 // Copies of one task: 16 rows of a packed matrix (rows lo .. lo + 7, then
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 #pragma unroll
       for (int w = 0; w < 4; ++w)
         xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(xrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-      task_mma(d, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb);
+      if (!task_mma(d, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb)) S.range = 1;
       __syncwarp();  // the slot is read: refill it
       if (issued < n_items * tpw + n_dn) issue_task(issued++);
     }
@@ -438,15 +438,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
                 part[((warp + 8) * 4 + r) * 32 + lane]) +
                part[((warp + 12) * 4 + r) * 32 + lane];
       const int pc = tc::perm8_pos(n0 + 8 * warp + g8);
+      bool big = false, nz = false;
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
         const int t = 2 * c4 + jj;
         if (t < T) {
-          const __half hv = __float2half_rn(silu_f32(v[jj]) * v[2 + jj] * S.slot_wt[s][t]);
-          if (__hisinf(hv)) S.range = 1;
+          // The floor is checked on h itself: the stored value also carries
+          // the routing weight, which may be tiny when the expert adds
+          // next to nothing to y.
+          const float hu = silu_f32(v[jj]) * v[2 + jj], hw = hu * S.slot_wt[s][t];
+          const __half hv = __float2half_rn(hw);
+          if (fabsf(hw) >= 65520.f) S.range = 1;  // inf in fp16
+          big |= fabsf(hu) >= kFp16Floor;
+          nz |= hu != 0.f;
           a.h[((size_t)s * T + t) * I + pc] = hv;
         }
       }
+      // the unit's 8 columns of h for every token, all below the fp16 floor
+      if (__any_sync(0xffffffffu, nz) && !__any_sync(0xffffffffu, big)) S.range = 1;
     }
     __syncthreads();
     if (tid == 0 && b != a.stall_block) red_release_add(a.cnt + s, 1u);
@@ -636,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-        task_mma(acc, sdn + (size_t)warp * kTaskBytes, g8, c4, xb);
+        if (!task_mma(acc, sdn + (size_t)warp * kTaskBytes, g8, c4, xb)) S.range = 1;
       }
       // the routed slots' tasks of this batch, in ring order
       for (; k < ntasks; ++k) {
@@ -649,7 +658,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-        task_mma(acc, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb);
+        if (!task_mma(acc, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb)) S.range = 1;
         __syncwarp();
         if (issued < ntasks) issue_task(issued++);
       }

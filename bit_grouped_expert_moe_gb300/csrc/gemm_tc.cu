@@ -126,11 +126,6 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return p + (((a + 1023u) & ~1023u) - a);
 }
 
-__device__ __forceinline__ __half2 bf16_to_h2(uint32_t bits16) {
-  const __half h = __float2half_rn(bf16_bits_to_f32(bits16));
-  return __halves2half2(h, h);
-}
-
 __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
@@ -145,7 +140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_s_codes,
                  const __grid_constant__ CUtensorMap tm_h, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
-  if (device_failed(p.t.status)) return;
+  if (block_failed(p.t.status)) return;
   const int num_tiles = *p.t.num_tiles;
   const int items = num_tiles * p.per_tile;
   if ((int)blockIdx.x >= items) return;
@@ -368,6 +363,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     // One stage of this group: the codes of both rows, the wait for the
     // MMAs that last read this A slot, both rows dequantised into the slot,
     // then one lane releases the A slot and the code slot.
+    // sa, ba / sb, bb: scale * 2^14 and bias of this group in rows 0 and 1
+    // (group_scale_bias), in both halves.
     auto stage = [&](__half2 sa, __half2 ba, __half2 sb, __half2 bb) -> bool {
       const int cs = it % kCS, as = it % kAS;
       if (!mbar_wait(&ctl->c_full[cs], (it / kCS) & 1, abort_flag, deadline)) return false;
@@ -405,18 +402,18 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
                         uint4 s0, uint4 c0, uint4 s1, uint4 c1) {
       if (chunked) {
         // scales/biases 8 groups per 16-byte load; this group's 4 (scale,
-        // bias) pairs of each row are converted to fp16 once per chunk and
-        // the next chunk is loaded while the 4 stages run
+        // bias) pairs of each row are picked out once per chunk and the next
+        // chunk is loaded while the 4 stages run
         for (int k0 = 0; ok && k0 < num_k; k0 += 8) {
           uint32_t pa[4], pb[4];
+          bool fits = true;  // every scale below 4 (group_scale_bias)
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
             const int g = grp + 2 * m;
-            const __half2 ha = __floats2half2_rn(bf16_bits_to_f32(bf16_of(s0, g)), bf16_bits_to_f32(bf16_of(c0, g)));
-            const __half2 hb = __floats2half2_rn(bf16_bits_to_f32(bf16_of(s1, g)), bf16_bits_to_f32(bf16_of(c1, g)));
-            pa[m] = *reinterpret_cast<const uint32_t*>(&ha);
-            pb[m] = *reinterpret_cast<const uint32_t*>(&hb);
+            fits &= group_scale_bias(bf16_bits_to_f32(bf16_of(s0, g)), bf16_bits_to_f32(bf16_of(c0, g)), pa[m]);
+            fits &= group_scale_bias(bf16_bits_to_f32(bf16_of(s1, g)), bf16_bits_to_f32(bf16_of(c1, g)), pb[m]);
           }
+          if (!fits) flag_range(p.status);
           if (k0 + 8 < num_k) {
             s0 = ldg_nc_v4(srow0 + k0 + 8);
             c0 = ldg_nc_v4(brow0 + k0 + 8);
@@ -434,9 +431,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           }
         }
       } else {
-        for (int k = grp; ok && k < num_k; k += 2)
-          ok = stage(bf16_to_h2(__ldg(srow0 + k)), bf16_to_h2(__ldg(brow0 + k)), bf16_to_h2(__ldg(srow1 + k)),
-                     bf16_to_h2(__ldg(brow1 + k)));
+        for (int k = grp; ok && k < num_k; k += 2) {
+          uint32_t pa, pb;
+          const bool fits = group_scale_bias(bf16_bits_to_f32(__ldg(srow0 + k)), bf16_bits_to_f32(__ldg(brow0 + k)), pa) &
+                            group_scale_bias(bf16_bits_to_f32(__ldg(srow1 + k)), bf16_bits_to_f32(__ldg(brow1 + k)), pb);
+          if (!fits) flag_range(p.status);
+          const __half2 ha = *reinterpret_cast<const __half2*>(&pa), hb = *reinterpret_cast<const __half2*>(&pb);
+          ok = stage(__low2half2(ha), __high2half2(ha), __low2half2(hb), __high2half2(hb));
+        }
       }
     };
     const uint4 z4 = make_uint4(0, 0, 0, 0);
@@ -492,6 +494,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       if (!mbar_wait(&ctl->acc_full[buf], (ii >> 1) & 1, abort_flag, deadline)) break;
       tc_fence_after();
       const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16) + buf * 256;
+      // Largest |h| or |o| this lane stores: past fp16 (>= 65520, where the
+      // value rounds to inf) is MOE_ERR_RANGE; so is a warp's h tile that is
+      // all under the fp16 floor and not all zero (o is checked row by row
+      // where it is combined). One max per value keeps the check cheap.
+      float mx = 0.f;
       if (kGateUp) {
         const int pn = perm8_pos(sub * 128 + q * 32 + lane);
         for (int j0 = 0; j0 < N; j0 += 32) {
@@ -501,7 +508,11 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int j = j0 + jj;
-            if (j < rows) p.out[(size_t)(row0 + j) * I + pn] = __float2half_rn(silu_f32(g[jj]) * u[jj]);
+            if (j < rows) {
+              const float hf = silu_f32(g[jj]) * u[jj];
+              mx = fmaxf(mx, fabsf(hf));
+              p.out[(size_t)(row0 + j) * I + pn] = __float2half_rn(hf);
+            }
           }
         }
       } else {
@@ -515,12 +526,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
             const int j = j0 + jj;
             if (j < rows) {
               __half* orow = p.out + (size_t)(row0 + j) * H;
+              mx = fmaxf(mx, fmaxf(fabsf(v0[jj]), fabsf(v1[jj])));
               orow[m] = __float2half_rn(v0[jj]);
               orow[m + 128] = __float2half_rn(v1[jj]);
             }
           }
         }
       }
+      bool inf = mx >= 65520.f;
+      if (kGateUp && __any_sync(0xffffffffu, mx > 0.f) && !__any_sync(0xffffffffu, mx >= kFp16Floor))
+        inf |= lane == 0;
+      if (inf) flag_range(p.status);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->acc_empty[buf]);

@@ -68,7 +68,7 @@ gemv_gate_up_kernel(int H, int I, int E, int K, int A, const uint16_t* __restric
   extern __shared__ __align__(16) float xs[];  // [kTokChunk][H/32][kPad]
   __shared__ int tok_s[kTokChunk];
   const int tile = blockIdx.x;
-  if (device_failed(t.status) || tile >= *t.num_tiles) return;
+  if (block_failed(t.status) || tile >= *t.num_tiles) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = t.tile_expert[tile], r0 = t.tile_row0[tile], nr = t.tile_rows[tile];
   const bool sh = e == E;
@@ -129,13 +129,22 @@ gemv_gate_up_kernel(int H, int I, int E, int K, int A, const uint16_t* __restric
         au[j] += __shfl_xor_sync(0xffffffffu, au[j], o);
       }
     }
+    bool big = false, nz = false;
     if (lane < nc) {
       float g = ag[0], u = au[0];
 #pragma unroll
       for (int j = 1; j < kTokChunk; ++j)
         if (lane == j) { g = ag[j]; u = au[j]; }
-      h[(size_t)(r0 + c0 + lane) * I + n] = __float2half_rn(silu_f32(g) * u);
+      const float hf = silu_f32(g) * u;
+      if (fabsf(hf) >= 65520.f) flag_range(t.status);  // inf in fp16
+      big = fabsf(hf) >= kFp16Floor;
+      nz = hf != 0.f;
+      h[(size_t)(r0 + c0 + lane) * I + n] = __float2half_rn(hf);
     }
+    // The block's kGemvWarps columns of h for these tokens, all below the
+    // fp16 floor (o is checked row by row where it is combined).
+    const int any_big = __syncthreads_or(big), any_nz = __syncthreads_or(nz);
+    if (threadIdx.x == 0 && any_nz && !any_big) flag_range(t.status);
   }
 }
 
@@ -146,7 +155,7 @@ gemv_down_kernel(int H, int I, int E, int rows_per_block, const __half* __restri
   extern __shared__ __align__(16) float hs[];  // [kTokChunk][I/32][kPad]
   __shared__ int row_s[kTokChunk];
   const int tile = blockIdx.x;
-  if (device_failed(t.status) || tile >= *t.num_tiles) return;
+  if (block_failed(t.status) || tile >= *t.num_tiles) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = t.tile_expert[tile], r0 = t.tile_row0[tile], nr = t.tile_rows[tile];
   const bool sh = e == E;
@@ -201,7 +210,10 @@ gemv_down_kernel(int H, int I, int E, int rows_per_block, const __half* __restri
       if (m < H) {
 #pragma unroll
         for (int j = 0; j < kTokChunk; ++j)
-          if (j < nc && (j % L) == sub) o[(size_t)(r0 + c0 + j) * H + m] = __float2half_rn(acc[j]);
+          if (j < nc && (j % L) == sub) {
+            if (fabsf(acc[j]) >= 65520.f) flag_range(t.status);  // inf in fp16
+            o[(size_t)(r0 + c0 + j) * H + m] = __float2half_rn(acc[j]);
+          }
       }
     }
   }

@@ -73,12 +73,16 @@ router_logits_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict_
   // magnitude >= 2^-14), K-permuted within groups of 8 as 0,4,1,5,2,6,3,7 to
   // match the order in which the 4-bit codes unpack.
   if (x16 != nullptr && blockIdx.x == 0) {
+    bool big = false;
     for (int i = threadIdx.x; i < nt * H; i += blockDim.x) {
       const int j = i / H, k = i - j * H;
       const int r = k & 7;
       const int pk = (k & ~7) | (r < 4 ? 2 * r : 2 * (r - 4) + 1);
-      x16[(size_t)(t0 + j) * H + pk] = __half_as_ushort(__float2half_rn(bf16_bits_to_f32(xs[j * H + k])));
+      const float v = bf16_bits_to_f32(xs[j * H + k]);
+      big |= fp16_overflows(v);
+      x16[(size_t)(t0 + j) * H + pk] = __half_as_ushort(__float2half_rn(v));
     }
+    if (big) flag_range(status);
   }
   if (!has_row) return;
 

@@ -179,6 +179,10 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
             }
           }
           if (p.x16 != nullptr) {
+            bool big = false;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) big |= fp16_overflows(xf[m]);
+            if (big) flag_range(p.status);
             // K order 0,4,1,5,2,6,3,7 inside the group of 8
             const __half2 h0 = __floats2half2_rn(xf[0], xf[4]), h1 = __floats2half2_rn(xf[1], xf[5]);
             const __half2 h2 = __floats2half2_rn(xf[2], xf[6]), h3 = __floats2half2_rn(xf[3], xf[7]);

@@ -199,30 +199,48 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 // W = scale * q + bias, with pairs (q0,q4), (q1,q5), (q2,q6), (q3,q7): the
 // operands' K order inside every group of 8 is 0,4,1,5,2,6,3,7, which the
 // activations share (a permutation of K applied to both operands leaves the
-// product unchanged). 0x6400 is fp16 1024, whose unit in the last place is
-// 1, so OR-ing a code into its low mantissa bits gives exactly 1024 + q.
+// product unchanged).
+//
+// s2 holds scale * 2^14 and b2 the bias (group_scale_bias), and the codes
+// come out as q * 2^-14, so that W = fma(q 2^-14, scale 2^14, bias): the
+// product is exact and W is rounded once, at its own magnitude. (Taking the
+// scale itself to fp16 would round any scale below 2^-14 to a subnormal with
+// a fixed step of 2^-24, an error that q, up to 15, then multiplies.)
+// 0x2C00 is fp16 2^-4, whose unit in the last place is 2^-14: OR-ing a code
+// into its low mantissa bits gives exactly 2^-4 + q 2^-14, and a code 4 bits
+// up gives 2^-4 + q 2^-10; (2^-4 + q 2^-14) - 2^-4 and
+// (2^-4 + q 2^-10) 2^-4 - 2^-8 are then exactly q 2^-14.
 __device__ __forceinline__ void dequant8_f16(uint32_t w, __half2 s2, __half2 b2, uint32_t (&out)[4]) {
-  const uint32_t kMagic = 0x64006400u;
+  const uint32_t kMagic = 0x2C002C00u;
   uint32_t lo0, hi0, lo1, hi1;
   const uint32_t w8 = w >> 8;
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(lo0) : "r"(w), "r"(0x000F000Fu), "r"(kMagic));
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(hi0) : "r"(w), "r"(0x00F000F0u), "r"(kMagic));
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(lo1) : "r"(w8), "r"(0x000F000Fu), "r"(kMagic));
   asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(hi1) : "r"(w8), "r"(0x00F000F0u), "r"(kMagic));
-  const __half2 k1024 = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
-  const __half2 k1_16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
-  const __half2 km64 = __halves2half2(__ushort_as_half(0xD400), __ushort_as_half(0xD400));   // -64
-  // lo: 1024 + q  ->  q ; hi: 1024 + 16 q  ->  (1024 + 16 q) / 16 - 64 = q  (all exact)
-  const __half2 q04 = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k1024);
-  const __half2 q15 = __hfma2(*reinterpret_cast<const __half2*>(&hi0), k1_16, km64);
-  const __half2 q26 = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k1024);
-  const __half2 q37 = __hfma2(*reinterpret_cast<const __half2*>(&hi1), k1_16, km64);
+  const __half2 k4 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 2^-4
+  const __half2 km8 = __halves2half2(__ushort_as_half(0x9C00), __ushort_as_half(0x9C00));  // -2^-8
+  const __half2 q04 = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k4);
+  const __half2 q15 = __hfma2(*reinterpret_cast<const __half2*>(&hi0), k4, km8);
+  const __half2 q26 = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k4);
+  const __half2 q37 = __hfma2(*reinterpret_cast<const __half2*>(&hi1), k4, km8);
   const __half2 r0 = __hfma2(q04, s2, b2), r1 = __hfma2(q15, s2, b2);
   const __half2 r2 = __hfma2(q26, s2, b2), r3 = __hfma2(q37, s2, b2);
   out[0] = *reinterpret_cast<const uint32_t*>(&r0);
   out[1] = *reinterpret_cast<const uint32_t*>(&r1);
   out[2] = *reinterpret_cast<const uint32_t*>(&r2);
   out[3] = *reinterpret_cast<const uint32_t*>(&r3);
+}
+
+// A group's bf16 scale and bias as the fp16 scale * 2^14 and bias that
+// dequant8_f16 takes, packed (scale low, bias high). The scaled scale is
+// exact for 2^-28 <= |scale| < 4; smaller scales move a weight by less than
+// one fp16 step. Returns false for |scale| >= 4 (scale * 2^14 past fp16),
+// which the caller reports as MOE_ERR_RANGE.
+__device__ __forceinline__ bool group_scale_bias(float s, float b, uint32_t& packed) {
+  const __half2 h = __floats2half2_rn(s * 16384.f, b);
+  packed = *reinterpret_cast<const uint32_t*>(&h);
+  return fabsf(s) < 4.f;
 }
 
 // Position of logical column n inside its group of 8 in the permuted K order

@@ -39,16 +39,34 @@
  * buffers must stay valid until the stream passes the call.
  *
  * Errors: argument, shape and workspace errors, and launch errors, are
- * returned synchronously. A device-side failure (a bounded wait that expired)
- * is written to the int32 status word of the call (route_out->status, or the
- * workspace's own status word for moe_forward without route_out) and the
- * kernels after it do no work; read it with moe_status_read.
+ * returned synchronously. A device-side failure (a bounded wait that expired,
+ * or a value outside the fp16 range below) is written to the int32 status
+ * word of the call (route_out->status, or the workspace's own status word for
+ * moe_forward without route_out) and the kernels after it do no work; read it
+ * with moe_status_read. On any nonzero status y (and r_next) are not valid.
  *
- * Numerics: logits, softmax, gate and y are fp32. Routed and shared expert
- * intermediates h and o are stored as fp16 (|value| < 65504 is required);
- * the tensor-core path feeds the MMA fp16 operands (dequantised weights and
- * x converted from bf16, which is exact for |x| >= 2^-14) with fp32
- * accumulation. Results are bit-identical from run to run (no float atomics).
+ * Numerics: logits, softmax, gate and y are fp32. The expert products take
+ * fp16 operands with fp32 accumulation: each weight is formed in fp16 as
+ * fma(q 2^-14, scale 2^14, bias), an exact product rounded once (the GEMV
+ * path keeps weights and x in fp32); x is rounded from bf16 to fp16; h (and
+ * o, except on the fused decode path, which writes y from fp32 sums) are
+ * stored as fp16. fp16 holds 11 significant bits on 2^-14 <= |v| <= 65504
+ * and a fixed step of 2^-24 below. Ranges:
+ *   x      |x| < 65520 (larger becomes inf in fp16): else MOE_ERR_RANGE.
+ *   h, o   |value| < 65520: else MOE_ERR_RANGE. At the other end, a slice of
+ *          h or o held together by one warp or block (8 to 512 values of
+ *          one row or tile) whose values are all below 2^-16 and not all
+ *          zero: MOE_ERR_RANGE (fp16's fixed step there exceeds 2^-9 of the
+ *          slice's largest value).
+ *   scale  |scale| < 4 on the fused decode and tensor-core paths (scale 2^14
+ *          must fit fp16), else MOE_ERR_RANGE; any bf16 on the GEMV path.
+ *          Small scales lose nothing beyond the weight's own rounding: a
+ *          weight below 2^-14 is an fp16 subnormal (absolute error at most
+ *          2^-25). Scales spread over 1e-7 .. 1e-4, with biases -8 scale +
+ *          N(0, 1e-3) or following the scale, keep the layer within its
+ *          tolerance (rel-L2 3e-3, max-abs 1e-2 RMS on y).
+ *   bias   any bf16 value (rounded once to fp16).
+ * Results are bit-identical from run to run (no float atomics).
  */
 #ifndef BGMOE_MOE_H
 #define BGMOE_MOE_H
@@ -70,7 +88,9 @@ typedef enum moe_status {
   MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
   MOE_ERR_DEVICE_TIMEOUT = 5,      /* a bounded device-side wait expired */
   MOE_ERR_RANGE = 6                /* a value left the fp16 range of the expert path's operands
-                                      (|x|, |h| or |o| >= 65520); the outputs are not valid */
+                                      (|x|, |h| or |o| >= 65520, a slice of h or o all under
+                                      2^-16, or |scale| >= 4 where weights are fp16; see
+                                      Numerics); the outputs are not valid */
 } moe_status;
 
 /* Shape of one call. Supported: T >= 0; H and I multiples of 64 with

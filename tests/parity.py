@@ -51,10 +51,11 @@ def experts_arg(L):
     return routed, shared
 
 
-def gpu_forward(m, spec, L, x, block_m=16, keep_route=True, path=None):
+def gpu_forward(m, spec, L, x, block_m=16, keep_route=True, path=None, check_status=True):
     """One moe_forward call through the C ABI (moe_forward_timed with the
     given expert path when `path` is set). Returns (y fp32 [T,H] on CPU,
-    routing outputs as CPU numpy arrays or None)."""
+    routing outputs as CPU numpy arrays or None); with check_status=False,
+    ((y, routing outputs), the call's device status)."""
     T = x.shape[0]
     shape = m.make_shape(T, spec.H, spec.I, spec.E, spec.top_k, spec.shared, block_m)
     dev = x.device
@@ -67,9 +68,13 @@ def gpu_forward(m, spec, L, x, block_m=16, keep_route=True, path=None):
     else:
         m.forward_timed(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro, path=path)
     torch.cuda.synchronize()
+    status = None
     if ro is not None:
-        assert m.status_read(ro["status"]) == 0
+        status = m.status_read(ro["status"])
+        assert not check_status or status == 0, m.status_string(status)
         ro = {k: v.cpu().numpy() for k, v in ro.items()}
+    if not check_status:
+        return (y.cpu().numpy(), ro), status
     return y.cpu().numpy(), ro
 
 
