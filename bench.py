@@ -929,12 +929,14 @@ def run_gdn_reference(args, spec, rank, world):
 
 # ----------------------------------------------------------- CPU oracle --
 
+ORACLE_THREADS = 1  # the C++ oracle (oracle/moe_ref.cpp) runs on the calling thread
+
 def _oracle_layer_sample(spec, layer_idx, tokens):
     """One oracle call of the workload on `tokens` of a layer; weights are
     regenerated on the CPU (not timed) and the oracle's own work (routing,
     dequantisation of every used expert, the products) is timed."""
     import numpy as np
-    import oracle
+    import oracle.cpp as oracle  # the C++ oracle, one thread
     from tests._util import bits16, expert_fn_lazy
     x = synth.activations(spec, T=max(tokens) + 1)
     wr, wsg = synth.router_weights(spec, layer_idx)
@@ -975,8 +977,8 @@ def cpu_baseline(spec, seconds):
             toks += n
         value, unit = toks / spent, "tokens/s"
         sample = f"{calls} calls of {n} sampled tokens of layer 0"
-    return {"value": round(value, 3), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": sample + " (numpy fp64; BLAS multithreaded, dequantisation single-threaded)",
+    return {"value": round(value, 3), "unit": unit, "cores": ORACLE_THREADS, "kind": "oracle",
+            "sample": sample + " (the C++ oracle: plain fp64 loops on one thread)",
             "seconds": round(spent, 2)}
 
 
@@ -1015,8 +1017,9 @@ def run_reference(args, spec, rank, world):
            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": spec.name, "T": spec.T, "H": spec.H, "I": spec.I, "E": spec.E,
                       "top_k": spec.top_k, "layers": spec.layers},
-           "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": os.cpu_count(), "kind": "oracle",
-                            "sample": sample + f"; capped at {budget:.0f} s of oracle work"},
+           "cpu_baseline": {"value": round(value, 3), "unit": unit, "cores": ORACLE_THREADS, "kind": "oracle",
+                            "sample": sample + f" (the C++ oracle: plain fp64 loops on one thread); capped at "
+                                      f"{budget:.0f} s of oracle work"},
            "e2e": {"value": round(value, 3), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     return out
 

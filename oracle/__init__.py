@@ -2,8 +2,15 @@
 
 This package is the plain, slow, fp64 statement of what the layer computes. It
 exists to check the CUDA library and to serve as the timed CPU baseline; only
-the tests, the smoke check and the benchmark's CPU-baseline leg may import it.
-The product path never calls it and shares no code with it.
+the tests, the smoke check and the benchmark's CPU legs may import it. The
+product path never calls it and shares no code with it.
+
+The MoE layer is stated twice, independently: in plain C++ (`moe_ref.cpp`,
+reached through `cpp.py`, which only marshals arguments), the oracle the GPU
+parity tests, the smoke check and the benchmark's CPU legs use; and in numpy
+(`moe.py`), which the C++ one is cross-checked against. The same pins run on
+both, and planted mistakes in either make a pin fail. The attention and
+Gated DeltaNet oracles are numpy.
 
 Sources (three web pages on Perplexity's Lily engine for Qwen3.6-35B-A3B):
   [dothoosh]  "Perplexity Lily: 1.35x faster decode for Qwen3.6 on Apple

@@ -11,7 +11,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-import oracle
+import oracle.cpp as ORACLE  # the C++ oracle (oracle/moe_ref.cpp); the numpy one cross-checks it
 import synth
 from tests._util import bits16, u32
 
@@ -79,10 +79,19 @@ def gpu_forward(m, spec, L, x, block_m=16, keep_route=True, path=None, check_sta
 
 
 def oracle_forward(spec, L, x, tokens=None):
+    """The C++ oracle's layer for the listed tokens (all by default):
+    (y fp64 [n, H], ids, weights, gate, logits)."""
     fn = layer_expert_fn(L, spec.E)
     bias = None if L.bias is None else L.bias.cpu().numpy()
     wsg = None if L.wsg is None else bits16(L.wsg)
-    return oracle.moe_forward(bits16(x), bits16(L.wr), bias, wsg, spec.top_k, fn, tokens=tokens)
+    return ORACLE.moe_forward(bits16(x), bits16(L.wr), bias, wsg, spec.top_k, fn, tokens=tokens)
+
+
+def oracle_route(spec, L, x):
+    """The C++ oracle's routing of every token: (ids, weights, gate, logits)."""
+    bias = None if L.bias is None else L.bias.cpu().numpy()
+    wsg = None if L.wsg is None else bits16(L.wsg)
+    return ORACLE.route(bits16(x), bits16(L.wr), bias, wsg, spec.top_k)
 
 
 def topk_gap(logits, top_k):
@@ -142,7 +151,7 @@ def check_y(y_gpu, y_ref, excl=None):
 def check_tables(ro, ids_gpu, spec, T, block_m):
     """Routing tables bit-exact against the oracle's, given the GPU's ids."""
     K = spec.top_k
-    tab = oracle.routing_tables(np.asarray(ids_gpu)[: T * K].reshape(T, K), spec.E, block_m, spec.shared)
+    tab = ORACLE.routing_tables(np.asarray(ids_gpu)[: T * K].reshape(T, K), spec.E, block_m, spec.shared)
     A = T * K
     assert np.array_equal(ro["counts"], tab["counts"])
     assert np.array_equal(ro["offsets"], tab["offsets"])

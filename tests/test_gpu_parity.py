@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
+import oracle.cpp as oracle  # the C++ oracle
 import synth
 from tests import parity
 from tests._util import bits16, bf16_from_f64, read_golden
@@ -18,23 +18,33 @@ pytestmark = pytest.mark.gpu
 
 
 def _run_and_check(moelib, dev, spec, block_m=16, tokens=None, layer_idx=0, path=None):
+    """One call against the oracle: routing ids (as sets), weights, gate and
+    the routing tables on every token; y on every token, or on `tokens` (a
+    seeded sample at the largest sizes, where the oracle's plain loops would
+    take minutes)."""
     L = parity.device_layer(spec, layer_idx, dev)
     x = synth.activations(spec, device=dev)
     y, ro = parity.gpu_forward(moelib, spec, L, x, block_m, path=path)
-    y_ref, ids_ref, w_ref, g_ref, logits = parity.oracle_forward(spec, L, x, tokens=tokens)
-    sel = np.arange(spec.T) if tokens is None else np.asarray(tokens)
     K = spec.top_k
     ids_gpu = ro["ids"][: spec.T * K].reshape(spec.T, K)
-    excl = parity.check_ids(ids_gpu[sel], ids_ref, logits, K)
-    ok = ~excl
+    ids_ref, w_ref, g_ref, logits = parity.oracle_route(spec, L, x)
+    excl = parity.check_ids(ids_gpu, ids_ref, logits, K)
     # The GPU logits are fp32 sums of H products (|error| < 1e-5 at H = 2048);
     # a renormalised softmax weight moves by at most 2 max|dl| relative, and
     # the gate sigmoid by at most |dl| / 4.
-    parity.check_weights(ids_gpu[sel], ro["weights"][: spec.T * K].reshape(spec.T, K)[sel], ids_ref, w_ref, ok)
+    parity.check_weights(ids_gpu, ro["weights"][: spec.T * K].reshape(spec.T, K), ids_ref, w_ref, ~excl)
     if spec.shared:
-        assert np.allclose(ro["gate"][: spec.T][sel], g_ref, rtol=0, atol=3e-6)
+        assert np.allclose(ro["gate"][: spec.T], g_ref, rtol=0, atol=3e-6)
     parity.check_tables(ro, ids_gpu, spec, spec.T, block_m)
-    return parity.check_y(y[sel], y_ref, excl)
+    sel = np.arange(spec.T) if tokens is None else np.asarray(tokens)
+    y_ref, *_ = parity.oracle_forward(spec, L, x, tokens=sel)
+    return parity.check_y(y[sel], y_ref, excl[sel])
+
+
+def _sample(T, n, seed):
+    """n of T token indices, seeded, always with the first and the last."""
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, n - 2, replace=False)]))
 
 
 def test_generator_is_device_independent(cuda_dev):
@@ -86,13 +96,15 @@ def test_prefill_zipf_512(moelib, cuda_dev):
 
 
 def test_prefill_4096(moelib, cuda_dev):
+    """Routing on all 4096 tokens; y on a seeded sample of 512."""
     spec = synth.WORKLOADS["prefill-4096"]
-    _run_and_check(moelib, cuda_dev, spec, block_m=128)
+    _run_and_check(moelib, cuda_dev, spec, block_m=128, tokens=_sample(spec.T, 512, 1))
 
 
 def test_long_skew_chunks(moelib, cuda_dev):
-    """16384 tokens in 2048-token calls reusing one workspace; every chunk is
-    checked on a token sample, the first one in full."""
+    """16384 tokens in 2048-token calls reusing one workspace; every chunk's
+    routing is checked on all its tokens, its y on a seeded sample (384
+    tokens of the first chunk, 96 of each other)."""
     spec = synth.WORKLOADS["long-skew-16384"]
     L = parity.device_layer(spec, 0, cuda_dev)
     C = spec.chunk
@@ -110,12 +122,12 @@ def test_long_skew_chunks(moelib, cuda_dev):
         moelib.forward(shape, x, L.wr, L.bias, routed, shared, L.wsg, y, ws, route_out=ro)
         torch.cuda.synchronize()
         assert moelib.status_read(ro["status"]) == 0
-        tokens = None if c == 0 else np.sort(rng.choice(C, 96, replace=False))
-        y_ref, ids_ref, w_ref, g_ref, logits = parity.oracle_forward(chunk_spec, L, x, tokens=tokens)
-        sel = np.arange(C) if tokens is None else tokens
+        sel = np.sort(rng.choice(C, 384 if c == 0 else 96, replace=False))
+        ids_ref, _, _, logits = parity.oracle_route(chunk_spec, L, x)
         ids_gpu = ro["ids"].cpu().numpy()[: C * 8].reshape(C, 8)
-        excl = parity.check_ids(ids_gpu[sel], ids_ref, logits, 8)
-        parity.check_y(y.cpu().numpy()[sel], y_ref, excl)
+        excl = parity.check_ids(ids_gpu, ids_ref, logits, 8)
+        y_ref, *_ = parity.oracle_forward(chunk_spec, L, x, tokens=sel)
+        parity.check_y(y.cpu().numpy()[sel], y_ref, excl[sel])
         counts = ro["counts"].cpu().numpy()
         b = L.bias.cpu().numpy()
         hot_share.append(counts[:256][b > 0].sum() / (C * 8))
