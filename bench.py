@@ -47,33 +47,20 @@ METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM 
 CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_expert_moe_gb300", "csrc")
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
-        bytes=17068032,
-        sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
-                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
-                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
-    ("fused_decode_layer", "decode-t4"): dict(
-        bytes=56009216 + 545280,
-        sources={"decode.cu": "57aef7ec3f818f25b161bfe151e705f0eccf6e4b7668b2090ccb960bcdaf7d38",
-                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
-                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
-    ("expert_gate_up", "prefill-4096"): dict(
-        bytes=428123904 + 27014400,
-        sources={"gemm_tc.cu": "b5977a6e1abc72896a48b429af781c9b95580b7b091780f707ca05b26b382596",
-                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
-                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
-    ("attn_block_kernel", "attn-decode-32k"): dict(
-        bytes=67168512 + 133120,
-        sources={"attention.cu": "e8f852b2fde9ed15c26282ea26849de4a6a9042311d50698380afbe9442fe08b",
-                 "tc_ptx.cuh": "8ada52aa9cacbfb73552e970d7c67f982fde376e3c25ffae8127c98264534305",
-                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
-    ("gdn_scan_kernel", "gdn-prefill-4096"): dict(
-        bytes=70285312 + 26173696,
-        sources={"gdn.cu": "3d128b3587fd6d65c176086eff0449af4c6965844316f141c7afab279f923a23",
-                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
-    ("gdn_short_kernel", "gdn-decode-b64"): dict(
-        bytes=135300352 + 82013184,
-        sources={"gdn.cu": "3d128b3587fd6d65c176086eff0449af4c6965844316f141c7afab279f923a23",
-                 "common.cuh": "5c37cb444ef31e1c7ca343030c7528ef9e162f5cde46d5bddf8e582a11661424"}),
+        bytes=17080576 + 256,
+        sources={"decode.cu": "bf02442dc68de4829fec6dc7122d2be5f9690ddc2fb2d564c178037b8312f424",
+                 "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
+                 "common.cuh": "b2898e7f4e4172621fce3d3977ca0148bb17e084e16352c0e21960aa6ce2d26a"}),
+    ("expert_gate_up", "prefill-zipf-512"): dict(
+        bytes=134323456 + 4419840,
+        sources={"gemm_tc.cu": "2c8eacf10fd447db44320e98d5a4c81be6625f99edda2286fecdfb4c96ada1c2",
+                 "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
+                 "common.cuh": "b2898e7f4e4172621fce3d3977ca0148bb17e084e16352c0e21960aa6ce2d26a"}),
+    ("expert_gate_up", "long-skew-16384"): dict(
+        bytes=338957824 + 13563648,
+        sources={"gemm_tc.cu": "2c8eacf10fd447db44320e98d5a4c81be6625f99edda2286fecdfb4c96ada1c2",
+                 "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
+                 "common.cuh": "b2898e7f4e4172621fce3d3977ca0148bb17e084e16352c0e21960aa6ce2d26a"}),
 }
 
 
