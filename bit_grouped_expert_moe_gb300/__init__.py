@@ -250,7 +250,7 @@ def forward_timed(shape, x, w_router, router_bias, experts, shared, w_shared_gat
 def test_decode_stall(shape, x, w_router, router_bias, experts, shared, w_shared_gate, y, workspace, route_out: dict,
                       stalled_block: int, timeout_ns: int, stream=None):
     """moe_test_decode_stall: the fused decode path with one block that never
-    counts its gate/up items as done, and a short device timeout."""
+    publishes the h of its gate/up items, and a short device timeout."""
     ec = _experts_c(experts)
     sc = _experts_c(shared)
     r = _route_c(route_out)

@@ -108,7 +108,6 @@ struct Workspace {
   int32_t* tile_rows;
   int32_t* num_tiles;
   uint16_t* x16;              // [T][H] fp16 activations for the tensor-core path
-  unsigned int* cnt;          // [kDecodeMaxSlots] slot counters of the fused decode kernel
   __half* dh;                 // [kDecodeMaxSlots][T][I] h of the fused decode kernel (T <= 4 only)
   __half* h;                  // [rows][I]
   __half* o;                  // [rows][H]
@@ -139,7 +138,6 @@ Workspace carve(const Geometry& g, void* base) {
   w.tile_rows = static_cast<int32_t*>(take(sizeof(int32_t) * (size_t)g.max_tiles));
   w.num_tiles = static_cast<int32_t*>(take(sizeof(int32_t)));
   w.x16 = static_cast<uint16_t*>(take(sizeof(uint16_t) * (size_t)g.T * g.H));
-  w.cnt = static_cast<unsigned int*>(take(kDecodeMaxSlots * sizeof(unsigned int)));
   w.dh = static_cast<__half*>(take(g.T <= kDecodeMaxTokens ? sizeof(__half) * (size_t)kDecodeMaxSlots * g.T * g.I : 0));
   w.h = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.I));
   w.o = static_cast<__half*>(take(sizeof(__half) * (size_t)g.rows * g.H));
@@ -309,8 +307,8 @@ moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const voi
 
 namespace {
 // moe_forward_timed, plus the test-only fused-decode stall: with
-// stall_block >= 0 that block of the fused decode kernel never counts its
-// gate/up items as done and every wait of the call gives up after timeout_ns.
+// stall_block >= 0 that block of the fused decode kernel never publishes its
+// h and every wait of the call gives up after timeout_ns.
 moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_router, const float* router_bias,
                         const moe_experts* experts, const moe_experts* shared, const void* w_shared_gate, float* y,
                         const moe_route_out* route_out, void* workspace, size_t ws_bytes, void* const* events,
@@ -407,7 +405,6 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
     d.num_tiles = r.num_tiles;
     d.status = r.status;
     d.h = w.dh;
-    d.cnt = w.cnt;
     d.y = y;
     d.x_next = static_cast<uint16_t*>(x_next);
     d.timeout_ns = timeout_ns;

@@ -12,16 +12,17 @@
 //   gate/up: an item is (slot s, 32 h columns n0..n0+31); item i goes to
 //     block i mod G, so blocks 0..I/32-1 start with a shared item. The block
 //     forms h = w silu(gate) up for its columns (the routing weight, or the
-//     shared gate, folded in), stores it to the workspace and counts the
-//     item on the slot's counter (a release).
+//     shared gate, folded in), stores it to the workspace and pushes it out
+//     to L2 with a fence.
 //   down: block b owns output rows 16b..16b+15 (W_down rows of every slot:
-//     4 KB of codes per slot, contiguous). It waits for each slot's counter
-//     to reach I/32 (an acquire), reads that slot's h and adds its products
-//     into per-warp sums; the 16 warps' sums are added in a fixed order into
-//     y, so results are bit-identical run to run.
-// No grid-wide barrier: the router's logits are exchanged through a
-// sentinel the prelude writes (a reader polls the data itself), and h
-// through the per-slot counters.
+//     4 KB of codes per slot, contiguous). It reads the h of the slots,
+//     polling each 16-byte piece until it no longer holds the sentinel the
+//     prelude wrote, and adds the products into per-warp sums; the 16 warps'
+//     sums are added in a fixed order into y, so results are bit-identical
+//     run to run.
+// No grid-wide barrier and no counters: the router's logits and h are both
+// exchanged through sentinels the prelude writes (a reader polls the data
+// itself, one L2 round trip once the data is there).
 //
 // Tasks. Every unit of work is 16 weight rows x 128 K: a gate/up task (8
 // gate rows and the matching 8 up rows of one 8-column unit, one K block)
@@ -44,9 +45,9 @@
 //   1  blocks with routed work poll the T logit rows until no entry holds
 //      the sentinel, select the top-k and build the slot table;
 //   2  routed gate/up items;
-//   3  down: slot by slot as the counters complete (h staged in shared
-//      memory in batches), then the fixed-order sum into y and the next
-//      residual row bf16(r + y) when asked for.
+//   3  down: the slots' h polled into shared memory in batches, then the
+//      fixed-order sum into y and the next residual row bf16(r + y) when
+//      asked for.
 //
 // Products on mma.sync.m16n8k16 (fp16 operands, fp32 accumulation): 16
 // weight rows x 8 token columns per instruction. Each lane dequantises whole
@@ -73,7 +74,12 @@ constexpr int kGateWarp = kDecWarps - 1;      // computes the shared gate in blo
 // produces it (a NaN result is 0x7FFFFFFF), so a reader that sees any other
 // value sees the router's output.
 constexpr uint32_t kLogitSentinel = 0xFFFFFFFFu;
-static_assert(kDecodeMaxSlots >= kDecMaxA + 1, "slot counters");
+// The prelude fills the h of every slot a call can use with this fp16
+// pattern (a NaN that float-to-half conversion never produces; a computed
+// value with these bits is stored as another NaN and reported), so a reader
+// that finds no sentinel in a piece of h reads the producer's values.
+constexpr uint16_t kHSentinel = 0xFFFFu;
+static_assert(kDecodeMaxSlots >= kDecMaxA + 1, "slot table");
 
 struct DecodeSmall {
   int ids[kDecMaxA];
@@ -87,17 +93,11 @@ struct DecodeSmall {
   float slot_wt[kDecodeMaxSlots][kDecodeMaxTokens];  // weight of token t in the slot (0: not routed there)
   const uint8_t* slot_src[kDecodeMaxSlots][6];  // gate/up codes, scales, biases; down codes, scales, biases
   int nslots;
-  int failed;        // a logit poll or a counter wait ran out
+  int failed;        // a logit poll or an h poll ran out
   int range;         // an fp16 operand (x or h) left the fp16 range
 };
 
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
   uint32_t v;
@@ -105,10 +105,23 @@ __device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
   return v;
 }
 
-// Counts on a counter: release orders the block's earlier writes (made
-// visible to this thread by the preceding block barrier) before the add.
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// 16 bytes of h read past L1 (at the GPU scope, fresh on every call).
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Whether any of the 8 halves of a piece of h still holds the sentinel.
+__device__ __forceinline__ bool has_h_sentinel(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  bool any = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) any |= (w[i] & 0xFFFFu) == kHSentinel || (w[i] >> 16) == kHSentinel;
+  return any;
 }
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -408,7 +421,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // One gate/up item: tasks k0 .. k0 + tpw - 1 of this warp's ring; then h
-  // to the workspace and the item counted on its slot's counter.
+  // to the workspace, fenced out to L2.
   auto run_item = [&](int j, int k0) {
     const int item = b + G * j, s = item / cpi, n0 = (item - s * cpi) * kItemCols;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -447,18 +460,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
           // the routing weight, which may be tiny when the expert adds
           // next to nothing to y.
           const float hu = silu_f32(v[jj]) * v[2 + jj], hw = hu * S.slot_wt[s][t];
-          const __half hv = __float2half_rn(hw);
-          if (fabsf(hw) >= 65520.f) S.range = 1;  // inf in fp16
+          __half hv = __float2half_rn(hw);
+          if (!(fabsf(hw) < 65520.f)) S.range = 1;  // inf in fp16, or NaN
+          if (__half_as_ushort(hv) == kHSentinel) hv = __ushort_as_half((unsigned short)0x7FFFu);
           big |= fabsf(hu) >= kFp16Floor;
           nz |= hu != 0.f;
-          a.h[((size_t)s * T + t) * I + pc] = hv;
+          if (b != a.stall_block) a.h[((size_t)s * T + t) * I + pc] = hv;
         }
       }
       // the unit's 8 columns of h for every token, all below the fp16 floor
       if (__any_sync(0xffffffffu, nz) && !__any_sync(0xffffffffu, big)) S.range = 1;
+      // push the h just stored out to L2 now: readers poll it there
+      __threadfence();
     }
-    __syncthreads();
-    if (tid == 0 && b != a.stall_block) red_release_add(a.cnt + s, 1u);
+    __syncthreads();  // the partial sums are read before the next item writes them
   };
 
   int k = 0;  // next task of this warp's ring
@@ -619,23 +634,36 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     const int batch = (int)(a.hst_bytes / hb_bytes);  // slots whose h fits in shared memory at once
     for (int s0 = 0; s0 < nslots; s0 += batch) {
       const int s1 = min(nslots, s0 + batch);
-      // every item of these slots counted (one thread per slot)
-      if (tid >= s0 && tid < s1) {
-        const unsigned want = (unsigned)cpi;
-        while (ld_acquire_u32(a.cnt + tid) < want) {
-          if (global_timer_ns() > deadline) {
-            S.failed = 1;
-            break;
+      // h of the batch (fp16 [slot][T][I], K-permuted): each 16-byte piece is
+      // read past L1 until none of its halves holds the prelude's sentinel
+      // (every half is written once per call), up to 4 pieces per thread in
+      // flight at a time
+      {
+        const int nch = (s1 - s0) * hb_bytes / 16;
+        const uint4* hsrc = reinterpret_cast<const uint4*>(a.h + (size_t)s0 * T * I);
+        for (int i0 = tid; i0 < nch; i0 += 4 * kDecThreads) {
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (i0 + j * kDecThreads < nch) v[j] = ld_relaxed_v4(hsrc + i0 + j * kDecThreads);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * kDecThreads;
+            if (i >= nch) continue;
+            while (has_h_sentinel(v[j])) {
+              if (global_timer_ns() > deadline) {
+                S.failed = 1;
+                break;
+              }
+              __nanosleep(128);  // fewer polls of L2 while the weights stream in
+              v[j] = ld_relaxed_v4(hsrc + i);
+            }
+            reinterpret_cast<uint4*>(hst)[i] = v[j];
           }
-          __nanosleep(32);
         }
       }
       __syncthreads();
       if (S.failed) break;
-      // h of the batch (fp16 [slot][T][I], K-permuted), read past L1
-      for (int i = tid; i < (s1 - s0) * hb_bytes / 16; i += kDecThreads)
-        reinterpret_cast<uint4*>(hst)[i] = __ldcg(reinterpret_cast<const uint4*>(a.h + (size_t)s0 * T * I) + i);
-      __syncthreads();
       // the shared slot's tasks from their own buffer
       if (s0 == 0 && sh && warp < dkb) {
         cp_async_wait_dyn(issued);  // the oldest group: the shared down task
@@ -742,18 +770,23 @@ bool decode_supported(const Geometry& g) {
   return L.total <= kDecDynamicLimit && L.hst_bytes >= (size_t)g.T * g.I * 2;
 }
 
-// Fills the call's logits with the sentinel and clears the slot counters and
-// the status word. Launched with programmatic dependent launch, it starts
-// while the previous kernel on the stream (often the previous layer's decode
-// kernel) is finishing, lets the decode kernel start at once, and waits for
-// the previous kernel to complete before it writes; the decode kernel waits
-// for this grid before it reads x, the logits or the counters.
-__global__ void decode_prelude_kernel(float* logits, int n_logits, unsigned int* cnt, int32_t* status) {
+// Fills the call's logits and the h of every slot it can use with their
+// sentinels and clears the status word. Launched with programmatic dependent
+// launch, it starts while the previous kernel on the stream (often the
+// previous layer's decode kernel, the last reader of h) is finishing, lets
+// the decode kernel start at once, and waits for the previous kernel to
+// complete before it writes; the decode kernel waits for this grid before it
+// reads x, the logits or h.
+__global__ void decode_prelude_kernel(float* logits, int n_logits, uint4* h, int h_pieces, int32_t* status) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int i = threadIdx.x; i < n_logits; i += blockDim.x) reinterpret_cast<uint32_t*>(logits)[i] = kLogitSentinel;
-  for (int i = threadIdx.x; i < kDecodeMaxSlots; i += blockDim.x) cnt[i] = 0u;
-  if (threadIdx.x == 0) *status = 0;
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < n_logits; i += blockDim.x) reinterpret_cast<uint32_t*>(logits)[i] = kLogitSentinel;
+    if (threadIdx.x == 0) *status = 0;
+  }
+  const uint32_t s2 = ((uint32_t)kHSentinel << 16) | kHSentinel;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < h_pieces; i += gridDim.x * blockDim.x)
+    h[i] = make_uint4(s2, s2, s2, s2);
 }
 
 cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStream_t stream) {
@@ -772,8 +805,10 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   {
+    // the h of every slot this call can use: T K routed + 1 shared, T rows each
+    const int h_pieces = (g.T * g.K + 1) * g.T * g.I * 2 / 16;
     cudaLaunchConfig_t pc{};
-    pc.gridDim = dim3(1);
+    pc.gridDim = dim3((h_pieces + 255) / 256);  // one 16-byte store per thread
     pc.blockDim = dim3(256);
     pc.stream = stream;
     cudaLaunchAttribute pa[1];
@@ -781,7 +816,8 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
     pa[0].val.programmaticStreamSerializationAllowed = 1;
     pc.attrs = pa;
     pc.numAttrs = 1;
-    e = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.logits, g.T * (g.E + 1), args_in.cnt, args_in.status);
+    e = cudaLaunchKernelEx(&pc, decode_prelude_kernel, args_in.logits, g.T * (g.E + 1),
+                           reinterpret_cast<uint4*>(args_in.h), h_pieces, args_in.status);
     if (e != cudaSuccess) return e;
   }
   DecodeArgs args = args_in;

@@ -94,8 +94,8 @@ struct DecodeArgs {
   const uint16_t* wsg;   // bf16 [H] shared-expert gate row, or null
   float* logits;         // [T][E+1], filled with a sentinel by the prelude, then written by the router rows
   const float* bias;     // [E] or null
-  __half* h;             // fp16 [kDecodeMaxSlots][T][I] h of every slot (K order permuted within groups of 8)
-  unsigned int* cnt;     // [kDecodeMaxSlots] gate/up items done per slot, cleared by the prelude
+  __half* h;             // fp16 [kDecodeMaxSlots][T][I] h of every slot (K order permuted within groups of 8),
+                         // filled with a sentinel by the prelude, then written once per call
   ExpertArgs gu, dn;
   int32_t* ids;
   float* weights;
@@ -112,13 +112,13 @@ struct DecodeArgs {
   float* y;              // fp32 [T][H]
   uint16_t* x_next;      // bf16 [T][H] = bf16(r + y) (the next layer's residual stream), or null
   long long timeout_ns;
-  int stall_block;       // test only: this block never counts its gate/up items (-1: none)
+  int stall_block;       // test only: this block never publishes its h (-1: none)
   // shared-memory layout, filled in by launch_decode
   long long sdn_offset, x16_offset, xf_offset, part_offset, hst_bytes;
 };
 bool decode_supported(const Geometry& g);
-// Launches the prelude (sentinel logits, cleared slot counters and status
-// word) and then the decode kernel with programmatic dependent launch.
+// Launches the prelude (sentinel logits and h, cleared status word) and then
+// the decode kernel with programmatic dependent launch.
 cudaError_t launch_decode(const DecodeArgs& args, const Geometry& g, cudaStream_t stream);
 
 cudaError_t launch_combine(const Geometry& g, const __half* o, const int32_t* inv, const float* weights,

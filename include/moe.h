@@ -299,8 +299,8 @@ moe_status moe_test_route_stall(const moe_shape* shape, const void* x, const voi
 
 /* Test hook for the fused decode kernel's failure path: moe_forward_timed
  * with MOE_PATH_FUSED_DECODE, except that block `stalled_block` of the
- * decode kernel never counts its gate/up items as done, so the blocks that
- * need those items' h wait out `timeout_ns` (0 < timeout_ns <= 1 s; every
+ * decode kernel never publishes the h of its gate/up items, so the blocks
+ * that need that h wait out `timeout_ns` (0 < timeout_ns <= 1 s; every
  * device wait of the call gives up after it). The call's status word then
  * reads MOE_ERR_DEVICE_TIMEOUT, every block has returned (having let its own
  * copies land) and the context stays usable. Same arguments as moe_forward;

@@ -367,8 +367,8 @@ def test_device_timeout_is_reported_not_hung(moelib, cuda_dev):
 
 
 def test_fused_decode_timeout_is_reported_not_hung(moelib, cuda_dev):
-    """One block of the fused decode kernel never counts its gate/up items as
-    done: the blocks that need those items' h give up after a 20 ms limit and
+    """One block of the fused decode kernel never publishes the h of its
+    gate/up items: the blocks that need that h give up after a 20 ms limit and
     return (every block lets its own copies land first), the call reports
     MOE_ERR_DEVICE_TIMEOUT, and the next normal call on the same context and
     workspace is correct."""
