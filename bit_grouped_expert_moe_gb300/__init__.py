@@ -98,7 +98,8 @@ def lib() -> ctypes.CDLL:
         L.moe_attn_workspace_bytes.argtypes = [ap, ctypes.POINTER(sz)]
         L.moe_attn_decode.argtypes = [ap, P, P, P, P, ctypes.c_float, P, P, sz, P]
         L.moe_attn_decode_timed.argtypes = [ap, P, P, P, P, ctypes.c_float, P, P, sz, ctypes.POINTER(P), P]
-        for f in ("moe_attn_workspace_bytes", "moe_attn_decode", "moe_attn_decode_timed"):
+        L.moe_attn_test_stall.argtypes = [ap, P, P, P, P, ctypes.c_float, P, P, sz, i32, ctypes.c_int64, P]
+        for f in ("moe_attn_workspace_bytes", "moe_attn_decode", "moe_attn_decode_timed", "moe_attn_test_stall"):
             getattr(L, f).restype = i32
         gp = ctypes.POINTER(GdnShape)
         L.moe_gdn_scan.argtypes = [gp, P, P, P, P, P, P, P, P, P, P, P]
@@ -300,6 +301,16 @@ def attn_decode(shape, q, k_cache, v_cache, lens, o, workspace, scale=None, stre
     _check(lib().moe_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), s,
                                  _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)), "moe_attn_decode")
+
+
+def attn_test_stall(shape, q, k_cache, v_cache, lens, o, workspace, stalled_block: int, timeout_ns: int,
+                    scale=None, stream=None):
+    """moe_attn_test_stall: attn_decode with one grid block whose producer
+    issues no cache loads and a short device timeout (test only)."""
+    s = 1.0 / (shape.D ** 0.5) if scale is None else float(scale)
+    _check(lib().moe_attn_test_stall(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(lens), s,
+                                     _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     int(stalled_block), int(timeout_ns), _stream(stream)), "moe_attn_test_stall")
 
 
 def attn_decode_timed(shape, q, k_cache, v_cache, lens, o, workspace, events, scale=None, stream=None):

@@ -4,8 +4,21 @@
 #include <cstdio>
 #include <cstring>
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "kernels.h"
+
+// An NVTX range around the enqueue of one step of the path (K1 router,
+// K2 route, K3 gate/up, K4 down, K5 combine, or the fused decode layer), so
+// that a profiler can select a step's kernels by name, e.g.
+// `ncu --nvtx --nvtx-include "K3 gate/up/"`. NVTX is header-only here: with
+// no tool attached a range costs two calls through a null hook.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 namespace bgmoe {
 
@@ -204,7 +217,11 @@ moe_status enqueue_routing_only(const Geometry& g, const float* router_bias, con
   a.state = w.state;
   a.stalled_block = stalled_block;
   a.timeout_ns = timeout_ns;
-  cudaError_t e = launch_route(a, stream);
+  cudaError_t e;
+  {
+    NvtxRange nr("K2 route");
+    e = launch_route(a, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "routing kernel launch");
   return MOE_OK;
 }
@@ -216,7 +233,10 @@ moe_status enqueue_route(const Geometry& g, const void* x, const void* w_router,
   // of the call can record a failure in it.
   cudaError_t e = cudaMemsetAsync(r.status, 0, sizeof(int32_t), stream);
   if (e != cudaSuccess) return cuda_fail(e, "status clear");
-  e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, nullptr, stream);
+  {
+    NvtxRange nr("K1 router");
+    e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, nullptr, stream);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   return enqueue_routing_only(g, router_bias, r, w, stalled_block, timeout_ns, stream);
 }
@@ -409,7 +429,10 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
     d.x_next = static_cast<uint16_t*>(x_next);
     d.timeout_ns = timeout_ns;
     d.stall_block = stall_block;
-    e = launch_decode(d, g, s);
+    {
+      NvtxRange nr("K1-K5 fused decode");
+      e = launch_decode(d, g, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "fused decode launch");
     for (int i = 3; i < 6; ++i)
       if ((e = mark(i)) != cudaSuccess) return cuda_fail(e, "event record");
@@ -421,7 +444,10 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
   // recorded a failure before it is cleared.
   e = cudaMemsetAsync(r.status, 0, sizeof(int32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "status clear");
-  e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, tc ? w.x16 : nullptr, s);
+  {
+    NvtxRange nr("K1 router");
+    e = launch_router(g, x, w_router, g.shared ? w_shared_gate : nullptr, w, r.status, tc ? w.x16 : nullptr, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "router kernel launch");
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e, "event record");
   st = enqueue_routing_only(g, router_bias, r, w, -1, kDefaultTimeoutNs, s);
@@ -435,14 +461,24 @@ moe_status forward_impl(const moe_shape* shape, const void* x, const void* w_rou
   ExpertArgs dn{experts->down.codes, experts->down.scales, experts->down.biases,
                 g.shared ? shared->down.codes : nullptr, g.shared ? shared->down.scales : nullptr,
                 g.shared ? shared->down.biases : nullptr};
-  e = tc ? launch_gate_up_tc(g, w.x16, gu, t, w.h, r.status, kDefaultTimeoutNs, s)
-         : launch_gemv_gate_up(g, static_cast<const uint16_t*>(x), gu, t, w.h, s);
+  {
+    NvtxRange nr("K3 gate/up");
+    e = tc ? launch_gate_up_tc(g, w.x16, gu, t, w.h, r.status, kDefaultTimeoutNs, s)
+           : launch_gemv_gate_up(g, static_cast<const uint16_t*>(x), gu, t, w.h, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "expert gate/up launch");
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = tc ? launch_down_tc(g, w.h, dn, t, w.o, r.status, kDefaultTimeoutNs, s) : launch_gemv_down(g, w.h, dn, t, w.o, s);
+  {
+    NvtxRange nr("K4 down");
+    e = tc ? launch_down_tc(g, w.h, dn, t, w.o, r.status, kDefaultTimeoutNs, s)
+           : launch_gemv_down(g, w.h, dn, t, w.o, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "expert down launch");
   if ((e = mark(4)) != cudaSuccess) return cuda_fail(e, "event record");
-  e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, s);
+  {
+    NvtxRange nr("K5 combine");
+    e = launch_combine(g, w.o, r.inv, r.weights, r.gate, r.status, y, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if ((e = mark(5)) != cudaSuccess) return cuda_fail(e, "event record");
   return MOE_OK;

@@ -91,6 +91,7 @@ struct Params {
   float scale_log2;  // scale * log2(e)
   int B, Hq, Hkv, L_max, slots;
   long long timeout_ns;
+  int stall_block;   // test only: this grid block's producer issues no cache loads (-1: none)
 };
 
 __device__ __forceinline__ int nblocks(int n) { return (n + kPos - 1) / kPos; }
@@ -261,11 +262,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     tc::prefetch_tmap(&tm_k);
     tc::prefetch_tmap(&tm_v);
-    int it = 0;
+    int it = 0, issued = 0;  // stages whose loads were issued (all of them unless stalled)
+    const bool stalled = (int)blockIdx.x == p.stall_block;
     for (long long j = lo; j < hi; ++j, ++it) {
       const int s = it % kStages;
       if (it >= kStages && !warp_wait(&ctl->empty[s], ((it / kStages) & 1) ^ 1)) break;
-      if (elect_one()) {
+      if (!stalled && elect_one()) {
         uint8_t* st = smem + s * S::kStageBytes;
         const int pair = cur.b * p.Hkv + cur.g;
         mbar_arrive_expect_tx(&ctl->full[s], (uint32_t)S::kStageBytes);
@@ -276,12 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
+      if (!stalled) issued = it + 1;
       cur.advance(p);
     }
     if (lane == 0 && *abort_flag) {  // let this block's own copies land before it exits
       int dummy = 0;
       const uint64_t dl = global_timer_ns() + 100000000ull;
-      for (int k = it - kStages < 0 ? 0 : it - kStages; k < it; ++k)
+      for (int k = issued - kStages < 0 ? 0 : issued - kStages; k < issued; ++k)
         mbar_wait(&ctl->full[k % kStages], (k / kStages) & 1, &dummy, dl);
     }
   } else {
@@ -724,7 +727,7 @@ cudaError_t record(void* ev, cudaStream_t s) {
 
 moe_status decode(const moe_attn_shape* shape, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* lens, float scale, float* o, void* workspace, size_t ws_bytes, void* const* events,
-                  void* stream_) {
+                  void* stream_, int stall_block = -1, long long timeout_ns = kTimeoutNs) {
   if (!shape) return MOE_ERR_INVALID_ARG;
   const moe_attn_shape s = *shape;
   if (!shape_ok(s)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -753,7 +756,7 @@ moe_status decode(const moe_attn_shape* shape, const void* q, const void* k_cach
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256 + kMaxCtas * sizeof(int32_t));
   const int slots = kMaxCtas + pairs;
   Params prm{static_cast<const uint16_t*>(q), lens, part, flags, scale * kLog2e, s.B, s.Hq, s.Hkv, s.L_max, slots,
-             kTimeoutNs};
+             timeout_ns, stall_block};
   if (events && (e = record(events[0], stream)) != cudaSuccess)
     return fail(e, "event record");
   switch (s.D) {
@@ -806,6 +809,14 @@ moe_status moe_attn_decode_timed(const moe_attn_shape* shape, const void* q, con
                                  size_t ws_bytes, void* const* events, void* stream) {
   if (!events || !events[0] || !events[1] || !events[2]) return MOE_ERR_INVALID_ARG;
   return decode(shape, q, k_cache, v_cache, lens, scale, o, workspace, ws_bytes, events, stream);
+}
+
+moe_status moe_attn_test_stall(const moe_attn_shape* shape, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* lens, float scale, float* o, void* workspace, size_t ws_bytes,
+                               int32_t stalled_block, int64_t timeout_ns, void* stream) {
+  if (stalled_block < 0 || timeout_ns <= 0 || timeout_ns > kTimeoutNs) return MOE_ERR_INVALID_ARG;
+  return decode(shape, q, k_cache, v_cache, lens, scale, o, workspace, ws_bytes, nullptr, stream, stalled_block,
+                timeout_ns);
 }
 
 }  // extern "C"

@@ -81,6 +81,19 @@ moe_status moe_attn_decode_timed(const moe_attn_shape* shape, const void* q, con
                                  const void* v_cache, const int32_t* lens, float scale, float* o, void* workspace,
                                  size_t ws_bytes, void* const* events, void* stream);
 
+/* Test hook for the block kernel's failure path: moe_attn_decode, except that
+ * grid block `stalled_block` (0-based, below the grid of one block per SM; a
+ * block past the grid changes nothing) issues none of its cache loads, so its
+ * consumers' bounded waits run out after `timeout_ns` (0 < timeout_ns <= 1 s;
+ * every wait of the call gives up after it). The call's status word (the
+ * first 4 bytes of the workspace) then reads MOE_ERR_DEVICE_TIMEOUT, no block
+ * exits with a copy in flight, o is not valid, and the context stays usable.
+ * INVALID_ARG for a negative block or a timeout out of range; the other
+ * checks are moe_attn_decode's. */
+moe_status moe_attn_test_stall(const moe_attn_shape* shape, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* lens, float scale, float* o, void* workspace, size_t ws_bytes,
+                               int32_t stalled_block, int64_t timeout_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -148,6 +148,10 @@ def test_attention_host_side_errors_before_any_cuda_call(moelib):
     for bad in (0.0, -1.0, float("inf"), float("nan")):
         assert call(ctypes.byref(sh), q, k, v, lens, bad, o, ws, need, None) == 1
     assert L.moe_attn_decode_timed(ctypes.byref(sh), q, k, v, lens, 0.0625, o, ws, need, None, None) == 1
+    # the stall hook: a negative block or a timeout out of (0, 1 s] is refused
+    # before any CUDA call
+    for blk, to in [(-1, 10**6), (0, 0), (0, -5), (0, 10**10)]:
+        assert L.moe_attn_test_stall(ctypes.byref(sh), q, k, v, lens, 0.0625, o, ws, need, blk, to, None) == 1
 
 
 @pytest.mark.parametrize("shape,code", [

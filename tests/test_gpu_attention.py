@@ -134,3 +134,23 @@ def test_attention_invalid_length_sets_status(moelib):
     moelib.attn_decode(sh, q, k, v, lens, o, ws)
     assert moelib.status_read(ws[:4].view(torch.int32)) == moelib.MOE_ERR_INVALID_ARG
     assert torch.all(o == 7.0)
+
+
+def test_attention_timeout_is_reported_not_hung(moelib):
+    """One grid block issues none of its cache loads: its consumers' waits
+    run out after a 20 ms limit, the block exits with nothing in flight, the
+    call reports MOE_ERR_DEVICE_TIMEOUT, and the next normal call on the same
+    context and workspace matches the oracle."""
+    # 32768 positions = 1024 fixed blocks over 2 KV heads: every grid block has a run
+    spec = synth.AttnSpec("stall", lens=(32768,), Hq=16, Hkv=2, D=128)
+    q, k, v, lens = synth.attn_inputs(spec, device=DEV)
+    sh = moelib.attn_shape(spec.B, spec.Hq, spec.Hkv, spec.D, spec.Lmax)
+    ws = moelib.attn_alloc_workspace(sh, DEV)
+    o = torch.zeros(spec.B, spec.Hq, spec.D, dtype=torch.float32, device=DEV)
+    moelib.attn_test_stall(sh, q, k, v, lens, o, ws, stalled_block=3, timeout_ns=20_000_000)
+    torch.cuda.synchronize()
+    assert moelib.status_read(ws[:4].view(torch.int32)) == moelib.MOE_ERR_DEVICE_TIMEOUT
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    got = _run(moelib, qc, kc, vc, lens.cpu())
+    want = gqa_decode_attention(bits16(qc), bits16(kc), bits16(vc), spec.lens)
+    assert np.all(np.abs(got - want) <= _bound(qc, kc, vc, spec.lens))
