@@ -22,7 +22,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libbgmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE = 0, 1, 2
-MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_RANGE = 3, 4, 5, 6
+MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_RANGE, MOE_ERR_BOUNDS = 3, 4, 5, 6, 7
 PATH_AUTO, PATH_GEMV, PATH_TENSOR_CORE, PATH_FUSED_DECODE = 0, 1, 2, 3
 
 P = ctypes.c_void_p

@@ -33,15 +33,27 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+# The bounds-checking debug build: every index read from a device-written
+# table is checked before use and an out-of-range one reported as
+# MOE_ERR_BOUNDS (see checked() in csrc/common.cuh). It links to its own file.
+DEBUG_LIB = os.path.join(PKG, "libbgmoe_bounds.so")
+DEBUG_FLAGS = ("-DBGMOE_BOUNDS_CHECK",)
+
+
+def build_bounds_checked(verbose: bool = False, force: bool = False) -> str:
+    """The bounds-checking variant of the library (libbgmoe_bounds.so)."""
+    return build(verbose, force, DEBUG_FLAGS, build_dir=os.path.join(BUILD, "bounds"), lib=DEBUG_LIB)
+
+
+def build(verbose: bool = False, force: bool = False, extra_flags=(), build_dir: str = BUILD, lib: str = LIB) -> str:
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))
                      + glob.glob(os.path.join(ROOT, "include", "*.h")))
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src] + headers):
             cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
             r = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,12 +65,12 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    if force or _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs]
+    if force or _stale(lib, objs):
+        cmd = [nvcc, *ARCH, "-shared", "-o", lib, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

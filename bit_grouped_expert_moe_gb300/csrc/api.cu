@@ -275,6 +275,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
     case MOE_ERR_RANGE: return "a value left the fp16 operand range";
+    case MOE_ERR_BOUNDS: return "a device table index was out of range (bounds-checking build)";
   }
   return "unknown status";
 }

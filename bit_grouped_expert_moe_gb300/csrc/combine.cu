@@ -24,7 +24,7 @@ combine_kernel(int H, int K, int A, int shared, const __half* __restrict__ o, co
   float wt[kMaxTopK + 1];
 #pragma unroll
   for (int k = 0; k < kMaxTopK; ++k) {
-    rows[k] = k < K ? inv[(size_t)t * K + k] : 0;
+    rows[k] = k < K ? checked(inv[(size_t)t * K + k], 0, A - 1, status) : 0;
     wt[k] = k < K ? weights[(size_t)t * K + k] : 0.f;
   }
   rows[kMaxTopK] = A + t;

@@ -158,6 +158,27 @@ __device__ __forceinline__ bool fp16_overflows(float v) { return fabsf(v) >= 655
 // the precision the rest of the path keeps.
 constexpr float kFp16Floor = 1.52587890625e-05f;  // 2^-16
 
+// Debug build (-DBGMOE_BOUNDS_CHECK): an index read from a table that another
+// kernel or block wrote is checked against its range before it is used. A
+// value outside [lo, hi] is replaced by lo and MOE_ERR_BOUNDS recorded in the
+// status word (unless a failure is already there), so the access stays
+// inside its buffer and every barrier protocol still runs to the end; the
+// result of the call is then not valid. Without the flag the index passes
+// through unchanged and the check costs nothing.
+__device__ __forceinline__ int checked(int v, int lo, int hi, const int32_t* status) {
+#ifdef BGMOE_BOUNDS_CHECK
+  if (v < lo || v > hi) {
+    atomicCAS(const_cast<int32_t*>(status), 0, (int32_t)MOE_ERR_BOUNDS);
+    return lo;
+  }
+#else
+  (void)lo;
+  (void)hi;
+  (void)status;
+#endif
+  return v;
+}
+
 // A kernel after the routing kernel does nothing once a device error is set.
 __device__ __forceinline__ bool device_failed(const int32_t* status) {
   return *reinterpret_cast<const volatile int32_t*>(status) != 0;

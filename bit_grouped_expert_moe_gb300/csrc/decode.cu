@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       }
       __syncwarp();
       for (int q = lane + sh; q < d + sh; q += 32) {  // weight addresses of the routed slots
-        const int ex = S.slot_e[q];
+        const int ex = checked(S.slot_e[q], 0, E - 1, a.status);
         S.slot_src[q][0] = reinterpret_cast<const uint8_t*>(a.gu.codes + (size_t)ex * 2 * I * (H / 8));
         S.slot_src[q][1] = reinterpret_cast<const uint8_t*>(a.gu.scales + (size_t)ex * 2 * I * gpr);
         S.slot_src[q][2] = reinterpret_cast<const uint8_t*>(a.gu.biases + (size_t)ex * 2 * I * gpr);
@@ -588,8 +588,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     for (int i = tid; i < A; i += kDecThreads) {
       a.ids[i] = S.ids[i];
       a.weights[i] = S.w[i];
-      a.sorted[S.pos[i]] = i;
-      a.inv[i] = S.pos[i];
+      const int pos = checked(S.pos[i], 0, A - 1, a.status);
+      a.sorted[pos] = i;
+      a.inv[i] = pos;
     }
     if (a.shared)
       for (int t = tid; t < T; t += kDecThreads) a.gate[t] = S.g[t];

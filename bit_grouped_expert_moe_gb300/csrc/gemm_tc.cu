@@ -119,6 +119,7 @@ struct TcParams {
   __half* out;                // gate/up: h [rows][I]; down: o [rows][H]
   int32_t* status;
   long long timeout_ns;
+  int rows;                   // rows of h and o: A (+ T with a shared expert)
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
@@ -260,7 +261,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     bool ok = true;
     int rows_nx = p.t.tile_rows[blockIdx.x / p.per_tile];  // looked up a whole item ahead
     for (int w = blockIdx.x; ok && w < items; w += G, ++ii) {
-      const int N = (rows_nx + 15) & ~15;
+      const int N = (checked(rows_nx, 1, p.BM, p.status) + 15) & ~15;  // TMEM holds N <= 128 columns
       if (w + G < items) rows_nx = p.t.tile_rows[(w + G) / p.per_tile];
       const uint32_t idesc = idesc_f16_f32(128, N);
       const int buf = ii & 1;
@@ -305,13 +306,14 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       bool ok = true;
       for (int w = blockIdx.x; ok && w < items; w += G) {
         const int tile = w / p.per_tile;
-        const int row0 = p.t.tile_row0[tile], rows = p.t.tile_rows[tile];
+        const int rows = checked(p.t.tile_rows[tile], 1, p.BM, p.status);
+        const int row0 = checked(p.t.tile_row0[tile], 0, p.rows - rows, p.status);
         const int N = (rows + 15) & ~15;
         int tok[kMaxBN / 16];
 #pragma unroll
         for (int q = 0; q < kMaxBN / 16; ++q) {
           const int j = j0 + 16 * q, r = row0 + j;
-          tok[q] = j < rows ? (r < p.A ? p.t.sorted[r] / p.K : r - p.A) : 0;
+          tok[q] = j < rows ? checked(r < p.A ? p.t.sorted[r] / p.K : r - p.A, 0, p.A / p.K - 1, p.status) : 0;
         }
         for (int k = 0; k < num_k; ++k, ++it) {
           const int bs = it % kBS;
@@ -350,7 +352,7 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     const bool chunked = (gpr & 7) == 0;
     auto rows_of = [&](int w, int r, const uint16_t*& srow, const uint16_t*& brow) {
       const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
-      const int e = p.t.tile_expert[tile];
+      const int e = checked(p.t.tile_expert[tile], 0, p.E, p.status);
       const bool sh = e == p.E;
       size_t wrow;
       if (kGateUp) wrow = (size_t)(r < 128 ? 0 : I) + sub * 128 + (r & 127) + (sh ? 0 : (size_t)e * 2 * I);
@@ -488,7 +490,8 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     int ii = 0;
     for (int w = blockIdx.x; w < items; w += G, ++ii) {
       const int tile = w / p.per_tile, sub = w - tile * p.per_tile;
-      const int row0 = p.t.tile_row0[tile], rows = p.t.tile_rows[tile];
+      const int rows = checked(p.t.tile_rows[tile], 1, p.BM, p.status);
+      const int row0 = checked(p.t.tile_row0[tile], 0, p.rows - rows, p.status);
       const int N = (rows + 15) & ~15;
       const int buf = ii & 1;
       if (!mbar_wait(&ctl->acc_full[buf], (ii >> 1) & 1, abort_flag, deadline)) break;
@@ -634,7 +637,7 @@ cudaError_t launch_gate_up_tc(const Geometry& g, const uint16_t* x16, const Expe
     tms = tm;
   }
   TcParams p{g.H, g.I, g.E, g.K, g.A, g.BM, 0, g.I / 128, w.scales, w.biases, w.s_scales, w.s_biases, x16, t, h,
-             status, timeout_ns};
+             status, timeout_ns, g.rows};
   return launch_tc<true>(g, tm, tms, tm, p, stream);
 }
 
@@ -655,7 +658,7 @@ cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs&
               CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
   TcParams p{g.H, g.I, g.E, g.K, g.A, g.BM, 0, g.H / 256, w.scales, w.biases, w.s_scales, w.s_biases, nullptr, t, o,
-             status, timeout_ns};
+             status, timeout_ns, g.rows};
   return launch_tc<false>(g, tm, tms, tmh, p, stream);
 }
 

@@ -63,14 +63,17 @@ __device__ __forceinline__ void dot32(const uint4 c, float s, float b, const flo
 
 template <int kMaxIt>  // 16-byte loads per lane per weight row: ceil(H / 1024)
 __global__ void __launch_bounds__(kGemvWarps * 32)
-gemv_gate_up_kernel(int H, int I, int E, int K, int A, const uint16_t* __restrict__ x, ExpertArgs w,
+gemv_gate_up_kernel(int H, int I, int E, int K, int A, int rows_total, const uint16_t* __restrict__ x, ExpertArgs w,
                     TileArgs t, __half* __restrict__ h) {
   extern __shared__ __align__(16) float xs[];  // [kTokChunk][H/32][kPad]
   __shared__ int tok_s[kTokChunk];
   const int tile = blockIdx.x;
   if (block_failed(t.status) || tile >= *t.num_tiles) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = t.tile_expert[tile], r0 = t.tile_row0[tile], nr = t.tile_rows[tile];
+  const int T = A / K;
+  const int e = checked(t.tile_expert[tile], 0, E, t.status);
+  const int nr = checked(t.tile_rows[tile], 1, rows_total, t.status);  // rows of h: A (+ T with a shared expert)
+  const int r0 = checked(t.tile_row0[tile], 0, rows_total - nr, t.status);
   const bool sh = e == E;
   const size_t mat_words = (size_t)2 * I * (H / 8), mat_groups = (size_t)2 * I * (H / kGroup);
   const uint32_t* codes = sh ? w.s_codes : w.codes + (size_t)e * mat_words;
@@ -101,7 +104,7 @@ gemv_gate_up_kernel(int H, int I, int E, int K, int A, const uint16_t* __restric
     __syncthreads();
     if (threadIdx.x < nc) {
       const int r = r0 + c0 + threadIdx.x;
-      tok_s[threadIdx.x] = r < A ? t.sorted[r] / K : r - A;
+      tok_s[threadIdx.x] = checked(r < A ? t.sorted[r] / K : r - A, 0, T - 1, t.status);
     }
     __syncthreads();
     stage_rows(xs, x, tok_s, nc, H);
@@ -150,14 +153,16 @@ gemv_gate_up_kernel(int H, int I, int E, int K, int A, const uint16_t* __restric
 
 // Down projection: o[r][m] = sum_n h[r][n] * W_down[m][n].
 __global__ void __launch_bounds__(kGemvWarps * 32)
-gemv_down_kernel(int H, int I, int E, int rows_per_block, const __half* __restrict__ hbuf, ExpertArgs w,
+gemv_down_kernel(int H, int I, int E, int rows_total, int rows_per_block, const __half* __restrict__ hbuf, ExpertArgs w,
                  TileArgs t, __half* __restrict__ o) {
   extern __shared__ __align__(16) float hs[];  // [kTokChunk][I/32][kPad]
   __shared__ int row_s[kTokChunk];
   const int tile = blockIdx.x;
   if (block_failed(t.status) || tile >= *t.num_tiles) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = t.tile_expert[tile], r0 = t.tile_row0[tile], nr = t.tile_rows[tile];
+  const int e = checked(t.tile_expert[tile], 0, E, t.status);
+  const int nr = checked(t.tile_rows[tile], 1, rows_total, t.status);  // rows of h and o: A (+ T)
+  const int r0 = checked(t.tile_row0[tile], 0, rows_total - nr, t.status);
   const bool sh = e == E;
   const size_t mat_words = (size_t)H * (I / 8), mat_groups = (size_t)H * (I / kGroup);
   const uint32_t* codes = sh ? w.s_codes : w.codes + (size_t)e * mat_words;
@@ -226,7 +231,7 @@ static cudaError_t launch_gate_up_it(const Geometry& g, const uint16_t* x, const
   cudaError_t e = ensure_smem(gemv_gate_up_kernel<kIt>, smem, &smem_memo);
   if (e != cudaSuccess) return e;
   dim3 grid(g.max_tiles, g.I / kGemvWarps);
-  gemv_gate_up_kernel<kIt><<<grid, kGemvWarps * 32, smem, stream>>>(g.H, g.I, g.E, g.K, g.A, x, w, t, h);
+  gemv_gate_up_kernel<kIt><<<grid, kGemvWarps * 32, smem, stream>>>(g.H, g.I, g.E, g.K, g.A, g.rows, x, w, t, h);
   return cudaGetLastError();
 }
 
@@ -250,7 +255,7 @@ cudaError_t launch_gemv_down(const Geometry& g, const __half* h, const ExpertArg
   cudaError_t e = ensure_smem(gemv_down_kernel, smem, &smem_memo);
   if (e != cudaSuccess) return e;
   dim3 grid(g.max_tiles, (g.H + rows_per_block - 1) / rows_per_block);
-  gemv_down_kernel<<<grid, kGemvWarps * 32, smem, stream>>>(g.H, g.I, g.E, rows_per_block, h, w, t, o);
+  gemv_down_kernel<<<grid, kGemvWarps * 32, smem, stream>>>(g.H, g.I, g.E, g.rows, rows_per_block, h, w, t, o);
   return cudaGetLastError();
 }
 

@@ -198,10 +198,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   for (int base = lo; base < hi; base += 32) {
     const int i = base + lane;
     const bool valid = i < hi;
-    const int e = valid ? ids_s[i] : -1;
+    const int e = valid ? checked(ids_s[i], 0, E - 1, a.status) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     if (valid) {
-      const int pos = offs_s[e] + prefix_s[e] + hist[warp * E + e] + __popc(peers & lanemask_lt());
+      const int pos = checked(offs_s[e] + prefix_s[e] + hist[warp * E + e] + __popc(peers & lanemask_lt()), 0,
+                              a.T * K - 1, a.status);
       const int ag = t0 * K + i;
       a.sorted[pos] = ag;
       a.inv[ag] = pos;

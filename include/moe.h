@@ -87,10 +87,12 @@ typedef enum moe_status {
   MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* ws_bytes < moe_workspace_bytes() */
   MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
   MOE_ERR_DEVICE_TIMEOUT = 5,      /* a bounded device-side wait expired */
-  MOE_ERR_RANGE = 6                /* a value left the fp16 range of the expert path's operands
+  MOE_ERR_RANGE = 6,               /* a value left the fp16 range of the expert path's operands
                                       (|x|, |h| or |o| >= 65520, a slice of h or o all under
                                       2^-16, or |scale| >= 4 where weights are fp16; see
                                       Numerics); the outputs are not valid */
+  MOE_ERR_BOUNDS = 7               /* debug build only (BGMOE_BOUNDS_CHECK): an index read from a
+                                      device-written table was out of range; the outputs are not valid */
 } moe_status;
 
 /* Shape of one call. Supported: T >= 0; H and I multiples of 64 with
