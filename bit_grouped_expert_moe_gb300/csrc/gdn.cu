@@ -19,7 +19,9 @@
 // instead of once per row: k^ and q^ (normalised, fp32), alpha = exp(gate),
 // beta and v, so the per-token chain is loads, two dot products and the update.
 // Thread t of a row holds the 16-byte column pieces t, t+8, t+16, t+24, so the
-// 8 threads of a row read 8 consecutive pieces (no bank conflicts).
+// 8 threads of a row read 8 consecutive pieces (no bank conflicts; the rows
+// of the staged and prepared arrays are padded so that the prepare pass,
+// which spans two tokens per access phase, has none either).
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -37,18 +39,30 @@ constexpr int kThreads = kRows * kTPR;
 constexpr float kEps = 1e-6f;
 constexpr int kChunk = 32;       // tokens staged per shared-memory buffer
 
+// Row paddings of the shared-memory arrays. The prepare pass has 4 threads
+// per token, so each 8-thread phase of a 16-byte access covers two tokens:
+// with unpadded rows (256 B of bf16, 512 B of fp32, both multiples of the
+// 128-byte bank cycle) the two tokens hit the same banks. A bf16 row of 320 B
+// moves the next token by 4 bank groups of 16 B (the 8 accesses of a phase
+// then cover all 8 groups, and a cp.async target stays 16-byte aligned); an
+// fp32 row of 132 floats moves it by one group, which interleaves the two
+// tokens' groups the same way; 17 floats per value row spread the scalar v
+// stores.
+constexpr int kPadH = 32;  // bf16 elements
+constexpr int kPadF = 4;   // fp32 elements
+
 struct Stage {  // raw inputs of one chunk (cp.async target)
-  uint16_t k[kChunk][kD];
-  uint16_t q[kChunk][kD];
+  uint16_t k[kChunk][kD + kPadH];
+  uint16_t q[kChunk][kD + kPadH];
   uint16_t v[kChunk][kRows];
   float gate[kChunk];
   float beta[kChunk];
 };
 
 struct Prepared {  // what the token loop reads
-  float k[kChunk][kD];  // k^
-  float q[kChunk][kD];  // q^ (with 1/sqrt(Dk))
-  float v[kChunk][kRows];
+  float k[kChunk][kD + kPadF];  // k^
+  float q[kChunk][kD + kPadF];  // q^ (with 1/sqrt(Dk))
+  float v[kChunk][kRows + 1];
   float alpha[kChunk];
   float beta[kChunk];
 };
