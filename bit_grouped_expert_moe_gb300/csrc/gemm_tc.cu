@@ -370,10 +370,16 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
     auto stage = [&](__half2 sa, __half2 ba, __half2 sb, __half2 bb) -> bool {
       const int cs = it % kCS, as = it % kAS;
       if (!mbar_wait(&ctl->c_full[cs], (it / kCS) & 1, abort_flag, deadline)) return false;
-      const uint4 a0 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes);
-      const uint4 a1 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes + 16);
-      const uint4 b0 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes + 4096);
-      const uint4 b1 = *reinterpret_cast<const uint4*>(crow0 + cs * kCBytes + 4096 + 16);
+      // Each row's 32 bytes of codes as two 16-byte loads. The code tiles land
+      // with the 32-byte TMA swizzle (16-byte chunk c of row r at chunk
+      // c ^ ((r >> 2) & 1)), so the 8 rows of an access phase cover all 8
+      // bank groups instead of 4.
+      const int hf = (gt >> 2) & 1;
+      const uint8_t* cr = crow0 + cs * kCBytes;
+      const uint4 a0 = *reinterpret_cast<const uint4*>(cr + 16 * hf);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(cr + 16 * (hf ^ 1));
+      const uint4 b0 = *reinterpret_cast<const uint4*>(cr + 4096 + 16 * hf);
+      const uint4 b1 = *reinterpret_cast<const uint4*>(cr + 4096 + 16 * (hf ^ 1));
       {
         const int j = it - kAS + kAMargin;  // the MMAs of stage j must be complete
         if (j >= 0 && !mbar_wait(&ctl->stage_done[j % kDone], (j / kDone) & 1, abort_flag, deadline)) return false;
@@ -627,11 +633,11 @@ cudaError_t launch_gate_up_tc(const Geometry& g, const uint16_t* x16, const Expe
                               __half* h, int32_t* status, long long timeout_ns, cudaStream_t stream) {
   CUtensorMap tm, tms;
   cudaError_t e = tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, w.codes, g.H / 8, (uint64_t)g.E * 2 * g.I, 8, 128,
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
+                          CU_TENSOR_MAP_SWIZZLE_32B);
   if (e != cudaSuccess) return e;
   if (g.shared) {
     e = tmap_2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, w.s_codes, g.H / 8, (uint64_t)2 * g.I, 8, 128,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
+                CU_TENSOR_MAP_SWIZZLE_32B);
     if (e != cudaSuccess) return e;
   } else {
     tms = tm;
@@ -645,11 +651,11 @@ cudaError_t launch_down_tc(const Geometry& g, const __half* h, const ExpertArgs&
                            int32_t* status, long long timeout_ns, cudaStream_t stream) {
   CUtensorMap tm, tms, tmh;
   cudaError_t e = tmap_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, w.codes, g.I / 8, (uint64_t)g.E * g.H, 8, 128,
-                          CU_TENSOR_MAP_SWIZZLE_NONE);
+                          CU_TENSOR_MAP_SWIZZLE_32B);
   if (e != cudaSuccess) return e;
   if (g.shared) {
     e = tmap_2d(&tms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, w.s_codes, g.I / 8, (uint64_t)g.H, 8, 128,
-                CU_TENSOR_MAP_SWIZZLE_NONE);
+                CU_TENSOR_MAP_SWIZZLE_32B);
     if (e != cudaSuccess) return e;
   } else {
     tms = tm;
