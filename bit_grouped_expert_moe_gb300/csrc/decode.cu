@@ -12,8 +12,7 @@
 //   gate/up: an item is (slot s, 32 h columns n0..n0+31); item i goes to
 //     block i mod G, so blocks 0..I/32-1 start with a shared item. The block
 //     forms h = w silu(gate) up for its columns (the routing weight, or the
-//     shared gate, folded in), stores it to the workspace and pushes it out
-//     to L2 with a fence.
+//     shared gate, folded in) and stores it to the workspace.
 //   down: block b owns output rows 16b..16b+15 (W_down rows of every slot:
 //     4 KB of codes per slot, contiguous). It reads the h of the slots,
 //     polling each 16-byte piece until it no longer holds the sentinel the
@@ -156,31 +155,33 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 }
 
 // One task's products: this lane's 32 K of fragment rows g and g+8 (16-byte
-// code chunks at c * 16 of rows g and g + 8 of the slot, their scale and
-// bias from the slot's pair of groups) against the B fragments xb[w]
+// code chunks at c * 16 of rows g and g + 8 of the slot; the task's two
+// groups' scales at sb[row * rs + 0, 1] and biases at sb[row * rs + bo + 0, 1],
+// in bf16) against the B fragments xb[w]
 // (permuted activations, 8 K per 16-byte word): 8 MMAs. With g = lane / 4
 // and c = lane % 4, MMA k slots 2c, 2c+1, 2c+8, 2c+9 of word w hold K
-// offsets 8w + {0,4}, {1,5} (first MMA) and 8w + {2,6}, {3,7} (second), on A
-// and B alike. Returns false when a scale of 4 or more (scale * 2^14 past
-// fp16) was met.
-__device__ __forceinline__ bool task_mma(float (&d)[4], const uint8_t* t, int g8, int c4, const uint4 (&xb)[4]) {
+// offsets 8w + {0,4}, {1,5} (first MMA, into d0) and 8w + {2,6}, {3,7}
+// (second, into d1), on A and B alike: two accumulator chains, since one
+// warp's dependent MMAs are what this phase waits on. Returns false when a
+// scale of 4 or more (scale * 2^14 past fp16) was met.
+__device__ __forceinline__ bool task_mma(float (&d0)[4], float (&d1)[4], const uint8_t* t, const uint16_t* sb,
+                                         int rs, int bo, int g8, int c4, const uint4 (&xb)[4]) {
   const uint4 r0 = *reinterpret_cast<const uint4*>(t + g8 * 64 + c4 * 16);
   const uint4 r1 = *reinterpret_cast<const uint4*>(t + (8 + g8) * 64 + c4 * 16);
-  const uint16_t* sb = reinterpret_cast<const uint16_t*>(t + 1024);  // per row: scale pair, bias pair
   const int gs = c4 >> 1;  // this lane's 32 K lie in the second group of the pair when c >= 2
   // scale * 2^14 and bias per row (tc::dequant8_f16)
-  const __half2 s0 = __float2half2_rn(bf16_bits_to_f32(sb[g8 * 4 + gs]) * 16384.f);
-  const __half2 b0 = __float2half2_rn(bf16_bits_to_f32(sb[g8 * 4 + 2 + gs]));
-  const __half2 s1 = __float2half2_rn(bf16_bits_to_f32(sb[(8 + g8) * 4 + gs]) * 16384.f);
-  const __half2 b1 = __float2half2_rn(bf16_bits_to_f32(sb[(8 + g8) * 4 + 2 + gs]));
+  const __half2 s0 = __float2half2_rn(bf16_bits_to_f32(sb[g8 * rs + gs]) * 16384.f);
+  const __half2 b0 = __float2half2_rn(bf16_bits_to_f32(sb[g8 * rs + bo + gs]));
+  const __half2 s1 = __float2half2_rn(bf16_bits_to_f32(sb[(8 + g8) * rs + gs]) * 16384.f);
+  const __half2 b1 = __float2half2_rn(bf16_bits_to_f32(sb[(8 + g8) * rs + bo + gs]));
   const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     uint32_t p0[4], p1[4];
     tc::dequant8_f16(w0[w], s0, b0, p0);
     tc::dequant8_f16(w1[w], s1, b1, p1);
-    mma_16816(d, p0[0], p1[0], p0[1], p1[1], xb[w].x, xb[w].y);
-    mma_16816(d, p0[2], p1[2], p0[3], p1[3], xb[w].z, xb[w].w);
+    mma_16816(d0, p0[0], p1[0], p0[1], p1[1], xb[w].x, xb[w].y);
+    mma_16816(d1, p0[2], p1[2], p0[3], p1[3], xb[w].z, xb[w].w);
   }
   return !(__hisinf(__low2half(s0)) | __hisinf(__low2half(s1)));
 }
@@ -201,26 +202,31 @@ __device__ __forceinline__ void task_copy(uint8_t* td, const uint8_t* codes, con
   cp_async4(td + 1024 + r * 8 + kind * 4, (kind ? bi : sc) + (size_t)row * gpr + 2 * kb);
 }
 
-// x[t] . row for the router: lane l holds bf16 elements 8 (l + 32 q) .. +7 of
-// the row in w4[q]; the activations are fp32 in shared memory; fp32 sums in
-// lane order, then a butterfly over the warp (every lane gets the result).
-__device__ __forceinline__ float row_dot(const uint4 (&w4)[8], const float* xrow, int rvec, int lane) {
-  float acc = 0.f;
+// x[t] . row for the router: lane l holds bf16 elements 8 (l + 32 q) .. +7
+// of the row in w4[q]; the activations are fp32 in shared memory, elements
+// 8v..8v+3 at xrow[4v] and 8v+4..8v+7 at xrow[H/2 + 4v] (consecutive lanes
+// read consecutive 16-byte words). Four fp32 sums per lane (element pairs
+// 0-1, 2-3, 4-5, 6-7 of each vector, in q order), added as (0+1)+(2+3),
+// then a butterfly over the warp (every lane gets the result): one warp's
+// dependent chain is what this step waits on, so it is kept short.
+__device__ __forceinline__ float row_dot(const uint4 (&w4)[8], const float* xrow, int H, int rvec, int lane) {
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int v = lane + 32 * q;
     if (v < rvec) {
-      const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
-      const float4 xa = *reinterpret_cast<const float4*>(xrow + (size_t)v * 8);
-      const float4 xc = *reinterpret_cast<const float4*>(xrow + (size_t)v * 8 + 4);
+      const float4 xa = reinterpret_cast<const float4*>(xrow)[v];
+      const float4 xc = reinterpret_cast<const float4*>(xrow + H / 2)[v];
       const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+      const uint32_t ww[4] = {w4[q].x, w4[q].y, w4[q].z, w4[q].w};
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        acc = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), xv[2 * m], acc);
-        acc = fmaf(bf16_bits_to_f32(ww[m] >> 16), xv[2 * m + 1], acc);
+        a[m] = fmaf(bf16_bits_to_f32(ww[m] & 0xFFFFu), xv[2 * m], a[m]);
+        a[m] = fmaf(__uint_as_float(ww[m] & 0xFFFF0000u), xv[2 * m + 1], a[m]);
       }
     }
   }
+  float acc = (a[0] + a[1]) + (a[2] + a[3]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   return acc;
@@ -343,11 +349,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
           f[2 * q] = bf16_bits_to_f32(wv[q] & 0xFFFFu);
           f[2 * q + 1] = bf16_bits_to_f32(wv[q] >> 16);
         }
+        float s0 = 0.f, s1 = 0.f;  // two chains, then added: shorter dependences
 #pragma unroll
-        for (int q = 0; q < 8; ++q) ss[t] = fmaf(f[q], f[q], ss[t]);
-        float4* dst = reinterpret_cast<float4*>(xf + (size_t)t * H + (size_t)v * 8);
-        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        for (int q = 0; q < 4; ++q) {
+          s0 = fmaf(f[q], f[q], s0);
+          s1 = fmaf(f[4 + q], f[4 + q], s1);
+        }
+        ss[t] += s0 + s1;
+        // the router's layout: elements 8v..8v+3 at [4v], 8v+4..8v+7 at [H/2 + 4v]
+        reinterpret_cast<float4*>(xf + (size_t)t * H)[v] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(xf + (size_t)t * H + H / 2)[v] = make_float4(f[4], f[5], f[6], f[7]);
       }
   if (a.norm) {
 #pragma unroll
@@ -359,18 +370,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   }
   __syncthreads();
   if (a.norm && tid < T) {
-    float tot = 0.f;
-    for (int w = 0; w < kDecWarps; ++w) tot += part[w * kDecodeMaxTokens + tid];
+    float q4[4];  // the 16 warps' partials as a tree: 4 sums of 4, then pairs
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      q4[j] = (part[(4 * j) * kDecodeMaxTokens + tid] + part[(4 * j + 1) * kDecodeMaxTokens + tid]) +
+              (part[(4 * j + 2) * kDecodeMaxTokens + tid] + part[(4 * j + 3) * kDecodeMaxTokens + tid]);
+    const float tot = (q4[0] + q4[1]) + (q4[2] + q4[3]);
     S.inv_rms[tid] = 1.f / sqrtf(tot / (float)H + a.norm_eps);
   }
   __syncthreads();
   // the layer input: x (or RMSNorm(r) = r / rms(r) * gain, kept in fp32 for
   // the router), and its fp16 copy in the permuted K order for the MMAs
   for (int i = tid; i < T * H / 8; i += kDecThreads) {
-    const int t = i / (H / 8);
-    float4* src = reinterpret_cast<float4*>(xf + (size_t)i * 8);
+    const int t = i / (H / 8), v = i - t * (H / 8);
+    float4* src0 = reinterpret_cast<float4*>(xf + (size_t)t * H) + v;
+    float4* src1 = reinterpret_cast<float4*>(xf + (size_t)t * H + H / 2) + v;
     float f[8];
-    const float4 fa = src[0], fc = src[1];
+    const float4 fa = *src0, fc = *src1;
     f[0] = fa.x, f[1] = fa.y, f[2] = fa.z, f[3] = fa.w, f[4] = fc.x, f[5] = fc.y, f[6] = fc.z, f[7] = fc.w;
     if (a.norm) {
       const float s = S.inv_rms[t];
@@ -382,8 +398,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
         f[2 * q] = f[2 * q] * s * bf16_bits_to_f32(gv[q] & 0xFFFFu);
         f[2 * q + 1] = f[2 * q + 1] * s * bf16_bits_to_f32(gv[q] >> 16);
       }
-      src[0] = make_float4(f[0], f[1], f[2], f[3]);
-      src[1] = make_float4(f[4], f[5], f[6], f[7]);
+      *src0 = make_float4(f[0], f[1], f[2], f[3]);
+      *src1 = make_float4(f[4], f[5], f[6], f[7]);
     }
     bool big = false;
 #pragma unroll
@@ -404,14 +420,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   // for the other blocks; the shared gate itself where a shared item is here
   if (router_warp)
     for (int t = 0; t < T; ++t) {
-      const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
+      const float l = row_dot(w4, xf + (size_t)t * H, H, rvec, lane);
       // an atomic exchange is performed at L2, where the polling blocks read
       // (a plain store could sit in this SM's L1 for microseconds)
       if (lane == 0) atomicExch(a.logits + (size_t)t * (E + 1) + rrow, l);
     }
   if (shared_first && warp == kGateWarp)
     for (int t = 0; t < T; ++t) {
-      const float l = row_dot(w4, xf + (size_t)t * H, rvec, lane);
+      const float l = row_dot(w4, xf + (size_t)t * H, H, rvec, lane);
       if (lane == 0) {
         S.g[t] = 1.f / (1.f + expf(-l));
         S.slot_wt[0][t] = S.g[t];
@@ -421,10 +437,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // One gate/up item: tasks k0 .. k0 + tpw - 1 of this warp's ring; then h
-  // to the workspace, fenced out to L2.
+  // to the workspace.
   auto run_item = [&](int j, int k0) {
     const int item = b + G * j, s = item / cpi, n0 = (item - s * cpi) * kItemCols;
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float d[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
     for (int jj = 0; jj < tpw; ++jj) {
       const int k = k0 + jj;
       wait_task(k);
@@ -434,12 +450,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 #pragma unroll
       for (int w = 0; w < 4; ++w)
         xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(xrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-      if (!task_mma(d, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb)) S.range = 1;
+      const uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
+      if (!task_mma(d, d1, td, reinterpret_cast<const uint16_t*>(td + 1024), 4, 2, g8, c4, xb)) S.range = 1;
       __syncwarp();  // the slot is read: refill it
       if (issued < n_items * tpw + n_dn) issue_task(issued++);
     }
 #pragma unroll
-    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r];
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = d[r] + d1[r];
     __syncthreads();
     if (warp < kUnits) {
       // unit u = warp: warps u, u+4, u+8, u+12 hold its partial sums (fixed
@@ -447,9 +464,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       float v[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r)
-        v[r] = ((part[(warp * 4 + r) * 32 + lane] + part[((warp + 4) * 4 + r) * 32 + lane]) +
-                part[((warp + 8) * 4 + r) * 32 + lane]) +
-               part[((warp + 12) * 4 + r) * 32 + lane];
+        v[r] = (part[(warp * 4 + r) * 32 + lane] + part[((warp + 4) * 4 + r) * 32 + lane]) +
+               (part[((warp + 8) * 4 + r) * 32 + lane] + part[((warp + 12) * 4 + r) * 32 + lane]);
       const int pc = tc::perm8_pos(n0 + 8 * warp + g8);
       bool big = false, nz = false;
 #pragma unroll
@@ -470,8 +486,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       }
       // the unit's 8 columns of h for every token, all below the fp16 floor
       if (__any_sync(0xffffffffu, nz) && !__any_sync(0xffffffffu, big)) S.range = 1;
-      // push the h just stored out to L2 now: readers poll it there
-      __threadfence();
+      // no fence: every half of h is written once and readers poll each half
+      // for the sentinel at L2, so nothing is ordered after these stores; a
+      // fence here waited for this warp's copies still in flight as well
+      // (decode-t1 14.85 -> 14.53 us per layer without it)
     }
     __syncthreads();  // the partial sums are read before the next item writes them
   };
@@ -630,7 +648,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 
   // ---- phase 3: down, for the blocks with output rows
   if (has_rows && routed) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};  // rows g, g+8 x tokens 2c, 2c+1, over this warp's down tasks
+    // rows g, g+8 x tokens 2c, 2c+1, over this warp's down tasks (two chains)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     const int hb_bytes = T * I * 2;
     const int batch = (int)(a.hst_bytes / hb_bytes);  // slots whose h fits in shared memory at once
     for (int s0 = 0; s0 < nslots; s0 += batch) {
@@ -674,7 +693,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-        if (!task_mma(acc, sdn + (size_t)warp * kTaskBytes, g8, c4, xb)) S.range = 1;
+        const uint8_t* td = sdn + (size_t)warp * kTaskBytes;
+        if (!task_mma(acc, acc1, td, reinterpret_cast<const uint16_t*>(td + 1024), 4, 2, g8, c4, xb)) S.range = 1;
       }
       // the routed slots' tasks of this batch, in ring order
       for (; k < ntasks; ++k) {
@@ -687,7 +707,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-        if (!task_mma(acc, ring + (size_t)(k % kSlots) * kTaskBytes, g8, c4, xb)) S.range = 1;
+        const uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
+        if (!task_mma(acc, acc1, td, reinterpret_cast<const uint16_t*>(td + 1024), 4, 2, g8, c4, xb)) S.range = 1;
         __syncwarp();
         if (issued < ntasks) issue_task(issued++);
       }
@@ -695,13 +716,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     }
     // the 16 warps' sums in a fixed order: y and the next residual row
 #pragma unroll
-    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = acc[r];
+    for (int r = 0; r < 4; ++r) part[(warp * 4 + r) * 32 + lane] = acc[r] + acc1[r];
     __syncthreads();
     if (!S.failed && tid < 16 * T) {
       const int t = tid >> 4, row = tid & 15;
       const int ln = (row & 7) * 4 + (t >> 1), r = (t & 1) + ((row >> 3) << 1);
-      float y = 0.f;
-      for (int w = 0; w < kDecWarps; ++w) y += part[(w * 4 + r) * 32 + ln];
+      float q4[4];  // the 16 warps' sums as a tree: 4 sums of 4, then pairs
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        q4[j] = (part[((4 * j) * 4 + r) * 32 + ln] + part[((4 * j + 1) * 4 + r) * 32 + ln]) +
+                (part[((4 * j + 2) * 4 + r) * 32 + ln] + part[((4 * j + 3) * 4 + r) * 32 + ln]);
+      const float y = (q4[0] + q4[1]) + (q4[2] + q4[3]);
       const int m = 16 * b + row;
       a.y[(size_t)t * H + m] = y;
       if (a.x_next) {
