@@ -84,7 +84,6 @@ struct DecodeSmall {
   int ids[kDecMaxA];
   float w[kDecMaxA];
   float g[kDecodeMaxTokens];                   // shared gate per token
-  float inv_rms[kDecodeMaxTokens];             // 1 / rms of each token's residual row (pre-norm join)
   int pos[kDecMaxA];                           // expert-sorted position of assignment a
   int slot_e[kDecodeMaxSlots];                 // expert of each slot (slot 0 = shared when present)
   int slot_n[kDecodeMaxSlots];                 // rows (tokens) of the slot
@@ -330,17 +329,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
   if (router_warp) load_row(w4, rrow < E ? a.wr + (size_t)rrow * H : a.wsg, rvec, lane);
   if (shared_first && warp == kGateWarp) load_row(w4, a.wsg, rvec, lane);
 
+  // the gain row (a weight too): vector v = tid of it (H / 8 <= 256 vectors)
+  uint4 gw = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0 pairs
+  if (a.norm && a.norm_w && tid < H / 8) gw = ldg_nc_v4(a.norm_w + (size_t)tid * 8);
+
   // x (and this call's workspace) may be the previous kernel's output: wait
   // for the prelude, which itself waits for the previous layer's kernels.
   grid_dep_wait();
-  // x as fp32 (exact from bf16); with the pre-norm join, the sum of squares
-  // of each token's residual row as well (fixed order: per thread, then the
-  // warp butterfly, then the warps in order)
+  // The layer input x, or with the pre-norm join x = RMSNorm(r) = r / rms(r)
+  // * gain, in two parts. First every thread turns its vectors of the input
+  // row into fp32 (exact from bf16), times the gain, into xf in the router's
+  // layout (elements 8v..8v+3 at [4v], 8v+4..8v+7 at [H/2 + 4v]), with each
+  // token's sum of squares of r (per thread, the warp butterfly, then a tree
+  // over the warps: inv_rms below). The router rows are dotted with r * gain
+  // and scaled by 1 / rms(r) at the end, so the second part (the normalised
+  // fp16 copy for the MMAs and its range check) is left to the warps that
+  // have no top-k to run and is needed only once the routing is known.
   float ss[kDecodeMaxTokens] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
 #pragma unroll
-  for (int t = 0; t < kDecodeMaxTokens; ++t)
-    if (t < T)
-      for (int v = tid; v < H / 8; v += kDecThreads) {
+    for (int t = 0; t < kDecodeMaxTokens; ++t)
+      if (t < T && tid < H / 8) {
+        const int v = tid;
         const uint4 u = ldg_nc_v4(a.x + (size_t)t * H + (size_t)v * 8);
         const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
         float f[8];
@@ -355,11 +366,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
           s0 = fmaf(f[q], f[q], s0);
           s1 = fmaf(f[4 + q], f[4 + q], s1);
         }
-        ss[t] += s0 + s1;
-        // the router's layout: elements 8v..8v+3 at [4v], 8v+4..8v+7 at [H/2 + 4v]
+        ss[t] = s0 + s1;
+        if (a.norm)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            f[2 * q] *= bf16_bits_to_f32(gv[q] & 0xFFFFu);
+            f[2 * q + 1] *= bf16_bits_to_f32(gv[q] >> 16);
+          }
         reinterpret_cast<float4*>(xf + (size_t)t * H)[v] = make_float4(f[0], f[1], f[2], f[3]);
         reinterpret_cast<float4*>(xf + (size_t)t * H + H / 2)[v] = make_float4(f[4], f[5], f[6], f[7]);
       }
+  }
   if (a.norm) {
 #pragma unroll
     for (int t = 0; t < kDecodeMaxTokens; ++t) {
@@ -369,69 +386,60 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
     }
   }
   __syncthreads();
-  if (a.norm && tid < T) {
-    float q4[4];  // the 16 warps' partials as a tree: 4 sums of 4, then pairs
+  // 1 / rms(r) of token t from the 16 warps' partials (a tree: 4 sums of 4,
+  // then pairs), or 1 without the join
+  auto inv_rms = [&](int t) -> float {
+    if (!a.norm) return 1.f;
+    float q4[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      q4[j] = (part[(4 * j) * kDecodeMaxTokens + tid] + part[(4 * j + 1) * kDecodeMaxTokens + tid]) +
-              (part[(4 * j + 2) * kDecodeMaxTokens + tid] + part[(4 * j + 3) * kDecodeMaxTokens + tid]);
+      q4[j] = (part[(4 * j) * kDecodeMaxTokens + t] + part[(4 * j + 1) * kDecodeMaxTokens + t]) +
+              (part[(4 * j + 2) * kDecodeMaxTokens + t] + part[(4 * j + 3) * kDecodeMaxTokens + t]);
     const float tot = (q4[0] + q4[1]) + (q4[2] + q4[3]);
-    S.inv_rms[tid] = 1.f / sqrtf(tot / (float)H + a.norm_eps);
-  }
-  __syncthreads();
-  // the layer input: x (or RMSNorm(r) = r / rms(r) * gain, kept in fp32 for
-  // the router), and its fp16 copy in the permuted K order for the MMAs
-  for (int i = tid; i < T * H / 8; i += kDecThreads) {
-    const int t = i / (H / 8), v = i - t * (H / 8);
-    float4* src0 = reinterpret_cast<float4*>(xf + (size_t)t * H) + v;
-    float4* src1 = reinterpret_cast<float4*>(xf + (size_t)t * H + H / 2) + v;
-    float f[8];
-    const float4 fa = *src0, fc = *src1;
-    f[0] = fa.x, f[1] = fa.y, f[2] = fa.z, f[3] = fa.w, f[4] = fc.x, f[5] = fc.y, f[6] = fc.z, f[7] = fc.w;
-    if (a.norm) {
-      const float s = S.inv_rms[t];
-      uint4 gw = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // bf16 1.0 pairs
-      if (a.norm_w) gw = ldg_nc_v4(a.norm_w + (size_t)(i - t * (H / 8)) * 8);
-      const uint32_t gv[4] = {gw.x, gw.y, gw.z, gw.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        f[2 * q] = f[2 * q] * s * bf16_bits_to_f32(gv[q] & 0xFFFFu);
-        f[2 * q + 1] = f[2 * q + 1] * s * bf16_bits_to_f32(gv[q] >> 16);
-      }
-      *src0 = make_float4(f[0], f[1], f[2], f[3]);
-      *src1 = make_float4(f[4], f[5], f[6], f[7]);
-    }
-    bool big = false;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) big |= fabsf(f[q]) >= 65520.f;  // becomes inf in fp16
-    if (big) S.range = 1;
-    const __half2 p0 = __floats2half2_rn(f[0], f[4]), p1 = __floats2half2_rn(f[1], f[5]);
-    const __half2 p2 = __floats2half2_rn(f[2], f[6]), p3 = __floats2half2_rn(f[3], f[7]);
-    uint4 o;
-    o.x = *reinterpret_cast<const uint32_t*>(&p0);
-    o.y = *reinterpret_cast<const uint32_t*>(&p1);
-    o.z = *reinterpret_cast<const uint32_t*>(&p2);
-    o.w = *reinterpret_cast<const uint32_t*>(&p3);
-    reinterpret_cast<uint4*>(x16)[i] = o;
-  }
-  __syncthreads();
+    return 1.f / sqrtf(tot / (float)H + a.norm_eps);
+  };
 
   // ---- phase R: router logits l[t][r] (r = E: the shared gate row), stored
   // for the other blocks; the shared gate itself where a shared item is here
   if (router_warp)
     for (int t = 0; t < T; ++t) {
-      const float l = row_dot(w4, xf + (size_t)t * H, H, rvec, lane);
+      const float l = row_dot(w4, xf + (size_t)t * H, H, rvec, lane) * inv_rms(t);
       // an atomic exchange is performed at L2, where the polling blocks read
       // (a plain store could sit in this SM's L1 for microseconds)
       if (lane == 0) atomicExch(a.logits + (size_t)t * (E + 1) + rrow, l);
     }
   if (shared_first && warp == kGateWarp)
     for (int t = 0; t < T; ++t) {
-      const float l = row_dot(w4, xf + (size_t)t * H, H, rvec, lane);
+      const float l = row_dot(w4, xf + (size_t)t * H, H, rvec, lane) * inv_rms(t);
       if (lane == 0) {
         S.g[t] = 1.f / (1.f + expf(-l));
         S.slot_wt[0][t] = S.g[t];
       }
+    }
+  // The normalised input in fp16, in the permuted K order, for the MMAs, by
+  // warps T..15 (warps below T run the top-k next); fp16 keeps |x| < 65520.
+  if (warp >= T)
+    for (int i = tid - 32 * T; i < T * H / 8; i += kDecThreads - 32 * T) {
+      const int t = i / (H / 8), v = i - t * (H / 8);
+      const float4 fa = reinterpret_cast<const float4*>(xf + (size_t)t * H)[v];
+      const float4 fc = reinterpret_cast<const float4*>(xf + (size_t)t * H + H / 2)[v];
+      const float sc = inv_rms(t);
+      float f[8] = {fa.x, fa.y, fa.z, fa.w, fc.x, fc.y, fc.z, fc.w};
+      bool big = false;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        f[q] *= sc;
+        big |= fabsf(f[q]) >= 65520.f;  // becomes inf in fp16
+      }
+      if (big) S.range = 1;
+      const __half2 p0 = __floats2half2_rn(f[0], f[4]), p1 = __floats2half2_rn(f[1], f[5]);
+      const __half2 p2 = __floats2half2_rn(f[2], f[6]), p3 = __floats2half2_rn(f[3], f[7]);
+      uint4 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&p0);
+      o.y = *reinterpret_cast<const uint32_t*>(&p1);
+      o.z = *reinterpret_cast<const uint32_t*>(&p2);
+      o.w = *reinterpret_cast<const uint32_t*>(&p3);
+      reinterpret_cast<uint4*>(x16)[i] = o;
     }
   // The next call's prelude may launch now: it waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -496,6 +504,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
 
   int k = 0;  // next task of this warp's ring
   if (shared_first) {
+    __syncthreads();  // x16 is complete
     run_item(0, 0);
     k = tpw;
   }
