@@ -693,33 +693,41 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_layer_kernel(const Deco
       }
       __syncthreads();
       if (S.failed) break;
-      // the shared slot's tasks from their own buffer
-      if (s0 == 0 && sh && warp < dkb) {
-        cp_async_wait_dyn(issued);  // the oldest group: the shared down task
+      // this batch's tasks in order through one copy of the product code: the
+      // shared slot's task first (from its own buffer, in the first batch),
+      // then the routed slots' ring tasks
+      bool own = s0 == 0 && sh && warp < dkb;
+      for (;;) {
+        const uint8_t* td;
+        int s, kc;
+        if (own) {
+          cp_async_wait_dyn(issued);  // the oldest group: the shared down task
+          td = sdn + (size_t)warp * kTaskBytes;
+          s = 0;
+          kc = warp;
+        } else {
+          if (k >= ntasks) break;
+          const int q = warp + kDecWarps * (k - n_items * tpw);
+          s = sh + q / dkb;
+          kc = q - (s - sh) * dkb;
+          if (s >= s1) break;
+          cp_async_wait_dyn(issued - k - 1);
+          td = ring + (size_t)(k % kSlots) * kTaskBytes;
+        }
         __syncwarp();
-        uint4 xb[4];
-        const __half* hrow = hst + (size_t)(g8 < T ? g8 : 0) * I + warp * 128 + 32 * c4;
-#pragma unroll
-        for (int w = 0; w < 4; ++w)
-          xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-        const uint8_t* td = sdn + (size_t)warp * kTaskBytes;
-        if (!task_mma(acc, acc1, td, reinterpret_cast<const uint16_t*>(td + 1024), 4, 2, g8, c4, xb)) S.range = 1;
-      }
-      // the routed slots' tasks of this batch, in ring order
-      for (; k < ntasks; ++k) {
-        const int q = warp + kDecWarps * (k - n_items * tpw);
-        const int s = sh + q / dkb, kc = q - (s - sh) * dkb;
-        if (s >= s1) break;
-        wait_task(k);
         uint4 xb[4];
         const __half* hrow = hst + ((size_t)(s - s0) * T + (g8 < T ? g8 : 0)) * I + kc * 128 + 32 * c4;
 #pragma unroll
         for (int w = 0; w < 4; ++w)
           xb[w] = g8 < T ? *reinterpret_cast<const uint4*>(hrow + 8 * w) : make_uint4(0u, 0u, 0u, 0u);
-        const uint8_t* td = ring + (size_t)(k % kSlots) * kTaskBytes;
         if (!task_mma(acc, acc1, td, reinterpret_cast<const uint16_t*>(td + 1024), 4, 2, g8, c4, xb)) S.range = 1;
         __syncwarp();
-        if (issued < ntasks) issue_task(issued++);
+        if (own) {
+          own = false;
+        } else {
+          ++k;
+          if (issued < ntasks) issue_task(issued++);
+        }
       }
       __syncthreads();  // the batch's h is read
     }
