@@ -47,20 +47,20 @@ METRIC = "MoE-layer tokens/s (prefill) & µs/layer (decode); % of BF16 TC / HBM 
 CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_expert_moe_gb300", "csrc")
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
-        bytes=17080576 + 256,
-        sources={"decode.cu": "bf02442dc68de4829fec6dc7122d2be5f9690ddc2fb2d564c178037b8312f424",
+        bytes=17084416 + 2048,
+        sources={"decode.cu": "2e22962576e6fdedfd39210cf362eaafa11c5a3d2e157f5138e1c6ddb823fa8d",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
-                 "common.cuh": "b2898e7f4e4172621fce3d3977ca0148bb17e084e16352c0e21960aa6ce2d26a"}),
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-zipf-512"): dict(
-        bytes=134323456 + 4419840,
-        sources={"gemm_tc.cu": "2c8eacf10fd447db44320e98d5a4c81be6625f99edda2286fecdfb4c96ada1c2",
+        bytes=134096640 + 4404480,
+        sources={"gemm_tc.cu": "740d06935fc5ebbbd2f6eed21900ef53b5da617d58b27d310df7ec61d143bfa7",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
-                 "common.cuh": "b2898e7f4e4172621fce3d3977ca0148bb17e084e16352c0e21960aa6ce2d26a"}),
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
-        bytes=338957824 + 13563648,
-        sources={"gemm_tc.cu": "2c8eacf10fd447db44320e98d5a4c81be6625f99edda2286fecdfb4c96ada1c2",
+        bytes=338956032 + 14036992,
+        sources={"gemm_tc.cu": "740d06935fc5ebbbd2f6eed21900ef53b5da617d58b27d310df7ec61d143bfa7",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
-                 "common.cuh": "b2898e7f4e4172621fce3d3977ca0148bb17e084e16352c0e21960aa6ce2d26a"}),
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
 }
 
 
