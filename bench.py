@@ -56,6 +56,19 @@ PROFILED_TRAFFIC = {
         sources={"gemm_tc.cu": "740d06935fc5ebbbd2f6eed21900ef53b5da617d58b27d310df7ec61d143bfa7",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
+    ("attn_block_kernel", "attn-decode-32k"): dict(
+        bytes=67168768 + 154112,
+        sources={"attention.cu": "67f37e5399b9ed695e74164575c004b001aab86a4e69cf8343d4638d21e0a4c6",
+                 "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
+    ("gdn_scan_kernel", "gdn-prefill-4096"): dict(
+        bytes=70285824 + 25867776,
+        sources={"gdn.cu": "339557a34a9bfaba2e0943b1aa6090ab83f5a3e506864ca491ee1e56e8527aec",
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
+    ("gdn_short_kernel", "gdn-decode-b64"): dict(
+        bytes=135301376 + 81671424,
+        sources={"gdn.cu": "339557a34a9bfaba2e0943b1aa6090ab83f5a3e506864ca491ee1e56e8527aec",
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
         bytes=338956032 + 14036992,
         sources={"gemm_tc.cu": "740d06935fc5ebbbd2f6eed21900ef53b5da617d58b27d310df7ec61d143bfa7",
