@@ -52,8 +52,8 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-zipf-512"): dict(
-        bytes=134096640 + 4404480,
-        sources={"gemm_tc.cu": "740d06935fc5ebbbd2f6eed21900ef53b5da617d58b27d310df7ec61d143bfa7",
+        bytes=132907264 + 4936960,
+        sources={"gemm_tc.cu": "d390cf2ddf266fae9db04d1fee78b291057db3a3c415a968009435ea35ce6d07",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
@@ -70,8 +70,8 @@ PROFILED_TRAFFIC = {
         sources={"gdn.cu": "339557a34a9bfaba2e0943b1aa6090ab83f5a3e506864ca491ee1e56e8527aec",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
-        bytes=338956032 + 14036992,
-        sources={"gemm_tc.cu": "740d06935fc5ebbbd2f6eed21900ef53b5da617d58b27d310df7ec61d143bfa7",
+        bytes=329211648 + 13866752,
+        sources={"gemm_tc.cu": "d390cf2ddf266fae9db04d1fee78b291057db3a3c415a968009435ea35ce6d07",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
 }

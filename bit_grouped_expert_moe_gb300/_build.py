@@ -45,6 +45,18 @@ def build_bounds_checked(verbose: bool = False, force: bool = False) -> str:
     return build(verbose, force, DEBUG_FLAGS, build_dir=os.path.join(BUILD, "bounds"), lib=DEBUG_LIB)
 
 
+# Variants of the tensor-core expert GEMM's ring depths (codes, A, B), built to
+# their own files for the test that checks results do not depend on them.
+RING_VARIANTS = {"a4b4": ("-DBGMOE_TC_AS=4", "-DBGMOE_TC_BS=4"),
+                 "a5b3c2": ("-DBGMOE_TC_AS=5", "-DBGMOE_TC_BS=3", "-DBGMOE_TC_CS=2")}
+
+
+def build_ring_variant(name: str, verbose: bool = False, force: bool = False) -> str:
+    """The library with other ring depths in the expert GEMM (libbgmoe_<name>.so)."""
+    return build(verbose, force, RING_VARIANTS[name], build_dir=os.path.join(BUILD, name),
+                 lib=os.path.join(PKG, f"libbgmoe_{name}.so"))
+
+
 def build(verbose: bool = False, force: bool = False, extra_flags=(), build_dir: str = BUILD, lib: str = LIB) -> str:
     os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
