@@ -53,7 +53,7 @@ PROFILED_TRAFFIC = {
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-zipf-512"): dict(
         bytes=132907264 + 4936960,
-        sources={"gemm_tc.cu": "d390cf2ddf266fae9db04d1fee78b291057db3a3c415a968009435ea35ce6d07",
+        sources={"gemm_tc.cu": "ae3aea6886508ff1992d00133154d5cda66e2eb85b7e61455a10fecfc1cbe272",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
@@ -71,7 +71,7 @@ PROFILED_TRAFFIC = {
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
         bytes=329211648 + 13866752,
-        sources={"gemm_tc.cu": "d390cf2ddf266fae9db04d1fee78b291057db3a3c415a968009435ea35ce6d07",
+        sources={"gemm_tc.cu": "ae3aea6886508ff1992d00133154d5cda66e2eb85b7e61455a10fecfc1cbe272",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
 }

@@ -23,7 +23,7 @@
 // Persistent blocks (one per SM) walk the items with a stride of the grid;
 // every ring runs on across item boundaries and the TMEM accumulator is
 // double buffered, so one item's epilogue overlaps the next item's MMAs.
-// Rings: codes (TMA) 4 deep, dequantised A 3 deep, B 5 deep; the MMAs of
+// Rings: codes (TMA) 4 deep, dequantised A 3 deep, B 4 deep; the MMAs of
 // each stage are committed once, to a ring of 8 stage-done barriers that
 // every producer of a slot waits on.
 // Warp roles (576 threads):

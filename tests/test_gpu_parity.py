@@ -322,8 +322,9 @@ def test_deterministic(moelib, cuda_dev):
 def test_tensor_core_repeatable(moelib, cuda_dev, name, bm):
     """The tensor-core path has no atomics, so repeated runs must agree bit
     for bit; a ring-slot race between the dequantisation, gather and MMA
-    warps would show up as differing values (and does, in builds that let
-    the dequantisation run three stages ahead of the completed MMAs)."""
+    warps would show up as differing values (and did, in an earlier layout
+    whose dequantisation ran three stages ahead of the completed MMAs; builds
+    with other ring depths are checked in test_gpu_ring_depths.py)."""
     spec = synth.WORKLOADS[name]
     L = parity.device_layer(spec, 0, cuda_dev)
     x = synth.activations(spec, device=cuda_dev)
