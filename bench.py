@@ -48,7 +48,7 @@ CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "bit_grouped_exp
 PROFILED_TRAFFIC = {
     ("fused_decode_layer", "decode-t1"): dict(
         bytes=17084416 + 2048,
-        sources={"decode.cu": "2e22962576e6fdedfd39210cf362eaafa11c5a3d2e157f5138e1c6ddb823fa8d",
+        sources={"decode.cu": "8a228a712d37d2c49389418197e855d6786da04591294aecee6811eff5f4dbf7",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-zipf-512"): dict(

@@ -846,7 +846,7 @@ cudaError_t launch_decode(const DecodeArgs& args_in, const Geometry& g, cudaStre
   int per_sm = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_layer_kernel, kDecThreads, L.total);
   if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  if (!all_blocks_resident(per_sm, grid, grid)) return cudaErrorCooperativeLaunchTooLarge;
   {
     // the h of every slot this call can use: T K routed + 1 shared, T rows each
     const int h_pieces = (g.T * g.K + 1) * g.T * g.I * 2 / 16;

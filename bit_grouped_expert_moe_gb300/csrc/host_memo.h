@@ -19,6 +19,16 @@ namespace bgmoe {
 
 constexpr int kMaxDevices = 64;
 
+// Whether a grid whose blocks wait for one another (each polls data that
+// other blocks write, with no grid barrier the runtime would check) can have
+// every block resident at once: `blocks_per_sm` is the occupancy the runtime
+// reports for the kernel's block size and shared memory. A launch that fails
+// this is refused, not attempted: its resident blocks would wait until their
+// deadline for blocks that never start.
+inline bool all_blocks_resident(int blocks_per_sm, int sm_count, int grid) {
+  return blocks_per_sm >= 1 && sm_count >= 1 && grid >= 1 && (long long)grid <= (long long)blocks_per_sm * sm_count;
+}
+
 // The largest dynamic shared-memory size allowed so far for one kernel.
 class SmemLimitMemo {
  public:

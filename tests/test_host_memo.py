@@ -2,7 +2,9 @@
 plain C++ program on the CPU: a kernel's raised shared-memory limit and a
 device array's address are remembered per device and per context, so a
 second device, or a new context on the same device (as after
-cudaDeviceReset), runs the set-up again, and concurrent host threads agree."""
+cudaDeviceReset), runs the set-up again, and concurrent host threads agree.
+The same program checks the residency rule the fused decode launch applies
+before it starts a grid whose blocks wait for one another."""
 import os
 import shutil
 import subprocess
@@ -63,6 +65,15 @@ int main() {
   for (auto& t : th) t.join();
   CHECK(tcalls == 1);
   for (int r : rc) CHECK(r == 0);
+
+  // the fused decode launch's residency rule: one block per SM on every SM
+  CHECK(all_blocks_resident(1, 152, 152));
+  CHECK(all_blocks_resident(2, 152, 304));
+  CHECK(!all_blocks_resident(0, 152, 152));   // the block does not fit on an SM at all
+  CHECK(!all_blocks_resident(1, 152, 153));   // more blocks than can be resident
+  CHECK(!all_blocks_resident(1, 0, 1));
+  CHECK(!all_blocks_resident(1, 152, 0));
+  CHECK(all_blocks_resident(1 << 20, 1 << 20, 1 << 30));  // no overflow in the product
   std::printf("ok\n");
   return 0;
 }
