@@ -92,6 +92,31 @@ __device__ __forceinline__ float row_sum(float x) {
   return x;
 }
 
+// Two fp32 lanes packed in 64 bits (lane 0 in the low half, as a float2 in
+// memory). The packed operations round each lane exactly as the scalar ones
+// (fma.rn / mul.rn per lane), so a pair of scalar chains run as one packed
+// chain gives the same bits with half the instructions.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float2 unpack2(uint64_t v) {
+  float2 f;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(v));
+  return f;
+}
+
 __device__ __forceinline__ void cp_async(void* dst, const void* src, int bytes16) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   if (bytes16)
@@ -111,14 +136,14 @@ __global__ void __launch_bounds__(kThreads) gdn_scan_kernel(const Params p) {
   const int tc = threadIdx.x % kTPR;   // column pieces tc, tc+8, tc+16, tc+24 (4 columns each)
 
   const size_t srow = (((size_t)b * p.Hv + h) * kD + row) * kD;
-  float S[kCols];
+  // this thread's 16 state columns as 8 packed pairs: S2[2j], S2[2j + 1] hold
+  // columns 32j + 4tc + {0, 1} and {2, 3}
+  uint64_t S2[kCols / 2];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float4 s4 = __ldcs(reinterpret_cast<const float4*>(p.state_in + srow + 32 * j + 4 * tc));
-    S[4 * j] = s4.x;
-    S[4 * j + 1] = s4.y;
-    S[4 * j + 2] = s4.z;
-    S[4 * j + 3] = s4.w;
+    const ulonglong2 s4 = __ldcs(reinterpret_cast<const ulonglong2*>(p.state_in + srow + 32 * j + 4 * tc));
+    S2[2 * j] = s4.x;
+    S2[2 * j + 1] = s4.y;
   }
   int t0 = __ldg(p.offsets + b), t1 = __ldg(p.offsets + b + 1);
   if (t0 < 0 || t1 > p.T || t0 > t1) {
@@ -234,45 +259,43 @@ __global__ void __launch_bounds__(kThreads) gdn_scan_kernel(const Params p) {
           po[jj] = 0.f;
           continue;
         }
-        float kv[kCols], qv[kCols];
+        // k^ and q^ as packed pairs, in the layout of S2
+        uint64_t kv2[kCols / 2], qv2[kCols / 2];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const float4 k4 = *reinterpret_cast<const float4*>(&x.k[r][32 * j + 4 * tc]);
-          const float4 q4 = *reinterpret_cast<const float4*>(&x.q[r][32 * j + 4 * tc]);
-          kv[4 * j] = k4.x;
-          kv[4 * j + 1] = k4.y;
-          kv[4 * j + 2] = k4.z;
-          kv[4 * j + 3] = k4.w;
-          qv[4 * j] = q4.x;
-          qv[4 * j + 1] = q4.y;
-          qv[4 * j + 2] = q4.z;
-          qv[4 * j + 3] = q4.w;
+          const ulonglong2 k4 = *reinterpret_cast<const ulonglong2*>(&x.k[r][32 * j + 4 * tc]);
+          const ulonglong2 q4 = *reinterpret_cast<const ulonglong2*>(&x.q[r][32 * j + 4 * tc]);
+          kv2[2 * j] = k4.x;
+          kv2[2 * j + 1] = k4.y;
+          qv2[2 * j] = q4.x;
+          qv2[2 * j + 1] = q4.y;
         }
         const float alpha = x.alpha[r];
-        // u = S_j . k^ (before the decay; the decayed product is alpha u)
-        float u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+        // u = S_j . k^ (before the decay; the decayed product is alpha u), in
+        // four chains over columns 4i + c: chains 0 and 1 as one packed
+        // chain, 2 and 3 as another
+        uint64_t u01 = 0ull, u23 = 0ull;
 #pragma unroll
-        for (int i = 0; i < kCols; i += 4) {
-          u0 = fmaf(S[i], kv[i], u0);
-          u1 = fmaf(S[i + 1], kv[i + 1], u1);
-          u2 = fmaf(S[i + 2], kv[i + 2], u2);
-          u3 = fmaf(S[i + 3], kv[i + 3], u3);
+        for (int j = 0; j < 4; ++j) {
+          u01 = fma2(S2[2 * j], kv2[2 * j], u01);
+          u23 = fma2(S2[2 * j + 1], kv2[2 * j + 1], u23);
         }
-        const float u = row_sum((u0 + u1) + (u2 + u3));
+        const float2 ua = unpack2(u01), ub = unpack2(u23);
+        const float u = row_sum((ua.x + ua.y) + (ub.x + ub.y));
         const float w = x.beta[r] * (x.v[r][ri] - alpha * u);
-        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+        // S = alpha S + w k^ per column, then the output dot with q^ in the
+        // same four chains
+        const uint64_t alpha2 = pack2(alpha, alpha), w2 = pack2(w, w);
+        uint64_t o01 = 0ull, o23 = 0ull;
 #pragma unroll
-        for (int i = 0; i < kCols; i += 4) {
-          S[i] = fmaf(alpha, S[i], w * kv[i]);
-          S[i + 1] = fmaf(alpha, S[i + 1], w * kv[i + 1]);
-          S[i + 2] = fmaf(alpha, S[i + 2], w * kv[i + 2]);
-          S[i + 3] = fmaf(alpha, S[i + 3], w * kv[i + 3]);
-          o0 = fmaf(S[i], qv[i], o0);
-          o1 = fmaf(S[i + 1], qv[i + 1], o1);
-          o2 = fmaf(S[i + 2], qv[i + 2], o2);
-          o3 = fmaf(S[i + 3], qv[i + 3], o3);
+        for (int j = 0; j < 4; ++j) {
+          S2[2 * j] = fma2(alpha2, S2[2 * j], mul2(w2, kv2[2 * j]));
+          S2[2 * j + 1] = fma2(alpha2, S2[2 * j + 1], mul2(w2, kv2[2 * j + 1]));
+          o01 = fma2(S2[2 * j], qv2[2 * j], o01);
+          o23 = fma2(S2[2 * j + 1], qv2[2 * j + 1], o23);
         }
-        po[jj] = (o0 + o1) + (o2 + o3);
+        const float2 oa = unpack2(o01), ob = unpack2(o23);
+        po[jj] = (oa.x + oa.y) + (ob.x + ob.y);
       }
       // reduce-scatter over the row's 8 threads: thread tc ends with token r8 + tc
 #pragma unroll
@@ -300,8 +323,7 @@ __global__ void __launch_bounds__(kThreads) gdn_scan_kernel(const Params p) {
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    __stcs(reinterpret_cast<float4*>(p.state_out + srow + 32 * j + 4 * tc),
-           make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]));
+    __stcs(reinterpret_cast<ulonglong2*>(p.state_out + srow + 32 * j + 4 * tc), make_ulonglong2(S2[2 * j], S2[2 * j + 1]));
 }
 
 // Sequences of a token or two (decode): no staging, each thread reads its
