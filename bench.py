@@ -62,12 +62,12 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("gdn_scan_kernel", "gdn-prefill-4096"): dict(
-        bytes=70285824 + 25867776,
-        sources={"gdn.cu": "339557a34a9bfaba2e0943b1aa6090ab83f5a3e506864ca491ee1e56e8527aec",
+        bytes=70283776 + 24791040,
+        sources={"gdn.cu": "0e6cd58b752512d1bf7c2fc631398474c866923587ccd2ea93e0e780e54f56c4",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("gdn_short_kernel", "gdn-decode-b64"): dict(
         bytes=135301376 + 81671424,
-        sources={"gdn.cu": "339557a34a9bfaba2e0943b1aa6090ab83f5a3e506864ca491ee1e56e8527aec",
+        sources={"gdn.cu": "0e6cd58b752512d1bf7c2fc631398474c866923587ccd2ea93e0e780e54f56c4",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
         bytes=329211648 + 13866752,
