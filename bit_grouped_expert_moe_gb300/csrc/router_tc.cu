@@ -150,14 +150,8 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
 #pragma unroll
       for (int i = 0; i < kMaxPer; ++i)
         if (i < per_lane && p.wsg != nullptr) wv[i] = ldg_nc_v4(p.wsg + (lane + 32 * i) * 8);
-      for (int tl = warp - 2; tl < kRtTok; tl += kRtWarps - 2) {
-        const int t = t0 + tl;
-        if (t >= p.T) break;
-        const uint16_t* xr = p.x + (size_t)t * p.H;
-        uint4 xv[kMaxPer];
-#pragma unroll
-        for (int i = 0; i < kMaxPer; ++i)
-          if (i < per_lane) xv[i] = ldg_nc_v4(xr + (lane + 32 * i) * 8);
+      // one token's shared-gate logit and fp16 copy from its x row xv
+      auto token = [&](int t, const uint4 (&xv)[kMaxPer]) {
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < kMaxPer; ++i) {
@@ -199,6 +193,23 @@ router_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant
           for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
           if (lane == 0) p.logits[(size_t)t * (p.E + 1) + p.E] = acc;
         }
+      };
+      // two tokens per pass: both rows' loads go out before either is used
+      constexpr int kStride = kRtWarps - 2;
+      for (int tl = warp - 2; tl < kRtTok; tl += 2 * kStride) {
+        const int ta = t0 + tl, tb = ta + kStride;
+        if (ta >= p.T) break;
+        const bool has_b = tl + kStride < kRtTok && tb < p.T;
+        uint4 xa[kMaxPer], xb[kMaxPer];
+#pragma unroll
+        for (int i = 0; i < kMaxPer; ++i)
+          if (i < per_lane) xa[i] = ldg_nc_v4(p.x + (size_t)ta * p.H + (lane + 32 * i) * 8);
+        if (has_b)
+#pragma unroll
+          for (int i = 0; i < kMaxPer; ++i)
+            if (i < per_lane) xb[i] = ldg_nc_v4(p.x + (size_t)tb * p.H + (lane + 32 * i) * 8);
+        token(ta, xa);
+        if (has_b) token(tb, xb);
       }
     }
   }
