@@ -45,10 +45,11 @@ def build_bounds_checked(verbose: bool = False, force: bool = False) -> str:
     return build(verbose, force, DEBUG_FLAGS, build_dir=os.path.join(BUILD, "bounds"), lib=DEBUG_LIB)
 
 
-# Variants of the tensor-core expert GEMM's ring depths (codes, A, B), built to
-# their own files for the test that checks results do not depend on them.
-RING_VARIANTS = {"a4b4": ("-DBGMOE_TC_AS=4", "-DBGMOE_TC_BS=4"),
-                 "a5b3c2": ("-DBGMOE_TC_AS=5", "-DBGMOE_TC_BS=3", "-DBGMOE_TC_CS=2")}
+# Variants of the tensor-core expert GEMM's ring depths (gate/up A, down A, B,
+# codes), built to their own files for the test that checks results do not
+# depend on them.
+RING_VARIANTS = {"a4d3b4": ("-DBGMOE_TC_AS=4", "-DBGMOE_TC_AS_DOWN=3", "-DBGMOE_TC_BS=4"),
+                 "a5d5b3c2": ("-DBGMOE_TC_AS=5", "-DBGMOE_TC_AS_DOWN=5", "-DBGMOE_TC_BS=3", "-DBGMOE_TC_CS=2")}
 
 
 def build_ring_variant(name: str, verbose: bool = False, force: bool = False) -> str:

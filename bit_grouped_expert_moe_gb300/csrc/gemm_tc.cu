@@ -23,9 +23,9 @@
 // Persistent blocks (one per SM) walk the items with a stride of the grid;
 // every ring runs on across item boundaries and the TMEM accumulator is
 // double buffered, so one item's epilogue overlaps the next item's MMAs.
-// Rings: codes (TMA) 4 deep, dequantised A 3 deep, B 4 deep; the MMAs of
-// each stage are committed once, to a ring of 8 stage-done barriers that
-// every producer of a slot waits on.
+// Rings: codes (TMA) 4 deep, dequantised A 3 deep (down: 4), B 4 deep; the
+// MMAs of each stage are committed once, to a ring of 8 stage-done barriers
+// that every producer of a slot waits on.
 // Warp roles (576 threads):
 //   warp 0      TMA producer: code tiles (and h boxes for the down GEMM)
 //   warp 1      TMEM allocation and the single MMA-issuing thread
@@ -55,15 +55,22 @@ constexpr int kTcThreads = 576;
 #ifndef BGMOE_TC_BS
 #define BGMOE_TC_BS 4
 #endif
+#ifndef BGMOE_TC_AS_DOWN
+#define BGMOE_TC_AS_DOWN 4
+#endif
 #ifndef BGMOE_TC_A_MARGIN
 #define BGMOE_TC_A_MARGIN 1
 #endif
-// Ring depths: codes, A, B. Any depths within the stage_done ring and the
-// shared-memory limit are correct (the macros let a test build others). The
-// defaults are the fastest measured at 4096 tokens: a 5-deep B ring was 4 %
-// slower on gate/up than 4 and a 3-deep one 17 % slower (deeper A rings take
-// their shared memory from the B ring and are slower too).
-constexpr int kCS = BGMOE_TC_CS, kAS = BGMOE_TC_AS, kBS = BGMOE_TC_BS;
+// Ring depths: codes, A (gate/up and down GEMM), B. Any depths within the
+// stage_done ring and the shared-memory limit are correct (the macros let a
+// test build others). The defaults are the fastest measured: on gate/up at
+// 4096 tokens a 5-deep B ring was 4 % slower than 4 and a 3-deep one 17 %
+// slower, and a 4-deep A ring 2 % slower than 3; the down GEMM (8 stages an
+// item) is 1-6 % faster with a 4-deep A ring than with 3.
+constexpr int kCS = BGMOE_TC_CS, kBS = BGMOE_TC_BS;
+template <bool kGateUp>
+constexpr int kAStages = kGateUp ? BGMOE_TC_AS : BGMOE_TC_AS_DOWN;
+constexpr int kASMax = BGMOE_TC_AS > BGMOE_TC_AS_DOWN ? BGMOE_TC_AS : BGMOE_TC_AS_DOWN;
 // Generic-proxy stores into an A slot wait for the commit of the MMAs of
 // kAMargin stages AFTER the slot's previous use. Measured on GB300: rewriting
 // a slot as soon as the commit of the MMAs that read it had arrived corrupted
@@ -71,13 +78,13 @@ constexpr int kCS = BGMOE_TC_CS, kAS = BGMOE_TC_AS, kBS = BGMOE_TC_BS;
 // (the two accumulator chains of an item finish at different times); with a
 // one-stage margin no corruption was seen in any repeated run.
 constexpr int kAMargin = BGMOE_TC_A_MARGIN;
-static_assert(kAMargin >= 0 && kAMargin < kAS, "A-slot margin must leave the dequant a stage of lead");
+static_assert(kAMargin >= 0 && kAMargin < kAStages<true> && kAMargin < kAStages<false>,
+              "A-slot margin must leave the dequant a stage of lead");
 // An earlier layout, in which every dequantisation warp wrote one row of
 // every stage, gave wrong h rows with a 4-deep A ring and this margin (the
 // dequant waiting for the MMAs three iterations back). With the two groups
-// below, 4- and 5-deep rings give results bit-identical to the 3-deep one in
-// every repeat (a GPU test builds them), so the depth is free; 3 is the
-// fastest, the deeper rings taking their shared memory from the B ring.
+// below, 3-, 4- and 5-deep rings give bit-identical results in every repeat
+// (a GPU test builds them), so the depth is free.
 #ifndef BGMOE_TC_B_MARGIN
 #define BGMOE_TC_B_MARGIN 1
 #endif
@@ -90,17 +97,18 @@ static_assert(kBMargin >= 0 && kBMargin < kBS, "B-slot margin must leave the gat
 // kDone stages back before it tests a parity, and no waiter falls kDone
 // stages behind the MMAs (they need its output first).
 constexpr int kDone = 8;
-static_assert(kDone >= kAS && kDone >= kBS, "stage_done ring shorter than a data ring");
+static_assert(kDone >= kASMax && kDone >= kBS, "stage_done ring shorter than a data ring");
 constexpr int kMaxBN = 128;               // token rows per tile (block_m <= 128)
 constexpr int kTmemCols = 512;            // 2 buffers x (2 x 128 columns)
 constexpr int kCBytes = 8192;             // 256 rows x 32 B of codes
 constexpr int kABytes = 32768;            // 256 rows x 64 k fp16
 constexpr int kBBytes = 16384;            // 128 rows x 64 k fp16
-constexpr int kSmemData = kCS * kCBytes + kAS * kABytes + kBS * kBBytes;
+template <bool kGateUp>
+constexpr int kSmemData = kCS * kCBytes + kAStages<kGateUp> * kABytes + kBS * kBBytes;
 
 struct TcCtl {
   uint64_t c_full[kCS], c_empty[kCS];
-  uint64_t a_full[kAS];
+  uint64_t a_full[kASMax];
   uint64_t b_full[kBS];
   uint64_t stage_done[kDone];
   uint64_t acc_full[2], acc_empty[2];
@@ -143,6 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_constant__ CUtensorMap tm_s_codes,
                  const __grid_constant__ CUtensorMap tm_h, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
+  constexpr int kAS = kAStages<kGateUp>;  // A-ring depth of this GEMM
   if (block_failed(p.t.status)) return;
   const int num_tiles = *p.t.num_tiles;
   const int items = num_tiles * p.per_tile;
@@ -271,7 +280,13 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
       for (int k = 0; k < num_k; ++k, ++it) {
         const int as = it % kAS, bs = it % kBS;
-        if (!warp_wait(&ctl->a_full[as], (it / kAS) & 1) || !warp_wait(&ctl->b_full[bs], (it / kBS) & 1)) {
+        // Both barriers are tested at once, so a ready stage (the usual
+        // case) costs one shared-memory round trip, not two: the tensor pipe
+        // holds about one queued MMA, so it idles while this warp waits.
+        const bool ra = mbar_test_wait(&ctl->a_full[as], (it / kAS) & 1);
+        const bool rb = mbar_test_wait(&ctl->b_full[bs], (it / kBS) & 1);
+        if (!__all_sync(0xffffffffu, ra && rb) &&
+            (!warp_wait(&ctl->a_full[as], (it / kAS) & 1) || !warp_wait(&ctl->b_full[bs], (it / kBS) & 1))) {
           ok = false;
           break;
         }
@@ -597,7 +612,8 @@ cudaError_t tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-constexpr size_t kSmemBytes = kSmemData + sizeof(TcCtl) + 1024;
+template <bool kGateUp>
+constexpr size_t kSmemBytes = kSmemData<kGateUp> + sizeof(TcCtl) + 1024;
 
 int tc_sm_count() {
   static int sms[64] = {0};
@@ -612,14 +628,14 @@ template <bool kGateUp>
 cudaError_t launch_tc(const Geometry& g, const CUtensorMap& tm, const CUtensorMap& tms, const CUtensorMap& tmh,
                       const TcParams& p, cudaStream_t stream) {
   static SmemLimitMemo smem_memo;
-  cudaError_t e = ensure_smem(expert_tc_kernel<kGateUp>, kSmemBytes, &smem_memo);
+  cudaError_t e = ensure_smem(expert_tc_kernel<kGateUp>, kSmemBytes<kGateUp>, &smem_memo);
   if (e != cudaSuccess) return e;
   const int sms = tc_sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   // at most one item per block beyond the upper bound of the item count
   const int max_items = g.max_tiles * p.per_tile;
   const int grid = max_items < sms ? max_items : sms;
-  expert_tc_kernel<kGateUp><<<grid, kTcThreads, kSmemBytes, stream>>>(tm, tms, tmh, p);
+  expert_tc_kernel<kGateUp><<<grid, kTcThreads, kSmemBytes<kGateUp>, stream>>>(tm, tms, tmh, p);
   return cudaGetLastError();
 }
 
@@ -627,7 +643,7 @@ cudaError_t launch_tc(const Geometry& g, const CUtensorMap& tm, const CUtensorMa
 
 bool tc_path_supported(const Geometry& g) {
   if (g.H % 256 != 0 || g.I % 128 != 0 || g.BM > kMaxBN) return false;
-  if (kSmemBytes > 232448) return false;
+  if (kSmemBytes<true> > 232448 || kSmemBytes<false> > 232448) return false;
   return encode_fn() != nullptr;
 }
 

@@ -5,10 +5,12 @@ depths of the code, A and B rings, so a build with other depths must give the
 same bits. A race between the dequantisation, gather and MMA warps over a
 ring slot (a slot rewritten before the MMAs that read it were done) would
 show up as differing values, most readily with deeper rings, where the
-dequantisation runs further ahead of the completed MMAs. Builds with a 4- and
-a 5-deep A ring (libbgmoe_a4b4.so, libbgmoe_a5b3c2.so) run the 4096-token and
-the Zipf-skewed 512-token layers three times each in their own processes,
-and every output must equal the default build's bit for bit."""
+dequantisation runs further ahead of the completed MMAs. The default build
+has a 3-deep A ring in the gate/up GEMM and a 4-deep one in the down GEMM;
+builds with 4 and 3 (libbgmoe_a4d3b4.so) and with 5 and 5 and shallower code
+and B rings (libbgmoe_a5d5b3c2.so) run the 4096-token and the Zipf-skewed
+512-token layers three times each in their own processes, and every output
+must equal the default build's bit for bit."""
 import os
 import subprocess
 import sys
