@@ -52,8 +52,13 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-zipf-512"): dict(
-        bytes=132907264 + 4936960,
-        sources={"gemm_tc.cu": "ae3aea6886508ff1992d00133154d5cda66e2eb85b7e61455a10fecfc1cbe272",
+        bytes=132445440 + 4795904,
+        sources={"gemm_tc.cu": "a41874dd9244732326b9c0a49e4f9c165e8586f2435e03cbf6511ea55e450393",
+                 "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
+                 "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
+    ("expert_gate_up", "prefill-4096"): dict(
+        bytes=416270848 + 27324160,
+        sources={"gemm_tc.cu": "a41874dd9244732326b9c0a49e4f9c165e8586f2435e03cbf6511ea55e450393",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
@@ -70,8 +75,8 @@ PROFILED_TRAFFIC = {
         sources={"gdn.cu": "0e6cd58b752512d1bf7c2fc631398474c866923587ccd2ea93e0e780e54f56c4",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
-        bytes=329211648 + 13866752,
-        sources={"gemm_tc.cu": "ae3aea6886508ff1992d00133154d5cda66e2eb85b7e61455a10fecfc1cbe272",
+        bytes=327885056 + 13973760,
+        sources={"gemm_tc.cu": "a41874dd9244732326b9c0a49e4f9c165e8586f2435e03cbf6511ea55e450393",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
 }
