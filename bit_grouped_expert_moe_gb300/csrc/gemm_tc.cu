@@ -534,34 +534,35 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       float mx = 0.f;
       if (kGateUp) {
         const int pn = perm8_pos(sub * 128 + q * 32 + lane);
-        for (int j0 = 0; j0 < N; j0 += 32) {
+        __half* hcol = p.out + (size_t)row0 * I + pn;  // this lane's column of the tile's rows
+        for (int j0 = 0; j0 < N; j0 += 32, hcol += (size_t)32 * I) {
           float g[32], u[32];
           tmem_ld_32(lane_addr + j0, g);
           tmem_ld_32(lane_addr + 128 + j0, u);
+          const int lim = rows - j0;  // rows of this 32-row block that exist
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            if (j < rows) {
+            if (jj < lim) {
               const float hf = silu_fast(g[jj]) * u[jj];
               mx = fmaxf(mx, fabsf(hf));
-              p.out[(size_t)(row0 + j) * I + pn] = __float2half_rn(hf);
+              hcol[jj * I] = __float2half_rn(hf);
             }
           }
         }
       } else {
         const int m = sub * 256 + q * 32 + lane;
-        for (int j0 = 0; j0 < N; j0 += 32) {
+        __half* ocol = p.out + (size_t)row0 * H + m;  // this lane's column of the tile's rows
+        for (int j0 = 0; j0 < N; j0 += 32, ocol += (size_t)32 * H) {
           float v0[32], v1[32];
           tmem_ld_32(lane_addr + j0, v0);
           tmem_ld_32(lane_addr + 128 + j0, v1);
+          const int lim = rows - j0;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
-            const int j = j0 + jj;
-            if (j < rows) {
-              __half* orow = p.out + (size_t)(row0 + j) * H;
+            if (jj < lim) {
               mx = fmaxf(mx, fmaxf(fabsf(v0[jj]), fabsf(v1[jj])));
-              orow[m] = __float2half_rn(v0[jj]);
-              orow[m + 128] = __float2half_rn(v1[jj]);
+              ocol[jj * H] = __float2half_rn(v0[jj]);
+              ocol[jj * H + 128] = __float2half_rn(v1[jj]);
             }
           }
         }
