@@ -540,12 +540,21 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           tmem_ld_32(lane_addr + j0, g);
           tmem_ld_32(lane_addr + 128 + j0, u);
           const int lim = rows - j0;  // rows of this 32-row block that exist
+          if (lim >= 32) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            if (jj < lim) {
+            for (int jj = 0; jj < 32; ++jj) {
               const float hf = silu_fast(g[jj]) * u[jj];
               mx = fmaxf(mx, fabsf(hf));
               hcol[jj * I] = __float2half_rn(hf);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              if (jj < lim) {
+                const float hf = silu_fast(g[jj]) * u[jj];
+                mx = fmaxf(mx, fabsf(hf));
+                hcol[jj * I] = __float2half_rn(hf);
+              }
             }
           }
         }
@@ -557,12 +566,21 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
           tmem_ld_32(lane_addr + j0, v0);
           tmem_ld_32(lane_addr + 128 + j0, v1);
           const int lim = rows - j0;
+          if (lim >= 32) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            if (jj < lim) {
+            for (int jj = 0; jj < 32; ++jj) {
               mx = fmaxf(mx, fmaxf(fabsf(v0[jj]), fabsf(v1[jj])));
               ocol[jj * H] = __float2half_rn(v0[jj]);
               ocol[jj * H + 128] = __float2half_rn(v1[jj]);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              if (jj < lim) {
+                mx = fmaxf(mx, fmaxf(fabsf(v0[jj]), fabsf(v1[jj])));
+                ocol[jj * H] = __float2half_rn(v0[jj]);
+                ocol[jj * H + 128] = __float2half_rn(v1[jj]);
+              }
             }
           }
         }
