@@ -148,6 +148,11 @@ __device__ __forceinline__ uint32_t u4_get(const uint4& v, int i) {
 // them on each scheduler need (gate/up 233 -> 224 us at 4096 tokens).
 __device__ __forceinline__ float silu_fast(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
+// 16 bytes to a shared-memory address
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
 __device__ __forceinline__ uint32_t bf16_of(const uint4& v, int g) {
   const uint32_t w = u4_get(v, g >> 1);
   return (g & 1) ? (w >> 16) : (w & 0xFFFFu);
@@ -411,14 +416,17 @@ expert_tc_kernel(const __grid_constant__ CUtensorMap tm_codes, const __grid_cons
       // the slot was last read by the tensor core (async proxy): order
       // those reads before these generic-proxy stores
       fence_proxy_async();
-      uint8_t* dst = arow0 + as * kABytes;
+      // row gt's chunk q sits at chunk q ^ (gt & 7) of its 128-byte row (the
+      // 128-byte swizzle); the row starts 128-byte aligned, so its address is
+      // (row | (gt & 7) << 4) ^ q << 4: one XOR per store
+      const uint32_t dsx = smem_u32(arow0 + as * kABytes) | ((uint32_t)(gt & 7) << 4);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         uint32_t o[4], u[4];
         dequant8_f16(q < 4 ? u4_get(a0, q) : u4_get(a1, q - 4), sa, ba, o);
         dequant8_f16(q < 4 ? u4_get(b0, q) : u4_get(b1, q - 4), sb, bb, u);
-        *reinterpret_cast<uint4*>(dst + ((q ^ (gt & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(dst + 16384 + ((q ^ (gt & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+        sts128(dsx ^ (uint32_t)(q << 4), o[0], o[1], o[2], o[3]);
+        sts128((dsx ^ (uint32_t)(q << 4)) + 16384u, u[0], u[1], u[2], u[3]);
       }
       fence_proxy_async();
       __syncwarp();
