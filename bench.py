@@ -52,13 +52,13 @@ PROFILED_TRAFFIC = {
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-zipf-512"): dict(
-        bytes=132445440 + 4795904,
-        sources={"gemm_tc.cu": "a41874dd9244732326b9c0a49e4f9c165e8586f2435e03cbf6511ea55e450393",
+        bytes=132567040 + 4606720,
+        sources={"gemm_tc.cu": "23068ea0388ed111f7d85c44483b2fe8cac112c3d26632fee35e3ee16cb1b6cc",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "prefill-4096"): dict(
-        bytes=416270848 + 27324160,
-        sources={"gemm_tc.cu": "a41874dd9244732326b9c0a49e4f9c165e8586f2435e03cbf6511ea55e450393",
+        bytes=415157504 + 28314880,
+        sources={"gemm_tc.cu": "23068ea0388ed111f7d85c44483b2fe8cac112c3d26632fee35e3ee16cb1b6cc",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("attn_block_kernel", "attn-decode-32k"): dict(
@@ -75,8 +75,8 @@ PROFILED_TRAFFIC = {
         sources={"gdn.cu": "0e6cd58b752512d1bf7c2fc631398474c866923587ccd2ea93e0e780e54f56c4",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
     ("expert_gate_up", "long-skew-16384"): dict(
-        bytes=327885056 + 13973760,
-        sources={"gemm_tc.cu": "a41874dd9244732326b9c0a49e4f9c165e8586f2435e03cbf6511ea55e450393",
+        bytes=328094976 + 14594048,
+        sources={"gemm_tc.cu": "23068ea0388ed111f7d85c44483b2fe8cac112c3d26632fee35e3ee16cb1b6cc",
                  "tc_ptx.cuh": "91cf5c0848386f35a604cc2a0ae91ff9fe4fb195eb7e41d989b49257ac65cd7d",
                  "common.cuh": "50bd4e54a129b106017f859e988153a6e556e0b58fca272f8d3712d8150c02c4"}),
 }
